@@ -1,0 +1,371 @@
+/*
+ * kvq_oracle.c -- the CPU oracle for the FP8 E4M3 paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product (the fp8_paged_kv_kvq_gb300
+ * package, its CUDA library or its C ABI) includes, links or calls this file.
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline / reference
+ * leg load it.  It shares no code, header, table or constant generator with the
+ * CUDA path: everything here is written from the format definition and from the
+ * pages' description of the method, in the plainest form, single-threaded.
+ *
+ * Build: plain C11, -O2 -ffp-contract=off, no -ffast-math, so that every float
+ * operation below is one IEEE-754 binary32 operation rounded to nearest-even.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [ATOM]   ROCm/ATOM PR #2655, "fix(qwen4-exp): register the QSA FP8 scale
+ *           planes for KV offload" -- PR description, K/V bullet: E4M3 codes
+ *           with one FP32 scale per (token, KV head) = row amax / FP8 max; the
+ *           attention kernel multiplies the key scale into its score column and
+ *           folds the value scale into the probability before PV.
+ *  [FT]     FlashML-org/FreeToken PR #354, "feat(kvcache): store the KV cache as
+ *           fp8 e4m3 codes (--kv-cache-dtype fp8)" -- PR description: head_dim
+ *           codes plus one fp32 symmetric scale per row, codes in a uint8 buffer
+ *           with the geometry of the 16-bit KV buffer, fused quantize+scatter to
+ *           device slot ids; review thread and fix commit "give the V tensor its
+ *           own row pitch in the fp8 KV store": K and V each have their own row
+ *           pitch; codes are checked against a round-to-nearest-even reference.
+ *  [SGJ]    sgl-project/sglang-jax #1776, "feat(dsa): implement fp8 KV cache
+ *           (e4m3) with a bf16 indexer cache" -- design points: e4m3 range 448,
+ *           0.0156 floor of the normal range, ~6% worst-case relative error.
+ *
+ * Readings of points the pages leave open (each one is listed in the design doc):
+ *  - the encode divides by the stored fp32 scale: q = fl32(x / s);
+ *  - rounding is round-to-nearest-even onto the e4m3 grid, |q| >= 448 saturates
+ *    to the largest finite code (0x7E magnitude); NaN codes are never produced;
+ *  - an all-zero row stores s = 0 and all codes 0x00 (even for -0.0 inputs);
+ *  - in a nonzero row the sign of zero is kept (-0.0 or a negative value that
+ *    rounds to zero gives 0x80);
+ *  - GQA maps query head hq to KV head hq / (Hq / H);
+ *  - a request with R query rows (multi-token verify) is causal: row i sees the
+ *    first L - R + 1 + i cached tokens; a row that sees nothing outputs zeros;
+ *  - slot ids < 0 are padding and are skipped; ids >= num_slots are skipped and
+ *    reported in the error word (bit 0).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KVQO_ERR_SLOT_RANGE 1
+#define KVQO_ERR_BLOCK_RANGE 2
+#define KVQO_ERR_CONTEXT_RANGE 4
+
+/* ------------------------------------------------------------------------ */
+/* bfloat16 <-> float, by definition of the format (upper half of binary32). */
+
+float kvqo_bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a finite float to bfloat16, nearest-even: the 16 dropped bits decide. */
+uint16_t kvqo_float_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t upper = u >> 16;
+    uint32_t lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;
+    return (uint16_t)upper;
+}
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 ("fn" variant: no infinities, S.1111.111 is NaN, max finite 448).
+ * A code is 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits.
+ *   E in 1..15: value = 2^(E-7) * (1 + M/8)
+ *   E == 0:     value = 2^(-6) * (M/8)          (subnormal)
+ * [SGJ] design points give the 448 top and the 0.0156 bottom of the normal
+ * range; the format itself is the OCP 8-bit floating point "E4M3" encoding. */
+
+double kvqo_e4m3_decode(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Encode a finite binary32 value: round to the nearest representable e4m3
+ * magnitude, ties to the code whose mantissa is even, saturating at 448.
+ * The search runs over the 127 finite nonnegative magnitudes 0x00..0x7E, which
+ * increase with the code, so a bisection finds the two neighbours of |q|. */
+uint8_t kvqo_e4m3_encode(float q)
+{
+    uint8_t sign = signbit(q) ? 0x80 : 0x00;
+    double a = fabs((double)q);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    /* invariant: value(lo) <= a < value(hi) */
+    int lo = 0, hi = 0x7E;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (kvqo_e4m3_decode((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double vlo = kvqo_e4m3_decode((uint8_t)lo);
+    double vhi = kvqo_e4m3_decode((uint8_t)hi);
+    double half = 0.5 * (vlo + vhi); /* exact: both have few significant bits */
+    int pick;
+    if (a < half)
+        pick = lo;
+    else if (a > half)
+        pick = hi;
+    else
+        pick = (lo & 1) ? hi : lo; /* the mantissa LSB is the code LSB */
+    return (uint8_t)(sign | pick);
+}
+
+/* Element-wise forms of the two functions above, for arrays. */
+void kvqo_e4m3_encode_array(const float *q, int64_t n, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = kvqo_e4m3_encode(q[i]);
+}
+
+void kvqo_float_to_bf16_array(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kvqo_float_to_bf16(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* One (token, KV head) row: [ATOM] PR description (K/V bullet) and [FT] PR
+ * description: scale = row amax / FP8 max (448), codes = e4m3(x / scale). */
+
+void kvqo_quantize_row(const uint16_t *x, int D, uint8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(kvqo_bf16_to_float(x[d]));
+        if (a > amax)
+            amax = a;
+    }
+    if (amax == 0.0f) {
+        *scale = 0.0f;
+        memset(codes, 0, (size_t)D);
+        return;
+    }
+    float s = amax / 448.0f;
+    *scale = s;
+    for (int d = 0; d < D; ++d) {
+        float q = kvqo_bf16_to_float(x[d]) / s;
+        codes[d] = kvqo_e4m3_encode(q);
+    }
+}
+
+/* Fused quantize + scatter, [FT] PR description and fix commit: token t's K
+ * row for head h starts at k + t*k_token_stride + h*D (elements), V's at
+ * v + t*v_token_stride + h*D, each with its own pitch; the codes land in the
+ * cache at slot slot_ids[t], laid out [num_slots, H, D] (the 16-bit buffer's
+ * geometry), the scales at [num_slots, H]. Returns the error word. */
+int32_t kvqo_quantize_scatter(const uint16_t *k, int64_t k_token_stride,
+                              const uint16_t *v, int64_t v_token_stride,
+                              int64_t num_tokens, int H, int D,
+                              const int64_t *slot_ids, int64_t num_slots,
+                              uint8_t *k_codes, uint8_t *v_codes,
+                              float *k_scales, float *v_scales)
+{
+    int32_t err = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_ids[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {
+            err |= KVQO_ERR_SLOT_RANGE;
+            continue;
+        }
+        for (int h = 0; h < H; ++h) {
+            int64_t row = slot * H + h;
+            kvqo_quantize_row(k + t * k_token_stride + (int64_t)h * D, D,
+                              k_codes + row * D, &k_scales[row]);
+            kvqo_quantize_row(v + t * v_token_stride + (int64_t)h * D, D,
+                              v_codes + row * D, &v_scales[row]);
+        }
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantize rows at the given slots: value = fl32(decode(c) * s), one IEEE
+ * multiply (decode(c) is exact in binary32); out_dtype 1 rounds that float
+ * once more to bfloat16 (nearest-even). Layout of out: [n, H, D]. */
+
+void kvqo_dequant_rows(const uint8_t *codes, const float *scales, int64_t num_slots,
+                       int H, int D, const int64_t *slot_ids, int64_t n,
+                       int out_dtype, void *out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t slot = slot_ids[i];
+        for (int h = 0; h < H; ++h) {
+            for (int d = 0; d < D; ++d) {
+                int64_t o = (i * H + h) * D + d;
+                float val = 0.0f;
+                if (slot >= 0 && slot < num_slots) {
+                    int64_t row = slot * H + h;
+                    val = (float)kvqo_e4m3_decode(codes[row * D + d]) * scales[row];
+                }
+                if (out_dtype == 0)
+                    ((float *)out)[o] = val;
+                else
+                    ((uint16_t *)out)[o] = kvqo_float_to_bf16(val);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged GQA attention in fp64 over the dequantised cache.
+ *
+ * Requests r = 0..N-1 each have R query rows (R = 1: decode; R > 1: the rows
+ * of a multi-token verify, the last R tokens already in the cache) and Hq
+ * query heads sharing H KV heads (G = Hq / H, head hq reads KV head hq / G).
+ * Cached token j of request r lives at slot
+ *     block_tables[r * max_blocks + j / bs] * bs + j % bs.
+ * Row i of request r sees the first  L_r - R + 1 + i  tokens.
+ *
+ * For each visible token: k_hat = decode(code) * k_scale, v_hat likewise
+ * (exact in double); score = sm_scale * <q, k_hat>; p = softmax(score);
+ * out = sum_j p_j * v_hat_j.  Multiplying the key scale into the score column
+ * and folding the value scale into p before PV ([ATOM] PR description) is the
+ * same quantity in exact arithmetic; the oracle takes the plain definition.
+ *
+ * q: bf16 [N*R, Hq, D]; out: double [N*R, Hq, D]. Returns the error word
+ * (bit 1: a block id outside [0, num_slots/bs); bit 2: a context length
+ * outside [0, max_blocks*bs]); offending tokens / rows are left out.
+ * `scores` is caller scratch of at least max_blocks*bs doubles. */
+static int32_t attention_row(const uint8_t *k_codes, const uint8_t *v_codes,
+                             const float *k_scales, const float *v_scales,
+                             int64_t num_slots, int H, int D, int bs,
+                             const uint16_t *qrow, int kvh,
+                             const int32_t *bt_row, int visible, double sm_scale,
+                             double *scores, double *out)
+{
+    int32_t err = 0;
+    int64_t num_blocks = num_slots / bs;
+    double mx = -INFINITY;
+    for (int j = 0; j < visible; ++j) {
+        int64_t blk = bt_row[j / bs];
+        if (blk < 0 || blk >= num_blocks) {
+            err |= KVQO_ERR_BLOCK_RANGE;
+            scores[j] = -INFINITY;
+            continue;
+        }
+        int64_t row = (blk * bs + j % bs) * H + kvh;
+        double ks = (double)k_scales[row];
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) {
+            double kh = kvqo_e4m3_decode(k_codes[row * D + d]) * ks;
+            dot += (double)kvqo_bf16_to_float(qrow[d]) * kh;
+        }
+        scores[j] = sm_scale * dot;
+        if (scores[j] > mx)
+            mx = scores[j];
+    }
+    for (int d = 0; d < D; ++d)
+        out[d] = 0.0;
+    if (mx == -INFINITY)
+        return err; /* nothing visible: zeros */
+    double l = 0.0;
+    for (int j = 0; j < visible; ++j) {
+        if (scores[j] == -INFINITY)
+            continue;
+        double p = exp(scores[j] - mx);
+        l += p;
+        int64_t row = ((int64_t)bt_row[j / bs] * bs + j % bs) * H + kvh;
+        double vs = (double)v_scales[row];
+        for (int d = 0; d < D; ++d)
+            out[d] += p * (kvqo_e4m3_decode(v_codes[row * D + d]) * vs);
+    }
+    for (int d = 0; d < D; ++d)
+        out[d] /= l;
+    return err;
+}
+
+int32_t kvqo_paged_attention(const uint8_t *k_codes, const uint8_t *v_codes,
+                             const float *k_scales, const float *v_scales,
+                             int64_t num_slots, int H, int D, int bs,
+                             const uint16_t *q, int N, int R, int Hq,
+                             const int32_t *block_tables, int max_blocks,
+                             const int32_t *context_lens, double sm_scale,
+                             double *out)
+{
+    int32_t err = 0;
+    int G = Hq / H;
+    double *scores = (double *)malloc(sizeof(double) * ((size_t)max_blocks * bs + 1));
+    if (!scores)
+        return -1;
+    for (int r = 0; r < N; ++r) {
+        int L = context_lens[r];
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks * bs) {
+            err |= KVQO_ERR_CONTEXT_RANGE;
+            L = L < 0 ? 0 : max_blocks * bs;
+        }
+        for (int i = 0; i < R; ++i) {
+            int visible = L - R + 1 + i;
+            if (visible < 0)
+                visible = 0;
+            for (int hq = 0; hq < Hq; ++hq) {
+                int64_t orow = ((int64_t)(r * R + i) * Hq + hq);
+                err |= attention_row(k_codes, v_codes, k_scales, v_scales, num_slots,
+                                     H, D, bs, q + orow * D, hq / G,
+                                     block_tables + (int64_t)r * max_blocks, visible,
+                                     sm_scale, scores, out + orow * D);
+            }
+        }
+    }
+    free(scores);
+    return err;
+}
+
+/* The same attention for a chosen list of (request, row, query head) units,
+ * written to out[u * D ..]: lets a test or a timing sample cover part of a
+ * large batch. units: int32 triples (r, i, hq). */
+int32_t kvqo_paged_attention_units(const uint8_t *k_codes, const uint8_t *v_codes,
+                                   const float *k_scales, const float *v_scales,
+                                   int64_t num_slots, int H, int D, int bs,
+                                   const uint16_t *q, int N, int R, int Hq,
+                                   const int32_t *block_tables, int max_blocks,
+                                   const int32_t *context_lens, double sm_scale,
+                                   const int32_t *units, int64_t num_units,
+                                   double *out)
+{
+    int32_t err = 0;
+    int G = Hq / H;
+    double *scores = (double *)malloc(sizeof(double) * ((size_t)max_blocks * bs + 1));
+    if (!scores)
+        return -1;
+    for (int64_t u = 0; u < num_units; ++u) {
+        int r = units[3 * u], i = units[3 * u + 1], hq = units[3 * u + 2];
+        if (r < 0 || r >= N || i < 0 || i >= R || hq < 0 || hq >= Hq) {
+            free(scores);
+            return -1;
+        }
+        int L = context_lens[r];
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks * bs) {
+            err |= KVQO_ERR_CONTEXT_RANGE;
+            L = L < 0 ? 0 : max_blocks * bs;
+        }
+        int visible = L - R + 1 + i;
+        if (visible < 0)
+            visible = 0;
+        int64_t orow = ((int64_t)(r * R + i) * Hq + hq);
+        err |= attention_row(k_codes, v_codes, k_scales, v_scales, num_slots, H, D, bs,
+                             q + orow * D, hq / G, block_tables + (int64_t)r * max_blocks,
+                             visible, sm_scale, scores, out + u * D);
+    }
+    free(scores);
+    return err;
+}
