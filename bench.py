@@ -1,0 +1,741 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 E4M3 paged KV cache on GB300.
+
+One step = one pass of the whole hot path over one batch: the fused
+quantize-scatter of the step's new K/V rows (R per request) into the FP8 cache,
+then paged GQA decode / verify attention over the cache (split-K partials, then
+the combine).  Inputs are synthetic and seeded (workloads/), resident in HBM
+before the timed region; L2 is flushed (a 256 MiB write) before every timed
+step and the step time is the sum of per-step CUDA-event intervals taken on the
+launching stream.
+
+Default workload: the decode batch -- 32 requests, context lengths uniform in
+[1024, 8192], 32 query heads / 8 KV heads, head_dim 128, block size 16,
+log-normal row magnitudes, one query row per request.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
+                  [--workload decode|verify|longctx|store|tiny]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (oracle/)
+on bounded samples of the same workload; it is a deliberately slow program, a
+reported baseline and not the target.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged FP8-KV decode attn: achieved HBM GB/s (% of 8 TB/s); KV rows quantized/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 256 << 20
+
+DESCRIPTIONS = {
+    "tiny": "tiny: 1 request x 64 tokens, 32 q heads / 8 KV heads, head_dim 128, block 16",
+    "decode": ("decode batch: 32 requests, context U[1024, 8192], 32 q heads / 8 KV heads, "
+               "head_dim 128, block 16, log-normal rows, 1 query row per request"),
+    "verify": ("MTP verify: 64 requests x 4 query rows, context 32768, 64 q heads / 8 KV heads, "
+               "head_dim 128, block 64, 32 stacked rows per KV head"),
+    "longctx": ("long-context split-K: 2 requests x 1,048,576 tokens, 32 q heads / 8 KV heads, "
+                "head_dim 128, block 64"),
+    "store": ("prefill store under CUDA graph: 16,384 tokens as strided K/V views of a fused "
+              "qkv [16384, 6144], 1% outliers x50, zero rows, permuted int64 slot ids, block 64"),
+}
+
+DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "verify": 1500, "longctx": 1500, "store": 5000}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--workload", choices=list(DESCRIPTIONS), default="decode")
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="no L2 flush, clocks, e2e or CPU baseline: a short run for ncu")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed (replicas: every rank runs its own copy of the workload)
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def dist_max(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, committed ncu traffic
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while it runs."""
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.sel = str(device_index)
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t_start: float, t_stop: float):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, val in zip(names, r[2][1:]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def ncu_traffic(kernel: str, workload: str, source: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/ncu_traffic.json), or None when the kernel's source file
+    changed since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            e = json.load(f)[f"{kernel}:{workload}"]
+        with open(os.path.join(ROOT, source), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if e.get("source_sha256_16") != h:
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# workload on the device
+
+class DeviceWorkload:
+    def __init__(self, name: str, device, partition_tokens: int = 0):
+        import fp8_paged_kv_kvq_gb300 as kvq
+        self.kvq = kvq
+        self.lib = kvq.load()
+        self.name = name
+        self.w = w = workloads.WORKLOADS[name]
+        self.device = device
+        self.stream = torch.cuda.Stream(device)
+        H, D = w.num_kv_heads, w.head_dim
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        if name == "store":
+            self._init_store()
+            return
+        self.lens = workloads.context_lengths(w)
+        self.bt, nblk = workloads.block_tables(self.lens, w.block_size, w.seed)
+        self.S = nblk * w.block_size
+        self.cache = kvq.Cache.empty(self.S, H, D, w.block_size, device=device)
+        ct = workloads.chunk_tokens(w)
+        for r in range(w.num_requests):
+            L = int(self.lens[r])
+            slots_all = workloads.token_slots(self.bt, r, L, w.block_size)
+            for c0 in range(0, L, ct):
+                n = min(ct, L - c0)
+                k, v = workloads.request_kv(w, r, c0, n, device=device)
+                kvq.quantize_scatter(self.cache, k, v,
+                                     torch.from_numpy(slots_all[c0:c0 + n]).to(device), self.err)
+        R = w.rows_per_request
+        # the step's new rows: the last R tokens of every request (already in
+        # the cache with the same values, so storing them again is idempotent)
+        ks, vs, sl = [], [], []
+        for r in range(w.num_requests):
+            L = int(self.lens[r])
+            k, v = workloads.request_kv(w, r, L - R, R, device=device)
+            ks.append(k)
+            vs.append(v)
+            sl.append(workloads.token_slots(self.bt, r, L, w.block_size)[L - R:])
+        self.new_k = torch.cat(ks).contiguous()
+        self.new_v = torch.cat(vs).contiguous()
+        self.new_slots = torch.from_numpy(np.concatenate(sl)).to(device)
+        self.q = workloads.queries(w, device=device)
+        self.bt_d = torch.from_numpy(self.bt).to(device)
+        self.cl_d = torch.from_numpy(self.lens).to(device)
+        self.max_ctx = int(self.lens.max())
+        self.P = partition_tokens or kvq.paged_decode_partition_tokens(
+            w.num_requests, H, w.block_size, self.max_ctx)
+        self.n_parts = (self.max_ctx + self.P - 1) // self.P
+        need = kvq.paged_decode_workspace_size(w.num_requests, R, w.num_q_heads, H, D,
+                                               w.block_size, self.max_ctx, self.P)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.out = torch.empty_like(self.q)
+        torch.cuda.synchronize(device)
+        assert int(self.err.item()) == 0, "setup store reported an error"
+        self._bind()
+
+    def _init_store(self):
+        w = self.w
+        qkv, _, _, slots, S = workloads.store_qkv(w, device=self.device)
+        self.qkv = qkv
+        Hq, H, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+        self.new_k = qkv[:, Hq * D:(Hq + H) * D].view(-1, H, D)
+        self.new_v = qkv[:, (Hq + H) * D:].view(-1, H, D)
+        self.new_slots = slots
+        self.S = S
+        self.n_parts = 0
+        self.cache = self.kvq.Cache.empty(S, H, D, w.block_size, device=self.device)
+        torch.cuda.synchronize(self.device)
+        self._bind()
+
+    def _bind(self):
+        """Pre-built ctypes argument lists for the C-ABI calls of one step."""
+        w, P = self.w, ctypes.c_void_p
+        self._cst = self.cache.struct()
+        sp = P(self.stream.cuda_stream)
+        T = self.new_k.shape[0]
+        self._q_args = (ctypes.byref(self._cst), P(self.new_k.data_ptr()), self.new_k.stride(0),
+                        P(self.new_v.data_ptr()), self.new_v.stride(0), T,
+                        P(self.new_slots.data_ptr()), P(self.err.data_ptr()), sp)
+        if self.name == "store":
+            return
+        R, N = w.rows_per_request, w.num_requests
+        self._p_args = (ctypes.byref(self._cst), P(self.q.data_ptr()), N, R, w.num_q_heads,
+                        P(self.bt_d.data_ptr()), self.bt.shape[1], P(self.cl_d.data_ptr()),
+                        self.max_ctx, ctypes.c_float(w.sm_scale), self.P, P(self.out.data_ptr()),
+                        P(self.ws.data_ptr()), self.ws.numel(), P(self.err.data_ptr()), sp)
+        self._c_args = (ctypes.byref(self._cst), N, R, w.num_q_heads, self.bt.shape[1],
+                        P(self.cl_d.data_ptr()), self.max_ctx, self.P, P(self.out.data_ptr()),
+                        P(self.ws.data_ptr()), self.ws.numel(), sp)
+
+    # the launches of a step, through the C ABI
+    def quantize(self):
+        st = self.lib.kvq_quantize_scatter(*self._q_args)
+        if st:
+            raise RuntimeError(f"kvq_quantize_scatter: status {st}")
+
+    def partials(self):
+        st = self.lib.kvq_paged_decode_partials(*self._p_args)
+        if st:
+            raise RuntimeError(f"kvq_paged_decode_partials: status {st}")
+
+    def combine(self):
+        st = self.lib.kvq_paged_decode_combine(*self._c_args)
+        if st:
+            raise RuntimeError(f"kvq_paged_decode_combine: status {st}")
+
+    @property
+    def launches_per_step(self):
+        if self.name == "store":
+            return 1
+        return 2 + (1 if self.n_parts > 1 else 0)
+
+    # algorithmic bytes: attention = codes + scales + q + out + block tables +
+    # context lengths; store = bf16 K/V read + codes + scales + slot ids
+    def store_bytes(self):
+        w = self.w
+        T = self.new_k.shape[0]
+        H, D = w.num_kv_heads, w.head_dim
+        return T * H * (2 * D * 2 + 2 * D + 2 * 4) + T * 8
+
+    def attn_bytes(self):
+        if self.name == "store":
+            return 0
+        w = self.w
+        H, D = w.num_kv_heads, w.head_dim
+        tok = int(self.lens.sum())
+        bt = sum((int(L) + w.block_size - 1) // w.block_size for L in self.lens) * 4
+        return tok * H * 2 * (D + 4) + 2 * self.q.numel() * 2 + bt + 4 * w.num_requests
+
+    def rows_quantized(self):
+        return self.new_k.shape[0] * self.w.num_kv_heads * 2
+
+    def tokens(self):
+        return self.new_k.shape[0]
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+
+def run_kvq(args, rank, local, world):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    W = max(3, args.warmup if args.warmup is not None else min(50, max(3, K // 10)))
+    wl = DeviceWorkload(args.workload, dev, args.partition_tokens)
+    with torch.cuda.stream(wl.stream):
+        return _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W)
+
+
+def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
+    stream = wl.stream
+    flush = None if args.profile else torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    graph = None
+    if args.workload == "store":
+        wl.quantize()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            wl.quantize()
+        torch.cuda.synchronize(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        if graph is not None:
+            graph.replay()
+            if evs is not None:
+                for e in evs[1:]:
+                    e.record(stream)
+            return
+        wl.quantize()
+        if evs is not None:
+            evs[1].record(stream)
+        wl.partials()
+        if evs is not None:
+            evs[2].record(stream)
+        wl.combine()
+        if evs is not None:
+            evs[3].record(stream)
+
+    for i in range(W):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    peak, peak_src = measured_peaks()
+    sampler = ClockSampler(local) if not args.profile else None
+    dist_barrier(world)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        if flush is not None:
+            flush.fill_((i + 7) & 0xFF)
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    wall1 = time.perf_counter()
+    if sampler:
+        sampler.stop()
+    dist_barrier(world)
+    st_q = [e[0].elapsed_time(e[1]) for e in evs]
+    st_p = [e[1].elapsed_time(e[2]) for e in evs]
+    st_c = [e[2].elapsed_time(e[3]) for e in evs]
+    st = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = dist_max(sum(st) / K, world)
+    if int(wl.err.item()) != 0:
+        raise RuntimeError("device error flags set during the benchmark")
+
+    step_bytes = wl.store_bytes() + wl.attn_bytes()
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": DESCRIPTIONS[args.workload],
+            "name": args.workload,
+            "l2": ("flushed before every timed step (256 MiB write); step time = sum of "
+                   "per-step CUDA-event intervals") if flush is not None else
+                  "not flushed (profile mode)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "storage": "e4m3 codes (uint8) + fp32 row scales; bf16 q/out; bf16 tensor-core "
+                       "operands, fp32 accumulate",
+        },
+        "pct_of_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "kv_rows_quantized_per_s": round(world * wl.rows_quantized() / (step_ms * 1e-3), 1),
+        "tokens_per_s": round(world * wl.tokens() / (step_ms * 1e-3), 1),
+        "kernels_us": {"quantize_scatter": round(1e3 * sum(st_q) / K, 3)},
+        "gpu_launches": K * wl.launches_per_step,
+        "wall_s_timed_region": round(wall1 - wall0, 3),
+    }
+    if args.workload != "store":
+        res["config"]["partition_tokens"] = wl.P
+        res["config"]["partitions"] = wl.n_parts
+        res["kernels_us"]["paged_decode_partials"] = round(1e3 * sum(st_p) / K, 3)
+        res["kernels_us"]["paged_decode_combine"] = round(1e3 * sum(st_c) / K, 3)
+        dom_ms, dom_bytes = sum(st_p) / K, wl.attn_bytes()
+        dom_name, dom_src = "attn_partials_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention.cu"
+    else:
+        dom_ms, dom_bytes = sum(st_q) / K, wl.store_bytes()
+        dom_name, dom_src = "quantize_scatter_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_quantize.cu"
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    res["roofline"] = {
+        "kernel": dom_name,
+        "bound": "hbm",
+        "achieved": round(achieved, 2),
+        "peak": peak,
+        "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                        else "fallback 6.8 TB/s"),
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "algorithmic_bytes_per_launch": dom_bytes,
+        "traffic": ncu_traffic(dom_name, args.workload, dom_src),
+    }
+    if sampler:
+        res["clocks"] = sampler.summary(wall0, wall1)
+    if not args.profile and not args.no_e2e:
+        n_e2e = max(20, min(K, 300))
+        res["e2e"] = (run_e2e_store(wl, dev, n_e2e, world) if args.workload == "store"
+                      else run_e2e(wl, dev, n_e2e, world))
+    if rank == 0 and world == 1 and not args.profile and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
+    return res
+
+
+def _timed(stream, dev, K, body, flush):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        body()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in ev) / K
+
+
+def run_e2e(wl: DeviceWorkload, dev, K, world):
+    """The same step through the C ABI with host buffers: the step's inputs
+    (q, new K/V rows, slot ids, block tables, context lengths) are copied from
+    pinned host memory and the output back, inside the timed region."""
+    host = {}
+    for name in ("q", "new_k", "new_v", "new_slots", "bt_d", "cl_d"):
+        t = getattr(wl, name)
+        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def body():
+        for name, t in host.items():
+            getattr(wl, name).copy_(t, non_blocking=True)
+        wl.quantize()
+        wl.partials()
+        wl.combine()
+        out_h.copy_(wl.out, non_blocking=True)
+
+    for _ in range(3):
+        body()
+    torch.cuda.synchronize(dev)
+    ms = dist_max(_timed(wl.stream, dev, K, body, flush), world)
+    value = world * (wl.store_bytes() + wl.attn_bytes()) / (ms * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_e2e_store(wl: DeviceWorkload, dev, K, world):
+    w = wl.w
+    Hq, D = w.num_q_heads, w.head_dim
+    host_kv = torch.empty(wl.qkv[:, Hq * D:].shape, dtype=wl.qkv.dtype,
+                          pin_memory=True).copy_(wl.qkv[:, Hq * D:])
+    host_slots = torch.empty(wl.new_slots.shape, dtype=torch.int64,
+                             pin_memory=True).copy_(wl.new_slots)
+    out_h = torch.empty(wl.cache.k_scales.shape, dtype=torch.float32, pin_memory=True)
+    h2d = host_kv.numel() * 2 + host_slots.numel() * 8
+    d2h = out_h.numel() * 4
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def body():
+        wl.qkv[:, Hq * D:].copy_(host_kv, non_blocking=True)
+        wl.new_slots.copy_(host_slots, non_blocking=True)
+        wl.quantize()
+        out_h.copy_(wl.cache.k_scales, non_blocking=True)
+
+    for _ in range(3):
+        body()
+    torch.cuda.synchronize(dev)
+    ms = dist_max(_timed(wl.stream, dev, K, body, flush), world)
+    value = world * wl.store_bytes() / (ms * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on bounded samples (cpu_baseline and the reference arm)
+
+class OracleSampler:
+    """Units of the workload the oracle processes one at a time: a unit is one
+    (request, query row, query head) attention output plus the quantize-scatter
+    of that request's new rows for the head's KV head.  The oracle's cache for a
+    (request, KV head) is built from the same seeded bf16 rows, untimed, the
+    first time a unit needs it."""
+
+    def __init__(self, name: str, token_cap: int | None = None):
+        import oracle
+        self.oracle = oracle
+        self.w = w = workloads.WORKLOADS[name]
+        self.name = name
+        self.token_cap = token_cap
+        if name == "store":
+            return
+        self.lens = workloads.context_lengths(w)
+        self.bt, nblk = workloads.block_tables(self.lens, w.block_size, w.seed)
+        self.S = nblk * w.block_size
+        self.q = workloads.bf16_bits(workloads.queries(w, device="cpu"))
+        self._key = None
+        # (request, KV head)-major order: consecutive units share one oracle cache
+        self.units = [(r, i, h * w.group + g) for r in range(w.num_requests)
+                      for h in range(w.num_kv_heads) for g in range(w.group)
+                      for i in range(w.rows_per_request)]
+        self.pos = 0
+
+    def _head_cache(self, r, h):
+        if self._key != (r, h):
+            w = self.w
+            L, D = int(self.lens[r]), w.head_dim
+            oc = self.oracle.empty_cache(self.S, 1, D)
+            ct = workloads.chunk_tokens(w)
+            dev = "cuda" if torch.cuda.is_available() and L > 8192 else "cpu"
+            ks, vs = [], []
+            for c0 in range(0, L, ct):
+                n = min(ct, L - c0)
+                k, v = workloads.request_kv(w, r, c0, n, device=dev)
+                ks.append(workloads.bf16_bits(k[:, h:h + 1]))
+                vs.append(workloads.bf16_bits(v[:, h:h + 1]))
+            kb, vb = np.concatenate(ks).reshape(-1), np.concatenate(vs).reshape(-1)
+            slots = workloads.token_slots(self.bt, r, L, w.block_size)
+            self.oracle.quantize_scatter(kb, D, vb, D, L, 1, D, slots, oc)
+            R = w.rows_per_request
+            self._new = (kb[(L - R) * D:], vb[(L - R) * D:])
+            self._oc = oc
+            self._key = (r, h)
+        return self._oc
+
+    def next_unit(self):
+        """Prepare the next unit (untimed); returns (callable, algorithmic bytes
+        of the unit: its even share of its request's step bytes)."""
+        w = self.w
+        r, i, hq = self.units[self.pos % len(self.units)]
+        self.pos += 1
+        h = hq // w.group
+        oc = self._head_cache(r, h)
+        L = int(self.lens[r])
+        Lc = L if self.token_cap is None else min(L, self.token_cap)
+        R, D, G = w.rows_per_request, w.head_dim, w.group
+        lens = np.array([Lc], dtype=np.int32)
+        qrow = self.q[r * R:(r + 1) * R, h * G:(h + 1) * G]
+        bt = self.bt[r:r + 1]
+        kb, vb = self._new
+        scratch = self.oracle.empty_cache(R, 1, D)
+        new_slots = np.arange(R, dtype=np.int64)
+        ora = self.oracle
+        unit = np.array([[0, i, hq - h * G]], dtype=np.int32)
+
+        def run():
+            ora.quantize_scatter(kb, D, vb, D, R, 1, D, new_slots, scratch)
+            ora.paged_attention_units(oc, qrow, 1, R, G, bt, lens, w.block_size, w.sm_scale,
+                                      unit)
+
+        H, Hq = w.num_kv_heads, w.num_q_heads
+        req = (Lc * H * 2 * (D + 4) + ((Lc + w.block_size - 1) // w.block_size) * 4 + 4
+               + R * Hq * 2 * D * 2 + R * H * (2 * D * 2 + 2 * D + 2 * 4) + R * 8)
+        return run, req / (R * Hq)
+
+    def store_run(self, rows: int):
+        """Store workload: quantise about `rows` (token, head) rows of the qkv."""
+        w = self.w
+        if not hasattr(self, "_qkv"):
+            qkv, _, _, slots, _ = workloads.store_qkv(w, device="cpu")
+            self._qkv = workloads.bf16_bits(qkv)
+            self._slots = slots.numpy()
+            self._cache = self.oracle.empty_cache(self._qkv.shape[0], w.num_kv_heads,
+                                                  w.head_dim)
+        Hq, H, D = w.num_q_heads, w.num_kv_heads, w.head_dim
+        T = min(max(1, rows // (2 * H)), self._qkv.shape[0])
+        flat = self._qkv.reshape(-1)
+        pitch = self._qkv.shape[1]
+        slots = self._slots[:T]
+        ora, cache = self.oracle, self._cache
+
+        def run():
+            ora.quantize_scatter(flat[Hq * D:], pitch, flat[(Hq + H) * D:], pitch, T, H, D,
+                                 slots, cache)
+
+        return run, T * H * (2 * D * 2 + 2 * D + 8) + T * 8
+
+
+def cpu_baseline(name: str, budget_s: float):
+    """The oracle, as it stands, on one host thread, over a bounded sample."""
+    s = OracleSampler(name)
+    done_bytes, elapsed, units = 0.0, 0.0, 0
+    setup0 = time.perf_counter()
+    while elapsed < budget_s and time.perf_counter() - setup0 < 4 * budget_s:
+        run, nb = s.store_run(2 * 8 * 512) if name == "store" else s.next_unit()
+        t0 = time.perf_counter()
+        run()
+        elapsed += time.perf_counter() - t0
+        done_bytes += nb
+        units += 1
+    what = ("(request, query row, query head) units: attention output over the full context "
+            "plus the unit's share of the new-row store" if name != "store"
+            else "blocks of 512 tokens (8192 rows) of the store")
+    return {"value": round(done_bytes / elapsed / 1e9, 5), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{units} {what}; {elapsed:.1f} s single-thread CPU time "
+                      f"({done_bytes / 1e6:.1f} MB algorithmic)"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle on the host, each step a bounded sample."""
+    if rank != 0:
+        return None
+    K = args.steps if args.steps is not None else 60
+    W = max(3, args.warmup if args.warmup is not None else 3)
+    name = args.workload
+    per_step_s = min(2.0, 150.0 / (K + W))   # W + K steps within a few minutes
+    s = OracleSampler(name)
+    if name != "store":
+        s.token_cap = 1024                     # calibrate cost per cached token
+        run, _ = s.next_unit()
+        t0 = time.perf_counter()
+        run()
+        per_tok = (time.perf_counter() - t0) / 1024
+        s.token_cap = max(16, int(per_step_s / max(per_tok, 1e-9)))
+        s.pos = 0
+    rows_per_step = 16 * 8 * 2
+
+    def one():
+        return s.store_run(rows_per_step) if name == "store" else s.next_unit()
+
+    for _ in range(W):
+        run, _ = one()
+        run()
+    total_t, total_b = 0.0, 0.0
+    for _ in range(K):
+        run, nb = one()
+        t0 = time.perf_counter()
+        run()
+        total_t += time.perf_counter() - t0
+        total_b += nb
+    value = total_b / total_t / 1e9
+    sample = (f"each step one (request, query row, query head) unit, context capped at "
+              f"{s.token_cap} tokens, plus its share of the new-row store"
+              if name != "store" else f"each step {rows_per_step} rows of the store")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(1e3 * total_t / K, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": DESCRIPTIONS[name], "name": name},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, local, world = dist_init()
+    res = run_reference(args, rank, world) if args.impl == "reference" else \
+        run_kvq(args, rank, local, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

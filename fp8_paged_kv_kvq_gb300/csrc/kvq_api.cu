@@ -1,0 +1,268 @@
+// kvq_api.cu -- the C ABI of libkvq (declared in include/kvq.h): host-side
+// argument validation, shape decisions and the kernel launches.  Nothing here
+// allocates, synchronises or reads device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace {
+
+constexpr int32_t kAbiVersion = 1;
+constexpr int32_t kMaxRowsPerKvHead = 128;
+constexpr int32_t kMaxPartitionTokens = 1 << 20;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int32_t log2_exact(int64_t x) {
+  int32_t l = 0;
+  while ((int64_t(1) << l) < x) ++l;
+  return l;
+}
+
+int current_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;
+  }
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 152;
+  }
+  cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+kvq_status check_cache(const kvq_cache *c, bool need_block_size) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->num_slots < 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->head_dim != kvq::kHeadDimAbi) return KVQ_ERR_UNSUPPORTED;
+  if (c->num_slots > 0 &&
+      (c->k_codes == nullptr || c->v_codes == nullptr || c->k_scales == nullptr ||
+       c->v_scales == nullptr))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(c->k_codes, 16) || !aligned(c->v_codes, 16) || !aligned(c->k_scales, 4) ||
+      !aligned(c->v_scales, 4))
+    return KVQ_ERR_MISALIGNED;
+  if (need_block_size) {
+    if (c->block_size <= 0) return KVQ_ERR_INVALID_ARGUMENT;
+    if (!is_pow2(c->block_size)) return KVQ_ERR_UNSUPPORTED;
+  }
+  return KVQ_OK;
+}
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t max_context_len) {
+  const int64_t sms = current_sm_count();
+  const int64_t work = static_cast<int64_t>(num_requests > 0 ? num_requests : 1) *
+                       (num_kv_heads > 0 ? num_kv_heads : 1) *
+                       (max_context_len > 0 ? max_context_len : 1);
+  const int64_t target = work / (sms * 16);
+  int32_t p = 256;
+  while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
+  return p;
+}
+
+// Validates the decode arguments shared by the partials and combine calls and
+// fills the shape.
+kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows_per_request,
+                      int32_t num_q_heads, int32_t max_blocks_per_req,
+                      int32_t max_context_len, int32_t partition_tokens, kvq::AttnShape *s) {
+  kvq_status st = check_cache(cache, true);
+  if (st != KVQ_OK) return st;
+  if (num_requests < 0 || rows_per_request < 1 || num_q_heads < 1 || max_blocks_per_req < 0 ||
+      max_context_len < 0 || partition_tokens < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_q_heads % cache->num_kv_heads != 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (partition_tokens % 64 != 0 || partition_tokens > kMaxPartitionTokens)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  const int32_t G = num_q_heads / cache->num_kv_heads;
+  const int64_t M = static_cast<int64_t>(rows_per_request) * G;
+  if (M > kMaxRowsPerKvHead) return KVQ_ERR_UNSUPPORTED;
+  if (num_requests > 65535) return KVQ_ERR_UNSUPPORTED;
+  s->num_requests = num_requests;
+  s->rows_per_request = rows_per_request;
+  s->num_q_heads = num_q_heads;
+  s->group = G;
+  s->rows = static_cast<int32_t>(M);
+  s->row_groups = static_cast<int32_t>((M + 31) / 32);
+  s->max_blocks_per_req = max_blocks_per_req;
+  s->max_context_len = max_context_len;
+  s->partition_tokens = partition_tokens > 0
+                            ? partition_tokens
+                            : heuristic_partition(num_requests, cache->num_kv_heads,
+                                                  max_context_len);
+  const int64_t np = (static_cast<int64_t>(max_context_len) + s->partition_tokens - 1) /
+                     s->partition_tokens;
+  if (np > 65535) return KVQ_ERR_UNSUPPORTED;
+  s->num_partitions = np > 0 ? static_cast<int32_t>(np) : 1;
+  if (static_cast<int64_t>(cache->num_kv_heads) * s->row_groups > 0x7FFFFFFF)
+    return KVQ_ERR_UNSUPPORTED;
+  s->log2_block = log2_exact(cache->block_size);
+  return KVQ_OK;
+}
+
+size_t workspace_for(const kvq::AttnShape &s) {
+  const int64_t rows_total =
+      static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
+  return kvq::attn_workspace_bytes(rows_total, s.num_partitions);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case KVQ_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int32_t kvq_abi_version(void) { return kAbiVersion; }
+
+size_t kvq_cache_bytes(int64_t num_slots, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_slots < 0 || num_kv_heads < 0 || head_dim < 0) return 0;
+  return 2u * static_cast<size_t>(num_slots) * static_cast<size_t>(num_kv_heads) *
+         (static_cast<size_t>(head_dim) + sizeof(float));
+}
+
+kvq_status kvq_quantize_scatter(const kvq_cache *cache, const void *k, int64_t k_token_stride,
+                                const void *v, int64_t v_token_stride, int64_t num_tokens,
+                                const int64_t *slot_ids, int32_t *err_flags,
+                                kvq_stream_t stream) {
+  kvq_status st = check_cache(cache, false);
+  if (st != KVQ_OK) return st;
+  if (num_tokens < 0 || k_token_stride < 0 || v_token_stride < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;
+  if (k == nullptr || v == nullptr || slot_ids == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k, 16) || !aligned(v, 16) || (k_token_stride % 8) != 0 ||
+      (v_token_stride % 8) != 0 || !aligned(slot_ids, 8) || !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  if ((num_tokens + 7) / 8 > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
+  return from_cuda(kvq::launch_quantize_scatter(*cache, k, k_token_stride, v, v_token_stride,
+                                                num_tokens, slot_ids, err_flags,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t num_kv_heads,
+                                          int32_t block_size, int32_t max_context_len) {
+  (void)block_size;
+  return heuristic_partition(num_requests, num_kv_heads, max_context_len);
+}
+
+size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size,
+                                       int32_t max_context_len, int32_t partition_tokens) {
+  kvq_cache c{};
+  c.num_slots = 0;
+  c.num_kv_heads = num_kv_heads;
+  c.head_dim = head_dim;
+  c.block_size = block_size;
+  kvq::AttnShape s;
+  if (make_shape(&c, num_requests, rows_per_request, num_q_heads, 1, max_context_len,
+                 partition_tokens, &s) != KVQ_OK)
+    return 0;
+  return workspace_for(s);
+}
+
+kvq_status kvq_paged_decode_partials(const kvq_cache *cache, const void *q, int32_t num_requests,
+                                     int32_t rows_per_request, int32_t num_q_heads,
+                                     const int32_t *block_tables, int32_t max_blocks_per_req,
+                                     const int32_t *context_lens, int32_t max_context_len,
+                                     float sm_scale, int32_t partition_tokens, void *out,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *err_flags, kvq_stream_t stream) {
+  kvq::AttnShape s;
+  kvq_status st = make_shape(cache, num_requests, rows_per_request, num_q_heads,
+                             max_blocks_per_req, max_context_len, partition_tokens, &s);
+  if (st != KVQ_OK) return st;
+  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_requests == 0) return KVQ_OK;
+  if (q == nullptr || out == nullptr || block_tables == nullptr || context_lens == nullptr)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+      !aligned(context_lens, 4) || !aligned(workspace, 16) || !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  const size_t need = workspace_for(s);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(kvq::launch_attn_partials(*cache, s, q, block_tables, context_lens, sm_scale,
+                                             out, workspace, err_flags,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests,
+                                    int32_t rows_per_request, int32_t num_q_heads,
+                                    int32_t max_blocks_per_req, const int32_t *context_lens,
+                                    int32_t max_context_len, int32_t partition_tokens,
+                                    void *out, void *workspace, size_t workspace_bytes,
+                                    kvq_stream_t stream) {
+  kvq::AttnShape s;
+  kvq_status st = make_shape(cache, num_requests, rows_per_request, num_q_heads,
+                             max_blocks_per_req, max_context_len, partition_tokens, &s);
+  if (st != KVQ_OK) return st;
+  if (num_requests == 0 || s.num_partitions <= 1) return KVQ_OK;
+  if (out == nullptr || context_lens == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(out, 16) || !aligned(context_lens, 4) || !aligned(workspace, 16))
+    return KVQ_ERR_MISALIGNED;
+  const size_t need = workspace_for(s);
+  if (workspace == nullptr || workspace_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(kvq::launch_attn_combine(s, context_lens, out, workspace,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q, int32_t num_requests,
+                            int32_t rows_per_request, int32_t num_q_heads,
+                            const int32_t *block_tables, int32_t max_blocks_per_req,
+                            const int32_t *context_lens, int32_t max_context_len,
+                            float sm_scale, int32_t partition_tokens, void *out,
+                            void *workspace, size_t workspace_bytes, int32_t *err_flags,
+                            kvq_stream_t stream) {
+  kvq_status st = kvq_paged_decode_partials(
+      cache, q, num_requests, rows_per_request, num_q_heads, block_tables, max_blocks_per_req,
+      context_lens, max_context_len, sm_scale, partition_tokens, out, workspace,
+      workspace_bytes, err_flags, stream);
+  if (st != KVQ_OK) return st;
+  return kvq_paged_decode_combine(cache, num_requests, rows_per_request, num_q_heads,
+                                  max_blocks_per_req, context_lens, max_context_len,
+                                  partition_tokens, out, workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_dequant_rows(const kvq_cache *cache, const int64_t *slot_ids, int64_t n,
+                            int32_t out_dtype, void *out_k, void *out_v, int32_t *err_flags,
+                            kvq_stream_t stream) {
+  kvq_status st = check_cache(cache, false);
+  if (st != KVQ_OK) return st;
+  if (n < 0 || (out_dtype != 0 && out_dtype != 1)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (n == 0 || (out_k == nullptr && out_v == nullptr)) return KVQ_OK;
+  if (slot_ids == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(slot_ids, 8) || !aligned(out_k, 16) || !aligned(out_v, 16) ||
+      !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  if ((n + 7) / 8 > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
+  return from_cuda(kvq::launch_dequant_rows(*cache, slot_ids, n, out_dtype, out_k, out_v,
+                                            err_flags, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,664 @@
+// kvq_attention.cu -- paged GQA decode / multi-row verify attention over the
+// FP8 E4M3 cache: split-K partials on the tensor cores, then a combine pass.
+//
+// ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for KV
+// offload", PR description:
+//  * K/V bullet: the attention reads E4M3 tiles, multiplies the key scale into
+//    its score column and folds the value scale into the probability before PV;
+//  * stacked decode scorer: the query rows of one verify (4 rows) and the heads
+//    that share the keys are stacked into one M operand, so a request's keys
+//    are read once per verify and meet every row in a single dot.
+// sgl-project/sglang-jax #1776 "feat(dsa): implement fp8 KV cache (e4m3) with
+// a bf16 indexer cache", Modifications: the cached block is upcast to the query
+// dtype before the score dot, and P is never rounded to fp8.
+//
+// Work decomposition.  One CTA = (KV head h, row group, context partition p,
+// request r).  The CTA's M rows are the (query row i, head g) pairs of request r
+// that read KV head h, stacked as m = i*G + g (at most 32 per row group: one or
+// two m16 tiles).  Four warps stream the partition's tokens through a 3-stage
+// cp.async pipeline of 64-token stages (16 tokens per warp per stage); each
+// token's 128-byte code rows are found through the block table.  Per 16-token
+// chunk a warp:
+//   1. decodes the K codes exactly to bf16 in registers (bit placement + one
+//      exact bf16 multiply) straight into mma B fragments, and runs S = Q K^T
+//      with m16n8k16 bf16 MMAs (fp32 accumulate);
+//   2. multiplies each score column by its key scale and sm_scale*log2(e),
+//      masks causally (row i sees tokens j < L - R + 1 + i), and updates a
+//      running max per row, rescaling the accumulators only when the max grows
+//      by more than 2^8 (so p <= 256);
+//   3. folds the value scale into p (P' = p * v_scale, rounded once to bf16),
+//      accumulates the denominator with the unscaled p, and runs O += P' V with
+//      V decoded the same way.
+// The warps' (max, denominator, O) are merged through shared memory; a request
+// with a single partition writes its bf16 output directly, otherwise the
+// partial is stored and the combine kernel merges the partitions (log-sum-exp
+// weights).
+//
+// The contraction index of Q K^T is permuted so that each lane's B fragment
+// comes from 4 consecutive code bytes of one token: in k-step s, the lane with
+// c = lane % 4 feeds dims 32c + 4s + {0, 2 | 1, 3} as k = {2c, 2c+1 | 2c+8,
+// 2c+9}; Q's A fragments use the same map.  For P V the output columns are
+// permuted instead: n-tile i, column u stands for dim 16u + i, so each lane
+// reads 16 consecutive code bytes per token.  Shared-memory code rows are
+// stored with their 16-byte chunks XOR-swizzled by (token & 7), which keeps
+// both read patterns free of bank conflicts.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStageTok = 64;
+constexpr int kStages = 3;
+constexpr int kGroupRows = 32;
+constexpr float kLazyRescale = 8.0f;   // rescale only when the max grows by > 2^8
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct StageBuf {
+  uint8_t k[kStageTok * kHeadDim];
+  uint8_t v[kStageTok * kHeadDim];
+  float ks[kStageTok];
+  float vs[kStageTok];
+};
+
+struct AttnParams {
+  const uint8_t *k_codes;
+  const uint8_t *v_codes;
+  const float *k_scales;
+  const float *v_scales;
+  int64_t num_blocks;
+  int32_t H;
+  int32_t log2_bs;
+  const uint16_t *q;
+  uint16_t *out;
+  const int32_t *block_tables;
+  int32_t max_blocks;
+  const int32_t *context_lens;
+  int32_t ctx_limit;        // min(max_context_len, max_blocks << log2_bs)
+  int32_t R, Hq, G, M;
+  int32_t row_groups;
+  float qk_scale;           // sm_scale * log2(e)
+  int32_t part_tokens;
+  int32_t n_parts_max;
+  float *o_part;
+  float2 *ml_part;
+  int32_t *err_flags;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+__device__ __forceinline__ int clamp_context(const AttnParams &p, int r, bool report) {
+  int L = p.context_lens[r];
+  if (L < 0 || L > p.ctx_limit) {
+    if (report && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
+    L = L < 0 ? 0 : p.ctx_limit;
+  }
+  return L;
+}
+
+// Issue the cp.async copies of one 64-token stage (tokens [tok0, tok0+64) of
+// the request; those at or past t_end are zero-filled).
+__device__ __forceinline__ void issue_stage(const AttnParams &p, StageBuf &sb, int r, int h,
+                                            int tok0, int t_end, int tid) {
+  const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks;
+  const int bs_mask = (1 << p.log2_bs) - 1;
+  // code rows: 128 rows (64 K then 64 V) x 8 chunks of 16 bytes; thread tid
+  // copies chunk tid%8 of rows tid/8 + 16*it, so 8 consecutive lanes move one
+  // full 128-byte row.
+  const int chunk = tid & 7;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int row = (tid >> 3) + 16 * it;
+    const int tl = row & (kStageTok - 1);
+    const bool is_v = row >= kStageTok;
+    const int j = tok0 + tl;
+    const uint8_t *base = is_v ? p.v_codes : p.k_codes;
+    const uint8_t *src = base;
+    uint32_t nbytes = 0;
+    if (j < t_end) {
+      const int64_t blk = bt[j >> p.log2_bs];
+      if (blk >= 0 && blk < p.num_blocks) {
+        const int64_t slot = (blk << p.log2_bs) + (j & bs_mask);
+        src = base + (slot * p.H + h) * kHeadDim + chunk * 16;
+        nbytes = 16;
+      } else if (p.err_flags) {
+        atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
+      }
+    }
+    uint8_t *dst = (is_v ? sb.v : sb.k) + tl * kHeadDim + ((chunk ^ (tl & 7)) << 4);
+    cp_async_16(dst, src, nbytes);
+  }
+  // scales: thread tid copies token tid%64's K (tid < 64) or V scale
+  {
+    const int tl = tid & (kStageTok - 1);
+    const bool is_v = tid >= kStageTok;
+    const int j = tok0 + tl;
+    const float *base = is_v ? p.v_scales : p.k_scales;
+    const float *src = base;
+    uint32_t nbytes = 0;
+    if (j < t_end) {
+      const int64_t blk = bt[j >> p.log2_bs];
+      if (blk >= 0 && blk < p.num_blocks) {
+        const int64_t slot = (blk << p.log2_bs) + (j & bs_mask);
+        src = base + slot * p.H + h;
+        nbytes = 4;
+      }
+    }
+    cp_async_4((is_v ? sb.vs : sb.ks) + tl, src, nbytes);
+  }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, (MT == 1) ? 3 : 2)
+attn_partials_kernel(const AttnParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  StageBuf *stages = reinterpret_cast<StageBuf *>(smem);
+  uint4 *qfrag = reinterpret_cast<uint4 *>(smem + kStages * sizeof(StageBuf));
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int g4 = lane >> 2;
+  const int c4 = lane & 3;
+  const int h = blockIdx.x / p.row_groups;
+  const int row_base = (blockIdx.x - h * p.row_groups) * kGroupRows;
+  const int part = blockIdx.y;
+  const int r = blockIdx.z;
+
+  const int L = clamp_context(p, r, part == 0 && tid == 0 && blockIdx.x == 0);
+  const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
+  if (part >= (n_parts > 0 ? n_parts : 1)) return;
+  const int t0 = part * p.part_tokens;
+  const int t_end = min(L, t0 + p.part_tokens);
+  const int n_stages = (t_end > t0) ? (t_end - t0 + kStageTok - 1) / kStageTok : 0;
+
+  // Start the pipeline before anything else.
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < n_stages) issue_stage(p, stages[s], r, h, t0 + s * kStageTok, t_end, tid);
+    cp_async_commit();
+  }
+
+  // Q fragments, in the permuted contraction order, stored per lane.
+  for (int idx = warp; idx < MT * 8; idx += kWarps) {
+    const int mt = idx >> 3, s = idx & 7;
+    uint2 qa = make_uint2(0u, 0u), qb = make_uint2(0u, 0u);
+    const int ma = row_base + mt * 16 + g4, mb = ma + 8;
+    const int d0 = 32 * c4 + 4 * s;
+    if (ma < p.M) {
+      const int i = ma / p.G, gq = ma - i * p.G;
+      const int64_t qrow = (static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq;
+      qa = *reinterpret_cast<const uint2 *>(p.q + qrow * kHeadDim + d0);
+    }
+    if (mb < p.M) {
+      const int i = mb / p.G, gq = mb - i * p.G;
+      const int64_t qrow = (static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq;
+      qb = *reinterpret_cast<const uint2 *>(p.q + qrow * kHeadDim + d0);
+    }
+    uint4 f;
+    f.x = prmt(qa.x, qa.y, 0x5410u);   // (dim d0,   dim d0+2) -> k = 2c, 2c+1
+    f.y = prmt(qb.x, qb.y, 0x5410u);
+    f.z = prmt(qa.x, qa.y, 0x7632u);   // (dim d0+1, dim d0+3) -> k = 2c+8, 2c+9
+    f.w = prmt(qb.x, qb.y, 0x7632u);
+    qfrag[idx * 32 + lane] = f;
+  }
+
+  // Per-thread rows: (mt, half) -> M row row_base + mt*16 + g4 + 8*half.
+  int vis[MT][2];
+  float m_run[MT][2], l_run[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int m = row_base + mt * 16 + g4 + 8 * hf;
+      vis[mt][hf] = (m < p.M) ? (L - p.R + 1 + m / p.G) : 0;
+      m_run[mt][hf] = -INFINITY;
+      l_run[mt][hf] = 0.0f;
+    }
+  float o[MT][16][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][i][e] = 0.0f;
+
+  for (int st = 0; st < n_stages; ++st) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    {
+      const int nxt = st + kStages - 1;
+      if (nxt < n_stages)
+        issue_stage(p, stages[nxt % kStages], r, h, t0 + nxt * kStageTok, t_end, tid);
+      cp_async_commit();
+    }
+    const StageBuf &sb = stages[st % kStages];
+    const int tb = warp * 16;                         // this warp's 16 tokens
+    const int jbase = t0 + st * kStageTok + tb;       // request position of token tb
+
+    // ---- S = Q K^T over this warp's 16 tokens (two n-tiles of 8)
+    float sacc[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
+    uint32_t kw[2][8];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int tl = tb + nt * 8 + g4;
+      const uint8_t *row = sb.k + tl * kHeadDim;
+      const uint4 k0 = lds128(row + (((2 * c4) ^ (tl & 7)) << 4));
+      const uint4 k1 = lds128(row + (((2 * c4 + 1) ^ (tl & 7)) << 4));
+      kw[nt][0] = k0.x; kw[nt][1] = k0.y; kw[nt][2] = k0.z; kw[nt][3] = k0.w;
+      kw[nt][4] = k1.x; kw[nt][5] = k1.y; kw[nt][6] = k1.z; kw[nt][7] = k1.w;
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t a[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint4 f = qfrag[(mt * 8 + s) * 32 + lane];
+        a[mt][0] = f.x; a[mt][1] = f.y; a[mt][2] = f.z; a[mt][3] = f.w;
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t b0 = e4m3x2_b02_to_bf16x2(kw[nt][s]);
+        const uint32_t b1 = e4m3x2_b13_to_bf16x2(kw[nt][s]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(sacc[mt][nt], a[mt], b0, b1);
+      }
+    }
+
+    // ---- scale, mask, online softmax (lazy rescale)
+    float ksc[2][2], vsc[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float2 kk = *reinterpret_cast<const float2 *>(sb.ks + tb + nt * 8 + 2 * c4);
+      const float2 vv = *reinterpret_cast<const float2 *>(sb.vs + tb + nt * 8 + 2 * c4);
+      ksc[nt][0] = kk.x * p.qk_scale;
+      ksc[nt][1] = kk.y * p.qk_scale;
+      vsc[nt][0] = vv.x;
+      vsc[nt][1] = vv.y;
+    }
+    float fac[MT][2];
+    bool grow = false;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = jbase + nt * 8 + 2 * c4 + e;
+            float x = sacc[mt][nt][2 * hf + e] * ksc[nt][e];
+            x = (j < vis[mt][hf]) ? x : -INFINITY;
+            sacc[mt][nt][2 * hf + e] = x;
+            mx = fmaxf(mx, x);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float mold = m_run[mt][hf];
+        if (mx > mold + kLazyRescale) {
+          fac[mt][hf] = ex2(mold - mx);
+          m_run[mt][hf] = mx;
+          grow = true;
+        } else {
+          fac[mt][hf] = 1.0f;
+        }
+      }
+    if (__any_sync(0xFFFFFFFFu, grow)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          l_run[mt][hf] *= fac[mt][hf];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            o[mt][i][2 * hf] *= fac[mt][hf];
+            o[mt][i][2 * hf + 1] *= fac[mt][hf];
+          }
+        }
+    }
+    uint32_t pa[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float pv[2][4];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float msub = (m_run[mt][hf] == -INFINITY) ? 0.0f : m_run[mt][hf];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float pr = ex2(sacc[mt][nt][2 * hf + e] - msub);
+            l_run[mt][hf] += pr;
+            pv[nt][2 * hf + e] = pr * vsc[nt][e];
+          }
+      }
+      pa[mt][0] = pack_bf16x2(pv[0][0], pv[0][1]);   // row g4,   tokens 2c, 2c+1
+      pa[mt][1] = pack_bf16x2(pv[0][2], pv[0][3]);   // row g4+8, tokens 2c, 2c+1
+      pa[mt][2] = pack_bf16x2(pv[1][0], pv[1][1]);   // row g4,   tokens 2c+8, 2c+9
+      pa[mt][3] = pack_bf16x2(pv[1][2], pv[1][3]);   // row g4+8, tokens 2c+8, 2c+9
+    }
+
+    // ---- O += P' V.  Lane reads dims [16*g4, 16*g4+16) of tokens 2c, 2c+1, 2c+8, 2c+9.
+    uint4 va, vb, vc, vd;
+    {
+      const int t_a = tb + 2 * c4, t_b = t_a + 1, t_c = t_a + 8, t_d = t_a + 9;
+      va = lds128(sb.v + t_a * kHeadDim + ((g4 ^ (t_a & 7)) << 4));
+      vb = lds128(sb.v + t_b * kHeadDim + ((g4 ^ (t_b & 7)) << 4));
+      vc = lds128(sb.v + t_c * kHeadDim + ((g4 ^ (t_c & 7)) << 4));
+      vd = lds128(sb.v + t_d * kHeadDim + ((g4 ^ (t_d & 7)) << 4));
+    }
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w};
+    const uint32_t wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      const uint32_t ab01 = prmt(wa[wi], wb[wi], 0x5410u);   // [a0 a1 b0 b1]
+      const uint32_t ab23 = prmt(wa[wi], wb[wi], 0x7632u);   // [a2 a3 b2 b3]
+      const uint32_t cd01 = prmt(wc[wi], wd[wi], 0x5410u);
+      const uint32_t cd23 = prmt(wc[wi], wd[wi], 0x7632u);
+      uint32_t b0[4], b1[4];
+      b0[0] = e4m3x2_b02_to_bf16x2(ab01); b1[0] = e4m3x2_b02_to_bf16x2(cd01);
+      b0[1] = e4m3x2_b13_to_bf16x2(ab01); b1[1] = e4m3x2_b13_to_bf16x2(cd01);
+      b0[2] = e4m3x2_b02_to_bf16x2(ab23); b1[2] = e4m3x2_b02_to_bf16x2(cd23);
+      b0[3] = e4m3x2_b13_to_bf16x2(ab23); b1[3] = e4m3x2_b13_to_bf16x2(cd23);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(o[mt][4 * wi + e], pa[mt], b0[e], b1[e]);
+    }
+  }
+
+  // ---- merge the four warps' partial results.  Warps 1..3 park their
+  // (rescaled) accumulators in shared memory in fragment order (conflict-free
+  // 16-byte stores), warp 0 adds them to its registers and writes the rows.
+  cp_async_wait<0>();
+  __syncthreads();
+  constexpr int kRows = MT * 16;
+  float *m_w = reinterpret_cast<float *>(smem);                   // [kWarps][kRows]
+  float *l_w = m_w + kWarps * kRows;                              // [kWarps][kRows]
+  float4 *parked = reinterpret_cast<float4 *>(l_w + kWarps * kRows);  // [3][MT][16][32]
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      float l = l_run[mt][hf];
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
+      l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
+      l_run[mt][hf] = l;
+      if (c4 == 0) {
+        const int rl = mt * 16 + g4 + 8 * hf;
+        m_w[warp * kRows + rl] = m_run[mt][hf];
+        l_w[warp * kRows + rl] = l;
+      }
+    }
+  __syncthreads();
+  float mrow[MT][2], lrow[MT][2], frow[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int rl = mt * 16 + g4 + 8 * hf;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, m_w[w * kRows + rl]);
+      float lt = 0.0f;
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) lt += l_w[w * kRows + rl] * ex2(m_w[w * kRows + rl] - mx);
+      }
+      mrow[mt][hf] = mx;
+      lrow[mt][hf] = lt;
+      frow[mt][hf] = (mx == -INFINITY) ? 0.0f : ex2(m_run[mt][hf] - mx);
+    }
+  if (warp > 0) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        parked[(((warp - 1) * MT + mt) * 16 + i) * 32 + lane] =
+            make_float4(o[mt][i][0] * frow[mt][0], o[mt][i][1] * frow[mt][0],
+                        o[mt][i][2] * frow[mt][1], o[mt][i][3] * frow[mt][1]);
+  }
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float4 acc = make_float4(o[mt][i][0] * frow[mt][0], o[mt][i][1] * frow[mt][0],
+                               o[mt][i][2] * frow[mt][1], o[mt][i][3] * frow[mt][1]);
+#pragma unroll
+      for (int w = 0; w < kWarps - 1; ++w) {
+        const float4 x = parked[((w * MT + mt) * 16 + i) * 32 + lane];
+        acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+      }
+      o[mt][i][0] = acc.x; o[mt][i][1] = acc.y; o[mt][i][2] = acc.z; o[mt][i][3] = acc.w;
+    }
+
+  // ---- write.  Lane (g4, c4) holds, for row g4 (+8), dims 32*c4 + i (element
+  // 0/2 of n-tile i) and 32*c4 + 16 + i (element 1/3): 32 consecutive dims.
+  const bool direct = n_parts <= 1;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int m = row_base + mt * 16 + g4 + 8 * hf;
+      if (m >= p.M) continue;
+      const int i = m / p.G, gq = m - i * p.G;
+      const int64_t orow = (static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq;
+      const int d0 = 32 * c4;
+      if (direct) {
+        const float inv = (lrow[mt][hf] > 0.0f) ? 1.0f / lrow[mt][hf] : 0.0f;
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          pk[j] = pack_bf16x2(o[mt][2 * j][2 * hf] * inv, o[mt][2 * j + 1][2 * hf] * inv);
+          pk[8 + j] = pack_bf16x2(o[mt][2 * j][2 * hf + 1] * inv, o[mt][2 * j + 1][2 * hf + 1] * inv);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + d0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      } else {
+        const int64_t slot = orow * p.n_parts_max + part;
+        float4 *dst = reinterpret_cast<float4 *>(p.o_part + slot * kHeadDim + d0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dst[j] = make_float4(o[mt][4 * j][2 * hf], o[mt][4 * j + 1][2 * hf],
+                               o[mt][4 * j + 2][2 * hf], o[mt][4 * j + 3][2 * hf]);
+          dst[4 + j] = make_float4(o[mt][4 * j][2 * hf + 1], o[mt][4 * j + 1][2 * hf + 1],
+                                   o[mt][4 * j + 2][2 * hf + 1], o[mt][4 * j + 3][2 * hf + 1]);
+        }
+        if (c4 == 0) p.ml_part[slot] = make_float2(mrow[mt][hf], lrow[mt][hf]);
+      }
+    }
+}
+
+// ---------------------------------------------------------------------------
+struct CombineParams {
+  const int32_t *context_lens;
+  int32_t ctx_limit;
+  int32_t R, Hq;
+  int64_t rows_total;
+  int32_t part_tokens;
+  int32_t n_parts_max;
+  const float *o_part;
+  const float2 *ml_part;
+  uint16_t *out;
+};
+
+constexpr int kCombineWarps = 4;
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
+attn_combine_kernel(const CombineParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  if (row >= p.rows_total) return;
+  const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
+  int L = p.context_lens[r];
+  L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
+  const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
+  if (n_parts <= 1) return;                       // written by the partials kernel
+  const float2 *ml = p.ml_part + row * p.n_parts_max;
+  float mx = -INFINITY;
+  for (int q = lane; q < n_parts; q += 32) mx = fmaxf(mx, ml[q].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.0f;
+  if (mx != -INFINITY) {
+    const float *op = p.o_part + row * p.n_parts_max * kHeadDim + 4 * lane;
+#pragma unroll 4
+    for (int q = 0; q < n_parts; ++q) {
+      const float2 v = ml[q];
+      const float w = ex2(v.x - mx);
+      const float4 o = *reinterpret_cast<const float4 *>(op + static_cast<int64_t>(q) * kHeadDim);
+      lsum += w * v.y;
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+  }
+  const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
+}
+
+template <int MT>
+size_t partials_smem_bytes() {
+  return kStages * sizeof(StageBuf) + MT * 8 * 32 * sizeof(uint4);
+}
+
+template <int MT>
+cudaError_t launch_partials_mt(const AttnParams &p, dim3 grid, cudaStream_t stream) {
+  const size_t smem = partials_smem_bytes<MT>();
+  static_assert(sizeof(StageBuf) * kStages >=
+                    2 * kWarps * MT * 16 * sizeof(float) +
+                        (kWarps - 1) * MT * 16 * 32 * sizeof(float4),
+                "epilogue buffers must fit in the stage buffers");
+  // the shared-memory opt-in is a per-device function attribute: set it once
+  // per device (a host-side call, no stream work)
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(attn_partials_kernel<MT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  attn_partials_kernel<MT><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+void carve_workspace(void *ws, int64_t rows_total, int32_t n_parts, float **o_part,
+                     float2 **ml_part) {
+  const size_t o = static_cast<size_t>(rows_total) * n_parts * kHeadDim * sizeof(float);
+  *o_part = static_cast<float *>(ws);
+  *ml_part = reinterpret_cast<float2 *>(static_cast<char *>(ws) + ((o + 255) / 256) * 256);
+}
+
+int32_t context_cap(const AttnShape &s) {
+  const int64_t cap = static_cast<int64_t>(s.max_blocks_per_req) << s.log2_block;
+  return static_cast<int32_t>(cap < s.max_context_len ? cap : s.max_context_len);
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int64_t rows_total, int32_t num_partitions) {
+  if (num_partitions <= 1) return 0;
+  const size_t o = static_cast<size_t>(rows_total) * num_partitions * kHeadDim * sizeof(float);
+  const size_t ml = static_cast<size_t>(rows_total) * num_partitions * 2 * sizeof(float);
+  const size_t total = ((o + 255) / 256) * 256 + ml;
+  return ((total + 255) / 256) * 256;
+}
+
+cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const void *q,
+                                 const int32_t *block_tables, const int32_t *context_lens,
+                                 float sm_scale, void *out, void *workspace,
+                                 int32_t *err_flags, cudaStream_t stream) {
+  AttnParams p;
+  p.k_codes = c.k_codes;
+  p.v_codes = c.v_codes;
+  p.k_scales = c.k_scales;
+  p.v_scales = c.v_scales;
+  p.num_blocks = c.num_slots >> s.log2_block;
+  p.H = c.num_kv_heads;
+  p.log2_bs = s.log2_block;
+  p.q = static_cast<const uint16_t *>(q);
+  p.out = static_cast<uint16_t *>(out);
+  p.block_tables = block_tables;
+  p.max_blocks = s.max_blocks_per_req;
+  p.context_lens = context_lens;
+  p.ctx_limit = context_cap(s);
+  p.R = s.rows_per_request;
+  p.Hq = s.num_q_heads;
+  p.G = s.group;
+  p.M = s.rows;
+  p.row_groups = s.row_groups;
+  p.qk_scale = sm_scale * kLog2e;
+  p.part_tokens = s.partition_tokens;
+  p.n_parts_max = s.num_partitions;
+  p.err_flags = err_flags;
+  const int64_t rows_total =
+      static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
+  p.o_part = nullptr;
+  p.ml_part = nullptr;
+  if (s.num_partitions > 1)
+    carve_workspace(workspace, rows_total, s.num_partitions, &p.o_part, &p.ml_part);
+  dim3 grid(c.num_kv_heads * s.row_groups, s.num_partitions, s.num_requests);
+  if (s.rows <= 16) return launch_partials_mt<1>(p, grid, stream);
+  return launch_partials_mt<2>(p, grid, stream);
+}
+
+cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,
+                                void *workspace, cudaStream_t stream) {
+  if (s.num_partitions <= 1) return cudaSuccess;
+  CombineParams p;
+  p.context_lens = context_lens;
+  p.ctx_limit = context_cap(s);
+  p.R = s.rows_per_request;
+  p.Hq = s.num_q_heads;
+  p.rows_total = static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
+  p.part_tokens = s.partition_tokens;
+  p.n_parts_max = s.num_partitions;
+  float *o_part;
+  float2 *ml_part;
+  carve_workspace(workspace, p.rows_total, s.num_partitions, &o_part, &ml_part);
+  p.o_part = o_part;
+  p.ml_part = ml_part;
+  p.out = static_cast<uint16_t *>(out);
+  const int64_t blocks = (p.rows_total + kCombineWarps - 1) / kCombineWarps;
+  attn_combine_kernel<<<static_cast<unsigned>(blocks), kCombineWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,137 @@
+// kvq_device.cuh -- device-side building blocks shared by the libkvq kernels:
+// the software E4M3 codec, packed bf16 helpers, cp.async and mma.sync wrappers.
+//
+// The E4M3 ("fn") format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+// bits; E = 0 is subnormal (M * 2^-9); S.1111.111 is NaN; the largest finite
+// magnitude is 448.  FreeToken PR #354 "feat(kvcache): store the KV cache as
+// fp8 e4m3 codes", PR description: codes live in a plain uint8 buffer and are
+// encoded / decoded in software with bit operations, never through an fp8
+// type, so every card holds the same bytes.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+
+// ---------------------------------------------------------------------------
+// Encode.  q = fl32(x / s) (IEEE division, round-to-nearest-even), then the
+// nearest e4m3 magnitude, ties to the even mantissa, |q| >= 448 saturating to
+// 448.  The sign is taken from x, which equals the sign of q for s > 0 and
+// keeps the sign of zero.  Works on the binary32 bit pattern:
+//  * |q| >= 2^-6 (e4m3 normal range): drop the 20 low mantissa bits with
+//    round-half-even; the rounded exponent/mantissa field, rebased from bias
+//    127 to bias 7 (subtract 120 << 3), is the code, carries included;
+//  * |q| < 2^-6 (subnormal range): adding 2^14 rounds |q| to a multiple of
+//    2^-9 (the ulp of 2^14) with the hardware's nearest-even addition, and the
+//    bit-pattern difference to 2^14 is the subnormal mantissa 0..8 (8 lands
+//    exactly on the smallest normal code).
+__device__ __forceinline__ uint32_t e4m3_encode_div(float x, float s) {
+  const float q = __fdiv_rn(x, s);
+  const uint32_t a = __float_as_uint(q) & 0x7FFFFFFFu;
+  const uint32_t sign = (__float_as_uint(x) >> 24) & 0x80u;
+  uint32_t mag;
+  if (a >= 0x43E00000u) {                       // >= 448
+    mag = 0x7Eu;
+  } else if (a >= 0x3C800000u) {                // >= 2^-6
+    mag = ((a + 0x7FFFFu + ((a >> 20) & 1u)) >> 20) - 0x3C0u;
+  } else {
+    mag = __float_as_uint(__fadd_rn(__uint_as_float(a), 16384.0f)) - 0x46800000u;
+  }
+  return mag | sign;
+}
+
+// ---------------------------------------------------------------------------
+// Decode to bf16, exactly.  Placing the 7 magnitude bits of a code at bf16 bits
+// 10..4 (exponent low bits + top mantissa bits) and its sign at bit 15 gives a
+// bf16 whose value is e4m3(c) * 2^-120 exactly -- subnormal codes land on bf16
+// subnormals with the same mantissa -- and one bf16 multiply by 2^120 (exact:
+// a power of two, result in the normal range) restores e4m3(c).
+//
+// Pair helpers take two codes held in the same byte of the two 16-bit halves of
+// a word and return the bf16x2 of their values (low half from the low code).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+constexpr uint32_t kBf16x2Pow2_120 = 0x7B807B80u;   // bf16 2^120 in both halves
+
+// codes in bytes 0 and 2 of w (bytes 1 and 3 ignored)
+__device__ __forceinline__ uint32_t e4m3x2_b02_to_bf16x2(uint32_t w) {
+  const uint32_t mag = (w << 4) & 0x07F007F0u;
+  const uint32_t sgn = (w << 8) & 0x80008000u;
+  return bf16x2_mul(mag | sgn, kBf16x2Pow2_120);
+}
+
+// codes in bytes 1 and 3 of w (bytes 0 and 2 ignored)
+__device__ __forceinline__ uint32_t e4m3x2_b13_to_bf16x2(uint32_t w) {
+  const uint32_t mag = (w >> 4) & 0x07F007F0u;
+  const uint32_t sgn = w & 0x80008000u;
+  return bf16x2_mul(mag | sgn, kBf16x2Pow2_120);
+}
+
+// Decode one code to fp32 exactly: bits at binary32 positions give
+// e4m3(c) * 2^-120 (subnormal codes become binary32 subnormals), times 2^120.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t bits = ((c & 0x7Fu) << 20) | ((c & 0x80u) << 24);
+  return __fmul_rn(__uint_as_float(bits), 0x1p120f);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// Asynchronous global -> shared copies (Ampere-style cp.async, available on
+// sm_103a).  src_bytes = 0 zero-fills the destination without reading.
+__device__ __forceinline__ void cp_async_16(void *smem, const void *gmem, uint32_t src_bytes) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+               :: "r"(s), "l"(gmem), "r"(src_bytes));
+}
+
+__device__ __forceinline__ void cp_async_4(void *smem, const void *gmem, uint32_t src_bytes) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n"
+               :: "r"(s), "l"(gmem), "r"(src_bytes));
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" :: "n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// D = A * B + D on the tensor cores, 16x8x16, bf16 operands, fp32 accumulate.
+// Fragment ownership (lane = 4*g + c):
+//   A (16x16, row-major): a0 = A[g][2c..2c+1], a1 = A[g+8][2c..2c+1],
+//                         a2 = A[g][2c+8..2c+9], a3 = A[g+8][2c+8..2c+9]
+//   B (16x8, col-major):  b0 = B[2c..2c+1][g],  b1 = B[2c+8..2c+9][g]
+//   C (16x8):             c0,c1 = C[g][2c..2c+1], c2,c3 = C[g+8][2c..2c+1]
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+}  // namespace kvq

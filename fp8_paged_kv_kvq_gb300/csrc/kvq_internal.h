@@ -1,0 +1,52 @@
+// kvq_internal.h -- launchers shared between the C-ABI layer (kvq_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// The only head_dim the kernels implement; the ABI refuses any other.
+constexpr int32_t kHeadDimAbi = 128;
+
+// Shape of one paged attention call after host-side validation.
+struct AttnShape {
+  int32_t num_requests;
+  int32_t rows_per_request;   // R
+  int32_t num_q_heads;        // Hq
+  int32_t group;              // G = Hq / H
+  int32_t rows;               // M = R * G
+  int32_t row_groups;         // ceil(M / 32)
+  int32_t max_blocks_per_req;
+  int32_t max_context_len;
+  int32_t partition_tokens;   // P, multiple of 64
+  int32_t num_partitions;     // ceil(max_context_len / P), >= 1
+  int32_t log2_block;
+};
+
+// Workspace carve-up: partial outputs [rows_total][num_partitions][128] fp32,
+// then (max, denominator) pairs [rows_total][num_partitions][2] fp32.
+size_t attn_workspace_bytes(int64_t rows_total, int32_t num_partitions);
+
+cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k_stride,
+                                    const void *v, int64_t v_stride, int64_t num_tokens,
+                                    const int64_t *slot_ids, int32_t *err_flags,
+                                    cudaStream_t stream);
+
+cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int64_t n,
+                                int32_t out_dtype, void *out_k, void *out_v,
+                                int32_t *err_flags, cudaStream_t stream);
+
+cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const void *q,
+                                 const int32_t *block_tables, const int32_t *context_lens,
+                                 float sm_scale, void *out, void *workspace,
+                                 int32_t *err_flags, cudaStream_t stream);
+
+cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,
+                                void *workspace, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,223 @@
+// kvq_quantize.cu -- fused quantize + scatter of bf16 K/V rows into the FP8
+// E4M3 paged cache, and the row dequantiser.
+//
+// FreeToken PR #354 "feat(kvcache): store the KV cache as fp8 e4m3 codes", PR
+// description: one (token, KV head) row of K and of V becomes head_dim e4m3
+// codes plus one fp32 symmetric scale (ROCm/ATOM PR #2655, PR description, K/V
+// bullet: scale = row amax / FP8 max), written by one launch for K and V to
+// slot ids held in device memory, so the launch can be captured in a CUDA
+// graph.  The fix commit "give the V tensor its own row pitch in the fp8 KV
+// store": K and V each carry their own token pitch.
+//
+// Layout of the work: one warp per token; each 8-lane group owns one 128-
+// element row (16 elements, 32 bytes, per lane: two 16-byte loads), so a warp
+// covers four rows at a time and loops over the token's 2*H rows (K heads, then
+// V heads).  The row amax is an integer max over the bf16 magnitude bits
+// (order-preserving for finite values) reduced across the 8 lanes with
+// shuffles; the 16 codes of a lane leave as one 16-byte store, so a row's 128
+// codes are one contiguous 128-byte line.
+#include <cuda_runtime.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kQuantWarps = 8;
+
+struct QuantParams {
+  const uint16_t *k;
+  const uint16_t *v;
+  int64_t k_stride;
+  int64_t v_stride;
+  int64_t num_tokens;
+  const int64_t *slot_ids;
+  uint8_t *k_codes;
+  uint8_t *v_codes;
+  float *k_scales;
+  float *v_scales;
+  int64_t num_slots;
+  int32_t num_kv_heads;
+  int32_t *err_flags;
+};
+
+__device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
+  const uint32_t m = 0x7FFF7FFFu;
+  uint32_t r = __vmaxu2(a.x & m, a.y & m);
+  r = __vmaxu2(r, a.z & m);
+  r = __vmaxu2(r, a.w & m);
+  r = __vmaxu2(r, b.x & m);
+  r = __vmaxu2(r, b.y & m);
+  r = __vmaxu2(r, b.z & m);
+  r = __vmaxu2(r, b.w & m);
+  return r;
+}
+
+// Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3).
+__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s) {
+  const uint32_t c0 = e4m3_encode_div(bf16_lo(w0), s);
+  const uint32_t c1 = e4m3_encode_div(bf16_hi(w0), s);
+  const uint32_t c2 = e4m3_encode_div(bf16_lo(w1), s);
+  const uint32_t c3 = e4m3_encode_div(bf16_hi(w1), s);
+  return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+}
+
+__global__ void __launch_bounds__(kQuantWarps * 32)
+quantize_scatter_kernel(const QuantParams p) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;                       // lane within the row's 8 lanes
+  const int grp = lane >> 3;                      // which of the warp's 4 rows
+  const unsigned gmask = 0xFFu << (lane & 24);
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (t >= p.num_tokens) return;
+  const int64_t slot = p.slot_ids[t];
+  if (slot < 0) return;
+  const int H = p.num_kv_heads;
+  if (slot >= p.num_slots) {
+    if (lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
+    return;
+  }
+  const uint16_t *krow = p.k + t * p.k_stride;
+  const uint16_t *vrow = p.v + t * p.v_stride;
+  for (int r = grp; r < 2 * H; r += 4) {
+    const bool is_v = r >= H;
+    const int h = is_v ? r - H : r;
+    const uint16_t *src = (is_v ? vrow : krow) + h * kHeadDim + sub * 16;
+    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
+    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 8));
+    uint32_t m = max_mag_bf16x2(a, b);
+    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 1));
+    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 2));
+    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 4));
+    const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    float s = 0.0f;
+    if (amax != 0.0f) {
+      s = __fdiv_rn(amax, 448.0f);
+      out.x = encode4(a.x, a.y, s);
+      out.y = encode4(a.z, a.w, s);
+      out.z = encode4(b.x, b.y, s);
+      out.w = encode4(b.z, b.w, s);
+    }
+    const int64_t row = slot * H + h;
+    uint8_t *dst = (is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * 16;
+    *reinterpret_cast<uint4 *>(dst) = out;
+    if (sub == 0) (is_v ? p.v_scales : p.k_scales)[row] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+struct DequantParams {
+  const uint8_t *k_codes;
+  const uint8_t *v_codes;
+  const float *k_scales;
+  const float *v_scales;
+  int64_t num_slots;
+  int32_t num_kv_heads;
+  const int64_t *slot_ids;
+  int64_t n;
+  int32_t out_bf16;
+  void *out_k;
+  void *out_v;
+  int32_t *err_flags;
+};
+
+__global__ void __launch_bounds__(kQuantWarps * 32)
+dequant_rows_kernel(const DequantParams p) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int grp = lane >> 3;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (i >= p.n) return;
+  const int64_t slot = p.slot_ids[i];
+  const bool valid = slot >= 0 && slot < p.num_slots;
+  if (slot >= p.num_slots && lane == 0 && p.err_flags)
+    atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
+  const int H = p.num_kv_heads;
+  for (int r = grp; r < 2 * H; r += 4) {
+    const bool is_v = r >= H;
+    const int h = is_v ? r - H : r;
+    void *outp = is_v ? p.out_v : p.out_k;
+    if (outp == nullptr) continue;
+    uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+    float s = 0.0f;
+    if (valid) {
+      const int64_t row = slot * H + h;
+      codes = __ldg(reinterpret_cast<const uint4 *>(
+          (is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * 16));
+      s = __ldg((is_v ? p.v_scales : p.k_scales) + row);
+    }
+    float v[16];
+    const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      v[j] = __fmul_rn(e4m3_to_f32((w[j >> 2] >> (8 * (j & 3))) & 0xFFu), s);
+    const int64_t o = (i * H + h) * kHeadDim + sub * 16;
+    if (p.out_bf16) {
+      uint4 lo, hi;
+      lo.x = pack_bf16x2(v[0], v[1]);   lo.y = pack_bf16x2(v[2], v[3]);
+      lo.z = pack_bf16x2(v[4], v[5]);   lo.w = pack_bf16x2(v[6], v[7]);
+      hi.x = pack_bf16x2(v[8], v[9]);   hi.y = pack_bf16x2(v[10], v[11]);
+      hi.z = pack_bf16x2(v[12], v[13]); hi.w = pack_bf16x2(v[14], v[15]);
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(outp) + o);
+      dst[0] = lo;
+      dst[1] = hi;
+    } else {
+      float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(outp) + o);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+      dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+      dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k_stride,
+                                    const void *v, int64_t v_stride, int64_t num_tokens,
+                                    const int64_t *slot_ids, int32_t *err_flags,
+                                    cudaStream_t stream) {
+  QuantParams p;
+  p.k = static_cast<const uint16_t *>(k);
+  p.v = static_cast<const uint16_t *>(v);
+  p.k_stride = k_stride;
+  p.v_stride = v_stride;
+  p.num_tokens = num_tokens;
+  p.slot_ids = slot_ids;
+  p.k_codes = c.k_codes;
+  p.v_codes = c.v_codes;
+  p.k_scales = c.k_scales;
+  p.v_scales = c.v_scales;
+  p.num_slots = c.num_slots;
+  p.num_kv_heads = c.num_kv_heads;
+  p.err_flags = err_flags;
+  const int64_t blocks = (num_tokens + kQuantWarps - 1) / kQuantWarps;
+  quantize_scatter_kernel<<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int64_t n,
+                                int32_t out_dtype, void *out_k, void *out_v,
+                                int32_t *err_flags, cudaStream_t stream) {
+  DequantParams p;
+  p.k_codes = c.k_codes;
+  p.v_codes = c.v_codes;
+  p.k_scales = c.k_scales;
+  p.v_scales = c.v_scales;
+  p.num_slots = c.num_slots;
+  p.num_kv_heads = c.num_kv_heads;
+  p.slot_ids = slot_ids;
+  p.n = n;
+  p.out_bf16 = out_dtype == 1;
+  p.out_k = out_k;
+  p.out_v = out_v;
+  p.err_flags = err_flags;
+  const int64_t blocks = (n + kQuantWarps - 1) / kQuantWarps;
+  dequant_rows_kernel<<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

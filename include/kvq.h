@@ -1,0 +1,223 @@
+/*
+ * kvq.h -- C ABI of libkvq: an FP8 E4M3 paged KV cache with one FP32 scale per
+ * (token, KV head) row, for NVIDIA GB300 (sm_103a).
+ *
+ * What the operations compute, and where that is defined:
+ *
+ *  - Row format.  ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8
+ *    scale planes for KV offload", PR description (K/V bullet), and
+ *    FlashML-org/FreeToken PR #354 "feat(kvcache): store the KV cache as fp8
+ *    e4m3 codes", PR description: each (token, KV head) row of K and of V is
+ *    stored as head_dim E4M3 codes plus ONE fp32 symmetric scale,
+ *        scale = amax(|x|) / 448,   code_d = e4m3_rne(x_d / scale),
+ *    so the row's largest element maps to +-448 and nothing saturates.  Codes
+ *    live in a plain uint8 buffer with exactly the geometry of a 16-bit KV
+ *    buffer ([num_slots, num_kv_heads, head_dim]); the scales in a sidecar
+ *    [num_slots, num_kv_heads] fp32.  Division and rounding are IEEE binary32,
+ *    round-to-nearest-even; |x / scale| >= 448 saturates to 448; an all-zero
+ *    row stores scale 0 and codes 0x00; a NaN code is never written.
+ *
+ *  - Attention.  ATOM PR #2655, PR description (K/V bullet): the attention
+ *    reads E4M3 tiles, multiplies the key scale into its score column and folds
+ *    the value scale into the probability before PV.  With G = Hq / H query
+ *    heads per KV head (query head hq reads KV head hq / G), for request r with
+ *    context length L and R query rows (R = 1: decode; R > 1: the rows of a
+ *    multi-token verify whose last R tokens are already cached, as in the
+ *    stacked MTP-verify rows of ATOM PR #2655), row i sees cached tokens
+ *    j < L - R + 1 + i and
+ *        s_j  = sm_scale * k_scale_j * sum_d q_d * e4m3(kc_{j,d})
+ *        out  = sum_j (p_j * v_scale_j) * e4m3(vc_j) / sum_j p_j,
+ *        p_j  = exp(s_j - max_j s_j).
+ *    A row that sees no token outputs zeros.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device memory must be device (or managed) memory of the
+ *    current CUDA device; the caller owns every buffer.  The library never
+ *    allocates, never synchronises and never reads device data on the host, so
+ *    each call is asynchronous on `stream` and can be captured in a CUDA graph.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - Arguments are validated on the host before anything is launched; a
+ *    violation returns a status and launches nothing.  A launch failure returns
+ *    KVQ_ERR_CUDA.  Unsupported shapes are refused, never silently handled by
+ *    a slower path.
+ *  - Errors that depend on device data (an out-of-range slot id, block id or
+ *    context length) cannot be seen on the host: the offending write or read is
+ *    skipped and a bit is OR-ed into the optional device word `err_flags`
+ *    (KVQ_ERRF_*); read it after the stream completes.  Outputs that depend on
+ *    skipped data are unspecified but every access stays inside the buffers.
+ *  - head_dim must be 128.  Alignment: code buffers, q, out, k, v and the
+ *    workspace 16 bytes; token strides of k and v multiples of 8 elements;
+ *    slot ids 8 bytes; scales, block tables and context lengths 4 bytes.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                      /* the type cudaStream_t points to */
+typedef struct CUstream_st *kvq_stream_t;
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARGUMENT = 1,        /* null pointer, negative size, bad shape     */
+    KVQ_ERR_UNSUPPORTED = 2,             /* valid but not implemented (e.g. head_dim)  */
+    KVQ_ERR_MISALIGNED = 3,              /* a pointer or stride breaks the alignment   */
+    KVQ_ERR_WORKSPACE_TOO_SMALL = 4,     /* workspace_bytes below the required size    */
+    KVQ_ERR_CUDA = 5                     /* a CUDA call or kernel launch failed        */
+} kvq_status;
+
+/* Bits OR-ed into *err_flags by the kernels. */
+#define KVQ_ERRF_SLOT_RANGE 1            /* slot id >= num_slots (write/read skipped)  */
+#define KVQ_ERRF_BLOCK_RANGE 2           /* block id outside [0, num_slots/block_size) */
+#define KVQ_ERRF_CONTEXT_RANGE 4         /* context length < 0, > max_context_len or
+                                            > max_blocks_per_req * block_size          */
+
+/* The cache: codes and scales always travel together (ATOM PR #2655,
+ * "Motivation": a restore that drops the scale planes decodes rows under the
+ * wrong scales).  All four arrays are device memory owned by the caller.
+ *   k_codes, v_codes   uint8 [num_slots, num_kv_heads, head_dim]
+ *   k_scales, v_scales fp32  [num_slots, num_kv_heads]
+ * Slot s of a paged cache belongs to block s / block_size. */
+typedef struct kvq_cache {
+    uint8_t *k_codes;
+    uint8_t *v_codes;
+    float *k_scales;
+    float *v_scales;
+    int64_t num_slots;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;                  /* a power of two; used by the decode only */
+} kvq_cache;
+
+/* Text for a status code (static storage). */
+const char *kvq_status_string(kvq_status status);
+
+/* ABI version of this header (incremented on any signature change). */
+int32_t kvq_abi_version(void);
+
+/* Bytes of codes plus scales for a cache of this size, K and V together:
+ * 2 * num_slots * num_kv_heads * (head_dim + 4).  FreeToken PR #354, PR
+ * description: the pool counts codes plus the scale sidecar.  Returns 0 for a
+ * negative argument. */
+size_t kvq_cache_bytes(int64_t num_slots, int32_t num_kv_heads, int32_t head_dim);
+
+/* Fused quantize + scatter of K and V rows into the cache (one launch).
+ * FreeToken PR #354, PR description (fused quantize+scatter, one launch under
+ * CUDA graph capture, slot ids as a device tensor) and fix commit "give the V
+ * tensor its own row pitch in the fp8 KV store" (K and V each have a pitch).
+ *   k, v            device bf16; token t's row for KV head h starts at element
+ *                   t*k_token_stride + h*head_dim of k (v: v_token_stride); the
+ *                   head_dim elements of a row are contiguous.  Either may be a
+ *                   strided view of a fused qkv projection output.
+ *   k_token_stride, v_token_stride   in elements, multiples of 8, >= 0
+ *   num_tokens      rows to store (0 launches nothing)
+ *   slot_ids        device int64 [num_tokens]; id < 0 skips the token (padding);
+ *                   id >= num_slots skips it and sets KVQ_ERRF_SLOT_RANGE.
+ *                   Ids must be unique (two tokens writing one slot race).
+ *   err_flags       device int32, optional (NULL)
+ * Writes codes and scales of every valid token's K and V rows. */
+kvq_status kvq_quantize_scatter(const kvq_cache *cache,
+                                const void *k, int64_t k_token_stride,
+                                const void *v, int64_t v_token_stride,
+                                int64_t num_tokens, const int64_t *slot_ids,
+                                int32_t *err_flags, kvq_stream_t stream);
+
+/* Tokens per split-K partition that kvq_paged_decode uses when passed 0: a
+ * power of two in [256, 8192] chosen from the batch shape and the current
+ * device's SM count (152 is assumed when no device is visible); always a
+ * multiple of 64. */
+int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t num_kv_heads,
+                                          int32_t block_size, int32_t max_context_len);
+
+/* Workspace bytes kvq_paged_decode needs for this shape (0 when every request
+ * fits one partition): num_requests*rows_per_request*num_q_heads *
+ * ceil(max_context_len / partition) * (head_dim + 2) * 4, each of the two
+ * parts rounded up to 256.  partition_tokens 0 means the value
+ * kvq_paged_decode_partition_tokens gives.  Returns 0 for invalid arguments. */
+size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size,
+                                       int32_t max_context_len, int32_t partition_tokens);
+
+/* Paged GQA decode / multi-row verify attention over the FP8 cache, split-K
+ * over partitions of the context (flash-decoding) followed by a combine launch
+ * when any request spans more than one partition.
+ *   q               device bf16 [num_requests*rows_per_request, num_q_heads,
+ *                   head_dim], contiguous; row r*rows_per_request + i is query
+ *                   row i of request r.
+ *   rows_per_request R >= 1; R * (num_q_heads/num_kv_heads) <= 128 (the rows
+ *                   of one KV head are processed in groups of at most 32 that
+ *                   each read the head's codes once).
+ *   num_q_heads     a multiple of cache->num_kv_heads
+ *   block_tables    device int32 [num_requests, max_blocks_per_req]: physical
+ *                   block of each logical block of the request
+ *   context_lens    device int32 [num_requests]: cached tokens per request,
+ *                   the R query tokens included
+ *   max_context_len host bound on every context length (sizes the grid, so a
+ *                   captured graph stays valid while lengths stay below it)
+ *   sm_scale        softmax scale applied to q.k (e.g. 1/sqrt(head_dim))
+ *   partition_tokens tokens per split-K partition, a multiple of 64 in
+ *                   [64, 1<<20]; 0 = kvq_paged_decode_partition_tokens()
+ *   out             device bf16, same shape as q (written, round-to-nearest)
+ *   workspace       device, >= kvq_paged_decode_workspace_size(...) bytes
+ *                   (may be NULL when that size is 0)
+ *   err_flags       device int32, optional
+ * Calls that share a workspace must not run concurrently. */
+kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q,
+                            int32_t num_requests, int32_t rows_per_request,
+                            int32_t num_q_heads, const int32_t *block_tables,
+                            int32_t max_blocks_per_req, const int32_t *context_lens,
+                            int32_t max_context_len, float sm_scale,
+                            int32_t partition_tokens, void *out, void *workspace,
+                            size_t workspace_bytes, int32_t *err_flags,
+                            kvq_stream_t stream);
+
+/* The two launches of kvq_paged_decode, exposed so a caller can time or
+ * schedule them separately.  kvq_paged_decode_partials takes kvq_paged_decode's
+ * arguments and makes the split-K launch: requests that fit one partition get
+ * their final output written to `out`, the others leave per-partition partials
+ * (running max, denominator, unnormalised output) in the workspace.
+ * kvq_paged_decode_combine merges those partials into `out`; it must follow
+ * kvq_paged_decode_partials on the same stream with the same shape, partition
+ * size and workspace, and does nothing when no request spans two partitions. */
+kvq_status kvq_paged_decode_partials(const kvq_cache *cache, const void *q,
+                                     int32_t num_requests, int32_t rows_per_request,
+                                     int32_t num_q_heads, const int32_t *block_tables,
+                                     int32_t max_blocks_per_req,
+                                     const int32_t *context_lens, int32_t max_context_len,
+                                     float sm_scale, int32_t partition_tokens, void *out,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *err_flags, kvq_stream_t stream);
+
+kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests,
+                                    int32_t rows_per_request, int32_t num_q_heads,
+                                    int32_t max_blocks_per_req, const int32_t *context_lens,
+                                    int32_t max_context_len, int32_t partition_tokens,
+                                    void *out, void *workspace, size_t workspace_bytes,
+                                    kvq_stream_t stream);
+
+/* Dequantise whole rows back to real values: out = fl32(e4m3(c) * scale), one
+ * IEEE multiply, or that value rounded once more to bf16 (nearest-even).
+ * sglang-jax #1776 "feat(dsa): implement fp8 KV cache (e4m3) with a bf16
+ * indexer cache", Modifications: a consumer upcasts the cached block before it
+ * is used.
+ *   slot_ids    device int64 [n]; an id outside [0, num_slots) gives a zero row
+ *               (ids >= num_slots also set KVQ_ERRF_SLOT_RANGE)
+ *   out_dtype   0 = fp32, 1 = bf16
+ *   out_k, out_v device [n, num_kv_heads, head_dim] of out_dtype; either may be
+ *               NULL to skip that half
+ *   err_flags   device int32, optional */
+kvq_status kvq_dequant_rows(const kvq_cache *cache, const int64_t *slot_ids, int64_t n,
+                            int32_t out_dtype, void *out_k, void *out_v,
+                            int32_t *err_flags, kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

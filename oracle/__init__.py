@@ -74,6 +74,8 @@ def _load():
             lib.kvqo_float_to_bf16_array.argtypes = [P, i64, P]
             lib.kvqo_quantize_row.restype = None
             lib.kvqo_quantize_row.argtypes = [P, ctypes.c_int, P, P]
+            lib.kvqo_quantize_rows.restype = None
+            lib.kvqo_quantize_rows.argtypes = [P, i64, ctypes.c_int, P, P]
             lib.kvqo_quantize_scatter.restype = i32
             lib.kvqo_quantize_scatter.argtypes = [P, i64, P, i64, i64, ctypes.c_int,
                                                   ctypes.c_int, P, i64, P, P, P, P]
@@ -146,9 +148,7 @@ def quantize_rows(x_bf16_bits: np.ndarray):
     rows = x.reshape(-1, D)
     codes = np.empty(rows.shape, dtype=np.uint8)
     scales = np.empty(rows.shape[0], dtype=np.float32)
-    for i in range(rows.shape[0]):
-        lib.kvqo_quantize_row(_ptr(rows[i]), D, _ptr(codes[i]),
-                              ctypes.c_void_p(scales.ctypes.data + 4 * i))
+    lib.kvqo_quantize_rows(_ptr(rows), rows.shape[0], D, _ptr(codes), _ptr(scales))
     return codes.reshape(x.shape), scales.reshape(x.shape[:-1])
 
 

@@ -96,27 +96,42 @@ double kvqo_e4m3_decode(uint8_t c)
     return sign ? -mag : mag;
 }
 
+/* The 127 finite nonnegative magnitudes, grid[c] = decode(c) for c = 0..0x7E,
+ * filled once when the library loads. */
+static double grid[0x7F];
+
+/* decode(c) for all 256 codes, for the attention loops below. */
+static double dec[256];
+
+__attribute__((constructor)) static void fill_tables(void)
+{
+    for (int c = 0; c < 0x7F; ++c)
+        grid[c] = kvqo_e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 256; ++c)
+        dec[c] = kvqo_e4m3_decode((uint8_t)c);
+}
+
 /* Encode a finite binary32 value: round to the nearest representable e4m3
  * magnitude, ties to the code whose mantissa is even, saturating at 448.
- * The search runs over the 127 finite nonnegative magnitudes 0x00..0x7E, which
- * increase with the code, so a bisection finds the two neighbours of |q|. */
+ * The magnitudes increase with the code, so a bisection over the grid finds
+ * the two neighbours of |q|. */
 uint8_t kvqo_e4m3_encode(float q)
 {
     uint8_t sign = signbit(q) ? 0x80 : 0x00;
     double a = fabs((double)q);
     if (a >= 448.0)
         return (uint8_t)(sign | 0x7E);
-    /* invariant: value(lo) <= a < value(hi) */
+    /* invariant: grid[lo] <= a < grid[hi] */
     int lo = 0, hi = 0x7E;
     while (hi - lo > 1) {
         int mid = (lo + hi) / 2;
-        if (kvqo_e4m3_decode((uint8_t)mid) <= a)
+        if (grid[mid] <= a)
             lo = mid;
         else
             hi = mid;
     }
-    double vlo = kvqo_e4m3_decode((uint8_t)lo);
-    double vhi = kvqo_e4m3_decode((uint8_t)hi);
+    double vlo = grid[lo];
+    double vhi = grid[hi];
     double half = 0.5 * (vlo + vhi); /* exact: both have few significant bits */
     int pick;
     if (a < half)
@@ -164,6 +179,13 @@ void kvqo_quantize_row(const uint16_t *x, int D, uint8_t *codes, float *scale)
         float q = kvqo_bf16_to_float(x[d]) / s;
         codes[d] = kvqo_e4m3_encode(q);
     }
+}
+
+/* Many rows at once: x [n_rows, D] -> codes [n_rows, D], scales [n_rows]. */
+void kvqo_quantize_rows(const uint16_t *x, int64_t n_rows, int D, uint8_t *codes, float *scales)
+{
+    for (int64_t i = 0; i < n_rows; ++i)
+        kvqo_quantize_row(x + i * D, D, codes + i * D, &scales[i]);
 }
 
 /* Fused quantize + scatter, [FT] PR description and fix commit: token t's K
@@ -267,7 +289,7 @@ static int32_t attention_row(const uint8_t *k_codes, const uint8_t *v_codes,
         double ks = (double)k_scales[row];
         double dot = 0.0;
         for (int d = 0; d < D; ++d) {
-            double kh = kvqo_e4m3_decode(k_codes[row * D + d]) * ks;
+            double kh = dec[k_codes[row * D + d]] * ks;
             dot += (double)kvqo_bf16_to_float(qrow[d]) * kh;
         }
         scores[j] = sm_scale * dot;
@@ -287,7 +309,7 @@ static int32_t attention_row(const uint8_t *k_codes, const uint8_t *v_codes,
         int64_t row = ((int64_t)bt_row[j / bs] * bs + j % bs) * H + kvh;
         double vs = (double)v_scales[row];
         for (int d = 0; d < D; ++d)
-            out[d] += p * (kvqo_e4m3_decode(v_codes[row * D + d]) * vs);
+            out[d] += p * (dec[v_codes[row * D + d]] * vs);
     }
     for (int d = 0; d < D; ++d)
         out[d] /= l;

@@ -1,0 +1,127 @@
+"""The C ABI without a GPU: libkvq.so builds for sm_103a, loads, exports every
+function include/kvq.h declares, and its host-side validation and size
+helpers answer before anything would be launched."""
+import ctypes
+import subprocess
+
+import pytest
+
+import fp8_paged_kv_kvq_gb300 as kvq
+from fp8_paged_kv_kvq_gb300 import build as kbuild
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WS_SMALL = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kvq.load()
+
+
+def test_header_declares_the_boundary():
+    names = kvq.header_functions()
+    for n in ("kvq_quantize_scatter", "kvq_paged_decode", "kvq_dequant_rows"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for n in kvq.header_functions():
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_library_targets_sm_103a_only():
+    assert kbuild.ARCH == "-gencode=arch=compute_103a,code=sm_103a"
+    flags = kbuild._flags()
+    assert "-ftz=false" in flags and "-prec-div=true" in flags
+    assert not any("fast-math" in f for f in flags)
+
+
+def _cache(head_dim=128, block_size=16, slots=64, ptr=0x10000):
+    return kvq._CacheStruct(ptr, ptr + 0x100000, ptr + 0x200000, ptr + 0x300000, slots, 8,
+                            head_dim, block_size)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kvq_abi_version() == 1
+    for s in range(6):
+        assert lib.kvq_status_string(s)
+
+
+def test_cache_bytes_counts_codes_and_scales(lib):
+    # FreeToken PR #354: the pool counts codes plus the fp32 sidecar
+    assert lib.kvq_cache_bytes(1000, 8, 128) == 2 * 1000 * 8 * (128 + 4)
+    assert lib.kvq_cache_bytes(-1, 8, 128) == 0
+
+
+def test_quantize_validation_happens_before_launch(lib):
+    P = ctypes.c_void_p
+    c = _cache()
+    q = lib.kvq_quantize_scatter
+    assert q(ctypes.byref(c), P(0), 0, P(0), 0, 0, P(0), P(0), P(0)) == OK
+    assert q(None, P(16), 0, P(16), 0, 1, P(8), P(0), P(0)) == INVALID
+    assert q(ctypes.byref(c), P(0), 1024, P(16), 1024, 4, P(8), P(0), P(0)) == INVALID
+    assert q(ctypes.byref(c), P(16), 1024, P(16), 1024, -1, P(8), P(0), P(0)) == INVALID
+    assert q(ctypes.byref(c), P(18), 1024, P(16), 1024, 4, P(8), P(0), P(0)) == MISALIGNED
+    assert q(ctypes.byref(c), P(16), 1028, P(16), 1024, 4, P(8), P(0), P(0)) == MISALIGNED
+    assert q(ctypes.byref(c), P(16), 1024, P(16), 1024, 4, P(12), P(0), P(0)) == MISALIGNED
+    bad = _cache(head_dim=64)
+    assert q(ctypes.byref(bad), P(16), 1024, P(16), 1024, 4, P(8), P(0), P(0)) == UNSUPPORTED
+    mis = _cache(ptr=0x10008)
+    assert q(ctypes.byref(mis), P(16), 1024, P(16), 1024, 4, P(8), P(0), P(0)) == MISALIGNED
+
+
+def _decode(lib, c, q=16, N=2, R=1, Hq=32, bt=16, mb=4, cl=16, maxc=64, sm=0.1, part=0, out=16,
+            ws=0, wsb=0):
+    P = ctypes.c_void_p
+    return lib.kvq_paged_decode(ctypes.byref(c) if c is not None else None, P(q), N, R, Hq, P(bt),
+                                mb, P(cl), maxc, sm, part, P(out), P(ws), wsb, P(0), P(0))
+
+
+def test_decode_validation_happens_before_launch(lib):
+    c = _cache()
+    assert _decode(lib, c, N=0) == OK
+    assert _decode(lib, None) == INVALID
+    assert _decode(lib, c, Hq=30) == INVALID                   # not a multiple of H
+    assert _decode(lib, c, R=0) == INVALID
+    assert _decode(lib, c, part=100) == INVALID                # not a multiple of 64
+    assert _decode(lib, c, sm=float("nan")) == INVALID
+    assert _decode(lib, c, R=5, Hq=256) == UNSUPPORTED         # 5*32 rows per KV head
+    assert _decode(lib, _cache(head_dim=256)) == UNSUPPORTED
+    assert _decode(lib, _cache(block_size=24)) == UNSUPPORTED  # not a power of two
+    assert _decode(lib, _cache(block_size=0)) == INVALID
+    assert _decode(lib, c, q=24) == MISALIGNED
+    assert _decode(lib, c, out=8) == MISALIGNED
+    assert _decode(lib, c, bt=2) == MISALIGNED
+    assert _decode(lib, c, maxc=128, part=64) == WS_SMALL      # two partitions need a workspace
+    need = lib.kvq_paged_decode_workspace_size(2, 1, 32, 8, 128, 16, 128, 64)
+    assert _decode(lib, c, maxc=128, part=64, ws=256, wsb=need - 1) == WS_SMALL
+
+
+def test_workspace_size_formula(lib):
+    n = lib.kvq_paged_decode_workspace_size(32, 1, 32, 8, 128, 16, 8192, 512)
+    rows, parts = 32 * 32, 16
+    o = rows * parts * 128 * 4
+    ml = rows * parts * 2 * 4
+    assert n == ((((o + 255) // 256) * 256 + ml + 255) // 256) * 256
+    assert lib.kvq_paged_decode_workspace_size(32, 1, 32, 8, 128, 16, 512, 512) == 0
+    assert lib.kvq_paged_decode_workspace_size(32, 1, 32, 8, 64, 16, 512, 512) == 0  # invalid
+
+
+def test_partition_heuristic_is_a_power_of_two_multiple_of_64(lib):
+    for N, maxc in ((1, 64), (32, 8192), (64, 32768), (2, 1 << 20)):
+        p = lib.kvq_paged_decode_partition_tokens(N, 8, 16, maxc)
+        assert p % 64 == 0 and (p & (p - 1)) == 0 and 256 <= p <= 8192
+
+
+def test_dequant_validation(lib):
+    P = ctypes.c_void_p
+    c = _cache()
+    d = lib.kvq_dequant_rows
+    assert d(ctypes.byref(c), P(8), 0, 0, P(16), P(16), P(0), P(0)) == OK
+    assert d(ctypes.byref(c), P(8), 4, 2, P(16), P(16), P(0), P(0)) == INVALID
+    assert d(ctypes.byref(c), P(0), 4, 0, P(16), P(16), P(0), P(0)) == INVALID
+    assert d(ctypes.byref(c), P(8), 4, 0, P(20), P(16), P(0), P(0)) == MISALIGNED

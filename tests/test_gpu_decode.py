@@ -1,0 +1,208 @@
+"""kvq_paged_decode on the GPU against the fp64 oracle (the oracle quantises
+the same seeded bf16 rows itself): decode and multi-row verify shapes,
+single-partition and split-K paths, ragged tails, edge cases, and the large
+workloads at full size on sampled outputs."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_paged_kv_kvq_gb300 as kvq
+import oracle
+import workloads
+from kvq_testlib import (assert_attention_close, assert_cache_equal, build_paged, gpu_decode,
+                         oracle_decode)
+
+pytestmark = pytest.mark.gpu
+
+
+def _queries(w, N, R, seed):
+    g = workloads.generator(seed, 77)
+    return torch.randn(N * R, w.num_q_heads, w.head_dim, generator=g).to(torch.bfloat16)
+
+
+def test_tiny_workload():
+    w = workloads.WORKLOADS["tiny"]
+    lens = workloads.context_lengths(w)
+    built = build_paged(w, lens, spare_blocks=0)
+    assert_cache_equal(built["cache"], built["ocache"])
+    q = workloads.queries(w)
+    out = gpu_decode(built, q, 1, w.sm_scale)
+    ref, err = oracle_decode(built, q, 1, w.num_q_heads, w.sm_scale)
+    assert err == 0
+    assert_attention_close(out, ref, "tiny")
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 64, 128, 256, 1024])
+def test_decode_batch_scaled(partition_tokens):
+    """The decode-batch shape (GQA 4, block size 16, log-normal rows) with
+    fewer, shorter requests; ragged lengths exercise partial stages."""
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=5)
+    lens = np.array([1, 63, 64, 700, 1500], dtype=np.int32)
+    built = build_paged(w, lens)
+    assert_cache_equal(built["cache"], built["ocache"])
+    q = _queries(w, 5, 1, 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(built, q, 1, w.sm_scale, partition_tokens=partition_tokens, err=err)
+    ref, _ = oracle_decode(built, q, 1, w.num_q_heads, w.sm_scale)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, f"decode P={partition_tokens}")
+
+
+@pytest.mark.parametrize("R,Hq,H,bs", [
+    (4, 64, 8, 64),    # the verify shape: 4 rows x GQA 8 = 32 stacked rows
+    (4, 32, 8, 16),    # 16 rows
+    (2, 32, 8, 16),    # 8 rows
+    (1, 8, 8, 16),     # MHA
+    (4, 128, 8, 64),   # 64 rows: two row groups
+    (3, 12, 4, 32),    # 9 rows, odd group
+])
+@pytest.mark.parametrize("partition_tokens", [0, 128])
+def test_verify_shapes(R, Hq, H, bs, partition_tokens):
+    w = workloads.scaled(workloads.WORKLOADS["verify"], num_requests=3, rows_per_request=R,
+                         num_q_heads=Hq, num_kv_heads=H, block_size=bs)
+    lens = np.array([R, 333, 520], dtype=np.int32)
+    built = build_paged(w, lens)
+    q = _queries(w, 3, R, 2)
+    out = gpu_decode(built, q, R, w.sm_scale, partition_tokens=partition_tokens)
+    ref, _ = oracle_decode(built, q, R, Hq, w.sm_scale)
+    assert_attention_close(out, ref, f"R={R} Hq={Hq} H={H} P={partition_tokens}")
+
+
+def test_rows_that_see_nothing_and_empty_requests():
+    w = workloads.scaled(workloads.WORKLOADS["verify"], num_requests=4, rows_per_request=4,
+                         num_q_heads=16, num_kv_heads=4, block_size=16)
+    lens = np.array([0, 1, 2, 200], dtype=np.int32)   # L < R: leading rows see nothing
+    built = build_paged(w, lens)
+    q = _queries(w, 4, 4, 3)
+    for P in (0, 64):
+        out = gpu_decode(built, q, 4, w.sm_scale, partition_tokens=P, max_context_len=256)
+        ref, _ = oracle_decode(built, q, 4, 16, w.sm_scale)
+        assert torch.all(out[:4].float() == 0)                  # request 0: L = 0
+        assert torch.all(out[4:7].float() == 0)                 # request 1: rows 0..2 see nothing
+        assert_attention_close(out, ref, f"edge P={P}")
+
+
+def test_split_and_single_partition_agree():
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=2)
+    lens = np.array([2000, 4096], dtype=np.int32)
+    built = build_paged(w, lens, oracle_side=False)
+    q = _queries(w, 2, 1, 4)
+    one = gpu_decode(built, q, 1, w.sm_scale, partition_tokens=4096).float()
+    many = gpu_decode(built, q, 1, w.sm_scale, partition_tokens=64).float()
+    rel = (one - many).norm() / one.norm()
+    assert rel < 3e-3
+
+
+def test_bad_block_ids_and_lengths_are_flagged_not_faulted():
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=2)
+    lens = np.array([100, 300], dtype=np.int32)
+    built = build_paged(w, lens, oracle_side=False)
+    q = _queries(w, 2, 1, 5).cuda()
+    bt = torch.from_numpy(built["bt"]).cuda()
+    bad = bt.clone()
+    bad[1, 3] = 1 << 30
+    bad[1, 4] = -5
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cl = torch.from_numpy(lens).cuda()
+    kvq.paged_decode(built["cache"], q, bad, cl, 300, w.sm_scale, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & kvq.ERRF_BLOCK_RANGE
+    err.zero_()
+    cl_bad = torch.tensor([100, 10 ** 6], dtype=torch.int32, device="cuda")
+    out = kvq.paged_decode(built["cache"], q, bt, cl_bad, 300, w.sm_scale, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & kvq.ERRF_CONTEXT_RANGE
+    assert torch.all(torch.isfinite(out.float()))
+
+
+def test_graph_capture_of_decode():
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=3)
+    lens = np.array([300, 900, 50], dtype=np.int32)
+    built = build_paged(w, lens)
+    q = _queries(w, 3, 1, 6).cuda()
+    bt = torch.from_numpy(built["bt"]).cuda()
+    cl = torch.from_numpy(lens).cuda()
+    P = 128
+    need = kvq.paged_decode_workspace_size(3, 1, w.num_q_heads, w.num_kv_heads, 128,
+                                           w.block_size, 1024, P)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        kvq.paged_decode(built["cache"], q, bt, cl, 1024, w.sm_scale, partition_tokens=P,
+                         out=out, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        kvq.paged_decode(built["cache"], q, bt, cl, 1024, w.sm_scale, partition_tokens=P,
+                         out=out, workspace=ws)
+    out.zero_()
+    q.mul_(-1.0)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    ref, _ = oracle_decode(built, q.cpu(), 1, w.num_q_heads, w.sm_scale)
+    assert_attention_close(out, ref, "graph replay")
+
+
+def _full_size(name, sample_requests, heads):
+    """The named workload at full size, in the configuration the benchmark
+    times (default partition size), checked on sampled (request, KV head)
+    units: the oracle quantises those requests' rows for that KV head itself."""
+    w = workloads.WORKLOADS[name]
+    lens = workloads.context_lengths(w)
+    bt, nblk = workloads.block_tables(lens, w.block_size, w.seed)
+    S = nblk * w.block_size
+    H, D, G, R = w.num_kv_heads, w.head_dim, w.group, w.rows_per_request
+    cache = kvq.Cache.empty(S, H, D, w.block_size)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ct = workloads.chunk_tokens(w)
+    for r in range(w.num_requests):
+        L = int(lens[r])
+        slots_all = workloads.token_slots(bt, r, L, w.block_size)
+        for c0 in range(0, L, ct):
+            n = min(ct, L - c0)
+            k, v = workloads.request_kv(w, r, c0, n, device="cuda")
+            kvq.quantize_scatter(cache, k, v, torch.from_numpy(slots_all[c0:c0 + n]).cuda(), err)
+    q = workloads.queries(w, device="cuda")
+    out = kvq.paged_decode(cache, q, torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda(),
+                           int(lens.max()), w.sm_scale, rows_per_request=R, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    out_h = out.cpu()
+    for r, h in zip(sample_requests, heads):
+        L = int(lens[r])
+        slots = workloads.token_slots(bt, r, L, w.block_size)
+        oc = oracle.empty_cache(S, 1, D)          # the oracle's own cache, KV head h only
+        kall, vall = [], []
+        for c0 in range(0, L, ct):
+            n = min(ct, L - c0)
+            k, v = workloads.request_kv(w, r, c0, n, device="cuda")
+            kall.append(workloads.bf16_bits(k[:, h:h + 1]))
+            vall.append(workloads.bf16_bits(v[:, h:h + 1]))
+        kb = np.concatenate(kall).reshape(-1)
+        vb = np.concatenate(vall).reshape(-1)
+        oracle.quantize_scatter(kb, D, vb, D, L, 1, D, slots, oc)
+        sl = torch.from_numpy(slots).cuda()
+        assert np.array_equal(cache.k_codes[sl, h].cpu().numpy(), oc["k_codes"][slots, 0])
+        assert np.array_equal(cache.v_codes[sl, h].cpu().numpy(), oc["v_codes"][slots, 0])
+        assert np.array_equal(cache.v_scales[sl, h].cpu().numpy().view(np.uint32),
+                              oc["v_scales"][slots, 0].view(np.uint32))
+        qh = workloads.bf16_bits(q[r * R:(r + 1) * R, h * G:(h + 1) * G].cpu())
+        ref, _ = oracle.paged_attention(oc, qh, 1, R, G, bt[r:r + 1], lens[r:r + 1],
+                                        w.block_size, w.sm_scale)
+        gpu = out_h[r * R:(r + 1) * R, h * G:(h + 1) * G]
+        assert_attention_close(gpu, ref, f"{name} r={r} h={h}")
+
+
+def test_decode_batch_full_size():
+    _full_size("decode", [0, 17, 31], [0, 5, 7])
+
+
+def test_verify_full_size():
+    _full_size("verify", [0, 63], [3, 7])
+
+
+def test_long_context_full_size():
+    _full_size("longctx", [1], [6])
