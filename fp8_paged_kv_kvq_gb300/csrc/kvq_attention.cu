@@ -26,9 +26,14 @@
 //      masks causally (row i sees tokens j < L - R + 1 + i), and updates a
 //      running max per row, rescaling the accumulators only when the max grows
 //      by more than 2^8 (so p <= 256);
-//   3. folds the value scale into p (P' = p * v_scale, rounded once to bf16),
-//      accumulates the denominator with the unscaled p, and runs O += P' V with
-//      V decoded the same way.
+//   3. folds the value scale into p (P' = p * v_scale * 2^-E, rounded once to
+//      f16, where 2^E is a running power-of-two bound on the v_scales the warp
+//      has seen, so P' <= 256 always fits f16), accumulates the denominator
+//      with the unscaled p, and runs O += P' V with f16 MMAs on V codes decoded
+//      exactly to f16 (value * 2^-8; the 2^(E+8) is applied once at the end).
+//      f16 keeps 11 mantissa bits of P' where bf16 keeps 8: with the outputs'
+//      cancellation between large terms, bf16 P' alone costs up to ~1.6%
+//      elementwise, f16 about the output's own bf16 rounding.
 // The warps' (max, denominator, O) are merged through shared memory; a request
 // with a single partition writes its bf16 output directly, otherwise the
 // partial is stored and the combine kernel merges the partitions (log-sum-exp
@@ -237,6 +242,9 @@ attn_partials_kernel(const AttnParams p) {
     for (int i = 0; i < 16; ++i)
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[mt][i][e] = 0.0f;
+  // running exponent E: every v_scale this warp has folded so far is <= 2^E
+  // (warp-uniform; -1000 = none yet; otherwise clamped to [-126, 126])
+  int ev = -1000;
 
   for (int st = 0; st < n_stages; ++st) {
     cp_async_wait<kStages - 2>();
@@ -288,6 +296,7 @@ attn_partials_kernel(const AttnParams p) {
 
     // ---- scale, mask, online softmax (lazy rescale)
     float ksc[2][2], vsc[2][2];
+    float vmax = 0.0f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const float2 kk = *reinterpret_cast<const float2 *>(sb.ks + tb + nt * 8 + 2 * c4);
@@ -296,6 +305,31 @@ attn_partials_kernel(const AttnParams p) {
       ksc[nt][1] = kk.y * p.qk_scale;
       vsc[nt][0] = vv.x;
       vsc[nt][1] = vv.y;
+      vmax = fmaxf(vmax, fmaxf(vv.x, vv.y));
+    }
+    // the 4 lanes of a quad hold all 16 tokens' scales: the quad max is the
+    // chunk max, the same in every quad
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 1));
+    vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, 2));
+    float vfac = 1.0f;
+    bool vgrow = false;
+    {
+      const uint32_t bits = __float_as_uint(vmax);
+      const int ex = static_cast<int>((bits >> 23) & 0xFFu);
+      int ec = (ex == 0) ? -126 : ex - 127 + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
+      ec = ec > 126 ? 126 : ec;   // finite scales are below 2^120
+      if (ec > ev) {
+        const int d = ev - ec;   // < 0
+        vfac = (d >= -126) ? __int_as_float((127 + d) << 23) : 0.0f;
+        ev = ec;
+        vgrow = true;
+      }
+    }
+    const float vnorm = __int_as_float((127 - ev) << 23);   // 2^-E, E in [-126, 126]
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      vsc[nt][0] *= vnorm;
+      vsc[nt][1] *= vnorm;
     }
     float fac[MT][2];
     bool grow = false;
@@ -325,16 +359,17 @@ attn_partials_kernel(const AttnParams p) {
           fac[mt][hf] = 1.0f;
         }
       }
-    if (__any_sync(0xFFFFFFFFu, grow)) {
+    if (__any_sync(0xFFFFFFFFu, grow) || vgrow) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           l_run[mt][hf] *= fac[mt][hf];
+          const float f = fac[mt][hf] * vfac;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            o[mt][i][2 * hf] *= fac[mt][hf];
-            o[mt][i][2 * hf + 1] *= fac[mt][hf];
+            o[mt][i][2 * hf] *= f;
+            o[mt][i][2 * hf + 1] *= f;
           }
         }
     }
@@ -354,10 +389,10 @@ attn_partials_kernel(const AttnParams p) {
             pv[nt][2 * hf + e] = pr * vsc[nt][e];
           }
       }
-      pa[mt][0] = pack_bf16x2(pv[0][0], pv[0][1]);   // row g4,   tokens 2c, 2c+1
-      pa[mt][1] = pack_bf16x2(pv[0][2], pv[0][3]);   // row g4+8, tokens 2c, 2c+1
-      pa[mt][2] = pack_bf16x2(pv[1][0], pv[1][1]);   // row g4,   tokens 2c+8, 2c+9
-      pa[mt][3] = pack_bf16x2(pv[1][2], pv[1][3]);   // row g4+8, tokens 2c+8, 2c+9
+      pa[mt][0] = pack_f16x2(pv[0][0], pv[0][1]);   // row g4,   tokens 2c, 2c+1
+      pa[mt][1] = pack_f16x2(pv[0][2], pv[0][3]);   // row g4+8, tokens 2c, 2c+1
+      pa[mt][2] = pack_f16x2(pv[1][0], pv[1][1]);   // row g4,   tokens 2c+8, 2c+9
+      pa[mt][3] = pack_f16x2(pv[1][2], pv[1][3]);   // row g4+8, tokens 2c+8, 2c+9
     }
 
     // ---- O += P' V.  Lane reads dims [16*g4, 16*g4+16) of tokens 2c, 2c+1, 2c+8, 2c+9.
@@ -380,14 +415,14 @@ attn_partials_kernel(const AttnParams p) {
       const uint32_t cd01 = prmt(wc[wi], wd[wi], 0x5410u);
       const uint32_t cd23 = prmt(wc[wi], wd[wi], 0x7632u);
       uint32_t b0[4], b1[4];
-      b0[0] = e4m3x2_b02_to_bf16x2(ab01); b1[0] = e4m3x2_b02_to_bf16x2(cd01);
-      b0[1] = e4m3x2_b13_to_bf16x2(ab01); b1[1] = e4m3x2_b13_to_bf16x2(cd01);
-      b0[2] = e4m3x2_b02_to_bf16x2(ab23); b1[2] = e4m3x2_b02_to_bf16x2(cd23);
-      b0[3] = e4m3x2_b13_to_bf16x2(ab23); b1[3] = e4m3x2_b13_to_bf16x2(cd23);
+      b0[0] = e4m3x2_b02_to_f16x2_lo8(ab01); b1[0] = e4m3x2_b02_to_f16x2_lo8(cd01);
+      b0[1] = e4m3x2_b13_to_f16x2_lo8(ab01); b1[1] = e4m3x2_b13_to_f16x2_lo8(cd01);
+      b0[2] = e4m3x2_b02_to_f16x2_lo8(ab23); b1[2] = e4m3x2_b02_to_f16x2_lo8(cd23);
+      b0[3] = e4m3x2_b13_to_f16x2_lo8(ab23); b1[3] = e4m3x2_b13_to_f16x2_lo8(cd23);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(o[mt][4 * wi + e], pa[mt], b0[e], b1[e]);
+        for (int mt = 0; mt < MT; ++mt) mma_f16_16816(o[mt][4 * wi + e], pa[mt], b0[e], b1[e]);
     }
   }
 
@@ -431,7 +466,10 @@ attn_partials_kernel(const AttnParams p) {
       }
       mrow[mt][hf] = mx;
       lrow[mt][hf] = lt;
-      frow[mt][hf] = (mx == -INFINITY) ? 0.0f : ex2(m_run[mt][hf] - mx);
+      // softmax merge weight times 2^E (the accumulators hold O * 2^-(E+8);
+      // the remaining 2^8 is applied with a second multiply below)
+      frow[mt][hf] = (mx == -INFINITY || ev == -1000)
+                         ? 0.0f : ldexpf(ex2(m_run[mt][hf] - mx), ev);
     }
   if (warp > 0) {
 #pragma unroll
@@ -439,8 +477,8 @@ attn_partials_kernel(const AttnParams p) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         parked[(((warp - 1) * MT + mt) * 16 + i) * 32 + lane] =
-            make_float4(o[mt][i][0] * frow[mt][0], o[mt][i][1] * frow[mt][0],
-                        o[mt][i][2] * frow[mt][1], o[mt][i][3] * frow[mt][1]);
+            make_float4(o[mt][i][0] * 256.0f * frow[mt][0], o[mt][i][1] * 256.0f * frow[mt][0],
+                        o[mt][i][2] * 256.0f * frow[mt][1], o[mt][i][3] * 256.0f * frow[mt][1]);
   }
   __syncthreads();
   if (warp != 0) return;
@@ -448,8 +486,10 @@ attn_partials_kernel(const AttnParams p) {
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float4 acc = make_float4(o[mt][i][0] * frow[mt][0], o[mt][i][1] * frow[mt][0],
-                               o[mt][i][2] * frow[mt][1], o[mt][i][3] * frow[mt][1]);
+      float4 acc = make_float4(o[mt][i][0] * 256.0f * frow[mt][0],
+                               o[mt][i][1] * 256.0f * frow[mt][0],
+                               o[mt][i][2] * 256.0f * frow[mt][1],
+                               o[mt][i][3] * 256.0f * frow[mt][1]);
 #pragma unroll
       for (int w = 0; w < kWarps - 1; ++w) {
         const float4 x = parked[((w * MT + mt) * 16 + i) * 32 + lane];

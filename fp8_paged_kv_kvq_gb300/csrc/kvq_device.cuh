@@ -74,6 +74,21 @@ __device__ __forceinline__ uint32_t e4m3x2_b13_to_bf16x2(uint32_t w) {
   return bf16x2_mul(mag | sgn, kBf16x2Pow2_120);
 }
 
+// Decode to f16 times 2^-8, exactly: the 7 magnitude bits at f16 bits 13..7
+// and the sign at bit 15 give a half whose value is e4m3(c) * 2^-8 (f16 has a
+// 5-bit exponent with bias 15 against e4m3's 4 bits with bias 7); subnormal
+// codes land on f16 subnormals (M * 2^-17) with the same mantissa.  No
+// multiply is needed: the 2^8 is folded into the operand on the other side.
+// codes in bytes 0 and 2 of w (bytes 1 and 3 ignored)
+__device__ __forceinline__ uint32_t e4m3x2_b02_to_f16x2_lo8(uint32_t w) {
+  return ((w << 7) & 0x3F803F80u) | ((w << 8) & 0x80008000u);
+}
+
+// codes in bytes 1 and 3 of w (bytes 0 and 2 ignored)
+__device__ __forceinline__ uint32_t e4m3x2_b13_to_f16x2_lo8(uint32_t w) {
+  return ((w >> 1) & 0x3F803F80u) | (w & 0x80008000u);
+}
+
 // Decode one code to fp32 exactly: bits at binary32 positions give
 // e4m3(c) * 2^-120 (subnormal codes become binary32 subnormals), times 2^120.
 __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
@@ -90,6 +105,12 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
 
@@ -129,6 +150,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
                                                uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The same with f16 operands.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));

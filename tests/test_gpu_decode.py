@@ -206,3 +206,67 @@ def test_verify_full_size():
 
 def test_long_context_full_size():
     _full_size("longctx", [1], [6])
+
+
+def _constructed_cache(L, bs, k_code_fn, v_code_fn, ks_fn, vs_fn):
+    """A cache written directly (codes and scales chosen by the test, not by
+    the quantiser): one request, one KV head, tokens in permuted blocks."""
+    lens = np.array([L], dtype=np.int32)
+    bt, nblk = workloads.block_tables(lens, bs, 123, spare_blocks=2)
+    S = nblk * bs
+    oc = oracle.empty_cache(S, 1, 128)
+    slots = workloads.token_slots(bt, 0, L, bs)
+    j = np.arange(L)[:, None]
+    d = np.arange(128)[None, :]
+    oc["k_codes"][slots, 0] = k_code_fn(j, d).astype(np.uint8)
+    oc["v_codes"][slots, 0] = v_code_fn(j, d).astype(np.uint8)
+    oc["k_scales"][slots, 0] = ks_fn(np.arange(L)).astype(np.float32)
+    oc["v_scales"][slots, 0] = vs_fn(np.arange(L)).astype(np.float32)
+    cache = kvq.Cache(*(torch.from_numpy(oc[n]).cuda() for n in
+                        ("k_codes", "v_codes", "k_scales", "v_scales")), bs)
+    return {"cache": cache, "ocache": oc, "bt": bt, "lens": lens, "S": S}
+
+
+def _no_nan(c):
+    c = np.where((c & 0x7F) == 0x7F, c & 0x80, c)
+    return c
+
+
+@pytest.mark.parametrize("vscale", [1000.0, 2.0 ** 110, 2.0 ** -100])
+def test_every_code_value_through_the_attention(vscale):
+    """Uniform attention (all K codes zero) over V rows built from chosen codes:
+    dims 0..7 hold the subnormal codes 0..7 in every token (so a flushed
+    subnormal would show), the rest cycle through every finite code; value
+    scales range over many binades around `vscale`."""
+    L, bs = 384, 16
+    built = _constructed_cache(
+        L, bs, lambda j, d: np.zeros((j.size, d.size)),
+        lambda j, d: np.where(d < 8, d + 0 * j, _no_nan((j * 7 + d * 3) % 256)),
+        lambda j: np.ones_like(j, dtype=np.float64),
+        lambda j: vscale * np.exp2((j % 9) - 4.0))
+    q = _queries(workloads.scaled(workloads.WORKLOADS["tiny"], num_q_heads=1,
+                                  num_kv_heads=1), 1, 1, 9)
+    for P in (0, 64):
+        out = gpu_decode(built, q, 1, 0.1, partition_tokens=P)
+        ref, _ = oracle_decode(built, q, 1, 1, 0.1)
+        g = out.float().cpu().numpy().astype(np.float64)
+        rel = np.abs(g - ref) / np.abs(ref).max()
+        assert rel.max() < 5e-3, (P, rel.max())
+        # the subnormal-code dims: mean of d * 2^-9 * v_scale over tokens
+        assert np.allclose(g[0, 0, 1:8], ref[0, 0, 1:8], rtol=8e-3, atol=0)
+
+
+def test_scores_with_extreme_key_scales():
+    """Key scales spanning 2^-60..2^60 with chosen codes: the score column
+    scaling happens in fp32 after the code dot."""
+    L, bs = 200, 16
+    built = _constructed_cache(
+        L, bs, lambda j, d: _no_nan((j * 5 + d * 11) % 256),
+        lambda j, d: _no_nan((j * 3 + d * 7 + 1) % 256),
+        lambda j: np.exp2((j % 13) * 10.0 - 60.0) * 1e-3,
+        lambda j: np.exp2((j % 5) - 2.0))
+    q = _queries(workloads.scaled(workloads.WORKLOADS["tiny"], num_q_heads=1,
+                                  num_kv_heads=1), 1, 1, 10)
+    out = gpu_decode(built, q, 1, 1.0 / np.sqrt(128))
+    ref, _ = oracle_decode(built, q, 1, 1, 1.0 / np.sqrt(128))
+    assert_attention_close(out, ref, "extreme key scales")
