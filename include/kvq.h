@@ -201,6 +201,32 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
                                     void *out, void *workspace, size_t workspace_bytes,
                                     kvq_stream_t stream);
 
+/* kvq_paged_decode for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for code that must not or
+ * cannot call cudaMalloc where it decodes (inside an allocator or memory-pool
+ * callback that must not re-enter the allocator, a plugin handed only its
+ * input and output buffers, a runtime that fixes its device memory budget at
+ * start-up).  Arguments and results are those of kvq_paged_decode without the
+ * workspace: the split-K scratch is a fixed 16 MiB array inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *  - A shape whose kvq_paged_decode_workspace_size exceeds 16 MiB (16777216
+ *    bytes) is refused with KVQ_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current) and caches it; make that first call
+ *    before any stream capture on the device.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs to start at zero: every byte the combine reads is
+ *    written by the same call's first launch.  Calls that overlap on the GPU
+ *    (on different streams, or from several host threads) race on the array
+ *    and give wrong results; order them on one stream or with events. */
+kvq_status kvq_paged_decode_noalloc(const kvq_cache *cache, const void *q,
+                                    int32_t num_requests, int32_t rows_per_request,
+                                    int32_t num_q_heads, const int32_t *block_tables,
+                                    int32_t max_blocks_per_req, const int32_t *context_lens,
+                                    int32_t max_context_len, float sm_scale,
+                                    int32_t partition_tokens, void *out, int32_t *err_flags,
+                                    kvq_stream_t stream);
+
 /* Dequantise whole rows back to real values: out = fl32(e4m3(c) * scale), one
  * IEEE multiply, or that value rounded once more to bf16 (nearest-even).
  * sglang-jax #1776 "feat(dsa): implement fp8 KV cache (e4m3) with a bf16
