@@ -47,9 +47,11 @@
 // reads 16 consecutive code bytes per token.  Shared-memory code rows are
 // stored with their 16-byte chunks XOR-swizzled by (token & 7), which keeps
 // both read patterns free of bank conflicts.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -66,12 +68,27 @@ constexpr int kGroupRows = 32;
 constexpr float kLazyRescale = 8.0f;   // rescale only when the max grows by > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct StageBuf {
-  uint8_t k[kStageTok * kHeadDim];
-  uint8_t v[kStageTok * kHeadDim];
-  float ks[kStageTok];
-  float vs[kStageTok];
-};
+// Shared memory, from a 1024-byte aligned base (the TMA 128-byte swizzle
+// pattern repeats every 1024 bytes):
+//   K code stages  kStages x 64 rows x 128 B   (row = one token of one head)
+//   V code stages  kStages x 64 rows x 128 B
+//   K, V scales    kStages x 64 fp32 each
+//   Q fragments    MT x 8 x 32 uint4
+//   block ids      kMaxPages int32          (TMA staging only)
+//   mbarriers      kStages x 8 B            (TMA staging only)
+// Within a code row the 16-byte chunk c of token row t sits at chunk c ^ (t & 7).
+constexpr int kCodeStage = kStageTok * kHeadDim;                 // 8 KiB
+constexpr int kOffK = 0;
+constexpr int kOffV = kStages * kCodeStage;
+constexpr int kOffKs = 2 * kStages * kCodeStage;
+constexpr int kOffVs = kOffKs + kStages * kStageTok * 4;
+constexpr int kOffQ = kOffVs + kStages * kStageTok * 4;
+constexpr int kMaxPages = 1024;
+constexpr int kMinTmaBlock = 8;    // a page box of >= 8 rows keeps 1024-byte alignment
+
+__host__ __device__ constexpr int off_bt(int mt) { return kOffQ + mt * 8 * 32 * 16; }
+__host__ __device__ constexpr int off_mbar(int mt) { return off_bt(mt) + kMaxPages * 4; }
+__host__ __device__ constexpr int smem_bytes(int mt) { return off_mbar(mt) + kStages * 8 + 1024; }
 
 struct AttnParams {
   const uint8_t *k_codes;
@@ -117,9 +134,11 @@ __device__ __forceinline__ int clamp_context(const AttnParams &p, int r, bool re
 }
 
 // Issue the cp.async copies of one 64-token stage (tokens [tok0, tok0+64) of
-// the request; those at or past t_end are zero-filled).
-__device__ __forceinline__ void issue_stage(const AttnParams &p, StageBuf &sb, int r, int h,
-                                            int tok0, int t_end, int tid) {
+// the request; those at or past t_end are zero-filled).  Used when the block
+// size is below kMinTmaBlock.
+__device__ __forceinline__ void issue_stage_cp(const AttnParams &p, uint8_t *kdst,
+                                               uint8_t *vdst, float *ksd, float *vsd, int r,
+                                               int h, int tok0, int t_end, int tid) {
   const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks;
   const int bs_mask = (1 << p.log2_bs) - 1;
   // code rows: 128 rows (64 K then 64 V) x 8 chunks of 16 bytes; thread tid
@@ -145,7 +164,7 @@ __device__ __forceinline__ void issue_stage(const AttnParams &p, StageBuf &sb, i
         atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
       }
     }
-    uint8_t *dst = (is_v ? sb.v : sb.k) + tl * kHeadDim + ((chunk ^ (tl & 7)) << 4);
+    uint8_t *dst = (is_v ? vdst : kdst) + tl * kHeadDim + ((chunk ^ (tl & 7)) << 4);
     cp_async_16(dst, src, nbytes);
   }
   // scales: thread tid copies token tid%64's K (tid < 64) or V scale
@@ -164,16 +183,72 @@ __device__ __forceinline__ void issue_stage(const AttnParams &p, StageBuf &sb, i
         nbytes = 4;
       }
     }
-    cp_async_4((is_v ? sb.vs : sb.ks) + tl, src, nbytes);
+    cp_async_4((is_v ? vsd : ksd) + tl, src, nbytes);
   }
 }
 
-template <int MT>
+// Issue one 64-token stage with TMA: thread 0 copies each page's 128-byte code
+// rows of KV head h (a box of min(bs, 64) rows) for K and for V, completing on
+// the stage's mbarrier; every thread copies one scale with cp.async.  Block
+// ids come from the partition's copy in shared memory (bt_s, first page
+// page0).  Pages at or past t_end, or with an out-of-range block id, are not
+// copied; their scales are zero-filled so the compute stays finite.
+__device__ __forceinline__ void issue_stage_tma(const AttnParams &p, const void *tmap_k,
+                                                const void *tmap_v, uint32_t kdst,
+                                                uint32_t vdst, float *ksd, float *vsd,
+                                                uint32_t bar, const int32_t *bt_s, int page0,
+                                                int h, int tok0, int t_end, int tid) {
+  const int bs_mask = (1 << p.log2_bs) - 1;
+  if (tid == 0) {
+    const int rows = p.log2_bs >= 6 ? kStageTok : (1 << p.log2_bs);
+    uint32_t bytes = 0;
+    bool bad = false;
+    fence_proxy_async_smem();   // earlier generic reads of this buffer come first
+    for (int i = 0; i < kStageTok / rows; ++i) {
+      const int j = tok0 + i * rows;
+      if (j >= t_end) break;
+      const int64_t blk = bt_s[(j >> p.log2_bs) - page0];
+      if (blk < 0 || blk >= p.num_blocks) {
+        bad = true;
+        continue;
+      }
+      const int z = static_cast<int>((blk << p.log2_bs) + (j & bs_mask));
+      tma_load_3d(kdst + i * rows * kHeadDim, tmap_k, 0, h, z, bar);
+      tma_load_3d(vdst + i * rows * kHeadDim, tmap_v, 0, h, z, bar);
+      bytes += 2u * rows * kHeadDim;
+    }
+    if (bad && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
+    mbar_arrive_expect_tx(bar, bytes);
+  }
+  {
+    const int tl = tid & (kStageTok - 1);
+    const bool is_v = tid >= kStageTok;
+    const int j = tok0 + tl;
+    const float *base = is_v ? p.v_scales : p.k_scales;
+    const float *src = base;
+    uint32_t nbytes = 0;
+    if (j < t_end) {
+      const int64_t blk = bt_s[(j >> p.log2_bs) - page0];
+      if (blk >= 0 && blk < p.num_blocks) {
+        src = base + ((blk << p.log2_bs) + (j & bs_mask)) * p.H + h;
+        nbytes = 4;
+      }
+    }
+    cp_async_4((is_v ? vsd : ksd) + tl, src, nbytes);
+  }
+}
+
+template <int MT, bool kTma>
 __global__ void __launch_bounds__(kThreads, (MT == 1) ? 3 : 2)
-attn_partials_kernel(const AttnParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  StageBuf *stages = reinterpret_cast<StageBuf *>(smem);
-  uint4 *qfrag = reinterpret_cast<uint4 *>(smem + kStages * sizeof(StageBuf));
+attn_partials_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint4 *qfrag = reinterpret_cast<uint4 *>(smem + kOffQ);
+  int32_t *bt_s = reinterpret_cast<int32_t *>(smem + off_bt(MT));
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + off_mbar(MT));
+  __shared__ int timed_out;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -191,11 +266,40 @@ attn_partials_kernel(const AttnParams p) {
   const int t0 = part * p.part_tokens;
   const int t_end = min(L, t0 + p.part_tokens);
   const int n_stages = (t_end > t0) ? (t_end - t0 + kStageTok - 1) / kStageTok : 0;
+  const int page0 = t0 >> p.log2_bs;
+
+  auto kst = [&](int b) { return smem + kOffK + b * kCodeStage; };
+  auto vst = [&](int b) { return smem + kOffV + b * kCodeStage; };
+  auto kss = [&](int b) { return reinterpret_cast<float *>(smem + kOffKs) + b * kStageTok; };
+  auto vss = [&](int b) { return reinterpret_cast<float *>(smem + kOffVs) + b * kStageTok; };
+  auto issue = [&](int s) {
+    const int b = s % kStages;
+    if constexpr (kTma) {
+      issue_stage_tma(p, &tmap_k, &tmap_v, smem_addr(kst(b)), smem_addr(vst(b)), kss(b), vss(b),
+                      smem_addr(&mbar[b]), bt_s, page0, h, t0 + s * kStageTok, t_end, tid);
+    } else {
+      issue_stage_cp(p, kst(b), vst(b), kss(b), vss(b), r, h, t0 + s * kStageTok, t_end, tid);
+    }
+  };
+
+  if constexpr (kTma) {
+    // the partition's block ids, once; then the barriers
+    const int n_pages = (t_end > t0) ? ((t_end - 1) >> p.log2_bs) - page0 + 1 : 0;
+    const int32_t *bt = p.block_tables + static_cast<int64_t>(r) * p.max_blocks + page0;
+    for (int i = tid; i < n_pages; i += kThreads) bt_s[i] = bt[i];
+    if (tid == 0) {
+      timed_out = 0;
+      for (int b = 0; b < kStages; ++b) mbar_init(smem_addr(&mbar[b]), 1);
+      fence_mbarrier_init();
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+  }
 
   // Start the pipeline before anything else.
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
-    if (s < n_stages) issue_stage(p, stages[s], r, h, t0 + s * kStageTok, t_end, tid);
+    if (s < n_stages) issue(s);
     cp_async_commit();
   }
 
@@ -248,14 +352,34 @@ attn_partials_kernel(const AttnParams p) {
 
   for (int st = 0; st < n_stages; ++st) {
     cp_async_wait<kStages - 2>();
+    if constexpr (kTma) {
+      if (!mbar_wait_bounded(smem_addr(&mbar[st % kStages]), (st / kStages) & 1))
+        timed_out = 1;
+    }
     __syncthreads();
+    if constexpr (kTma) {
+      if (timed_out) {
+        // give up on this CTA: report, let the copies in flight land (bounded),
+        // and leave without writing outputs
+        if (tid == 0) {
+          if (p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
+          for (int s2 = st; s2 < min(n_stages, st + kStages - 1); ++s2)
+            mbar_wait_bounded(smem_addr(&mbar[s2 % kStages]), (s2 / kStages) & 1);
+        }
+        cp_async_wait<0>();
+        return;
+      }
+    }
     {
       const int nxt = st + kStages - 1;
-      if (nxt < n_stages)
-        issue_stage(p, stages[nxt % kStages], r, h, t0 + nxt * kStageTok, t_end, tid);
+      if (nxt < n_stages) issue(nxt);
       cp_async_commit();
     }
-    const StageBuf &sb = stages[st % kStages];
+    const int sbuf = st % kStages;
+    const uint8_t *sb_k = kst(sbuf);
+    const uint8_t *sb_v = vst(sbuf);
+    const float *sb_ks = kss(sbuf);
+    const float *sb_vs = vss(sbuf);
     const int tb = warp * 16;                         // this warp's 16 tokens
     const int jbase = t0 + st * kStageTok + tb;       // request position of token tb
 
@@ -271,7 +395,7 @@ attn_partials_kernel(const AttnParams p) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int tl = tb + nt * 8 + g4;
-      const uint8_t *row = sb.k + tl * kHeadDim;
+      const uint8_t *row = sb_k + tl * kHeadDim;
       const uint4 k0 = lds128(row + (((2 * c4) ^ (tl & 7)) << 4));
       const uint4 k1 = lds128(row + (((2 * c4 + 1) ^ (tl & 7)) << 4));
       kw[nt][0] = k0.x; kw[nt][1] = k0.y; kw[nt][2] = k0.z; kw[nt][3] = k0.w;
@@ -299,8 +423,8 @@ attn_partials_kernel(const AttnParams p) {
     float vmax = 0.0f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const float2 kk = *reinterpret_cast<const float2 *>(sb.ks + tb + nt * 8 + 2 * c4);
-      const float2 vv = *reinterpret_cast<const float2 *>(sb.vs + tb + nt * 8 + 2 * c4);
+      const float2 kk = *reinterpret_cast<const float2 *>(sb_ks + tb + nt * 8 + 2 * c4);
+      const float2 vv = *reinterpret_cast<const float2 *>(sb_vs + tb + nt * 8 + 2 * c4);
       ksc[nt][0] = kk.x * p.qk_scale;
       ksc[nt][1] = kk.y * p.qk_scale;
       vsc[nt][0] = vv.x;
@@ -399,10 +523,10 @@ attn_partials_kernel(const AttnParams p) {
     uint4 va, vb, vc, vd;
     {
       const int t_a = tb + 2 * c4, t_b = t_a + 1, t_c = t_a + 8, t_d = t_a + 9;
-      va = lds128(sb.v + t_a * kHeadDim + ((g4 ^ (t_a & 7)) << 4));
-      vb = lds128(sb.v + t_b * kHeadDim + ((g4 ^ (t_b & 7)) << 4));
-      vc = lds128(sb.v + t_c * kHeadDim + ((g4 ^ (t_c & 7)) << 4));
-      vd = lds128(sb.v + t_d * kHeadDim + ((g4 ^ (t_d & 7)) << 4));
+      va = lds128(sb_v + t_a * kHeadDim + ((g4 ^ (t_a & 7)) << 4));
+      vb = lds128(sb_v + t_b * kHeadDim + ((g4 ^ (t_b & 7)) << 4));
+      vc = lds128(sb_v + t_c * kHeadDim + ((g4 ^ (t_c & 7)) << 4));
+      vd = lds128(sb_v + t_d * kHeadDim + ((g4 ^ (t_d & 7)) << 4));
     }
     const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
     const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
@@ -589,17 +713,52 @@ attn_combine_kernel(const CombineParams p) {
   *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
 }
 
-template <int MT>
-size_t partials_smem_bytes() {
-  return kStages * sizeof(StageBuf) + MT * 8 * 32 * sizeof(uint4);
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda); looked up once.
+EncodeTiledFn encode_tiled_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    f = reinterpret_cast<EncodeTiledFn>(ptr);
+    fn.store(f, std::memory_order_release);
+  }
+  return f;
 }
 
-template <int MT>
-cudaError_t launch_partials_mt(const AttnParams &p, dim3 grid, cudaStream_t stream) {
-  const size_t smem = partials_smem_bytes<MT>();
-  static_assert(sizeof(StageBuf) * kStages >=
-                    2 * kWarps * MT * 16 * sizeof(float) +
-                        (kWarps - 1) * MT * 16 * 32 * sizeof(float4),
+// A map over one code plane [num_slots, H, 128] uint8: boxes of `rows` slots of
+// one head, 128-byte swizzled in shared memory.
+bool encode_code_map(CUtensorMap *map, const uint8_t *codes, int64_t num_slots, int H, int rows) {
+  EncodeTiledFn f = encode_tiled_fn();
+  if (f == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(num_slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                 static_cast<cuuint64_t>(H) * kHeadDim};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(codes), dims, strides,
+           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MT, bool kTma>
+cudaError_t launch_partials_mt(const AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv,
+                               dim3 grid, cudaStream_t stream) {
+  constexpr int smem = smem_bytes(MT);
+  static_assert(kOffQ >= 2 * kWarps * MT * 16 * 4 + (kWarps - 1) * MT * 16 * 32 * 16,
                 "epilogue buffers must fit in the stage buffers");
   // the shared-memory opt-in is a per-device function attribute: set it once
   // per device (a host-side call, no stream work)
@@ -609,13 +768,12 @@ cudaError_t launch_partials_mt(const AttnParams &p, dim3 grid, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || !(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(attn_partials_kernel<MT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = cudaFuncSetAttribute(attn_partials_kernel<MT, kTma>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  attn_partials_kernel<MT><<<grid, kThreads, smem, stream>>>(p);
+  attn_partials_kernel<MT, kTma><<<grid, kThreads, smem, stream>>>(p, mk, mv);
   return cudaGetLastError();
 }
 
@@ -675,8 +833,25 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   if (s.num_partitions > 1)
     carve_workspace(workspace, rows_total, s.num_partitions, &p.o_part, &p.ml_part);
   dim3 grid(c.num_kv_heads * s.row_groups, s.num_partitions, s.num_requests);
-  if (s.rows <= 16) return launch_partials_mt<1>(p, grid, stream);
-  return launch_partials_mt<2>(p, grid, stream);
+  // TMA staging needs page boxes of >= 8 rows (1024-byte aligned swizzle
+  // atoms), a partition's block ids in shared memory and 32-bit slot
+  // coordinates; other shapes stage with cp.async
+  CUtensorMap mk, mv;
+  const int rows = s.log2_block >= 6 ? kStageTok : (1 << s.log2_block);
+  const int64_t pages = static_cast<int64_t>(s.partition_tokens) / rows + 1;
+  const bool tma = (1 << s.log2_block) >= kMinTmaBlock && pages <= kMaxPages &&
+                   c.num_slots > 0 && c.num_slots < (int64_t(1) << 31) &&
+                   encode_code_map(&mk, c.k_codes, c.num_slots, c.num_kv_heads, rows) &&
+                   encode_code_map(&mv, c.v_codes, c.num_slots, c.num_kv_heads, rows);
+  if (!tma) {
+    memset(&mk, 0, sizeof(mk));
+    memset(&mv, 0, sizeof(mv));
+  }
+  if (s.rows <= 16)
+    return tma ? launch_partials_mt<1, true>(p, mk, mv, grid, stream)
+               : launch_partials_mt<1, false>(p, mk, mv, grid, stream);
+  return tma ? launch_partials_mt<2, true>(p, mk, mv, grid, stream)
+             : launch_partials_mt<2, false>(p, mk, mv, grid, stream);
 }
 
 cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,

@@ -76,6 +76,8 @@ typedef enum kvq_status {
 #define KVQ_ERRF_BLOCK_RANGE 2           /* block id outside [0, num_slots/block_size) */
 #define KVQ_ERRF_CONTEXT_RANGE 4         /* context length < 0, > max_context_len or
                                             > max_blocks_per_req * block_size          */
+#define KVQ_ERRF_WAIT_TIMEOUT 8          /* a bounded in-kernel wait for an async copy
+                                            gave up; that CTA's outputs are not written */
 
 /* The cache: codes and scales always travel together (ATOM PR #2655,
  * "Motivation": a restore that drops the scale planes decodes rows under the

@@ -56,6 +56,9 @@ def test_decode_batch_scaled(partition_tokens):
     (1, 8, 8, 16),     # MHA
     (4, 128, 8, 64),   # 64 rows: two row groups
     (3, 12, 4, 32),    # 9 rows, odd group
+    (1, 32, 8, 4),     # block size 4: cp.async staging
+    (2, 16, 4, 8),     # block size 8: smallest TMA page box
+    (4, 64, 8, 128),   # block larger than a 64-token stage
 ])
 @pytest.mark.parametrize("partition_tokens", [0, 128])
 def test_verify_shapes(R, Hq, H, bs, partition_tokens):
