@@ -19,9 +19,9 @@
 // cp.async pipeline of 64-token stages (16 tokens per warp per stage); each
 // token's 128-byte code rows are found through the block table.  Per 16-token
 // chunk a warp:
-//   1. decodes the K codes exactly to bf16 in registers (bit placement + one
-//      exact bf16 multiply) straight into mma B fragments, and runs S = Q K^T
-//      with m16n8k16 bf16 MMAs (fp32 accumulate);
+//   1. runs S = Q K^T on the FP8 tensor cores (m16n8k32 e4m3, fp32
+//      accumulate) with the K code bytes themselves as B fragments -- no
+//      decode -- against Q split exactly into two e4m3 pieces per element;
 //   2. multiplies each score column by its key scale and sm_scale*log2(e),
 //      masks causally (row i sees tokens j < L - R + 1 + i), and updates a
 //      running max per row, rescaling the accumulators only when the max grows
@@ -39,10 +39,10 @@
 // partial is stored and the combine kernel merges the partitions (log-sum-exp
 // weights).
 //
-// The contraction index of Q K^T is permuted so that each lane's B fragment
-// comes from 4 consecutive code bytes of one token: in k-step s, the lane with
-// c = lane % 4 feeds dims 32c + 4s + {0, 2 | 1, 3} as k = {2c, 2c+1 | 2c+8,
-// 2c+9}; Q's A fragments use the same map.  For P V the output columns are
+// The contraction index of Q K^T is permuted so that each lane's B fragments
+// are two words of its token's code row: in k32-step s2, the lane with
+// c = lane % 4 feeds dims 32c + 8 s2 + 0..3 as k = 4c..4c+3 and dims
+// 32c + 8 s2 + 4..7 as k = 4c+16..4c+19; Q's A fragments use the same map.  For P V the output columns are
 // permuted instead: n-tile i, column u stands for dim 16u + i, so each lane
 // reads 16 consecutive code bytes per token.  Shared-memory code rows are
 // stored with their 16-byte chunks XOR-swizzled by (token & 7), which keeps
@@ -76,6 +76,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 //   Q fragments    MT x 8 x 32 uint4
 //   block ids      kMaxPages int32          (TMA staging only)
 //   mbarriers      kStages x 8 B            (TMA staging only)
+//   row exponents  32 fp32                  (2^e_m of each query row)
 // Within a code row the 16-byte chunk c of token row t sits at chunk c ^ (t & 7).
 constexpr int kCodeStage = kStageTok * kHeadDim;                 // 8 KiB
 constexpr int kOffK = 0;
@@ -88,7 +89,8 @@ constexpr int kMinTmaBlock = 8;    // a page box of >= 8 rows keeps 1024-byte al
 
 __host__ __device__ constexpr int off_bt(int mt) { return kOffQ + mt * 8 * 32 * 16; }
 __host__ __device__ constexpr int off_mbar(int mt) { return off_bt(mt) + kMaxPages * 4; }
-__host__ __device__ constexpr int smem_bytes(int mt) { return off_mbar(mt) + kStages * 8 + 1024; }
+__host__ __device__ constexpr int off_rowexp(int mt) { return off_mbar(mt) + kStages * 8; }
+__host__ __device__ constexpr int smem_bytes(int mt) { return off_rowexp(mt) + 32 * 4 + 1024; }
 
 struct AttnParams {
   const uint8_t *k_codes;
@@ -303,29 +305,83 @@ attn_partials_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tma
     cp_async_commit();
   }
 
-  // Q fragments, in the permuted contraction order, stored per lane.
-  for (int idx = warp; idx < MT * 8; idx += kWarps) {
-    const int mt = idx >> 3, s = idx & 7;
-    uint2 qa = make_uint2(0u, 0u), qb = make_uint2(0u, 0u);
-    const int ma = row_base + mt * 16 + g4, mb = ma + 8;
-    const int d0 = 32 * c4 + 4 * s;
-    if (ma < p.M) {
-      const int i = ma / p.G, gq = ma - i * p.G;
-      const int64_t qrow = (static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq;
-      qa = *reinterpret_cast<const uint2 *>(p.q + qrow * kHeadDim + d0);
+  // Q as two e4m3 pieces per element, stored per lane in fragment order.
+  // Row m is scaled by 2^-e_m (e_m from the row's largest |q|, so the largest
+  // scaled element lies in [128, 256)); p1 = e4m3_rne(x) and p2 = e4m3_rne(x -
+  // p1).  x has 8 significant bits and p1 keeps the top 4, so the residual is a
+  // multiple of x's ulp no larger than 8 ulps and p2 holds it exactly unless it
+  // falls below e4m3's 2^-9 grid (elements under 2^-17 of the row's largest).
+  // q = 2^e_m * (p1 + p2); 2^e_m multiplies the row's scores later.
+  float *row_exp = reinterpret_cast<float *>(smem + off_rowexp(MT));   // [MT * 16]
+  const int rows_here = min(MT * 16, p.M - row_base);
+  auto q_row = [&](int m) {   // m < rows_here
+    const int mg = row_base + m;
+    const int i = mg / p.G, gq = mg - i * p.G;
+    return p.q + ((static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq) * kHeadDim;
+  };
+  // (a) row exponents
+  for (int m = warp; m < MT * 16; m += kWarps) {
+    float amax = 0.0f;
+    if (m < rows_here) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(q_row(m) + 4 * lane);
+      amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                   fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
     }
-    if (mb < p.M) {
-      const int i = mb / p.G, gq = mb - i * p.G;
-      const int64_t qrow = (static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq;
-      qb = *reinterpret_cast<const uint2 *>(p.q + qrow * kHeadDim + d0);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    if (lane == 0) {
+      // exponent e with 2^(e+7) <= amax < 2^(e+8), clamped so 2^-e is normal
+      const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+      int e = (ex == 0) ? -126 : ex - 127 - 7;
+      e = e < -126 ? -126 : (e > 126 ? 126 : e);
+      row_exp[m] = (amax == 0.0f) ? 0.0f : __int_as_float((127 + e) << 23);   // 2^e
     }
-    uint4 f;
-    f.x = prmt(qa.x, qa.y, 0x5410u);   // (dim d0,   dim d0+2) -> k = 2c, 2c+1
-    f.y = prmt(qb.x, qb.y, 0x5410u);
-    f.z = prmt(qa.x, qa.y, 0x7632u);   // (dim d0+1, dim d0+3) -> k = 2c+8, 2c+9
-    f.w = prmt(qb.x, qb.y, 0x7632u);
-    qfrag[idx * 32 + lane] = f;
   }
+  __syncthreads();
+  // (b) the two pieces of every element of the real rows, in row order, into
+  // the last stage's code buffers (not written by any copy before the main
+  // loop starts): plane 1 in the K buffer, plane 2 in the V buffer
+  uint8_t *plane1 = kst(kStages - 1);
+  uint8_t *plane2 = vst(kStages - 1);
+  for (int idx = tid; idx < MT * 16 * 32; idx += kThreads) {
+    const int m = idx >> 5, qd = idx & 31;
+    uint32_t c1w = 0u, c2w = 0u;
+    if (m < rows_here && row_exp[m] != 0.0f) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(q_row(m) + 4 * qd);
+      const float inv = __int_as_float((254u << 23) - __float_as_uint(row_exp[m]));   // 2^-e
+      const float xs[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = xs[e] * inv;
+        const uint32_t c1 = e4m3_round(x, x);
+        const float res = x - e4m3_to_f32(c1);
+        c1w |= c1 << (8 * e);
+        c2w |= e4m3_round(res, res) << (8 * e);
+      }
+    }
+    *reinterpret_cast<uint32_t *>(plane1 + m * kHeadDim + 4 * qd) = c1w;
+    *reinterpret_cast<uint32_t *>(plane2 + m * kHeadDim + 4 * qd) = c2w;
+  }
+  __syncthreads();
+  // (c) fragments: dims 32c + 8 s2 + 0..3 are k = 4c..4c+3, dims + 4..7 are
+  // k = 4c+16..4c+19
+  for (int idx = warp; idx < MT * 4; idx += kWarps) {
+    const int mt = idx >> 2, s2 = idx & 3;
+    const int off = 32 * c4 + 8 * s2;
+#pragma unroll
+    for (int pc = 0; pc < 2; ++pc) {
+      const uint8_t *pl = pc ? plane2 : plane1;
+      const uint2 a = *reinterpret_cast<const uint2 *>(pl + (mt * 16 + g4) * kHeadDim + off);
+      const uint2 b = *reinterpret_cast<const uint2 *>(pl + (mt * 16 + g4 + 8) * kHeadDim + off);
+      qfrag[((mt * 4 + s2) * 2 + pc) * 32 + lane] = make_uint4(a.x, b.x, a.y, b.y);
+    }
+  }
+  float rowf[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) rowf[mt][hf] = row_exp[mt * 16 + g4 + 8 * hf];
 
   // Per-thread rows: (mt, half) -> M row row_base + mt*16 + g4 + 8*half.
   int vis[MT][2];
@@ -402,19 +458,20 @@ attn_partials_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tma
       kw[nt][4] = k1.x; kw[nt][5] = k1.y; kw[nt][6] = k1.z; kw[nt][7] = k1.w;
     }
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t a[MT][4];
+    for (int s2 = 0; s2 < 4; ++s2) {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const uint4 f = qfrag[(mt * 8 + s) * 32 + lane];
-        a[mt][0] = f.x; a[mt][1] = f.y; a[mt][2] = f.z; a[mt][3] = f.w;
-      }
+      for (int pc = 0; pc < 2; ++pc) {
+        uint32_t a[MT][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t b0 = e4m3x2_b02_to_bf16x2(kw[nt][s]);
-        const uint32_t b1 = e4m3x2_b13_to_bf16x2(kw[nt][s]);
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint4 f = qfrag[((mt * 4 + s2) * 2 + pc) * 32 + lane];
+          a[mt][0] = f.x; a[mt][1] = f.y; a[mt][2] = f.z; a[mt][3] = f.w;
+        }
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(sacc[mt][nt], a[mt], b0, b1);
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            mma_e4m3_16832(sacc[mt][nt], a[mt], kw[nt][2 * s2], kw[nt][2 * s2 + 1]);
       }
     }
 
@@ -467,7 +524,7 @@ attn_partials_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tma
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int j = jbase + nt * 8 + 2 * c4 + e;
-            float x = sacc[mt][nt][2 * hf + e] * ksc[nt][e];
+            float x = sacc[mt][nt][2 * hf + e] * ksc[nt][e] * rowf[mt][hf];
             x = (j < vis[mt][hf]) ? x : -INFINITY;
             sacc[mt][nt][2 * hf + e] = x;
             mx = fmaxf(mx, x);
@@ -713,47 +770,6 @@ attn_combine_kernel(const CombineParams p) {
   *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against libcuda); looked up once.
-EncodeTiledFn encode_tiled_fn() {
-  static std::atomic<EncodeTiledFn> fn{nullptr};
-  EncodeTiledFn f = fn.load(std::memory_order_acquire);
-  if (f == nullptr) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || ptr == nullptr) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    f = reinterpret_cast<EncodeTiledFn>(ptr);
-    fn.store(f, std::memory_order_release);
-  }
-  return f;
-}
-
-// A map over one code plane [num_slots, H, 128] uint8: boxes of `rows` slots of
-// one head, 128-byte swizzled in shared memory.
-bool encode_code_map(CUtensorMap *map, const uint8_t *codes, int64_t num_slots, int H, int rows) {
-  EncodeTiledFn f = encode_tiled_fn();
-  if (f == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
-                              static_cast<cuuint64_t>(num_slots)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
-                                 static_cast<cuuint64_t>(H) * kHeadDim};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, static_cast<cuuint32_t>(rows)};
-  const cuuint32_t estride[3] = {1u, 1u, 1u};
-  return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(codes), dims, strides,
-           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int MT, bool kTma>
 cudaError_t launch_partials_mt(const AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv,
                                dim3 grid, cudaStream_t stream) {
@@ -790,6 +806,51 @@ int32_t context_cap(const AttnShape &s) {
 }
 
 }  // namespace
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda); looked up once.
+EncodeTiledFn encode_tiled_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    f = reinterpret_cast<EncodeTiledFn>(ptr);
+    fn.store(f, std::memory_order_release);
+  }
+  return f;
+}
+
+}  // namespace
+
+// A map over one code plane [num_slots, H, 128] uint8: boxes of `rows` slots of
+// one head, 128-byte swizzled in shared memory.
+bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_slots, int H,
+                            int rows) {
+  EncodeTiledFn f = encode_tiled_fn();
+  if (f == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(num_slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                 static_cast<cuuint64_t>(H) * kHeadDim};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1u, static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(codes), dims, strides,
+           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 size_t attn_workspace_bytes(int64_t rows_total, int32_t num_partitions) {
   if (num_partitions <= 1) return 0;
@@ -832,6 +893,9 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   p.ml_part = nullptr;
   if (s.num_partitions > 1)
     carve_workspace(workspace, rows_total, s.num_partitions, &p.o_part, &p.ml_part);
+  if (attn_skinny_supported(c, s))
+    return launch_attn_partials_skinny(c, s, q, block_tables, context_lens, sm_scale, out,
+                                       p.o_part, p.ml_part, err_flags, stream);
   dim3 grid(c.num_kv_heads * s.row_groups, s.num_partitions, s.num_requests);
   // TMA staging needs page boxes of >= 8 rows (1024-byte aligned swizzle
   // atoms), a partition's block ids in shared memory and 32-bit slot
@@ -841,8 +905,8 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   const int64_t pages = static_cast<int64_t>(s.partition_tokens) / rows + 1;
   const bool tma = (1 << s.log2_block) >= kMinTmaBlock && pages <= kMaxPages &&
                    c.num_slots > 0 && c.num_slots < (int64_t(1) << 31) &&
-                   encode_code_map(&mk, c.k_codes, c.num_slots, c.num_kv_heads, rows) &&
-                   encode_code_map(&mv, c.v_codes, c.num_slots, c.num_kv_heads, rows);
+                   encode_code_tensor_map(&mk, c.k_codes, c.num_slots, c.num_kv_heads, rows) &&
+                   encode_code_tensor_map(&mv, c.v_codes, c.num_slots, c.num_kv_heads, rows);
   if (!tma) {
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));

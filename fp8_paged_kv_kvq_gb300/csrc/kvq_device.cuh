@@ -28,6 +28,21 @@ constexpr int kHeadDim = 128;
 //    2^-9 (the ulp of 2^14) with the hardware's nearest-even addition, and the
 //    bit-pattern difference to 2^14 is the subnormal mantissa 0..8 (8 lands
 //    exactly on the smallest normal code).
+// The rounding step alone: code of the finite value q (sign from `sgn`).
+__device__ __forceinline__ uint32_t e4m3_round(float q, float sgn) {
+  const uint32_t a = __float_as_uint(q) & 0x7FFFFFFFu;
+  const uint32_t sign = (__float_as_uint(sgn) >> 24) & 0x80u;
+  uint32_t mag;
+  if (a >= 0x43E00000u) {                       // >= 448
+    mag = 0x7Eu;
+  } else if (a >= 0x3C800000u) {                // >= 2^-6
+    mag = ((a + 0x7FFFFu + ((a >> 20) & 1u)) >> 20) - 0x3C0u;
+  } else {
+    mag = __float_as_uint(__fadd_rn(__uint_as_float(a), 16384.0f)) - 0x46800000u;
+  }
+  return mag | sign;
+}
+
 __device__ __forceinline__ uint32_t e4m3_encode_div(float x, float s) {
   const float q = __fdiv_rn(x, s);
   const uint32_t a = __float_as_uint(q) & 0x7FFFFFFFu;
@@ -212,6 +227,20 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
                                               uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A * B + D, 16x8x32, e4m3 operands (the cache's own code bytes), fp32
+// accumulate.  Each register holds four consecutive k of one row (A) or one
+// column (B):
+//   a0 = A[g][4c..4c+3], a1 = A[g+8][4c..4c+3], a2 = A[g][4c+16..4c+19],
+//   a3 = A[g+8][4c+16..4c+19];  b0 = B[4c..4c+3][g], b1 = B[4c+16..4c+19][g]
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));

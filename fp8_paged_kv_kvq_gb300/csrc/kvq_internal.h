@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "kvq.h"
@@ -45,6 +46,19 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
                                  const int32_t *block_tables, const int32_t *context_lens,
                                  float sm_scale, void *out, void *workspace,
                                  int32_t *err_flags, cudaStream_t stream);
+
+// Tensor map over one code plane [num_slots, H, 128] uint8: boxes of `rows`
+// slots of one head, 128-byte swizzled in shared memory.
+bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_slots, int H,
+                            int rows);
+
+// The partials kernel for at most 8 stacked rows per KV head (block size >= 8).
+bool attn_skinny_supported(const kvq_cache &c, const AttnShape &s);
+cudaError_t launch_attn_partials_skinny(const kvq_cache &c, const AttnShape &s, const void *q,
+                                        const int32_t *block_tables, const int32_t *context_lens,
+                                        float sm_scale, void *out, float *o_part,
+                                        float2 *ml_part, int32_t *err_flags,
+                                        cudaStream_t stream);
 
 cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,
                                 void *workspace, cudaStream_t stream);

@@ -158,7 +158,9 @@ def test_padding_out_of_range_and_guard_bands():
     slots[3] = -1          # padding: skipped silently
     slots[5] = S           # out of range: skipped and flagged
     slots[6] = S + 1000
-    slots[7:] = torch.tensor([7, 8, 9, 10, 11, 0, 1, 2, 4], dtype=torch.int64)
+    # the rest unique and in range (ids must be unique: two tokens writing one
+    # slot race); slot 3 is never written
+    slots[7:] = torch.tensor([7, 8, 9, 10, 11, 5, 6, -1, -1], dtype=torch.int64)
     guard = 4096
     sentinel = 0xA5
     big = torch.full((2 * guard + S * H * D,), sentinel, dtype=torch.uint8, device="cuda")
