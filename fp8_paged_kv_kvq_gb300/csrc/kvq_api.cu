@@ -158,7 +158,8 @@ kvq_status kvq_quantize_scatter(const kvq_cache *cache, const void *k, int64_t k
   if (!aligned(k, 16) || !aligned(v, 16) || (k_token_stride % 8) != 0 ||
       (v_token_stride % 8) != 0 || !aligned(slot_ids, 8) || !aligned(err_flags, 4))
     return KVQ_ERR_MISALIGNED;
-  if ((num_tokens + 7) / 8 > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
+  // rows (token, K/V, head) are numbered in 32 bits
+  if (num_tokens > (int64_t(1) << 31) / (2 * cache->num_kv_heads) - 32) return KVQ_ERR_UNSUPPORTED;
   return from_cuda(kvq::launch_quantize_scatter(*cache, k, k_token_stride, v, v_token_stride,
                                                 num_tokens, slot_ids, err_flags,
                                                 reinterpret_cast<cudaStream_t>(stream)));

@@ -732,11 +732,19 @@ struct CombineParams {
 
 constexpr int kCombineWarps = 4;
 
+// One CTA per output row.  Every thread reads one partition's (max, sum) for
+// the row max; then warp w folds partitions w, w+4, ... (4 dims per lane, all
+// loads of a warp independent of each other), and the four warps' partial
+// sums meet in shared memory.
 __global__ void __launch_bounds__(kCombineWarps * 32)
 attn_combine_kernel(const CombineParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
-  if (row >= p.rows_total) return;
+  __shared__ float red[kCombineWarps];
+  __shared__ float4 part_o[kCombineWarps - 1][32];
+  __shared__ float part_l[kCombineWarps];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int64_t row = blockIdx.x;
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
   int L = p.context_lens[r];
   L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
@@ -744,15 +752,18 @@ attn_combine_kernel(const CombineParams p) {
   if (n_parts <= 1) return;                       // written by the partials kernel
   const float2 *ml = p.ml_part + row * p.n_parts_max;
   float mx = -INFINITY;
-  for (int q = lane; q < n_parts; q += 32) mx = fmaxf(mx, ml[q].x);
+  for (int q = tid; q < n_parts; q += kCombineWarps * 32) mx = fmaxf(mx, ml[q].x);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.0f;
   if (mx != -INFINITY) {
     const float *op = p.o_part + row * p.n_parts_max * kHeadDim + 4 * lane;
-#pragma unroll 4
-    for (int q = 0; q < n_parts; ++q) {
+#pragma unroll 8
+    for (int q = warp; q < n_parts; q += kCombineWarps) {
       const float2 v = ml[q];
       const float w = ex2(v.x - mx);
       const float4 o = *reinterpret_cast<const float4 *>(op + static_cast<int64_t>(q) * kHeadDim);
@@ -763,6 +774,16 @@ attn_combine_kernel(const CombineParams p) {
       acc.w += w * o.w;
     }
   }
+  if (warp > 0) part_o[warp - 1][lane] = acc;
+  if (lane == 0) part_l[warp] = lsum;
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps - 1; ++w) {
+    const float4 v = part_o[w][lane];
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  lsum = part_l[0] + part_l[1] + part_l[2] + part_l[3];
   const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
   uint2 packed;
   packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -935,8 +956,7 @@ cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens,
   p.o_part = o_part;
   p.ml_part = ml_part;
   p.out = static_cast<uint16_t *>(out);
-  const int64_t blocks = (p.rows_total + kCombineWarps - 1) / kCombineWarps;
-  attn_combine_kernel<<<static_cast<unsigned>(blocks), kCombineWarps * 32, 0, stream>>>(p);
+  attn_combine_kernel<<<static_cast<unsigned>(p.rows_total), kCombineWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

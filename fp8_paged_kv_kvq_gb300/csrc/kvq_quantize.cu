@@ -9,12 +9,12 @@
 // graph.  The fix commit "give the V tensor its own row pitch in the fp8 KV
 // store": K and V each carry their own token pitch.
 //
-// Layout of the work: one warp per token; each 8-lane group owns one 128-
-// element row (16 elements, 32 bytes, per lane: two 16-byte loads), so a warp
-// covers four rows at a time and loops over the token's 2*H rows (K heads, then
-// V heads).  The row amax is an integer max over the bf16 magnitude bits
-// (order-preserving for finite values) reduced across the 8 lanes with
-// shuffles; the 16 codes of a lane leave as one 16-byte store, so a row's 128
+// Layout of the work: each 8-lane group owns one 128-element row (16 elements,
+// 32 bytes, per lane: two 16-byte loads) of the grid-wide list of rows ordered
+// (token, K heads then V heads), so a token's K rows are one contiguous read
+// and every row costs one memory round trip.  The row amax is an integer max
+// over the bf16 magnitude bits (order-preserving for finite values) reduced
+// across the 8 lanes with shuffles; the 16 codes of a lane leave as one 16-byte store, so a row's 128
 // codes are one contiguous 128-byte line.
 #include <cuda_runtime.h>
 
@@ -68,44 +68,44 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 quantize_scatter_kernel(const QuantParams p) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & 7;                       // lane within the row's 8 lanes
-  const int grp = lane >> 3;                      // which of the warp's 4 rows
   const unsigned gmask = 0xFFu << (lane & 24);
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
-  if (t >= p.num_tokens) return;
-  const int64_t slot = p.slot_ids[t];
-  if (slot < 0) return;
+  // row id over (token, K/V, head); a whole 8-lane group shares it
+  const uint32_t rid = blockIdx.x * (kQuantWarps * 4) + (threadIdx.x >> 3);   // < 2^31
   const int H = p.num_kv_heads;
+  const uint32_t t32 = rid / static_cast<uint32_t>(2 * H);
+  if (t32 >= p.num_tokens) return;
+  const int64_t t = t32;
+  const int rem = static_cast<int>(rid - t32 * static_cast<uint32_t>(2 * H));
+  const bool is_v = rem >= H;
+  const int h = is_v ? rem - H : rem;
+  // the row's loads and the slot id load are independent: issue all first
+  const uint16_t *src = (is_v ? p.v + t * p.v_stride : p.k + t * p.k_stride) + h * kHeadDim + sub * 16;
+  const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
+  const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 8));
+  const int64_t slot = __ldg(p.slot_ids + t);
+  if (slot < 0) return;
   if (slot >= p.num_slots) {
-    if (lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
+    if (sub == 0 && rem == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
     return;
   }
-  const uint16_t *krow = p.k + t * p.k_stride;
-  const uint16_t *vrow = p.v + t * p.v_stride;
-  for (int r = grp; r < 2 * H; r += 4) {
-    const bool is_v = r >= H;
-    const int h = is_v ? r - H : r;
-    const uint16_t *src = (is_v ? vrow : krow) + h * kHeadDim + sub * 16;
-    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
-    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 8));
-    uint32_t m = max_mag_bf16x2(a, b);
-    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 1));
-    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 2));
-    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 4));
-    const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
-    uint4 out = make_uint4(0u, 0u, 0u, 0u);
-    float s = 0.0f;
-    if (amax != 0.0f) {
-      s = __fdiv_rn(amax, 448.0f);
-      out.x = encode4(a.x, a.y, s);
-      out.y = encode4(a.z, a.w, s);
-      out.z = encode4(b.x, b.y, s);
-      out.w = encode4(b.z, b.w, s);
-    }
-    const int64_t row = slot * H + h;
-    uint8_t *dst = (is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * 16;
-    *reinterpret_cast<uint4 *>(dst) = out;
-    if (sub == 0) (is_v ? p.v_scales : p.k_scales)[row] = s;
+  uint32_t m = max_mag_bf16x2(a, b);
+  m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 1));
+  m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 2));
+  m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 4));
+  const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+  uint4 out = make_uint4(0u, 0u, 0u, 0u);
+  float s = 0.0f;
+  if (amax != 0.0f) {
+    s = __fdiv_rn(amax, 448.0f);
+    out.x = encode4(a.x, a.y, s);
+    out.y = encode4(a.z, a.w, s);
+    out.z = encode4(b.x, b.y, s);
+    out.w = encode4(b.z, b.w, s);
   }
+  const int64_t row = slot * H + h;
+  uint8_t *dst = (is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * 16;
+  *reinterpret_cast<uint4 *>(dst) = out;
+  if (sub == 0) (is_v ? p.v_scales : p.k_scales)[row] = s;
 }
 
 // ---------------------------------------------------------------------------
@@ -194,7 +194,8 @@ cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k
   p.num_slots = c.num_slots;
   p.num_kv_heads = c.num_kv_heads;
   p.err_flags = err_flags;
-  const int64_t blocks = (num_tokens + kQuantWarps - 1) / kQuantWarps;
+  const int64_t rows = num_tokens * 2 * c.num_kv_heads;
+  const int64_t blocks = (rows + kQuantWarps * 4 - 1) / (kQuantWarps * 4);
   quantize_scatter_kernel<<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
