@@ -4,9 +4,10 @@
 // The E4M3 ("fn") format: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
 // bits; E = 0 is subnormal (M * 2^-9); S.1111.111 is NaN; the largest finite
 // magnitude is 448.  FreeToken PR #354 "feat(kvcache): store the KV cache as
-// fp8 e4m3 codes", PR description: codes live in a plain uint8 buffer and are
-// encoded / decoded in software with bit operations, never through an fp8
-// type, so every card holds the same bytes.
+// fp8 e4m3 codes", PR description: codes live in a plain uint8 buffer, so
+// every card holds the same bytes.  Decoding is done here with bit placement;
+// the store encodes with the hardware e4m3x2 conversion, whose rounding
+// (nearest-even, saturating) is the one defined below, bit for bit.
 #pragma once
 
 #include <cstdint>
@@ -43,19 +44,33 @@ __device__ __forceinline__ uint32_t e4m3_round(float q, float sgn) {
   return mag | sign;
 }
 
-__device__ __forceinline__ uint32_t e4m3_encode_div(float x, float s) {
-  const float q = __fdiv_rn(x, s);
-  const uint32_t a = __float_as_uint(q) & 0x7FFFFFFFu;
-  const uint32_t sign = (__float_as_uint(x) >> 24) & 0x80u;
-  uint32_t mag;
-  if (a >= 0x43E00000u) {                       // >= 448
-    mag = 0x7Eu;
-  } else if (a >= 0x3C800000u) {                // >= 2^-6
-    mag = ((a + 0x7FFFFu + ((a >> 20) & 1u)) >> 20) - 0x3C0u;
-  } else {
-    mag = __float_as_uint(__fadd_rn(__uint_as_float(a), 16384.0f)) - 0x46800000u;
-  }
-  return mag | sign;
+// Two codes at once through the hardware conversion (round-to-nearest-even,
+// saturating to +-448, the sign of zero kept): the low byte is lo's code.  It
+// rounds a binary32 value exactly as e4m3_round does.
+__device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Correctly rounded x / s given y = fl32(1 / s), by Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = x*y is within
+// 1.5 ulp of x / s; one step q1 = q0 + (x - s*q0)*y brings it within 1 ulp,
+// and with the remainder exact (an FMA) a second step rounds correctly.  Valid
+// while no step underflows: for s >= 2^-90 every quotient >= 2^-11 (the only
+// ones whose e4m3 code is not 0) has an exact remainder; smaller quotients
+// stay below 2^-10 and encode to zero either way.  The sign is copied from x
+// so that -0 stays -0.
+constexpr float kMarksteinMinScale = 0x1p-90f;
+
+__device__ __forceinline__ float div_markstein(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r0 = __fmaf_rn(-q0, s, x);
+  const float q1 = __fmaf_rn(r0, y, q0);
+  const float r1 = __fmaf_rn(-q1, s, x);
+  const float q2 = __fmaf_rn(r1, y, q1);
+  return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
 }
 
 // ---------------------------------------------------------------------------

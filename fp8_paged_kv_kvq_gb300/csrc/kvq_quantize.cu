@@ -55,13 +55,26 @@ __device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
   return r;
 }
 
-// Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3).
-__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s) {
-  const uint32_t c0 = e4m3_encode_div(bf16_lo(w0), s);
-  const uint32_t c1 = e4m3_encode_div(bf16_hi(w0), s);
-  const uint32_t c2 = e4m3_encode_div(bf16_lo(w1), s);
-  const uint32_t c3 = e4m3_encode_div(bf16_hi(w1), s);
-  return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+// Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3):
+// fl32(x / s) then e4m3 round-to-nearest-even.  kFast divides through the
+// row's reciprocal y with Markstein's correction (exact for s >= 2^-90);
+// otherwise plain IEEE division.
+template <bool kFast>
+__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s, float y) {
+  float q[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) q[e] = kFast ? div_markstein(q[e], s, y) : __fdiv_rn(q[e], s);
+  return e4m3x2_rn(q[0], q[1]) | (e4m3x2_rn(q[2], q[3]) << 16);
+}
+
+template <bool kFast>
+__device__ __forceinline__ uint4 encode16(uint4 a, uint4 b, float s, float y) {
+  uint4 out;
+  out.x = encode4<kFast>(a.x, a.y, s, y);
+  out.y = encode4<kFast>(a.z, a.w, s, y);
+  out.z = encode4<kFast>(b.x, b.y, s, y);
+  out.w = encode4<kFast>(b.z, b.w, s, y);
+  return out;
 }
 
 __global__ void __launch_bounds__(kQuantWarps * 32)
@@ -97,10 +110,10 @@ quantize_scatter_kernel(const QuantParams p) {
   float s = 0.0f;
   if (amax != 0.0f) {
     s = __fdiv_rn(amax, 448.0f);
-    out.x = encode4(a.x, a.y, s);
-    out.y = encode4(a.z, a.w, s);
-    out.z = encode4(b.x, b.y, s);
-    out.w = encode4(b.z, b.w, s);
+    if (s >= kMarksteinMinScale)
+      out = encode16<true>(a, b, s, __frcp_rn(s));
+    else
+      out = encode16<false>(a, b, s, 0.0f);
   }
   const int64_t row = slot * H + h;
   uint8_t *dst = (is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * 16;

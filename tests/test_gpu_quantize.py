@@ -94,6 +94,44 @@ def test_tiny_and_zero_rows():
     assert torch.all(cache.k_scales[16:18] == 0) and torch.all(cache.k_codes[16:18] == 0)
 
 
+def _rows_near_midpoints(rows: int, seed: int) -> torch.Tensor:
+    """bf16 rows [rows, 128] whose amax spans every bf16 binade (subnormal
+    amax included, so scales from fp32 subnormals up to 2^119) and whose other
+    elements are the bf16 values nearest to (e4m3 midpoint) * scale, +-2 bf16
+    ulps: their quotients x / scale fall within an ulp of an e4m3 rounding
+    boundary far more often than random data, exercising the division and the
+    nearest-even rounding at the cases where either could go wrong."""
+    rng = np.random.default_rng(seed)
+    expo = rng.integers(0, 255, rows, dtype=np.uint32)
+    mant = rng.integers(0, 128, rows, dtype=np.uint32)
+    mant[expo == 0] |= 1                                   # no zero amax here
+    amax_bits = ((expo << 7) | mant).astype(np.uint16)
+    amax = (amax_bits.astype(np.uint32) << 16).view(np.float32)
+    s = (amax / np.float32(448.0)).astype(np.float32)      # IEEE binary32
+    grid = oracle.e4m3_decode(np.arange(0x7F))
+    mids = np.concatenate([(grid[:-1] + grid[1:]) / 2, grid])
+    pick = mids[rng.integers(0, mids.size, (rows, 127))]
+    target = torch.from_numpy(pick * s.astype(np.float64)[:, None])
+    xb = B(target.to(torch.bfloat16)).astype(np.int32)
+    xb = np.clip(xb + rng.integers(-2, 3, xb.shape), 0, None)
+    xb = np.minimum(xb, amax_bits.astype(np.int32)[:, None])  # |x| <= amax
+    sign = rng.integers(0, 2, xb.shape).astype(np.int32) << 15
+    body = (xb | sign).astype(np.uint16)
+    full = np.concatenate([amax_bits[:, None], body], axis=1)
+    perm = rng.permuted(np.tile(np.arange(128), (rows, 1)), axis=1)
+    full = np.take_along_axis(full, perm, axis=1)
+    return torch.from_numpy(full.view(np.int16)).view(torch.bfloat16)
+
+
+def test_rounding_boundaries_every_scale_bit_exact():
+    T, H = 8192, 2
+    k = _rows_near_midpoints(T * H, 21).view(T, H, 128)
+    v = _rows_near_midpoints(T * H, 22).view(T, H, 128)
+    slots = torch.arange(T, dtype=torch.int64)
+    cache, oc, _, _ = _quantize_both(k.cuda(), v.cuda(), slots, T, H)
+    assert_cache_equal(cache, oc)
+
+
 @pytest.mark.parametrize("swap", [False, True])
 def test_strided_pitch_regression(swap):
     """FreeToken PR #354 review: K a view of the qkv slice (pitch 1152), V dense
