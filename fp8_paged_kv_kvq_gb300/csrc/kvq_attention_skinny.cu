@@ -11,10 +11,10 @@
 //    8-wide N side.  QK^T runs on FP8 tensor cores (m16n8k32 e4m3) with the K
 //    code bytes as the A operand as they sit in shared memory -- no decode --
 //    and Q as two exact e4m3 pieces per element (B operand, registers).  PV runs
-//    on f16 tensor cores (m16n8k16) with V codes decoded exactly to f16 * 2^-8
-//    and P'' = p * v_scale * 2^-E (E a running power-of-two bound on the value
-//    scales) moved from the S^T fragment layout to the B layout with four
-//    shuffles per 16 tokens.
+//    on f16 tensor cores (m16n8k16) with V codes converted exactly to f16 by
+//    the hardware e4m3x2 conversion and P'' = p * v_scale * 2^-E <= 1 (E a
+//    running power-of-two bound on the value scales) moved from the S^T
+//    fragment layout to the B layout with four shuffles per 16 tokens.
 //  * Every warp streams its own 16-token chunks (chunks w, w+4, ... of the
 //    partition) through its own 3-deep TMA pipeline: one box of min(bs, 16) code
 //    rows per page for K and for V, completing on the warp's own mbarrier, and
@@ -78,7 +78,7 @@ struct SkParams {
 
 __device__ __forceinline__ float sk_ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -257,12 +257,12 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
   for (int u = 0; u < n_my; ++u) {
     const int sb = u % kSkStages;
     cp_async_wait<kSkStages - 1>();
-    const bool ok = mbar_wait_bounded(smem_addr(&bar[sb]), (u / kSkStages) & 1);
+    const bool ok = mbar_wait_sleep_bounded(smem_addr(&bar[sb]), (u / kSkStages) & 1);
     if (__any_sync(0xFFFFFFFFu, !ok)) {
       // give up on this warp's chunks: let its copies in flight land (bounded)
       timed_out = true;
       for (int v = u; v < min(n_my, u + kSkStages); ++v)
-        mbar_wait_bounded(smem_addr(&bar[v % kSkStages]), (v / kSkStages) & 1);
+        mbar_wait_sleep_bounded(smem_addr(&bar[v % kSkStages]), (v / kSkStages) & 1);
       break;
     }
     __syncwarp();
@@ -389,14 +389,28 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
       wb[0] = Bv.x; wb[1] = Bv.y; wb[2] = Bv.z; wb[3] = Bv.w;
       wc[0] = C.x; wc[1] = C.y; wc[2] = C.z; wc[3] = C.w;
       wd[0] = Dv.x; wd[1] = Dv.y; wd[2] = Dv.z; wd[3] = Dv.w;
+      // tokens at or past the context end hold whatever the slot or the stage
+      // buffer held (a NaN code would poison the PV product even times p = 0)
+      const int lim = L - j0;
+      if (lim < kChunk) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          wa[e] = (ta < lim) ? wa[e] : 0u;
+          wb[e] = (tb < lim) ? wb[e] : 0u;
+          wc[e] = (tc < lim) ? wc[e] : 0u;
+          wd[e] = (td < lim) ? wd[e] : 0u;
+        }
+      }
     }
+    // m-tile i: dims 16g + 2i (a0, a2) and 16g + 2i + 1 (a1, a3) -- byte pairs
+    // (token 2c, 2c+1) and (2c+8, 2c+9) of code bytes 2i, 2i+1
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+      const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
       const uint32_t xab = prmt(wa[i >> 1], wb[i >> 1], sel);
       const uint32_t xcd = prmt(wc[i >> 1], wd[i >> 1], sel);
-      const uint32_t a[4] = {e4m3x2_b02_to_f16x2_lo8(xab), e4m3x2_b13_to_f16x2_lo8(xab),
-                             e4m3x2_b02_to_f16x2_lo8(xcd), e4m3x2_b13_to_f16x2_lo8(xcd)};
+      const uint32_t a[4] = {e4m3x2_to_f16x2(xab), e4m3x2_to_f16x2(xab >> 16),
+                             e4m3x2_to_f16x2(xcd), e4m3x2_to_f16x2(xcd >> 16)};
       mma_f16_16816(o[i], a, pb0, pb1);
     }
     __syncwarp();
@@ -446,15 +460,13 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       parked[((warp - 1) * 8 + i) * 32 + lane] =
-          make_float4(o[i][0] * 256.0f * frow[0], o[i][1] * 256.0f * frow[1],
-                      o[i][2] * 256.0f * frow[0], o[i][3] * 256.0f * frow[1]);
+          make_float4(o[i][0] * frow[0], o[i][1] * frow[1], o[i][2] * frow[0], o[i][3] * frow[1]);
   }
   __syncthreads();
   if (warp != 0) return;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float4 acc = make_float4(o[i][0] * 256.0f * frow[0], o[i][1] * 256.0f * frow[1],
-                             o[i][2] * 256.0f * frow[0], o[i][3] * 256.0f * frow[1]);
+    float4 acc = make_float4(o[i][0] * frow[0], o[i][1] * frow[1], o[i][2] * frow[0], o[i][3] * frow[1]);
 #pragma unroll
     for (int w = 0; w < kSkWarps - 1; ++w) {
       const float4 v = parked[(w * 8 + i) * 32 + lane];

@@ -104,6 +104,14 @@ __device__ __forceinline__ uint32_t e4m3x2_b13_to_bf16x2(uint32_t w) {
   return bf16x2_mul(mag | sgn, kBf16x2Pow2_120);
 }
 
+// Two codes (low byte -> low half) to their exact f16 values through the
+// hardware conversion; every e4m3 value, subnormals included, is an f16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w16) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<uint16_t>(w16)));
+  return d;
+}
+
 // Decode to f16 times 2^-8, exactly: the 7 magnitude bits at f16 bits 13..7
 // and the sign at bit 15 give a half whose value is e4m3(c) * 2^-8 (f16 has a
 // 5-bit exponent with bias 15 against e4m3's 4 bits with bias 7); subnormal
@@ -200,6 +208,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
   for (int i = 0; i < (1 << 20); ++i)
     if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// As mbar_try_wait, but a thread whose phase is not complete may sleep until it
+// completes or about `ns` nanoseconds pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
+  return ok != 0;
+}
+
+// Bounded sleeping wait: at most 2^19 tries of at most 2 us each (about a
+// second); returns false if the phase never completed.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < (1 << 19); ++i)
+    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
   return false;
 }
 
