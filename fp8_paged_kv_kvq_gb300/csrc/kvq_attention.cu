@@ -262,6 +262,8 @@ attn_partials_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tma
   const int part = blockIdx.y;
   const int r = blockIdx.z;
 
+  grid_dependency_wait();
+  allow_dependents_launch();
   const int L = clamp_context(p, r, part == 0 && tid == 0 && blockIdx.x == 0);
   const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
   if (part >= (n_parts > 0 ? n_parts : 1)) return;
@@ -746,6 +748,8 @@ attn_combine_kernel(const CombineParams p) {
   const int warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
+  grid_dependency_wait();
+  allow_dependents_launch();
   int L = p.context_lens[r];
   L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
   const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
@@ -810,8 +814,7 @@ cudaError_t launch_partials_mt(const AttnParams &p, const CUtensorMap &mk, const
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  attn_partials_kernel<MT, kTma><<<grid, kThreads, smem, stream>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_overlapped(attn_partials_kernel<MT, kTma>, grid, dim3(kThreads), smem, stream, p, mk, mv);
 }
 
 void carve_workspace(void *ws, int64_t rows_total, int32_t n_parts, float **o_part,
@@ -956,8 +959,8 @@ cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens,
   p.o_part = o_part;
   p.ml_part = ml_part;
   p.out = static_cast<uint16_t *>(out);
-  attn_combine_kernel<<<static_cast<unsigned>(p.rows_total), kCombineWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(attn_combine_kernel, dim3(static_cast<unsigned>(p.rows_total)),
+                           dim3(kCombineWarps * 32), 0, stream, p);
 }
 
 }  // namespace kvq

@@ -16,7 +16,7 @@
 //    running power-of-two bound on the value scales) moved from the S^T
 //    fragment layout to the B layout with four shuffles per 16 tokens.
 //  * Every warp streams its own 16-token chunks (chunks w, w+4, ... of the
-//    partition) through its own 3-deep TMA pipeline: one box of min(bs, 16) code
+//    partition) through its own 2-deep TMA pipeline: one box of min(bs, 16) code
 //    rows per page for K and for V, completing on the warp's own mbarrier, and
 //    the chunk's 32 scales by cp.async.  The main loop has no CTA-wide barrier.
 //  * The four warps' (max, denominator, O) merge in shared memory at the end.
@@ -36,7 +36,7 @@ namespace {
 constexpr int kSkWarps = 4;
 constexpr int kSkThreads = kSkWarps * 32;
 constexpr int kChunk = 16;                           // tokens per warp step
-constexpr int kSkStages = 3;                         // chunks in flight per warp
+constexpr int kSkStages = 2;                         // chunks in flight per warp
 constexpr int kChunkBytes = kChunk * kHeadDim;       // 2 KiB of codes per K or V
 constexpr int kSkMaxPages = 1024;
 constexpr int kSkRows = 8;                           // query rows per KV head handled
@@ -44,7 +44,7 @@ constexpr float kSkLazyRescale = 8.0f;
 constexpr float kSkLog2e = 1.4426950408889634f;
 
 // shared memory from a 1024-byte aligned base
-constexpr int kWarpCode = kSkStages * 2 * kChunkBytes;                    // 12 KiB
+constexpr int kWarpCode = kSkStages * 2 * kChunkBytes;                    // 8 KiB
 constexpr int kOffSkScales = kSkWarps * kWarpCode;                         // [w][stage][32] f32
 constexpr int kOffSkBar = kOffSkScales + kSkWarps * kSkStages * 2 * kChunk * 4;
 constexpr int kOffSkQ = kOffSkBar + kSkWarps * kSkStages * 8;             // 2 planes x 8 x 128 B
@@ -97,6 +97,8 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int part = blockIdx.y;
   const int r = blockIdx.z;
 
+  grid_dependency_wait();
+  allow_dependents_launch();
   int L = p.context_lens[r];
   if (L < 0 || L > p.ctx_limit) {
     if (part == 0 && tid == 0 && h == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
@@ -558,8 +560,7 @@ cudaError_t launch_attn_partials_skinny(const kvq_cache &c, const AttnShape &s, 
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   dim3 grid(c.num_kv_heads, s.num_partitions, s.num_requests);
-  attn_skinny_kernel<<<grid, kSkThreads, kSkSmem, stream>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_overlapped(attn_skinny_kernel, grid, dim3(kSkThreads), kSkSmem, stream, p, mk, mv);
 }
 
 }  // namespace kvq

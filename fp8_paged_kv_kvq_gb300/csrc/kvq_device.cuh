@@ -231,6 +231,19 @@ __device__ __forceinline__ bool mbar_wait_sleep_bounded(uint32_t bar, uint32_t p
   return false;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream drains:
+// grid_dependency_wait() returns once that kernel has completed and its writes
+// are visible, so it comes before the first read of anything a previous kernel
+// may have written; allow_dependents_launch() lets the next kernel start early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // Makes barrier initialisation visible to the copy engine.
 __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");

@@ -11,6 +11,26 @@
 
 namespace kvq {
 
+// Launches `kernel` with programmatic stream serialization, so that its launch
+// overlaps the drain of the previous kernel in the stream; every kernel
+// launched this way calls grid_dependency_wait() before its first read of
+// global memory another kernel may have written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // The only head_dim the kernels implement; the ABI refuses any other.
 constexpr int32_t kHeadDimAbi = 128;
 

@@ -86,6 +86,8 @@ quantize_scatter_kernel(const QuantParams p) {
   const uint32_t rid = blockIdx.x * (kQuantWarps * 4) + (threadIdx.x >> 3);   // < 2^31
   const int H = p.num_kv_heads;
   const uint32_t t32 = rid / static_cast<uint32_t>(2 * H);
+  grid_dependency_wait();
+  allow_dependents_launch();
   if (t32 >= p.num_tokens) return;
   const int64_t t = t32;
   const int rem = static_cast<int>(rid - t32 * static_cast<uint32_t>(2 * H));
@@ -143,6 +145,8 @@ dequant_rows_kernel(const DequantParams p) {
   const int sub = lane & 7;
   const int grp = lane >> 3;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  grid_dependency_wait();
+  allow_dependents_launch();
   if (i >= p.n) return;
   const int64_t slot = p.slot_ids[i];
   const bool valid = slot >= 0 && slot < p.num_slots;
@@ -209,8 +213,8 @@ cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k
   p.err_flags = err_flags;
   const int64_t rows = num_tokens * 2 * c.num_kv_heads;
   const int64_t blocks = (rows + kQuantWarps * 4 - 1) / (kQuantWarps * 4);
-  quantize_scatter_kernel<<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks)),
+                           dim3(kQuantWarps * 32), 0, stream, p);
 }
 
 cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int64_t n,
@@ -230,8 +234,8 @@ cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int
   p.out_v = out_v;
   p.err_flags = err_flags;
   const int64_t blocks = (n + kQuantWarps - 1) / kQuantWarps;
-  dequant_rows_kernel<<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(dequant_rows_kernel, dim3(static_cast<unsigned>(blocks)),
+                           dim3(kQuantWarps * 32), 0, stream, p);
 }
 
 }  // namespace kvq
