@@ -23,6 +23,7 @@ reported baseline and not the target.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import ctypes
 import hashlib
 import json
@@ -69,6 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--workload", choices=list(DESCRIPTIONS), default="decode")
     ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--requests", type=int, default=0,
+                    help="only the first N requests of the workload (a smaller case of the "
+                         "same shape, for profiler captures); 0 = all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--profile", action="store_true",
@@ -205,12 +209,14 @@ def ncu_traffic(kernel: str, workload: str, source: str):
 # workload on the device
 
 class DeviceWorkload:
-    def __init__(self, name: str, device, partition_tokens: int = 0):
+    def __init__(self, name: str, device, partition_tokens: int = 0, requests: int = 0):
         import fp8_paged_kv_kvq_gb300 as kvq
         self.kvq = kvq
         self.lib = kvq.load()
         self.name = name
         self.w = w = workloads.WORKLOADS[name]
+        if 0 < requests < w.num_requests:
+            self.w = w = dataclasses.replace(w, num_requests=requests)
         self.device = device
         self.stream = torch.cuda.Stream(device)
         H, D = w.num_kv_heads, w.head_dim
@@ -293,6 +299,15 @@ class DeviceWorkload:
                         P(self.cl_d.data_ptr()), self.max_ctx, self.P, P(self.out.data_ptr()),
                         P(self.ws.data_ptr()), self.ws.numel(), sp)
 
+    def partials_kernel(self):
+        """(kernel, source) the library launches for this shape's partials:
+        the skinny kernel for at most 8 stacked rows per KV head and pages of
+        at least 8 tokens, else the general one."""
+        w = self.w
+        if w.rows_per_request * w.group <= 8 and w.block_size >= 8:
+            return "attn_skinny_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_skinny.cu"
+        return "attn_partials_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention.cu"
+
     # the launches of a step, through the C ABI
     def quantize(self):
         st = self.lib.kvq_quantize_scatter(*self._q_args)
@@ -347,7 +362,7 @@ def run_kvq(args, rank, local, world):
     torch.cuda.set_device(dev)
     K = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
     W = max(3, args.warmup if args.warmup is not None else min(50, max(3, K // 10)))
-    wl = DeviceWorkload(args.workload, dev, args.partition_tokens)
+    wl = DeviceWorkload(args.workload, dev, args.partition_tokens, args.requests)
     with torch.cuda.stream(wl.stream):
         return _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W)
 
@@ -396,10 +411,12 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
     if sampler:
         sampler.start()
     wall0 = time.perf_counter()
+    torch.cuda.nvtx.range_push("kvq_timed")      # lets a profiler select the timed launches
     for i in range(K):
         if flush is not None:
             flush.fill_((i + 7) & 0xFF)
         step(evs[i])
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     wall1 = time.perf_counter()
     if sampler:
@@ -435,8 +452,9 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
                    "per-step CUDA-event intervals") if flush is not None else
                   "not flushed (profile mode)",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "storage": "e4m3 codes (uint8) + fp32 row scales; bf16 q/out; bf16 tensor-core "
-                       "operands, fp32 accumulate",
+            "storage": "e4m3 codes (uint8) + fp32 row scales; bf16 q/out; QK^T on e4m3 tensor "
+                       "cores (q as two exact e4m3 pieces), PV on f16 tensor cores, fp32 "
+                       "accumulate",
         },
         "pct_of_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
@@ -452,7 +470,7 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         res["kernels_us"]["paged_decode_partials"] = round(1e3 * sum(st_p) / K, 3)
         res["kernels_us"]["paged_decode_combine"] = round(1e3 * sum(st_c) / K, 3)
         dom_ms, dom_bytes = sum(st_p) / K, wl.attn_bytes()
-        dom_name, dom_src = "attn_partials_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention.cu"
+        dom_name, dom_src = wl.partials_kernel()
     else:
         dom_ms, dom_bytes = sum(st_q) / K, wl.store_bytes()
         dom_name, dom_src = "quantize_scatter_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_quantize.cu"
@@ -556,9 +574,9 @@ def run_e2e_store(wl: DeviceWorkload, dev, K, world):
 class OracleSampler:
     """Units of the workload the oracle processes one at a time: a unit is one
     (request, query row, query head) attention output plus the quantize-scatter
-    of that request's new rows for the head's KV head.  The oracle's cache for a
-    (request, KV head) is built from the same seeded bf16 rows, untimed, the
-    first time a unit needs it."""
+    of that request's new rows for the head's KV head.  The oracle's cache of a
+    request is built from the same seeded bf16 recipe, untimed, the first time a
+    unit needs it."""
 
     def __init__(self, name: str, token_cap: int | None = None):
         import oracle
@@ -573,32 +591,32 @@ class OracleSampler:
         self.S = nblk * w.block_size
         self.q = workloads.bf16_bits(workloads.queries(w, device="cpu"))
         self._key = None
-        # (request, KV head)-major order: consecutive units share one oracle cache
+        # request-major order: consecutive units share one oracle cache
         self.units = [(r, i, h * w.group + g) for r in range(w.num_requests)
                       for h in range(w.num_kv_heads) for g in range(w.group)
                       for i in range(w.rows_per_request)]
         self.pos = 0
 
-    def _head_cache(self, r, h):
-        if self._key != (r, h):
+    def _request_cache(self, r):
+        """The oracle's cache of request r, all KV heads, its L tokens at slots
+        0..L-1 (an identity block table), built untimed on first use."""
+        if self._key != r:
             w = self.w
-            L, D = int(self.lens[r]), w.head_dim
-            oc = self.oracle.empty_cache(self.S, 1, D)
-            ct = workloads.chunk_tokens(w)
-            dev = "cuda" if torch.cuda.is_available() and L > 8192 else "cpu"
-            ks, vs = [], []
-            for c0 in range(0, L, ct):
-                n = min(ct, L - c0)
-                k, v = workloads.request_kv(w, r, c0, n, device=dev)
-                ks.append(workloads.bf16_bits(k[:, h:h + 1]))
-                vs.append(workloads.bf16_bits(v[:, h:h + 1]))
-            kb, vb = np.concatenate(ks).reshape(-1), np.concatenate(vs).reshape(-1)
-            slots = workloads.token_slots(self.bt, r, L, w.block_size)
-            self.oracle.quantize_scatter(kb, D, vb, D, L, 1, D, slots, oc)
+            L, D, H = int(self.lens[r]), w.head_dim, w.num_kv_heads
+            nb = (L + w.block_size - 1) // w.block_size
+            self._oc = None
+            oc = self.oracle.empty_cache(nb * w.block_size, H, D)
+            dev = "cuda" if torch.cuda.is_available() else "cpu"
+            k, v = workloads.request_kv(w, r, 0, L, device=dev)
+            kb, vb = workloads.bf16_bits(k).reshape(-1), workloads.bf16_bits(v).reshape(-1)
+            self.oracle.quantize_scatter(kb, H * D, vb, H * D, L, H, D,
+                                         np.arange(L, dtype=np.int64), oc)
             R = w.rows_per_request
-            self._new = (kb[(L - R) * D:], vb[(L - R) * D:])
+            self._new = (kb[(L - R) * H * D:].reshape(R, H, D),
+                         vb[(L - R) * H * D:].reshape(R, H, D))
+            self._bt = np.arange(nb, dtype=np.int32)[None, :]
             self._oc = oc
-            self._key = (r, h)
+            self._key = r
         return self._oc
 
     def next_unit(self):
@@ -608,22 +626,23 @@ class OracleSampler:
         r, i, hq = self.units[self.pos % len(self.units)]
         self.pos += 1
         h = hq // w.group
-        oc = self._head_cache(r, h)
+        oc = self._request_cache(r)
         L = int(self.lens[r])
         Lc = L if self.token_cap is None else min(L, self.token_cap)
-        R, D, G = w.rows_per_request, w.head_dim, w.group
+        R, D, Hq = w.rows_per_request, w.head_dim, w.num_q_heads
         lens = np.array([Lc], dtype=np.int32)
-        qrow = self.q[r * R:(r + 1) * R, h * G:(h + 1) * G]
-        bt = self.bt[r:r + 1]
-        kb, vb = self._new
+        qreq = self.q[r * R:(r + 1) * R]
+        bt = self._bt
+        kb = np.ascontiguousarray(self._new[0][:, h]).reshape(-1)
+        vb = np.ascontiguousarray(self._new[1][:, h]).reshape(-1)
         scratch = self.oracle.empty_cache(R, 1, D)
         new_slots = np.arange(R, dtype=np.int64)
         ora = self.oracle
-        unit = np.array([[0, i, hq - h * G]], dtype=np.int32)
+        unit = np.array([[0, i, hq]], dtype=np.int32)
 
         def run():
             ora.quantize_scatter(kb, D, vb, D, R, 1, D, new_slots, scratch)
-            ora.paged_attention_units(oc, qrow, 1, R, G, bt, lens, w.block_size, w.sm_scale,
+            ora.paged_attention_units(oc, qreq, 1, R, Hq, bt, lens, w.block_size, w.sm_scale,
                                       unit)
 
         H, Hq = w.num_kv_heads, w.num_q_heads
