@@ -876,6 +876,21 @@ bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A map over one scale plane [num_slots, H] fp32: boxes of 4 consecutive heads
+// x `rows` slots, unswizzled (16 bytes per slot row in shared memory).
+bool encode_scale_tensor_map(CUtensorMap *map, const float *scales, int64_t num_slots, int H,
+                             int rows) {
+  EncodeTiledFn f = encode_tiled_fn();
+  if (f == nullptr || H % 4 != 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_slots)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * sizeof(float)};
+  const cuuint32_t box[2] = {4u, static_cast<cuuint32_t>(rows)};
+  const cuuint32_t estride[2] = {1u, 1u};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(scales), dims, strides,
+           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t attn_workspace_bytes(int64_t rows_total, int32_t num_partitions) {
   if (num_partitions <= 1) return 0;
   const size_t o = static_cast<size_t>(rows_total) * num_partitions * kHeadDim * sizeof(float);
@@ -920,6 +935,9 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   if (attn_skinny_supported(c, s))
     return launch_attn_partials_skinny(c, s, q, block_tables, context_lens, sm_scale, out,
                                        p.o_part, p.ml_part, err_flags, stream);
+  if (attn_tc_supported(c, s))
+    return launch_attn_partials_tc(c, s, q, block_tables, context_lens, sm_scale, out,
+                                   p.o_part, p.ml_part, err_flags, stream);
   dim3 grid(c.num_kv_heads * s.row_groups, s.num_partitions, s.num_requests);
   // TMA staging needs page boxes of >= 8 rows (1024-byte aligned swizzle
   // atoms), a partition's block ids in shared memory and 32-bit slot

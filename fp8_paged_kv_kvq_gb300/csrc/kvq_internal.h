@@ -72,6 +72,18 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
 bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_slots, int H,
                             int rows);
 
+// Tensor map over one scale plane [num_slots, H] fp32: boxes of 4 heads x `rows`
+// slots (H a multiple of 4, the plane 16-byte aligned).
+bool encode_scale_tensor_map(CUtensorMap *map, const float *scales, int64_t num_slots, int H,
+                             int rows);
+
+// The tcgen05 partials kernel for 9..32 stacked rows per KV head.
+bool attn_tc_supported(const kvq_cache &c, const AttnShape &s);
+cudaError_t launch_attn_partials_tc(const kvq_cache &c, const AttnShape &s, const void *q,
+                                    const int32_t *block_tables, const int32_t *context_lens,
+                                    float sm_scale, void *out, float *o_part, float2 *ml_part,
+                                    int32_t *err_flags, cudaStream_t stream);
+
 // The partials kernel for at most 8 stacked rows per KV head (block size >= 8).
 bool attn_skinny_supported(const kvq_cache &c, const AttnShape &s);
 cudaError_t launch_attn_partials_skinny(const kvq_cache &c, const AttnShape &s, const void *q,
