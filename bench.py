@@ -302,10 +302,16 @@ class DeviceWorkload:
     def partials_kernel(self):
         """(kernel, source) the library launches for this shape's partials:
         the skinny kernel for at most 8 stacked rows per KV head and pages of
-        at least 8 tokens, else the general one."""
+        at least 8 tokens, the tcgen05 kernel for 9..32 rows (pages of 16..128
+        tokens, KV heads a multiple of 4, partitions a multiple of 128 tokens),
+        else the general one."""
         w = self.w
-        if w.rows_per_request * w.group <= 8 and w.block_size >= 8:
+        rows = w.rows_per_request * w.group
+        if rows <= 8 and w.block_size >= 8:
             return "attn_skinny_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_skinny.cu"
+        if (rows <= 32 and 16 <= w.block_size <= 128 and w.num_kv_heads % 4 == 0
+                and self.P % 128 == 0):
+            return "attn_tc_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_tc.cu"
         return "attn_partials_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention.cu"
 
     # the launches of a step, through the C ABI

@@ -70,7 +70,7 @@ int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t 
   const int64_t work = static_cast<int64_t>(num_requests > 0 ? num_requests : 1) *
                        (num_kv_heads > 0 ? num_kv_heads : 1) *
                        (max_context_len > 0 ? max_context_len : 1);
-  const int64_t target = work / (sms * 16);
+  const int64_t target = work / (sms * 8);
   int32_t p = 256;
   while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
   return p;

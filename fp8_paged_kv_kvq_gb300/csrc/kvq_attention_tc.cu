@@ -8,14 +8,15 @@
 // KV head are stacked into one tile).  Laid out for sm_103a:
 //
 //  * CTA = (KV head, partition, request), one per SM, 14 warps with fixed
-//    roles.  Warp 12 (one lane) streams 128-token stages through a 3-deep ring
+//    roles.  Warp 12 (one lane) streams 128-token stages through a 4-deep ring
 //    with TMA: per page one box of K codes, one of V codes (128-byte swizzled
 //    rows) and one of each scale plane.
 //  * Warp 13 (one lane) issues the MMAs.  S^T = K Q^T is one M=128 (tokens) x
-//    N=32 (rows) x K=128 product on e4m3 operands (kind::f8f6f4): the K code
-//    tile straight from shared memory as A (K-major), Q as two exact e4m3
-//    pieces per element as B, accumulated over both pieces into one of two
-//    TMEM score buffers.  O^T += V^T P^T is M=128 (dims) x N=32 x K=128
+//    N=64 x K=128 product on e4m3 operands (kind::f8f6f4): the K code tile
+//    straight from shared memory as A (K-major), and as B the two exact e4m3
+//    pieces of Q stacked as 64 rows (piece 1 of the 32 rows, then piece 2), so
+//    each K step is one instruction; the softmax adds the two column halves.
+//    (A tcgen05 MMA costs about the same for N = 32 as for N = 128.)  O^T += V^T P^T is M=128 (dims) x N=32 x K=128
 //    (tokens) on f16 operands (kind::f16), both MN-major from shared memory,
 //    accumulating in TMEM for the whole partition.
 //  * Warps 0-7 run the softmax, two per TMEM lane quarter: a thread owns one
@@ -51,7 +52,7 @@ namespace kvq {
 namespace {
 
 constexpr int kTcTok = 128;                  // tokens per stage (the QK MMA's M)
-constexpr int kTcStages = 3;                 // code ring depth
+constexpr int kTcStages = 4;                 // code ring depth
 constexpr int kTcRows = 32;                  // stacked query rows (the MMAs' N), padded
 constexpr int kTcSoftWarps = 8;             // softmax: two per TMEM lane quarter
 constexpr int kTcHalf = 16;                 // rows per softmax thread
@@ -60,9 +61,9 @@ constexpr int kTcWarpTma = kTcSoftWarps + kTcConvertWarps;
 constexpr int kTcWarpMma = kTcWarpTma + 1;
 constexpr int kTcThreads = (kTcWarpMma + 1) * 32;
 constexpr int kTcMaxPages = 512;             // block ids of one partition kept in smem
-constexpr int kTcTmemCols = 512;             // S buffers 0, 1 | O buffers 0..13
-constexpr int kColS = 0;
-constexpr int kColO = 64;
+constexpr int kTcTmemCols = 512;             // S buffers 0, 1 | O buffers 0..11
+constexpr int kColS = 0;                     // S^T buffer b: columns 64 b .. 64 b + 63
+constexpr int kColO = 128;
 constexpr int kTcOBufs = (kTcTmemCols - kColO) / kTcRows;
 constexpr float kTcLazy = 14.0f;             // log2 of the largest unnormalised p
 constexpr float kTcOvershoot = 4.0f;         // a moved reference sits this far above the max
@@ -74,7 +75,7 @@ constexpr int kPBytes = kTcTok * kTcRows * 2;              // f16 P^T operand
 constexpr int kQBytes = kTcRows * kHeadDim;                // one e4m3 piece of Q
 constexpr int kScBytes = kTcTok * 16;                      // [token][4 heads] f32
 constexpr int kOffVf = kTcStages * kCodeStage;
-constexpr int kOffP = kOffVf + 2 * kVfBytes;
+constexpr int kOffP = kOffVf + kVfBytes;
 constexpr int kOffQ = kOffP + 2 * kPBytes;
 constexpr int kOffSc = kOffQ + 2 * kQBytes;
 constexpr int kOffBt = kOffSc + kTcStages * 2 * kScBytes;
@@ -96,7 +97,7 @@ static_assert(kOffVf % 1024 == 0 && kOffP % 1024 == 0 && kOffQ % 1024 == 0 &&
               kOffSc % 1024 == 0, "operand buffers need 1024-byte alignment");
 static_assert(kTcSmem <= 227 * 1024, "shared memory budget");
 
-constexpr uint32_t kIdescQK = mma_idesc(kTcTok, kTcRows, false, false);
+constexpr uint32_t kIdescQK = mma_idesc(kTcTok, 2 * kTcRows, false, false);
 constexpr uint32_t kIdescPV = mma_idesc(kHeadDim, kTcRows, true, true);
 
 struct TcParams {
@@ -331,14 +332,11 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_kc,
           if (s >= 2 && !tc_wait(BAR(kBarSEmpty + sb), ((s >> 1) - 1) & 1, abort_s)) break;
           tc_fence_after();
           const uint64_t ad = smem_desc(kc0 + b * kCodeStage, 16, 1024, kSmemSwizzle128);
+          const uint64_t bd = smem_desc(q0, 16, 1024, kSmemSwizzle128);   // both pieces, 64 rows
 #pragma unroll
-          for (int pc = 0; pc < 2; ++pc) {
-            const uint64_t bd = smem_desc(q0 + pc * kQBytes, 16, 1024, kSmemSwizzle128);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)    // K steps of 32 bytes inside the row
-              tc_mma_e4m3(tmem + kColS + 32 * sb, ad + 2 * kk, bd + 2 * kk, kIdescQK,
-                          (pc | kk) != 0);
-          }
+          for (int kk = 0; kk < 4; ++kk)      // K steps of 32 bytes inside the row
+            tc_mma_e4m3(tmem + kColS + 2 * kTcRows * sb, ad + 2 * kk, bd + 2 * kk, kIdescQK,
+                        kk != 0);
           tc_commit(BAR(kBarSFull + sb));
           last_bar = BAR(kBarSFull + sb);
           last_par = (s >> 1) & 1;
@@ -349,7 +347,7 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_kc,
           if (!tc_wait(BAR(kBarPReady + ub), (u >> 1) & 1, abort_s)) break;
           tc_fence_after();
           const int obu = ob_s[ub];                // the O buffer this stage accumulates into
-          const uint64_t ad = smem_desc(vf0 + ub * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
+          const uint64_t ad = smem_desc(vf0, kVfBytes / 2, 1024, kSmemSwizzle128);
           const uint64_t bd = smem_desc(p0 + ub * kPBytes, kPBytes, 512, kSmemSwizzle64);
 #pragma unroll
           for (int kk = 0; kk < kTcTok / 16; ++kk)   // 16 tokens: 2 groups of 8 rows
@@ -377,11 +375,11 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_kc,
       const int b = s % kTcStages, sb = s & 1;
       const bool valid = t < t_end - (t0 + s * kTcTok);
       bool ok = tc_wait(BAR(kBarKvFull + b), (s / kTcStages) & 1, abort_s);
-      // the f16 buffer of stage s - 2 is free once its PV has completed
-      if (s >= 2) ok = tc_wait(BAR(kBarPvDone + sb), ((s - 2) >> 1) & 1, abort_s) && ok;
+      // the f16 buffer is free once the PV of the previous stage has completed
+      if (s >= 1) ok = tc_wait(BAR(kBarPvDone + (sb ^ 1)), ((s - 1) >> 1) & 1, abort_s) && ok;
       if (__any_sync(0xFFFFFFFFu, !ok)) break;
       const uint8_t *vrow = smem + b * kCodeStage + kTcTok * kHeadDim + t * kHeadDim;
-      uint8_t *vf = smem + kOffVf + sb * kVfBytes + (t >> 3) * 1024 + (t & 7) * 128;
+      uint8_t *vf = smem + kOffVf + (t >> 3) * 1024 + (t & 7) * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
@@ -428,8 +426,11 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_kc,
       bool ok = tc_wait(BAR(kBarKvFull + b), (s / kTcStages) & 1, abort_s);
       ok = tc_wait(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s) && ok;
       tc_fence_after();
-      float x[kTcHalf];
-      tmem_ld16(tl + kColS + kTcRows * sb + kTcHalf * hf, x);
+      float x[kTcHalf], x2[kTcHalf];
+      tmem_ld16(tl + kColS + 2 * kTcRows * sb + kTcHalf * hf, x);             // piece 1
+      tmem_ld16(tl + kColS + 2 * kTcRows * sb + kTcRows + kTcHalf * hf, x2);  // piece 2
+#pragma unroll
+      for (int i = 0; i < kTcHalf; ++i) x[i] += x2[i];
       tc_fence_before();
       const bool valid = t < lim;
       const float *sc = reinterpret_cast<const float *>(smem + kOffSc + 2 * b * kScBytes);
@@ -497,23 +498,27 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_kc,
         if (lane < kTcHalf) red_i[qt * kTcRows + kTcHalf * hf + lane] = kmine;
         const bool next_buf = ob_used && ob + 1 < kTcOBufs;
         named_barrier(1, kSoftThreads);
+        // lane i (< 16) settles row i of the half, then the lanes share
+        float mo_l = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kTcHalf; ++i) mo_l = (lane == i) ? mr[i] : mo_l;
+        float mn_l = mo_l, f_l = 1.0f;
+        if (lane < kTcHalf) {
+          const int m = kTcHalf * hf + lane;
+          const int key = max(max(red_i[m], red_i[kTcRows + m]),
+                              max(red_i[2 * kTcRows + m], red_i[3 * kTcRows + m]));
+          if ((mine >> lane) & 1u) mn_l = fmaxf(key_float(key) + kTcOvershoot, mo_l);
+          f_l = (mn_l == mo_l) ? 1.0f : tc_ex2(mo_l - mn_l);
+          if (next_buf && qt == 0)              // row m's reference before the move
+            obm_s[ob * kTcRows + m] = mo_l;
+        }
         float f[kTcHalf];
-        float mo_l = 0.0f;
 #pragma unroll
         for (int i = 0; i < kTcHalf; ++i) {
-          const int m = kTcHalf * hf + i;
-          const float mo = mr[i];
-          mo_l = (lane == i) ? mo : mo_l;
-          const float mx =
-              fmaxf(fmaxf(key_float(red_i[m]), key_float(red_i[kTcRows + m])),
-                    fmaxf(key_float(red_i[2 * kTcRows + m]), key_float(red_i[3 * kTcRows + m])));
-          const float mn = ((mine >> i) & 1u) ? fmaxf(mx + kTcOvershoot, mo) : mo;
-          f[i] = (mn == mo) ? 1.0f : tc_ex2(mo - mn);
+          f[i] = __shfl_sync(0xFFFFFFFFu, f_l, i);
+          mr[i] = __shfl_sync(0xFFFFFFFFu, mn_l, i);
           lr[i] *= f[i];
-          mr[i] = mn;
         }
-        if (next_buf && qt == 0 && lane < kTcHalf)   // row `lane`'s reference before the move
-          obm_s[ob * kTcRows + kTcHalf * hf + lane] = mo_l;
         if (next_buf) {
           if (tid == 0) obe_s[ob] = E;
           ++ob;
