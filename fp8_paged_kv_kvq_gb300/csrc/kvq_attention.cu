@@ -734,10 +734,10 @@ struct CombineParams {
 
 constexpr int kCombineWarps = 4;
 
-// One CTA per output row.  Every thread reads one partition's (max, sum) for
-// the row max; then warp w folds partitions w, w+4, ... (4 dims per lane, all
-// loads of a warp independent of each other), and the four warps' partial
-// sums meet in shared memory.
+// One CTA per output row.  Warp w folds partitions w, w+4, ... (4 dims per
+// lane) with a running log-sum-exp, loading four partitions' (max, sum) and
+// outputs before using any, so the merge costs one memory round trip; the four
+// warps' (max, sum, output) meet in shared memory.
 __global__ void __launch_bounds__(kCombineWarps * 32)
 attn_combine_kernel(const CombineParams p) {
   __shared__ float red[kCombineWarps];
@@ -755,28 +755,48 @@ attn_combine_kernel(const CombineParams p) {
   const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
   if (n_parts <= 1) return;                       // written by the partials kernel
   const float2 *ml = p.ml_part + row * p.n_parts_max;
-  float mx = -INFINITY;
-  for (int q = tid; q < n_parts; q += kCombineWarps * 32) mx = fmaxf(mx, ml[q].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * p.n_parts_max * kHeadDim) +
+                     lane;
+  // warp w folds partitions w, w+4, ... with a running log-sum-exp; four of
+  // its partitions' (max, sum) and outputs are loaded before any is used
+  float m_w = -INFINITY, lsum = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.0f;
-  if (mx != -INFINITY) {
-    const float *op = p.o_part + row * p.n_parts_max * kHeadDim + 4 * lane;
-#pragma unroll 8
-    for (int q = warp; q < n_parts; q += kCombineWarps) {
-      const float2 v = ml[q];
-      const float w = ex2(v.x - mx);
-      const float4 o = *reinterpret_cast<const float4 *>(op + static_cast<int64_t>(q) * kHeadDim);
-      lsum += w * v.y;
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
+  for (int q0 = warp; q0 < n_parts; q0 += 4 * kCombineWarps) {
+    float2 v[4];
+    float4 o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = q0 + k * kCombineWarps;
+      v[k] = make_float2(-INFINITY, 0.0f);
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < n_parts) {
+        v[k] = ml[q];
+        o[k] = op[static_cast<int64_t>(q) * (kHeadDim / 4)];
+      }
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (v[k].x == -INFINITY) continue;          // a partition that saw no token
+      const float mn = fmaxf(m_w, v[k].x);
+      const float a = ex2(m_w - mn), b = ex2(v[k].x - mn);
+      lsum = lsum * a + v[k].y * b;
+      acc.x = acc.x * a + o[k].x * b;
+      acc.y = acc.y * a + o[k].y * b;
+      acc.z = acc.z * a + o[k].z * b;
+      acc.w = acc.w * a + o[k].w * b;
+      m_w = mn;
+    }
+  }
+  if (lane == 0) red[warp] = m_w;
+  __syncthreads();
+  const float mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  {
+    const float a = (m_w == -INFINITY) ? 0.0f : ex2(m_w - mx);
+    lsum *= a;
+    acc.x *= a;
+    acc.y *= a;
+    acc.z *= a;
+    acc.w *= a;
   }
   if (warp > 0) part_o[warp - 1][lane] = acc;
   if (lane == 0) part_l[warp] = lsum;
