@@ -60,8 +60,8 @@ __device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi) {
 // and with the remainder exact (an FMA) a second step rounds correctly.  Valid
 // while no step underflows: for s >= 2^-90 every quotient >= 2^-11 (the only
 // ones whose e4m3 code is not 0) has an exact remainder; smaller quotients
-// stay below 2^-10 and encode to zero either way.  The sign is copied from x
-// so that -0 stays -0.
+// stay below 2^-10 and encode to zero either way.  For x != 0 the result has
+// the sign of x; x = -0 gives +0 (the caller restores the sign of zero).
 constexpr float kMarksteinMinScale = 0x1p-90f;
 
 __device__ __forceinline__ float div_markstein(float x, float s, float y) {
@@ -69,8 +69,7 @@ __device__ __forceinline__ float div_markstein(float x, float s, float y) {
   const float r0 = __fmaf_rn(-q0, s, x);
   const float q1 = __fmaf_rn(r0, y, q0);
   const float r1 = __fmaf_rn(-q1, s, x);
-  const float q2 = __fmaf_rn(r1, y, q1);
-  return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+  return __fmaf_rn(r1, y, q1);
 }
 
 // ---------------------------------------------------------------------------

@@ -58,13 +58,16 @@ __device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
 // Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3):
 // fl32(x / s) then e4m3 round-to-nearest-even.  kFast divides through the
 // row's reciprocal y with Markstein's correction (exact for s >= 2^-90);
-// otherwise plain IEEE division.
+// otherwise plain IEEE division.  The four sign bits of x (bytes 1 and 3 of
+// each bf16 pair) are ORed into the code bytes: a nonzero code already has
+// its sign, and a zero code takes the sign of its input (-0 stays 0x80).
 template <bool kFast>
 __device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s, float y) {
   float q[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
 #pragma unroll
   for (int e = 0; e < 4; ++e) q[e] = kFast ? div_markstein(q[e], s, y) : __fdiv_rn(q[e], s);
-  return e4m3x2_rn(q[0], q[1]) | (e4m3x2_rn(q[2], q[3]) << 16);
+  const uint32_t signs = prmt(w0, w1, 0x7531u) & 0x80808080u;
+  return e4m3x2_rn(q[0], q[1]) | (e4m3x2_rn(q[2], q[3]) << 16) | signs;
 }
 
 template <bool kFast>
