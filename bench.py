@@ -301,12 +301,18 @@ class DeviceWorkload:
 
     def partials_kernel(self):
         """(kernel, source) the library launches for this shape's partials:
-        the skinny kernel for at most 8 stacked rows per KV head and pages of
-        at least 8 tokens, the tcgen05 kernel for 9..32 rows (pages of 16..128
-        tokens, KV heads a multiple of 4, partitions a multiple of 128 tokens),
-        else the general one."""
+        for at most 8 stacked rows per KV head the page-major kernel when its
+        grid (4 heads per CTA) is at least 9 CTAs per SM, else the skinny one
+        (pages of at least 8 tokens); the tcgen05 kernel for 9..32 rows (pages
+        of 16..128 tokens, KV heads a multiple of 4, partitions a multiple of
+        128 tokens); else the general one."""
         w = self.w
         rows = w.rows_per_request * w.group
+        page_ctas = (w.num_kv_heads // 4) * self.n_parts * w.num_requests
+        sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        if (rows <= 8 and w.block_size >= 16 and w.num_kv_heads % 4 == 0
+                and page_ctas >= 9 * sms):
+            return "attn_page_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_page.cu"
         if rows <= 8 and w.block_size >= 8:
             return "attn_skinny_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_skinny.cu"
         if (rows <= 32 and 16 <= w.block_size <= 128 and w.num_kv_heads % 4 == 0

@@ -65,13 +65,24 @@ kvq_status check_cache(const kvq_cache *c, bool need_block_size) {
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t max_context_len) {
+// Tokens per partition, a power of two in [256, 8192].  Long contexts (>= 64K
+// tokens) on pages of >= 16 tokens with KV heads in groups of 4 suit the
+// page-major kernel (one CTA per 4 heads, partition and request): the largest
+// P with at least ~12 such CTAs per SM.  Otherwise (one CTA per KV head,
+// partition and request) the largest P with 2P <= N H ctx / (8 SMs).
+int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t block_size,
+                            int32_t max_context_len) {
   const int64_t sms = current_sm_count();
-  const int64_t work = static_cast<int64_t>(num_requests > 0 ? num_requests : 1) *
-                       (num_kv_heads > 0 ? num_kv_heads : 1) *
-                       (max_context_len > 0 ? max_context_len : 1);
-  const int64_t target = work / (sms * 8);
+  const int64_t n = num_requests > 0 ? num_requests : 1;
+  const int64_t h = num_kv_heads > 0 ? num_kv_heads : 1;
+  const int64_t ctx = max_context_len > 0 ? max_context_len : 1;
   int32_t p = 256;
+  if (ctx >= 65536 && block_size >= 16 && h % 4 == 0) {
+    const int64_t target = n * (h / 4) * ctx / (12 * sms);
+    while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
+    return p;
+  }
+  const int64_t target = n * h * ctx / (sms * 8);
   while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
   return p;
 }
@@ -104,6 +115,7 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
   s->partition_tokens = partition_tokens > 0
                             ? partition_tokens
                             : heuristic_partition(num_requests, cache->num_kv_heads,
+                                                  cache->block_size,
                                                   max_context_len);
   const int64_t np = (static_cast<int64_t>(max_context_len) + s->partition_tokens - 1) /
                      s->partition_tokens;
@@ -112,6 +124,7 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
   if (static_cast<int64_t>(cache->num_kv_heads) * s->row_groups > 0x7FFFFFFF)
     return KVQ_ERR_UNSUPPORTED;
   s->log2_block = log2_exact(cache->block_size);
+  s->sms = current_sm_count();
   return KVQ_OK;
 }
 
@@ -167,8 +180,7 @@ kvq_status kvq_quantize_scatter(const kvq_cache *cache, const void *k, int64_t k
 
 int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t num_kv_heads,
                                           int32_t block_size, int32_t max_context_len) {
-  (void)block_size;
-  return heuristic_partition(num_requests, num_kv_heads, max_context_len);
+  return heuristic_partition(num_requests, num_kv_heads, block_size, max_context_len);
 }
 
 size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,

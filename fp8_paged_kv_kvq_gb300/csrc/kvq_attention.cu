@@ -732,12 +732,14 @@ struct CombineParams {
   uint16_t *out;
 };
 
-constexpr int kCombineWarps = 4;
 
-// One CTA per output row.  Warp w folds partitions w, w+4, ... (4 dims per
-// lane) with a running log-sum-exp, loading four partitions' (max, sum) and
-// outputs before using any, so the merge costs one memory round trip; the four
-// warps' (max, sum, output) meet in shared memory.
+// One CTA of kCombineWarps warps per output row (4, or 16 when a row can span
+// 64 or more partitions).  Warp w folds partitions w, w+kCombineWarps, ... (4
+// dims per lane) with a running log-sum-exp, loading four partitions' (max,
+// sum) and outputs before using any, so the merge costs one memory round trip
+// per four partitions of a warp; the warps' (max, sum, output) meet in shared
+// memory.
+template <int kCombineWarps>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 attn_combine_kernel(const CombineParams p) {
   __shared__ float red[kCombineWarps];
@@ -789,7 +791,9 @@ attn_combine_kernel(const CombineParams p) {
   }
   if (lane == 0) red[warp] = m_w;
   __syncthreads();
-  const float mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float mx = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, red[w]);
   {
     const float a = (m_w == -INFINITY) ? 0.0f : ex2(m_w - mx);
     lsum *= a;
@@ -807,7 +811,8 @@ attn_combine_kernel(const CombineParams p) {
     const float4 v = part_o[w][lane];
     acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
   }
-  lsum = part_l[0] + part_l[1] + part_l[2] + part_l[3];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) lsum += part_l[w];
   const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
   uint2 packed;
   packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -896,6 +901,21 @@ bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_code_tensor_map_strided(CUtensorMap *map, const uint8_t *codes, int64_t num_slots,
+                                    int H) {
+  EncodeTiledFn f = encode_tiled_fn();
+  if (f == nullptr || H < 4) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(num_slots),
+                              static_cast<cuuint64_t>(H)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * kHeadDim,
+                                 static_cast<cuuint64_t>(kHeadDim)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 16u, 4u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(codes), dims, strides,
+           box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A map over one scale plane [num_slots, H] fp32: boxes of 4 consecutive heads
 // x `rows` slots, unswizzled (16 bytes per slot row in shared memory).
 bool encode_scale_tensor_map(CUtensorMap *map, const float *scales, int64_t num_slots, int H,
@@ -952,6 +972,13 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   p.ml_part = nullptr;
   if (s.num_partitions > 1)
     carve_workspace(workspace, rows_total, s.num_partitions, &p.o_part, &p.ml_part);
+  // the page-major kernel reads 4 heads per CTA: worth it once its grid is at
+  // least ~3 waves (3 CTAs per SM); smaller grids go to one CTA per head
+  const int64_t page_ctas =
+      static_cast<int64_t>(c.num_kv_heads / 4) * s.num_partitions * s.num_requests;
+  if (attn_page_supported(c, s) && page_ctas >= 9LL * (s.sms > 0 ? s.sms : 152))
+    return launch_attn_partials_page(c, s, q, block_tables, context_lens, sm_scale, out,
+                                     p.o_part, p.ml_part, err_flags, stream);
   if (attn_skinny_supported(c, s))
     return launch_attn_partials_skinny(c, s, q, block_tables, context_lens, sm_scale, out,
                                        p.o_part, p.ml_part, err_flags, stream);
@@ -997,8 +1024,11 @@ cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens,
   p.o_part = o_part;
   p.ml_part = ml_part;
   p.out = static_cast<uint16_t *>(out);
-  return launch_overlapped(attn_combine_kernel, dim3(static_cast<unsigned>(p.rows_total)),
-                           dim3(kCombineWarps * 32), 0, stream, p);
+  if (s.num_partitions >= 64)
+    return launch_overlapped(attn_combine_kernel<16>, dim3(static_cast<unsigned>(p.rows_total)),
+                             dim3(16 * 32), 0, stream, p);
+  return launch_overlapped(attn_combine_kernel<4>, dim3(static_cast<unsigned>(p.rows_total)),
+                           dim3(4 * 32), 0, stream, p);
 }
 
 }  // namespace kvq

@@ -288,13 +288,16 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
       kh[0] = b0.x; kh[1] = b0.y; kh[2] = b0.z; kh[3] = b0.w;
       kh[4] = b1.x; kh[5] = b1.y; kh[6] = b1.z; kh[7] = b1.w;
     }
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // two independent accumulation chains (one per Q piece), added at the end
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int s2 = 0; s2 < 4; ++s2) {
       const uint32_t a[4] = {kl[2 * s2], kh[2 * s2], kl[2 * s2 + 1], kh[2 * s2 + 1]};
-#pragma unroll
-      for (int pc = 0; pc < 2; ++pc) mma_e4m3_16832(sacc, a, qb[s2][pc][0], qb[s2][pc][1]);
+      mma_e4m3_16832(sacc, a, qb[s2][0][0], qb[s2][0][1]);
+      mma_e4m3_16832(sacc2, a, qb[s2][1][0], qb[s2][1][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];
 
     // ---- scale, mask, online softmax.  sacc: [tok g][row 2c], [g][2c+1],
     // [g+8][2c], [g+8][2c+1]

@@ -47,6 +47,7 @@ struct AttnShape {
   int32_t partition_tokens;   // P, multiple of 64
   int32_t num_partitions;     // ceil(max_context_len / P), >= 1
   int32_t log2_block;
+  int32_t sms;                // SMs of the current device
 };
 
 // Workspace carve-up: partial outputs [rows_total][num_partitions][128] fp32,
@@ -76,6 +77,19 @@ bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_
 // slots (H a multiple of 4, the plane 16-byte aligned).
 bool encode_scale_tensor_map(CUtensorMap *map, const float *scales, int64_t num_slots, int H,
                              int rows);
+
+// Tensor map over one code plane [num_slots, H, 128] uint8 ordered (128 bytes,
+// slots, heads): boxes of 16 slots x 4 heads, 128-byte swizzled per head.
+bool encode_code_tensor_map_strided(CUtensorMap *map, const uint8_t *codes, int64_t num_slots,
+                                    int H);
+
+// The page-major partials kernel for at most 8 stacked rows per KV head
+// (pages of >= 16 tokens, KV heads a multiple of 4).
+bool attn_page_supported(const kvq_cache &c, const AttnShape &s);
+cudaError_t launch_attn_partials_page(const kvq_cache &c, const AttnShape &s, const void *q,
+                                      const int32_t *block_tables, const int32_t *context_lens,
+                                      float sm_scale, void *out, float *o_part, float2 *ml_part,
+                                      int32_t *err_flags, cudaStream_t stream);
 
 // The tcgen05 partials kernel for 9..32 stacked rows per KV head.
 bool attn_tc_supported(const kvq_cache &c, const AttnShape &s);
