@@ -69,7 +69,7 @@ kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR
 // tokens) on pages of >= 16 tokens with KV heads in groups of 4 suit the
 // page-major kernel (one CTA per 4 heads, partition and request): the largest
 // P with at least ~12 such CTAs per SM.  Otherwise (one CTA per KV head,
-// partition and request) the largest P with 2P <= N H ctx / (8 SMs).
+// partition and request) the largest P with 2P <= N H ctx / (4 SMs).
 int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t block_size,
                             int32_t max_context_len) {
   const int64_t sms = current_sm_count();
@@ -82,7 +82,7 @@ int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t 
     while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
     return p;
   }
-  const int64_t target = n * h * ctx / (sms * 8);
+  const int64_t target = n * h * ctx / (sms * 4);
   while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
   return p;
 }
