@@ -72,6 +72,36 @@ __device__ __forceinline__ float div_markstein(float x, float s, float y) {
   return __fmaf_rn(r1, y, q1);
 }
 
+// Packed pairs of fp32 (low half = first element) for the f32x2 arithmetic.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t d, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// div_markstein on a packed pair: x holds two dividends, ns and y hold -s and
+// fl32(1 / s) in both halves; the same five roundings per element as the
+// scalar form, on the f32x2 FMA path.
+__device__ __forceinline__ uint64_t div_markstein_x2(uint64_t x, uint64_t ns, uint64_t y) {
+  const uint64_t q0 = mul_f32x2(x, y);
+  const uint64_t r0 = fma_f32x2(q0, ns, x);
+  const uint64_t q1 = fma_f32x2(r0, y, q0);
+  const uint64_t r1 = fma_f32x2(q1, ns, x);
+  return fma_f32x2(r1, y, q1);
+}
+
 // ---------------------------------------------------------------------------
 // Decode to bf16, exactly.  Placing the 7 magnitude bits of a code at bf16 bits
 // 10..4 (exponent low bits + top mantissa bits) and its sign at bit 15 gives a

@@ -9,13 +9,17 @@
 // graph.  The fix commit "give the V tensor its own row pitch in the fp8 KV
 // store": K and V each carry their own token pitch.
 //
-// Layout of the work: each 8-lane group owns one 128-element row (16 elements,
-// 32 bytes, per lane: two 16-byte loads) of the grid-wide list of rows ordered
-// (token, K heads then V heads), so a token's K rows are one contiguous read
-// and every row costs one memory round trip.  The row amax is an integer max
-// over the bf16 magnitude bits (order-preserving for finite values) reduced
-// across the 8 lanes with shuffles; the 16 codes of a lane leave as one 16-byte store, so a row's 128
-// codes are one contiguous 128-byte line.
+// Layout of the work: each 4-lane group owns one 128-element row (32 elements,
+// 64 bytes, per lane: four 16-byte loads) of the grid-wide list of rows
+// ordered (token, K heads then V heads), so a token's K rows are one
+// contiguous read and every row costs one memory round trip.  The row amax is
+// an integer max over the bf16 magnitude bits (order-preserving for finite
+// values) reduced across the 4 lanes with shuffles; a lane's 32 codes leave as
+// two 16-byte stores, so a row's 128 codes are one contiguous 128-byte line.
+// Four lanes per row (rather than 8, 2 or 1) measured fastest: the per-row
+// work (token index, scale, reciprocal) is shared by fewer threads while each
+// thread still holds few registers.  The quotients run two at a time on the
+// packed f32x2 FMA path.
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -41,6 +45,8 @@ struct QuantParams {
   int64_t num_slots;
   int32_t num_kv_heads;
   int32_t *err_flags;
+  uint64_t rows_per_token_magic;   // ceil(2^shift / (2H)): row id / (2H) by a multiply
+  int32_t rows_per_token_shift;    // 32 + ceil(log2(2H))
 };
 
 __device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
@@ -57,15 +63,21 @@ __device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
 
 // Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3):
 // fl32(x / s) then e4m3 round-to-nearest-even.  kFast divides through the
-// row's reciprocal y with Markstein's correction (exact for s >= 2^-90);
-// otherwise plain IEEE division.  The four sign bits of x (bytes 1 and 3 of
+// row's reciprocal y with Markstein's correction (exact for s >= 2^-90), two
+// elements per packed f32x2 operation; otherwise plain IEEE division.  The four sign bits of x (bytes 1 and 3 of
 // each bf16 pair) are ORed into the code bytes: a nonzero code already has
 // its sign, and a zero code takes the sign of its input (-0 stays 0x80).
 template <bool kFast>
 __device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s, float y) {
   float q[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+  if (kFast) {
+    const uint64_t ns = pack_f32x2(-s, -s), yy = pack_f32x2(y, y);
+    unpack_f32x2(div_markstein_x2(pack_f32x2(q[0], q[1]), ns, yy), q[0], q[1]);
+    unpack_f32x2(div_markstein_x2(pack_f32x2(q[2], q[3]), ns, yy), q[2], q[3]);
+  } else {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) q[e] = kFast ? div_markstein(q[e], s, y) : __fdiv_rn(q[e], s);
+    for (int e = 0; e < 4; ++e) q[e] = __fdiv_rn(q[e], s);
+  }
   const uint32_t signs = prmt(w0, w1, 0x7531u) & 0x80808080u;
   return e4m3x2_rn(q[0], q[1]) | (e4m3x2_rn(q[2], q[3]) << 16) | signs;
 }
@@ -80,15 +92,21 @@ __device__ __forceinline__ uint4 encode16(uint4 a, uint4 b, float s, float y) {
   return out;
 }
 
+constexpr int kLanesPerRow = 4;
+constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+constexpr int kPerLane = kHeadDim / kLanesPerRow;      // elements
+constexpr int kVec = kPerLane / 16;                     // 16-element pieces per lane
+constexpr float kInv448 = 1.0f / 448.0f;               // fl32(1 / 448): rounded by the compiler
+
 __global__ void __launch_bounds__(kQuantWarps * 32)
 quantize_scatter_kernel(const QuantParams p) {
   const int lane = threadIdx.x & 31;
-  const int sub = lane & 7;                       // lane within the row's 8 lanes
-  const unsigned gmask = 0xFFu << (lane & 24);
-  // row id over (token, K/V, head); a whole 8-lane group shares it
-  const uint32_t rid = blockIdx.x * (kQuantWarps * 4) + (threadIdx.x >> 3);   // < 2^31
+  const int sub = lane & (kLanesPerRow - 1);
+  const unsigned gmask = ((1u << kLanesPerRow) - 1u) << (lane & ~(kLanesPerRow - 1));
+  const uint32_t rid = blockIdx.x * (kQuantWarps * kRowsPerWarp) + (threadIdx.x / kLanesPerRow);
   const int H = p.num_kv_heads;
-  const uint32_t t32 = rid / static_cast<uint32_t>(2 * H);
+  const uint32_t t32 =
+      static_cast<uint32_t>((static_cast<uint64_t>(rid) * p.rows_per_token_magic) >> p.rows_per_token_shift);
   grid_dependency_wait();
   allow_dependents_launch();
   if (t32 >= p.num_tokens) return;
@@ -96,33 +114,47 @@ quantize_scatter_kernel(const QuantParams p) {
   const int rem = static_cast<int>(rid - t32 * static_cast<uint32_t>(2 * H));
   const bool is_v = rem >= H;
   const int h = is_v ? rem - H : rem;
-  // the row's loads and the slot id load are independent: issue all first
-  const uint16_t *src = (is_v ? p.v + t * p.v_stride : p.k + t * p.k_stride) + h * kHeadDim + sub * 16;
-  const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
-  const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src + 8));
+  const uint16_t *src = (is_v ? p.v + t * p.v_stride : p.k + t * p.k_stride) + h * kHeadDim + sub * kPerLane;
+  uint4 a[kVec], b[kVec];
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    a[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k));
+    b[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k + 8));
+  }
   const int64_t slot = __ldg(p.slot_ids + t);
   if (slot < 0) return;
   if (slot >= p.num_slots) {
     if (sub == 0 && rem == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
     return;
   }
-  uint32_t m = max_mag_bf16x2(a, b);
-  m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 1));
-  m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 2));
-  m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 4));
+  uint32_t m = max_mag_bf16x2(a[0], b[0]);
+#pragma unroll
+  for (int k = 1; k < kVec; ++k) m = __vmaxu2(m, max_mag_bf16x2(a[k], b[k]));
+#pragma unroll
+  for (int off = 1; off < kLanesPerRow; off <<= 1) m = __vmaxu2(m, __shfl_xor_sync(gmask, m, off));
   const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
-  uint4 out = make_uint4(0u, 0u, 0u, 0u);
+  uint4 out[kVec];
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) out[k] = make_uint4(0u, 0u, 0u, 0u);
   float s = 0.0f;
   if (amax != 0.0f) {
-    s = __fdiv_rn(amax, 448.0f);
-    if (s >= kMarksteinMinScale)
-      out = encode16<true>(a, b, s, __frcp_rn(s));
-    else
-      out = encode16<false>(a, b, s, 0.0f);
+    // fl32(amax / 448): Markstein's correction through the correctly rounded
+    // constant reciprocal while no step underflows, else IEEE division
+    s = (amax >= kMarksteinMinScale) ? div_markstein(amax, 448.0f, kInv448)
+                                     : __fdiv_rn(amax, 448.0f);
+    if (s >= kMarksteinMinScale) {
+      const float y = __frcp_rn(s);
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) out[k] = encode16<true>(a[k], b[k], s, y);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) out[k] = encode16<false>(a[k], b[k], s, 0.0f);
+    }
   }
   const int64_t row = slot * H + h;
-  uint8_t *dst = (is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * 16;
-  *reinterpret_cast<uint4 *>(dst) = out;
+  uint4 *dst = reinterpret_cast<uint4 *>((is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * kPerLane);
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) dst[k] = out[k];
   if (sub == 0) (is_v ? p.v_scales : p.k_scales)[row] = s;
 }
 
@@ -214,8 +246,17 @@ cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k
   p.num_slots = c.num_slots;
   p.num_kv_heads = c.num_kv_heads;
   p.err_flags = err_flags;
+  {
+    // n / d == (n * ceil(2^S / d)) >> S for every n < 2^31 when S = 32 + ceil(log2 d):
+    // the multiplier's excess e = M d - 2^S is below d <= 2^(S-32), so n e < 2^S
+    const uint64_t d = 2u * static_cast<uint64_t>(c.num_kv_heads);
+    int l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    p.rows_per_token_shift = 32 + l;
+    p.rows_per_token_magic = ((uint64_t(1) << (32 + l)) + d - 1) / d;
+  }
   const int64_t rows = num_tokens * 2 * c.num_kv_heads;
-  const int64_t blocks = (rows + kQuantWarps * 4 - 1) / (kQuantWarps * 4);
+  const int64_t blocks = (rows + kQuantWarps * kRowsPerWarp - 1) / (kQuantWarps * kRowsPerWarp);
   return launch_overlapped(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks)),
                            dim3(kQuantWarps * 32), 0, stream, p);
 }
