@@ -29,7 +29,7 @@ namespace kvq {
 
 namespace {
 
-constexpr int kQuantWarps = 8;
+constexpr int kQuantWarps = 4;   // 128-thread CTAs, at least 12 resident per SM
 
 struct QuantParams {
   const uint16_t *k;
@@ -98,7 +98,7 @@ constexpr int kPerLane = kHeadDim / kLanesPerRow;      // elements
 constexpr int kVec = kPerLane / 16;                     // 16-element pieces per lane
 constexpr float kInv448 = 1.0f / 448.0f;               // fl32(1 / 448): rounded by the compiler
 
-__global__ void __launch_bounds__(kQuantWarps * 32)
+__global__ void __launch_bounds__(kQuantWarps * 32, 12)
 quantize_scatter_kernel(const QuantParams p) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & (kLanesPerRow - 1);
