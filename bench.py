@@ -5,9 +5,10 @@ One step = one pass of the whole hot path over one batch: the fused
 quantize-scatter of the step's new K/V rows (R per request) into the FP8 cache,
 then paged GQA decode / verify attention over the cache (split-K partials, then
 the combine).  Inputs are synthetic and seeded (workloads/), resident in HBM
-before the timed region; L2 is flushed (a 256 MiB write) before every timed
-step and the step time is the sum of per-step CUDA-event intervals taken on the
-launching stream.
+before the timed region; L2 is flushed before every timed step (a 256 MiB write,
+then a 256 MiB read that moves the write-back of those dirty lines out of the
+timed step) and the step time is the sum of per-step CUDA-event intervals taken
+on the launching stream.
 
 Default workload: the decode batch -- 32 requests, context lengths uniform in
 [1024, 8192], 32 query heads / 8 KV heads, head_dim 128, block size 16,
@@ -46,6 +47,22 @@ METRIC = "paged FP8-KV decode attn: achieved HBM GB/s (% of 8 TB/s); KV rows qua
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Between timed steps: a write of a 256 MiB buffer (twice L2) evicts every
+    line the previous step touched; a read of a second 256 MiB buffer then
+    evicts the write's dirty lines, so their write-back happens here and not
+    inside the next timed kernel, which starts with a clean L2 holding none of
+    its data."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self, i):
+        self.w.fill_(i & 0xFF)
+        torch.amax(self.r)
 
 DESCRIPTIONS = {
     "tiny": "tiny: 1 request x 64 tokens, 32 q heads / 8 KV heads, head_dim 128, block 16",
@@ -381,7 +398,7 @@ def run_kvq(args, rank, local, world):
 
 def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
     stream = wl.stream
-    flush = None if args.profile else torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = None if args.profile else L2Flush(dev)
     graph = None
     if args.workload == "store":
         wl.quantize()
@@ -391,7 +408,10 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
             wl.quantize()
         torch.cuda.synchronize(dev)
 
-    def step(evs=None):
+    def step(evs=None, split=False):
+        # split: events between the launches too (per-kernel durations); they
+        # are stream operations that keep a launch from starting while the
+        # previous kernel drains, so the step timing records only its ends
         if evs is not None:
             evs[0].record(stream)
         if graph is not None:
@@ -401,10 +421,10 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
                     e.record(stream)
             return
         wl.quantize()
-        if evs is not None:
+        if split:
             evs[1].record(stream)
         wl.partials()
-        if evs is not None:
+        if split:
             evs[2].record(stream)
         wl.combine()
         if evs is not None:
@@ -412,7 +432,7 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
 
     for i in range(W):
         if flush is not None:
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
         step()
     torch.cuda.synchronize(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
@@ -426,7 +446,7 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
     torch.cuda.nvtx.range_push("kvq_timed")      # lets a profiler select the timed launches
     for i in range(K):
         if flush is not None:
-            flush.fill_((i + 7) & 0xFF)
+            flush((i + 7) & 0xFF)
         step(evs[i])
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
@@ -434,11 +454,18 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
     if sampler:
         sampler.stop()
     dist_barrier(world)
-    st_q = [e[0].elapsed_time(e[1]) for e in evs]
-    st_p = [e[1].elapsed_time(e[2]) for e in evs]
-    st_c = [e[2].elapsed_time(e[3]) for e in evs]
     st = [e[0].elapsed_time(e[3]) for e in evs]
     step_ms = dist_max(sum(st) / K, world)
+    # per-kernel durations: a second pass of K steps, events between the launches
+    kevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(K):
+        if flush is not None:
+            flush((i + 11) & 0xFF)
+        step(kevs[i], split=True)
+    torch.cuda.synchronize(dev)
+    st_q = [e[0].elapsed_time(e[1]) for e in kevs]
+    st_p = [e[1].elapsed_time(e[2]) for e in kevs]
+    st_c = [e[2].elapsed_time(e[3]) for e in kevs]
     if int(wl.err.item()) != 0:
         raise RuntimeError("device error flags set during the benchmark")
 
@@ -460,8 +487,12 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         "config": {
             "workload": DESCRIPTIONS[args.workload],
             "name": args.workload,
-            "l2": ("flushed before every timed step (256 MiB write); step time = sum of "
-                   "per-step CUDA-event intervals") if flush is not None else
+            "l2": ("flushed before every timed step (256 MiB write, then a 256 MiB read "
+                   "that takes the write-back of its dirty lines out of the step); step "
+                   "time = sum of "
+                   "per-step CUDA-event intervals (events at the step's ends only; "
+                   "per-kernel times from a second pass of K steps with events between "
+                   "the launches)") if flush is not None else
                   "not flushed (profile mode)",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
             "storage": "e4m3 codes (uint8) + fp32 row scales; bf16 q/out; QK^T on e4m3 tensor "
@@ -473,7 +504,7 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         "kv_rows_quantized_per_s": round(world * wl.rows_quantized() / (step_ms * 1e-3), 1),
         "tokens_per_s": round(world * wl.tokens() / (step_ms * 1e-3), 1),
         "kernels_us": {"quantize_scatter": round(1e3 * sum(st_q) / K, 3)},
-        "gpu_launches": K * wl.launches_per_step,
+        "gpu_launches": K * wl.launches_per_step,   # in the step-timed pass
         "wall_s_timed_region": round(wall1 - wall0, 3),
     }
     if args.workload != "store":
@@ -515,7 +546,7 @@ def _timed(stream, dev, K, body, flush):
           for _ in range(K)]
     for i in range(K):
         if flush is not None:
-            flush.fill_(i & 0xFF)
+            flush(i & 0xFF)
         ev[i][0].record(stream)
         body()
         ev[i][1].record(stream)
@@ -534,7 +565,7 @@ def run_e2e(wl: DeviceWorkload, dev, K, world):
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def body():
         for name, t in host.items():
@@ -563,7 +594,7 @@ def run_e2e_store(wl: DeviceWorkload, dev, K, world):
     out_h = torch.empty(wl.cache.k_scales.shape, dtype=torch.float32, pin_memory=True)
     h2d = host_kv.numel() * 2 + host_slots.numel() * 8
     d2h = out_h.numel() * 4
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def body():
         wl.qkv[:, Hq * D:].copy_(host_kv, non_blocking=True)
