@@ -750,12 +750,14 @@ attn_combine_kernel(const CombineParams p) {
   const int warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
-  grid_dependency_wait();
+  // the context length is not written by the partials kernel: read it while
+  // that kernel drains, and wait only before reading the partials
   allow_dependents_launch();
   int L = p.context_lens[r];
   L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
   const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
   if (n_parts <= 1) return;                       // written by the partials kernel
+  grid_dependency_wait();
   const float2 *ml = p.ml_part + row * p.n_parts_max;
   const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * p.n_parts_max * kHeadDim) +
                      lane;

@@ -103,7 +103,11 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int part = blockIdx.y;
   const int r = blockIdx.z;
 
-  grid_dependency_wait();
+  // Everything before the first cache read (context length, block table,
+  // query pieces) runs while the previous kernel of the stream -- the
+  // quantize-scatter that writes the cache -- may still be running: none of it
+  // reads what that kernel writes.  The producer waits before its first copy,
+  // the head warps before their first global write.
   allow_dependents_launch();
   int L = p.context_lens[r];
   if (L < 0 || L > p.ctx_limit) {
@@ -143,6 +147,7 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
   if (warp == kPgHeads) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
+      grid_dependency_wait();
       int issued = 0;
       bool bad = false;
       for (int u = 0; u < n_chunks; ++u) {
@@ -409,6 +414,7 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
+  grid_dependency_wait();
   timed_out = __any_sync(0xFFFFFFFFu, timed_out);
   if (timed_out) {
     if (lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);

@@ -97,7 +97,10 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int part = blockIdx.y;
   const int r = blockIdx.z;
 
-  grid_dependency_wait();
+  // Everything before the first cache read (context length, block table,
+  // query pieces) runs while the previous kernel of the stream -- the
+  // quantize-scatter that writes the cache -- may still be running: none of it
+  // reads what that kernel writes.
   allow_dependents_launch();
   int L = p.context_lens[r];
   if (L < 0 || L > p.ctx_limit) {
@@ -202,6 +205,7 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
     cp_async_commit();
   };
 #pragma unroll
+  grid_dependency_wait();     // the cache (codes and scales) from here on
   for (int u = 0; u < kSkStages; ++u) issue(u);
 
   // ---- query pieces (two e4m3 per element, q = 2^e (p1 + p2)) into the B
