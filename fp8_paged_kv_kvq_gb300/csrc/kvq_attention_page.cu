@@ -191,14 +191,16 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
   };
   // query row exponents, then the two e4m3 pieces of each element:
   // q = 2^e (p1 + p2), 8 significant bits, all of bf16's
+  // (all rows' loads first: one memory round trip for the warp's rows)
+  uint2 vq[kPgRows];
+#pragma unroll
+  for (int m = 0; m < kPgRows; ++m)
+    vq[m] = (m < p.M) ? *reinterpret_cast<const uint2 *>(q_row(m) + 4 * lane) : make_uint2(0u, 0u);
+#pragma unroll
   for (int m = 0; m < kPgRows; ++m) {
-    float amax = 0.0f;
-    uint2 v = make_uint2(0u, 0u);
-    if (m < p.M) {
-      v = *reinterpret_cast<const uint2 *>(q_row(m) + 4 * lane);
-      amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                   fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
-    }
+    const uint2 v = vq[m];
+    float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                       fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));

@@ -138,21 +138,45 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
     const int i = m / p.G, gq = m - i * p.G;
     return p.q + ((static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq) * kHeadDim;
   };
-  for (int m = warp; m < kSkRows; m += kSkWarps) {
-    float amax = 0.0f;
-    if (m < p.M) {
-      const uint2 v = *reinterpret_cast<const uint2 *>(q_row(m) + 4 * lane);
-      amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                   fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+  // ---- query rows m = warp, warp + 4: both loaded at once, then per row its
+  // exponent and the two e4m3 pieces of each element, q = 2^e (p1 + p2), into
+  // the B planes
+  {
+    constexpr int kRowsPerWarp = kSkRows / kSkWarps;
+    uint2 v[kRowsPerWarp];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int m = warp + kSkWarps * k;
+      v[k] = (m < p.M) ? *reinterpret_cast<const uint2 *>(q_row(m) + 4 * lane) : make_uint2(0u, 0u);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    if (lane == 0) {
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      const int m = warp + kSkWarps * k;
+      float amax = fmaxf(fmaxf(fabsf(bf16_lo(v[k].x)), fabsf(bf16_hi(v[k].x))),
+                         fmaxf(fabsf(bf16_lo(v[k].y)), fabsf(bf16_hi(v[k].y))));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
       const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
       int e = (ex == 0) ? -126 : ex - 127 - 7;
       e = e < -126 ? -126 : (e > 126 ? 126 : e);
-      row_exp[m] = (amax == 0.0f) ? 0.0f : __int_as_float((127 + e) << 23);   // 2^e
+      const float rx = (amax == 0.0f) ? 0.0f : __int_as_float((127 + e) << 23);   // 2^e
+      if (lane == 0) row_exp[m] = rx;
+      uint32_t c1w = 0u, c2w = 0u;
+      if (rx != 0.0f) {
+        const float inv = __int_as_float((254u << 23) - __float_as_uint(rx));
+        const float xs[4] = {bf16_lo(v[k].x), bf16_hi(v[k].x), bf16_lo(v[k].y), bf16_hi(v[k].y)};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float x = xs[t] * inv;
+          const uint32_t c1 = e4m3_round(x, x);
+          const float res = x - e4m3_to_f32(c1);
+          c1w |= c1 << (8 * t);
+          c2w |= e4m3_round(res, res) << (8 * t);
+        }
+      }
+      *reinterpret_cast<uint32_t *>(plane + m * kHeadDim + 4 * lane) = c1w;
+      *reinterpret_cast<uint32_t *>(plane + kSkRows * kHeadDim + m * kHeadDim + 4 * lane) = c2w;
     }
   }
   __syncthreads();
@@ -204,32 +228,12 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
     cp_async_commit();
   };
-#pragma unroll
   grid_dependency_wait();     // the cache (codes and scales) from here on
+#pragma unroll
   for (int u = 0; u < kSkStages; ++u) issue(u);
 
-  // ---- query pieces (two e4m3 per element, q = 2^e (p1 + p2)) into the B
-  // fragments: b0 = rows' dims 32c + 8 s2 + 0..3, b1 = dims + 4..7, row g
-  for (int idx = tid; idx < kSkRows * 32; idx += kSkThreads) {
-    const int m = idx >> 5, qd = idx & 31;
-    uint32_t c1w = 0u, c2w = 0u;
-    if (m < p.M && row_exp[m] != 0.0f) {
-      const uint2 v = *reinterpret_cast<const uint2 *>(q_row(m) + 4 * qd);
-      const float inv = __int_as_float((254u << 23) - __float_as_uint(row_exp[m]));
-      const float xs[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = xs[e] * inv;
-        const uint32_t c1 = e4m3_round(x, x);
-        const float res = x - e4m3_to_f32(c1);
-        c1w |= c1 << (8 * e);
-        c2w |= e4m3_round(res, res) << (8 * e);
-      }
-    }
-    *reinterpret_cast<uint32_t *>(plane + m * kHeadDim + 4 * qd) = c1w;
-    *reinterpret_cast<uint32_t *>(plane + kSkRows * kHeadDim + m * kHeadDim + 4 * qd) = c2w;
-  }
-  __syncthreads();
+  // B fragments of the query pieces: b0 = rows' dims 32c + 8 s2 + 0..3,
+  // b1 = dims + 4..7, row g
   uint32_t qb[4][2][2];
 #pragma unroll
   for (int s2 = 0; s2 < 4; ++s2)
