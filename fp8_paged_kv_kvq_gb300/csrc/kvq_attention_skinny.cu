@@ -262,6 +262,11 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i][e] = 0.0f;
   int ev = -1000;
+  // cached forms of the running state: the rescale thresholds m_run + lazy
+  // margin, the exponent base (0 while no score was seen), the value bound
+  // 2^ev (below every scale before the first chunk) and 2^-ev
+  float thr[2] = {-INFINITY, -INFINITY}, ms[2] = {0.0f, 0.0f};
+  float vbound = -1.0f, vnorm = 1.0f;
   bool timed_out = false;
 
   for (int u = 0; u < n_my; ++u) {
@@ -322,55 +327,68 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
       x[2] = (j0 + g + 8 < vis[0]) ? x[2] : -INFINITY;
       x[3] = (j0 + g + 8 < vis[1]) ? x[3] : -INFINITY;
     }
-    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
-    float vmax = fmaxf(vs_lo, vs_hi);
+    // The running max moves only when a score passes it by more than the lazy
+    // margin and the value bound only when a scale passes it; after the first
+    // chunks both are rare, so the warp reductions and the rescale run only
+    // when some lane sees one (the same updates as reducing every chunk).
+    const bool need = x[0] > thr[0] || x[2] > thr[0] || x[1] > thr[1] || x[3] > thr[1] ||
+                      vs_lo > vbound || vs_hi > vbound;
+    if (__any_sync(0xFFFFFFFFu, need)) {
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+      float vmax = fmaxf(vs_lo, vs_hi);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
-      vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, off));
-    }
-    float fac[2] = {1.0f, 1.0f};
-    bool grow = false;
-    {
-      const float mxs[2] = {mx0, mx1};
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, off));
+      }
+      float fac[2] = {1.0f, 1.0f};
+      bool grow = false;
+      {
+        const float mxs[2] = {mx0, mx1};
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
-        if (mxs[e] > m_run[e] + kSkLazyRescale) {
-          fac[e] = sk_ex2(m_run[e] - mxs[e]);
-          m_run[e] = mxs[e];
-          grow = true;
+        for (int e = 0; e < 2; ++e)
+          if (mxs[e] > m_run[e] + kSkLazyRescale) {
+            fac[e] = sk_ex2(m_run[e] - mxs[e]);
+            m_run[e] = mxs[e];
+            grow = true;
+          }
+      }
+      float vfac = 1.0f;
+      bool vgrow = false;
+      {
+        const uint32_t bits = __float_as_uint(vmax);
+        const int ex = static_cast<int>((bits >> 23) & 0xFFu);
+        int ec = (ex == 0) ? -126 : ex - 127 + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
+        ec = ec > 126 ? 126 : ec;
+        if (ec > ev) {
+          const int d = ev - ec;
+          vfac = (d >= -126) ? __int_as_float((127 + d) << 23) : 0.0f;
+          ev = ec;
+          vgrow = true;
         }
-    }
-    float vfac = 1.0f;
-    bool vgrow = false;
-    {
-      const uint32_t bits = __float_as_uint(vmax);
-      const int ex = static_cast<int>((bits >> 23) & 0xFFu);
-      int ec = (ex == 0) ? -126 : ex - 127 + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
-      ec = ec > 126 ? 126 : ec;
-      if (ec > ev) {
-        const int d = ev - ec;
-        vfac = (d >= -126) ? __int_as_float((127 + d) << 23) : 0.0f;
-        ev = ec;
-        vgrow = true;
       }
-    }
-    if (__any_sync(0xFFFFFFFFu, grow) || vgrow) {
-      l_run[0] *= fac[0];
-      l_run[1] *= fac[1];
-      const float f0 = fac[0] * vfac, f1 = fac[1] * vfac;
+      if (__any_sync(0xFFFFFFFFu, grow) || vgrow) {
+        l_run[0] *= fac[0];
+        l_run[1] *= fac[1];
+        const float f0 = fac[0] * vfac, f1 = fac[1] * vfac;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[i][0] *= f0;
-        o[i][1] *= f1;
-        o[i][2] *= f0;
-        o[i][3] *= f1;
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] *= f0;
+          o[i][1] *= f1;
+          o[i][2] *= f0;
+          o[i][3] *= f1;
+        }
       }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        thr[e] = m_run[e] + kSkLazyRescale;
+        ms[e] = (m_run[e] == -INFINITY) ? 0.0f : m_run[e];
+      }
+      vbound = __int_as_float((127 + ev) << 23);      // 2^ev, ev in [-126, 126]
+      vnorm = __int_as_float((127 - ev) << 23);
     }
-    const float vnorm = __int_as_float((127 - ev) << 23);
-    const float ms0 = (m_run[0] == -INFINITY) ? 0.0f : m_run[0];
-    const float ms1 = (m_run[1] == -INFINITY) ? 0.0f : m_run[1];
+    const float ms0 = ms[0], ms1 = ms[1];
     const float p0 = sk_ex2(x[0] - ms0), p1 = sk_ex2(x[1] - ms1);
     const float p2 = sk_ex2(x[2] - ms0), p3 = sk_ex2(x[3] - ms1);
     l_run[0] += p0 + p2;
