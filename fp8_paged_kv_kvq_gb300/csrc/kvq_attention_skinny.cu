@@ -57,7 +57,7 @@ struct SkParams {
   const uint8_t *v_codes;
   const float *k_scales;
   const float *v_scales;
-  int64_t num_blocks;
+  uint32_t num_blocks;        // < 2^31 (slots < 2^31)
   int32_t H;
   int32_t log2_bs;
   int32_t box_rows;          // min(bs, 16)
@@ -184,6 +184,7 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
   // ---- the warp's pipeline: chunk u of this warp covers tokens
   // t0 + 16 * (warp + 4u) .. +16
   const int n_my = (n_chunks > warp) ? (n_chunks - warp + kSkWarps - 1) / kSkWarps : 0;
+  const float *scale_base = ((lane < 16) ? p.k_scales : p.v_scales) + h;
   auto issue = [&](int u) {
     if (u < n_my) {
       const int sb = u % kSkStages;
@@ -198,12 +199,12 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
         for (int i = 0; i < kChunk / p.box_rows; ++i) {
           const int j = j0 + i * p.box_rows;
           if (j >= t_end) break;
-          const int64_t blk = bt_s[(j >> p.log2_bs) - page0];
-          if (blk < 0 || blk >= p.num_blocks) {
+          const uint32_t blk = static_cast<uint32_t>(bt_s[(j >> p.log2_bs) - page0]);
+          if (blk >= p.num_blocks) {             // also every negative id
             bad = true;
             continue;
           }
-          const int z = static_cast<int>((blk << p.log2_bs) + (j & bs_mask));
+          const int z = static_cast<int>((blk << p.log2_bs) | (j & bs_mask));
           tma_load_3d(kdst + i * p.box_rows * kHeadDim, &tmap_k, 0, h, z, b);
           tma_load_3d(vdst + i * p.box_rows * kHeadDim, &tmap_v, 0, h, z, b);
           bytes += 2u * p.box_rows * kHeadDim;
@@ -211,16 +212,15 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
         if (bad && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
         mbar_arrive_expect_tx(b, bytes);
       }
-      // lanes 0..15: K scales, 16..31: V scales of the chunk's tokens
-      const int tl = lane & 15;
-      const int j = j0 + tl;
-      const float *base = (lane < 16) ? p.k_scales : p.v_scales;
-      const float *src = base;
+      // lanes 0..15: K scales, 16..31: V scales of the chunk's tokens (32-bit
+      // slot arithmetic: slots < 2^31)
+      const int j = j0 + (lane & 15);
+      const float *src = scale_base;
       uint32_t nbytes = 0;
       if (j < t_end) {
-        const int64_t blk = bt_s[(j >> p.log2_bs) - page0];
-        if (blk >= 0 && blk < p.num_blocks) {
-          src = base + ((blk << p.log2_bs) + (j & bs_mask)) * p.H + h;
+        const uint32_t blk = static_cast<uint32_t>(bt_s[(j >> p.log2_bs) - page0]);
+        if (blk < p.num_blocks) {
+          src = scale_base + static_cast<uint64_t>((blk << p.log2_bs) | (j & bs_mask)) * p.H;
           nbytes = 4;
         }
       }
@@ -269,6 +269,7 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
   float vbound = -1.0f, vnorm = 1.0f;
   bool timed_out = false;
 
+#pragma unroll 2
   for (int u = 0; u < n_my; ++u) {
     const int sb = u % kSkStages;
     cp_async_wait<kSkStages - 1>();
@@ -551,7 +552,7 @@ cudaError_t launch_attn_partials_skinny(const kvq_cache &c, const AttnShape &s, 
   p.v_codes = c.v_codes;
   p.k_scales = c.k_scales;
   p.v_scales = c.v_scales;
-  p.num_blocks = c.num_slots >> s.log2_block;
+  p.num_blocks = static_cast<uint32_t>(c.num_slots >> s.log2_block);
   p.H = c.num_kv_heads;
   p.log2_bs = s.log2_block;
   const int bs = 1 << s.log2_block;
