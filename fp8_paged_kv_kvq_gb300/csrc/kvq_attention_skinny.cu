@@ -232,18 +232,25 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
   for (int u = 0; u < kSkStages; ++u) issue(u);
 
-  // B fragments of the query pieces: b0 = rows' dims 32c + 8 s2 + 0..3,
-  // b1 = dims + 4..7, row g
+  // B fragments of the query pieces for k-step s2 (dims 32 s2 .. +31), row g:
+  // b0 = dims 32 s2 + 4c + 0..3, b1 = dims 32 s2 + 16 + 4c + 0..3
   uint32_t qb[4][2][2];
 #pragma unroll
   for (int s2 = 0; s2 < 4; ++s2)
 #pragma unroll
     for (int pc = 0; pc < 2; ++pc) {
-      const uint2 w = *reinterpret_cast<const uint2 *>(plane + pc * kSkRows * kHeadDim +
-                                                       g * kHeadDim + 32 * c + 8 * s2);
-      qb[s2][pc][0] = w.x;
-      qb[s2][pc][1] = w.y;
+      const uint8_t *qr = plane + pc * kSkRows * kHeadDim + g * kHeadDim + 32 * s2 + 4 * c;
+      qb[s2][pc][0] = *reinterpret_cast<const uint32_t *>(qr);
+      qb[s2][pc][1] = *reinterpret_cast<const uint32_t *>(qr + 16);
     }
+  // this lane's ldmatrix row address within a K tile, per k-step: token row
+  // (lane & 7) + 8 ((lane >> 3) & 1), 16-byte chunk 2 s2 + (lane >> 4), 128-byte
+  // swizzled (chunk ^ row & 7)
+  const int ld_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+  uint32_t ld_off[4];
+#pragma unroll
+  for (int s2 = 0; s2 < 4; ++s2)
+    ld_off[s2] = ld_row * kHeadDim + (((2 * s2 + (lane >> 4)) ^ (lane & 7)) << 4);
 
   // this thread's rows: n = 2c + e
   int vis[2];
@@ -288,27 +295,18 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
     const float *vsv = ksv + kChunk;
     const int j0 = t0 + kChunk * (warp + kSkWarps * u);
 
-    // ---- S^T = K Q^T: A = code rows of tokens g and g+8, dims 32c..32c+31
-    uint32_t kl[8], kh[8];
-    {
-      const uint8_t *rl = kb + g * kHeadDim;
-      const uint8_t *rh = kb + (g + 8) * kHeadDim;
-      const uint4 a0 = *reinterpret_cast<const uint4 *>(rl + (((2 * c) ^ (g & 7)) << 4));
-      const uint4 a1 = *reinterpret_cast<const uint4 *>(rl + (((2 * c + 1) ^ (g & 7)) << 4));
-      const uint4 b0 = *reinterpret_cast<const uint4 *>(rh + (((2 * c) ^ (g & 7)) << 4));
-      const uint4 b1 = *reinterpret_cast<const uint4 *>(rh + (((2 * c + 1) ^ (g & 7)) << 4));
-      kl[0] = a0.x; kl[1] = a0.y; kl[2] = a0.z; kl[3] = a0.w;
-      kl[4] = a1.x; kl[5] = a1.y; kl[6] = a1.z; kl[7] = a1.w;
-      kh[0] = b0.x; kh[1] = b0.y; kh[2] = b0.z; kh[3] = b0.w;
-      kh[4] = b1.x; kh[5] = b1.y; kh[6] = b1.z; kh[7] = b1.w;
-    }
-    // two independent accumulation chains (one per Q piece), added at the end
+    // ---- S^T = K Q^T: A = the K tile's code rows (tokens) by ldmatrix, in
+    // fragment order; two independent accumulation chains (one per Q piece)
     float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const uint32_t kbase = smem_addr(kb);
 #pragma unroll
-    for (int s2 = 0; s2 < 4; ++s2) {
-      const uint32_t a[4] = {kl[2 * s2], kh[2 * s2], kl[2 * s2 + 1], kh[2 * s2 + 1]};
-      mma_e4m3_16832(sacc, a, qb[s2][0][0], qb[s2][0][1]);
-      mma_e4m3_16832(sacc2, a, qb[s2][1][0], qb[s2][1][1]);
+      for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t a[4];
+        ldsm_x4(kbase + ld_off[s2], a);
+        mma_e4m3_16832(sacc, a, qb[s2][0][0], qb[s2][0][1]);
+        mma_e4m3_16832(sacc2, a, qb[s2][1][0], qb[s2][1][1]);
+      }
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) sacc[e] += sacc2[e];

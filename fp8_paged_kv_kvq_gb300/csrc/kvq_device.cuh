@@ -479,6 +479,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Four 8x8 matrices of 16-bit elements from shared memory in mma fragment
+// order: lanes 8m..8m+7 give the row addresses of matrix m; register m of
+// lane t holds row t/4, elements 2(t%4), 2(t%4)+1 of matrix m.  On byte
+// tiles (two bytes per element) this is the 8-bit m16n8k32 A fragment: rows
+// 0-7 / 8-15 in matrices 0/1 (k 0-15) and 2/3 (k 16-31).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
 // D = A * B + D, 16x8x32, e4m3 operands (the cache's own code bytes), fp32
 // accumulate.  Each register holds four consecutive k of one row (A) or one
 // column (B):
