@@ -272,7 +272,7 @@ class DeviceWorkload:
         self.cl_d = torch.from_numpy(self.lens).to(device)
         self.max_ctx = int(self.lens.max())
         self.P = partition_tokens or kvq.paged_decode_partition_tokens(
-            w.num_requests, H, w.block_size, self.max_ctx)
+            w.num_requests, R, w.num_q_heads, H, w.block_size, self.max_ctx)
         self.n_parts = (self.max_ctx + self.P - 1) // self.P
         need = kvq.paged_decode_workspace_size(w.num_requests, R, w.num_q_heads, H, D,
                                                w.block_size, self.max_ctx, self.P)

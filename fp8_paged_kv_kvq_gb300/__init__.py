@@ -81,7 +81,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "kvq_abi_version": (i32, []),
             "kvq_cache_bytes": (sz, [i64, i32, i32]),
             "kvq_quantize_scatter": (ctypes.c_int, [CP, P, i64, P, i64, i64, P, P, P]),
-            "kvq_paged_decode_partition_tokens": (i32, [i32, i32, i32, i32]),
+            "kvq_paged_decode_partition_tokens": (i32, [i32, i32, i32, i32, i32, i32]),
             "kvq_paged_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32, i32]),
             "kvq_paged_decode": (ctypes.c_int, [CP, P, i32, i32, i32, P, i32, P, i32,
                                                 ctypes.c_float, i32, P, P, sz, P, P]),
@@ -205,10 +205,11 @@ def quantize_scatter(cache: Cache, k: torch.Tensor, v: torch.Tensor, slot_ids: t
            "kvq_quantize_scatter")
 
 
-def paged_decode_partition_tokens(num_requests: int, num_kv_heads: int, block_size: int,
+def paged_decode_partition_tokens(num_requests: int, rows_per_request: int, num_q_heads: int,
+                                  num_kv_heads: int, block_size: int,
                                   max_context_len: int) -> int:
-    return load().kvq_paged_decode_partition_tokens(num_requests, num_kv_heads, block_size,
-                                                    max_context_len)
+    return load().kvq_paged_decode_partition_tokens(num_requests, rows_per_request, num_q_heads,
+                                                    num_kv_heads, block_size, max_context_len)
 
 
 def paged_decode_workspace_size(num_requests: int, rows_per_request: int, num_q_heads: int,

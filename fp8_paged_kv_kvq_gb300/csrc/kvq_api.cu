@@ -65,18 +65,27 @@ kvq_status check_cache(const kvq_cache *c, bool need_block_size) {
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-// Tokens per partition, a power of two in [256, 8192].  Long contexts (>= 64K
-// tokens) on pages of >= 16 tokens with KV heads in groups of 4 suit the
-// page-major kernel (one CTA per 4 heads, partition and request): the largest
-// P with at least ~12 such CTAs per SM.  Otherwise (one CTA per KV head,
-// partition and request) the largest P with 2P <= N H ctx / (4 SMs).
+// Tokens per partition, a power of two in [256, 8192] (up to 32768 for the
+// tcgen05 kernel).  9..32 stacked rows per KV head on pages of 16..128 tokens
+// with KV heads in groups of 4 go to the tcgen05 kernel (one CTA per SM, with
+// a per-CTA setup and epilogue): the longest P within its 512 pages that
+// still gives ~6 waves of CTAs.  Long contexts (>= 64K tokens) on pages of
+// >= 16 tokens with KV heads in groups of 4 suit the page-major kernel (one
+// CTA per 4 heads, partition and request): the largest P with at least ~12
+// such CTAs per SM.  Otherwise (one CTA per KV head, partition and request)
+// the largest P with 2P <= N H ctx / (4 SMs).
 int32_t heuristic_partition(int32_t num_requests, int32_t num_kv_heads, int32_t block_size,
-                            int32_t max_context_len) {
+                            int32_t max_context_len, int64_t rows) {
   const int64_t sms = current_sm_count();
   const int64_t n = num_requests > 0 ? num_requests : 1;
   const int64_t h = num_kv_heads > 0 ? num_kv_heads : 1;
   const int64_t ctx = max_context_len > 0 ? max_context_len : 1;
   int32_t p = 256;
+  if (rows > 8 && rows <= 32 && block_size >= 16 && block_size <= 128 && h % 4 == 0) {
+    const int64_t cap = std::min<int64_t>(32768, 512 * static_cast<int64_t>(block_size));
+    while (int64_t(p) * 2 <= cap && n * h * ((ctx + 2 * p - 1) / (2 * p)) >= 6 * sms) p *= 2;
+    return p;
+  }
   if (ctx >= 65536 && block_size >= 16 && h % 4 == 0) {
     const int64_t target = n * (h / 4) * ctx / (12 * sms);
     while (p < 8192 && int64_t(p) * 2 <= target) p *= 2;
@@ -115,8 +124,7 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
   s->partition_tokens = partition_tokens > 0
                             ? partition_tokens
                             : heuristic_partition(num_requests, cache->num_kv_heads,
-                                                  cache->block_size,
-                                                  max_context_len);
+                                                  cache->block_size, max_context_len, M);
   const int64_t np = (static_cast<int64_t>(max_context_len) + s->partition_tokens - 1) /
                      s->partition_tokens;
   if (np > 65535) return KVQ_ERR_UNSUPPORTED;
@@ -178,9 +186,13 @@ kvq_status kvq_quantize_scatter(const kvq_cache *cache, const void *k, int64_t k
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t num_kv_heads,
+int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t rows_per_request,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
                                           int32_t block_size, int32_t max_context_len) {
-  return heuristic_partition(num_requests, num_kv_heads, block_size, max_context_len);
+  const int64_t rows = (num_kv_heads > 0 && num_q_heads % num_kv_heads == 0 && rows_per_request > 0)
+                           ? static_cast<int64_t>(rows_per_request) * (num_q_heads / num_kv_heads)
+                           : 1;
+  return heuristic_partition(num_requests, num_kv_heads, block_size, max_context_len, rows);
 }
 
 size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,

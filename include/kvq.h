@@ -130,10 +130,12 @@ kvq_status kvq_quantize_scatter(const kvq_cache *cache,
                                 int32_t *err_flags, kvq_stream_t stream);
 
 /* Tokens per split-K partition that kvq_paged_decode uses when passed 0: a
- * power of two in [256, 8192] chosen from the batch shape and the current
- * device's SM count (152 is assumed when no device is visible); always a
- * multiple of 64. */
-int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t num_kv_heads,
+ * power of two in [256, 8192] (up to 32768 when 9..32 query rows per KV head,
+ * rows_per_request * num_q_heads / num_kv_heads, go to the tensor-core verify
+ * kernel) chosen from the batch shape and the current device's SM count (152
+ * is assumed when no device is visible); always a multiple of 64. */
+int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t rows_per_request,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
                                           int32_t block_size, int32_t max_context_len);
 
 /* Workspace bytes kvq_paged_decode needs for this shape (0 when every request

@@ -113,8 +113,13 @@ def test_workspace_size_formula(lib):
 
 def test_partition_heuristic_is_a_power_of_two_multiple_of_64(lib):
     for N, maxc in ((1, 64), (32, 8192), (64, 32768), (2, 1 << 20)):
-        p = lib.kvq_paged_decode_partition_tokens(N, 8, 16, maxc)
+        p = lib.kvq_paged_decode_partition_tokens(N, 1, 32, 8, 16, maxc)
         assert p % 64 == 0 and (p & (p - 1)) == 0 and 256 <= p <= 8192
+    # 9..32 stacked rows per KV head (tensor-core verify): longer partitions,
+    # within the kernel's 512 pages per partition
+    for N, bs, maxc in ((64, 64, 32768), (64, 16, 32768), (2, 128, 1 << 20)):
+        p = lib.kvq_paged_decode_partition_tokens(N, 4, 64, 8, bs, maxc)
+        assert p % 64 == 0 and (p & (p - 1)) == 0 and 256 <= p <= min(32768, 512 * bs)
 
 
 def test_dequant_validation(lib):
