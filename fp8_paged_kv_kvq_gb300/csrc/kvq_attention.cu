@@ -822,6 +822,63 @@ attn_combine_kernel(const CombineParams p) {
   *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
 }
 
+// Rows of few partitions (<= 16): one warp per row, eight rows per CTA.  Lane
+// l folds dims 4l..4l+3 over the row's partitions with a running log-sum-exp,
+// four partitions' (max, sum) and outputs loaded before any is used, and
+// writes the row: no shared memory, no CTA barrier.
+constexpr int kCombineRowsPerCta = 8;
+
+__global__ void __launch_bounds__(kCombineRowsPerCta * 32)
+attn_combine_rows_kernel(const CombineParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineRowsPerCta + (threadIdx.x >> 5);
+  allow_dependents_launch();
+  if (row >= p.rows_total) return;
+  const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
+  // the context length is not written by the partials kernel: read it while
+  // that kernel drains, and wait only before reading the partials
+  int L = p.context_lens[r];
+  L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
+  const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
+  if (n_parts <= 1) return;                       // written by the partials kernel
+  grid_dependency_wait();
+  const float2 *ml = p.ml_part + row * p.n_parts_max;
+  const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * p.n_parts_max * kHeadDim) +
+                     lane;
+  float m_w = -INFINITY, lsum = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = 0; q0 < n_parts; q0 += 4) {
+    float2 v[4];
+    float4 o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = make_float2(-INFINITY, 0.0f);
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q0 + k < n_parts) {
+        v[k] = ml[q0 + k];
+        o[k] = op[static_cast<int64_t>(q0 + k) * (kHeadDim / 4)];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (v[k].x == -INFINITY) continue;          // a partition that saw no token
+      const float mn = fmaxf(m_w, v[k].x);
+      const float a = ex2(m_w - mn), b = ex2(v[k].x - mn);
+      lsum = lsum * a + v[k].y * b;
+      acc.x = acc.x * a + o[k].x * b;
+      acc.y = acc.y * a + o[k].y * b;
+      acc.z = acc.z * a + o[k].z * b;
+      acc.w = acc.w * a + o[k].w * b;
+      m_w = mn;
+    }
+  }
+  const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
+}
+
 template <int MT, bool kTma>
 cudaError_t launch_partials_mt(const AttnParams &p, const CUtensorMap &mk, const CUtensorMap &mv,
                                dim3 grid, cudaStream_t stream) {
@@ -1026,6 +1083,11 @@ cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens,
   p.o_part = o_part;
   p.ml_part = ml_part;
   p.out = static_cast<uint16_t *>(out);
+  if (s.num_partitions <= 16) {
+    const int64_t ctas = (p.rows_total + kCombineRowsPerCta - 1) / kCombineRowsPerCta;
+    return launch_overlapped(attn_combine_rows_kernel, dim3(static_cast<unsigned>(ctas)),
+                             dim3(kCombineRowsPerCta * 32), 0, stream, p);
+  }
   if (s.num_partitions >= 64)
     return launch_overlapped(attn_combine_kernel<16>, dim3(static_cast<unsigned>(p.rows_total)),
                              dim3(16 * 32), 0, stream, p);
