@@ -739,7 +739,7 @@ struct CombineParams {
 // sum) and outputs before using any, so the merge costs one memory round trip
 // per four partitions of a warp; the warps' (max, sum, output) meet in shared
 // memory.
-template <int kCombineWarps>
+template <int kCombineWarps, int kPre>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 attn_combine_kernel(const CombineParams p) {
   __shared__ float red[kCombineWarps];
@@ -761,15 +761,15 @@ attn_combine_kernel(const CombineParams p) {
   const float2 *ml = p.ml_part + row * p.n_parts_max;
   const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * p.n_parts_max * kHeadDim) +
                      lane;
-  // warp w folds partitions w, w+4, ... with a running log-sum-exp; four of
+  // warp w folds partitions w, w+W, ... with a running log-sum-exp; kPre of
   // its partitions' (max, sum) and outputs are loaded before any is used
   float m_w = -INFINITY, lsum = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int q0 = warp; q0 < n_parts; q0 += 4 * kCombineWarps) {
-    float2 v[4];
-    float4 o[4];
+  for (int q0 = warp; q0 < n_parts; q0 += kPre * kCombineWarps) {
+    float2 v[kPre];
+    float4 o[kPre];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kPre; ++k) {
       const int q = q0 + k * kCombineWarps;
       v[k] = make_float2(-INFINITY, 0.0f);
       o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -779,7 +779,7 @@ attn_combine_kernel(const CombineParams p) {
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kPre; ++k) {
       if (v[k].x == -INFINITY) continue;          // a partition that saw no token
       const float mn = fmaxf(m_w, v[k].x);
       const float a = ex2(m_w - mn), b = ex2(v[k].x - mn);
@@ -1088,10 +1088,15 @@ cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens,
     return launch_overlapped(attn_combine_rows_kernel, dim3(static_cast<unsigned>(ctas)),
                              dim3(kCombineRowsPerCta * 32), 0, stream, p);
   }
+  // few, long rows (long contexts): more warps per row and more partitions
+  // per memory round trip
+  if (s.num_partitions >= 256)
+    return launch_overlapped(attn_combine_kernel<32, 8>, dim3(static_cast<unsigned>(p.rows_total)),
+                             dim3(32 * 32), 0, stream, p);
   if (s.num_partitions >= 64)
-    return launch_overlapped(attn_combine_kernel<16>, dim3(static_cast<unsigned>(p.rows_total)),
+    return launch_overlapped(attn_combine_kernel<16, 4>, dim3(static_cast<unsigned>(p.rows_total)),
                              dim3(16 * 32), 0, stream, p);
-  return launch_overlapped(attn_combine_kernel<4>, dim3(static_cast<unsigned>(p.rows_total)),
+  return launch_overlapped(attn_combine_kernel<4, 4>, dim3(static_cast<unsigned>(p.rows_total)),
                            dim3(4 * 32), 0, stream, p);
 }
 
