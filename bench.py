@@ -770,9 +770,14 @@ def run_reference(args, rank, world):
         total_t += time.perf_counter() - t0
         total_b += nb
     value = total_b / total_t / 1e9
-    sample = (f"each step one (request, query row, query head) unit, context capped at "
-              f"{s.token_cap} tokens, plus its share of the new-row store"
-              if name != "store" else f"each step {rows_per_step} rows of the store")
+    if name == "store":
+        sample = f"each step {rows_per_step} rows of the store"
+    else:
+        max_len = int(s.lens.max())
+        ctx = ("its full context" if s.token_cap >= max_len
+               else f"its context capped at {s.token_cap} tokens")
+        sample = (f"each step one (request, query row, query head) unit over {ctx}, plus its "
+                  f"share of the new-row store")
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
