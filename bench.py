@@ -271,11 +271,15 @@ class DeviceWorkload:
         self.bt_d = torch.from_numpy(self.bt).to(device)
         self.cl_d = torch.from_numpy(self.lens).to(device)
         self.max_ctx = int(self.lens.max())
+        # partition size passed to the library: 0 leaves it (and the kernel) to
+        # the library; self.P is the partition it would use for partitioned kernels
+        self.P_arg = partition_tokens
         self.P = partition_tokens or kvq.paged_decode_partition_tokens(
             w.num_requests, R, w.num_q_heads, H, w.block_size, self.max_ctx)
         self.n_parts = (self.max_ctx + self.P - 1) // self.P
+        self.balanced = self.P_arg == 0 and self._balanced_mode()
         need = kvq.paged_decode_workspace_size(w.num_requests, R, w.num_q_heads, H, D,
-                                               w.block_size, self.max_ctx, self.P)
+                                               w.block_size, self.max_ctx, self.P_arg)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty_like(self.q)
         torch.cuda.synchronize(device)
@@ -310,20 +314,40 @@ class DeviceWorkload:
         R, N = w.rows_per_request, w.num_requests
         self._p_args = (ctypes.byref(self._cst), P(self.q.data_ptr()), N, R, w.num_q_heads,
                         P(self.bt_d.data_ptr()), self.bt.shape[1], P(self.cl_d.data_ptr()),
-                        self.max_ctx, ctypes.c_float(w.sm_scale), self.P, P(self.out.data_ptr()),
+                        self.max_ctx, ctypes.c_float(w.sm_scale), self.P_arg, P(self.out.data_ptr()),
                         P(self.ws.data_ptr()), self.ws.numel(), P(self.err.data_ptr()), sp)
         self._c_args = (ctypes.byref(self._cst), N, R, w.num_q_heads, self.bt.shape[1],
-                        P(self.cl_d.data_ptr()), self.max_ctx, self.P, P(self.out.data_ptr()),
+                        P(self.cl_d.data_ptr()), self.max_ctx, self.P_arg, P(self.out.data_ptr()),
                         P(self.ws.data_ptr()), self.ws.numel(), sp)
+
+    def _balanced_mode(self):
+        """Whether the library runs the load-balanced kernel for this shape when
+        left to choose: at most 8 stacked rows, pages of >= 16 tokens, KV heads
+        in groups of 4, at most 1024 requests, a CTA's chunks within its 520
+        block ids, and a page-major partition grid under 9 CTAs per SM."""
+        w = self.w
+        rows = w.rows_per_request * w.group
+        sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        cmax = (self.max_ctx + 15) // 16
+        hg = w.num_kv_heads // 4
+        per_cta = (w.num_requests * hg * cmax + 3 * sms - 1) // (3 * sms)
+        b = max(per_cta, (cmax + 14) // 15)
+        page_ctas = hg * self.n_parts * w.num_requests
+        return (rows <= 8 and w.block_size >= 16 and w.num_kv_heads % 4 == 0
+                and 1 <= w.num_requests <= 1024 and b * 16 // w.block_size + 2 <= 520
+                and page_ctas < 9 * sms)
 
     def partials_kernel(self):
         """(kernel, source) the library launches for this shape's partials:
+        the load-balanced kernel when the library picks it (see _stream_mode);
         for at most 8 stacked rows per KV head the page-major kernel when its
         grid (4 heads per CTA) is at least 9 CTAs per SM, else the skinny one
         (pages of at least 8 tokens); the tcgen05 kernel for 9..32 rows (pages
         of 16..128 tokens, KV heads a multiple of 4, partitions a multiple of
         128 tokens); else the general one."""
         w = self.w
+        if self.balanced:
+            return "attn_stream_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_stream.cu"
         rows = w.rows_per_request * w.group
         page_ctas = (w.num_kv_heads // 4) * self.n_parts * w.num_requests
         sms = torch.cuda.get_device_properties(self.device).multi_processor_count
@@ -508,8 +532,12 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         "wall_s_timed_region": round(wall1 - wall0, 3),
     }
     if args.workload != "store":
-        res["config"]["partition_tokens"] = wl.P
-        res["config"]["partitions"] = wl.n_parts
+        if wl.balanced:
+            res["config"]["split"] = ("load-balanced: the batch's 16-token chunks split evenly "
+                                      "over a persistent grid (3 CTAs per SM)")
+        else:
+            res["config"]["partition_tokens"] = wl.P
+            res["config"]["partitions"] = wl.n_parts
         res["kernels_us"]["paged_decode_partials"] = round(1e3 * sum(st_p) / K, 3)
         res["kernels_us"]["paged_decode_combine"] = round(1e3 * sum(st_c) / K, 3)
         dom_ms, dom_bytes = sum(st_p) / K, wl.attn_bytes()

@@ -133,12 +133,41 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
     return KVQ_ERR_UNSUPPORTED;
   s->log2_block = log2_exact(cache->block_size);
   s->sms = current_sm_count();
+  s->stream = 0;
+  // With the partition size left to the library, batches of <= 8 stacked rows
+  // whose page-major partition grid would be small (under ~3 waves) go to the
+  // load-balanced kernel, which splits the batch's tokens evenly over a
+  // persistent grid.  It loads the scale planes by TMA; for planes that are
+  // not 16-byte aligned the partitioned kernels run instead, with partitions
+  // long enough to fit the same workspace (<= kStreamSlots of them).
+  if (partition_tokens == 0 && kvq::attn_stream_shape_ok(cache->num_kv_heads, *s)) {
+    const int64_t page_ctas = static_cast<int64_t>(cache->num_kv_heads / 4) * s->num_partitions *
+                              num_requests;
+    if (page_ctas < 9LL * s->sms) {
+      const bool aligned16 = aligned(cache->k_scales, 16) && aligned(cache->v_scales, 16);
+      if (aligned16) {
+        s->stream = 1;
+        s->num_partitions = kvq::kStreamSlots;
+      } else {
+        const int64_t need = (static_cast<int64_t>(max_context_len) + kvq::kStreamSlots - 1) /
+                             kvq::kStreamSlots;
+        const int64_t p64 = (need + 63) / 64 * 64;
+        if (p64 > s->partition_tokens) s->partition_tokens = static_cast<int32_t>(p64);
+        const int64_t np2 = (static_cast<int64_t>(max_context_len) + s->partition_tokens - 1) /
+                            s->partition_tokens;
+        s->num_partitions = np2 > 0 ? static_cast<int32_t>(np2) : 1;
+      }
+    }
+  }
   return KVQ_OK;
 }
 
 size_t workspace_for(const kvq::AttnShape &s) {
   const int64_t rows_total =
       static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
+  if (s.stream)
+    return kvq::attn_stream_plan_bytes(s.num_requests) +
+           kvq::attn_workspace_bytes(rows_total, kvq::kStreamSlots);
   return kvq::attn_workspace_bytes(rows_total, s.num_partitions);
 }
 

@@ -1031,6 +1031,9 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   p.ml_part = nullptr;
   if (s.num_partitions > 1)
     carve_workspace(workspace, rows_total, s.num_partitions, &p.o_part, &p.ml_part);
+  if (s.stream)
+    return launch_attn_partials_stream(c, s, q, block_tables, context_lens, sm_scale, out,
+                                       workspace, err_flags, stream);
   // the page-major kernel reads 4 heads per CTA: worth it once its grid is at
   // least ~3 waves (3 CTAs per SM); smaller grids go to one CTA per head
   const int64_t page_ctas =
@@ -1068,6 +1071,7 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
 
 cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,
                                 void *workspace, cudaStream_t stream) {
+  if (s.stream) return launch_attn_combine_stream(s, out, workspace, stream);
   if (s.num_partitions <= 1) return cudaSuccess;
   CombineParams p;
   p.context_lens = context_lens;

@@ -48,7 +48,28 @@ struct AttnShape {
   int32_t num_partitions;     // ceil(max_context_len / P), >= 1
   int32_t log2_block;
   int32_t sms;                // SMs of the current device
+  int32_t stream;             // 1: the load-balanced kernel (partials in stream slots)
 };
+
+// The load-balanced decode kernel's layout: a plan ([0] chunks per CTA, [1]
+// requests, [2 ..] per-request chunk prefix) then partials in kStreamSlots
+// slots per output row.
+constexpr int32_t kStreamSlots = 16;
+constexpr int32_t kStreamMaxRequests = 1024;
+size_t attn_stream_plan_bytes(int32_t num_requests);
+
+// Whether a shape suits the load-balanced kernel (apart from the cache's
+// scale alignment): at most 8 stacked rows, pages of >= 16 tokens, KV heads in
+// groups of 4, at most kStreamMaxRequests requests, a segment's block ids
+// within its window.
+bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s);
+cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, const void *q,
+                                        const int32_t *block_tables,
+                                        const int32_t *context_lens, float sm_scale, void *out,
+                                        void *workspace, int32_t *err_flags,
+                                        cudaStream_t stream);
+cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
+                                       cudaStream_t stream);
 
 // Workspace carve-up: partial outputs [rows_total][num_partitions][128] fp32,
 // then (max, denominator) pairs [rows_total][num_partitions][2] fp32.

@@ -72,6 +72,31 @@ def test_verify_shapes(R, Hq, H, bs, partition_tokens):
     assert_attention_close(out, ref, f"R={R} Hq={Hq} H={H} P={partition_tokens}")
 
 
+@pytest.mark.parametrize("R,Hq,H,lens", [
+    (1, 32, 8, [0, 1, 15, 16, 17, 300, 1000, 2047, 33, 4096, 5, 0, 777]),
+    (2, 16, 4, [3, 129, 640, 64, 2]),      # 8 stacked rows: 2 query rows x GQA 4
+    (1, 8, 8, [6000, 20, 40]),             # one dominant request: 15 pieces per head group
+])
+def test_load_balanced_split(R, Hq, H, lens):
+    """The library's own choice for small batches of <= 8 stacked rows on
+    pages of >= 16 tokens: the batch's 16-token chunks spread evenly over a
+    persistent grid, a (request, head group) cut into up to 16 pieces that the
+    combine merges; empty contexts give zero rows."""
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=len(lens),
+                         rows_per_request=R, num_q_heads=Hq, num_kv_heads=H)
+    lens = np.array(lens, dtype=np.int32)
+    built = build_paged(w, lens)
+    q = _queries(w, len(lens), R, 5)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(built, q, R, w.sm_scale, err=err)
+    ref, _ = oracle_decode(built, q, R, Hq, w.sm_scale)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    empty = np.repeat(lens == 0, R)
+    assert not out.float()[torch.from_numpy(empty)].any()
+    assert_attention_close(out, ref, f"balanced R={R} Hq={Hq} H={H}")
+
+
 def _build_custom(w, kv_per_request, spare_blocks=3):
     """GPU and oracle caches from given bf16 K/V rows [L, H, D] per request."""
     lens = np.array([k.shape[0] for k, _ in kv_per_request], dtype=np.int32)
