@@ -297,7 +297,7 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
     // ---- scale, mask, online softmax.  sacc: [tok g][row 2c], [g][2c+1],
     // [g+8][2c], [g+8][2c+1]
     const float ks_lo = ksv[4 * g], ks_hi = ksv[4 * (g + 8)];
-    const float vs_lo = vsv[4 * g], vs_hi = vsv[4 * (g + 8)];
+    float vs_lo = vsv[4 * g], vs_hi = vsv[4 * (g + 8)];
     float x[4];
     x[0] = sacc[0] * ks_lo * rowf[0];
     x[1] = sacc[1] * ks_lo * rowf[1];
@@ -308,6 +308,10 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
       x[1] = (j0 + g < vis[1]) ? x[1] : -INFINITY;
       x[2] = (j0 + g + 8 < vis[0]) ? x[2] : -INFINITY;
       x[3] = (j0 + g + 8 < vis[1]) ? x[3] : -INFINITY;
+      // slots past the context end hold whatever they held: keep their value
+      // scales out of the running bound
+      vs_lo = (j0 + g < L) ? vs_lo : 0.0f;
+      vs_hi = (j0 + g + 8 < L) ? vs_hi : 0.0f;
     }
     float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
     float vmax = fmaxf(vs_lo, vs_hi);

@@ -201,19 +201,25 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
 
   if (warp == kStHeads) {
     // ---------------------------------------------------------- producer
-    grid_dependency_wait();
     uint32_t u = 0;                    // chunks issued (lane 0's count)
     bool bad = false, stop = false;
-    for (int64_t x = x_begin; x < x_end && !stop;) {
-      const Segment sg = locate(pre, N, hg, x, x_end);
-      // the segment's block ids (all lanes), then lane 0 issues its chunks
+    // a segment's block ids into shared memory (all lanes); the first
+    // segment's before the dependency wait (the tables are not written by
+    // the previous kernel)
+    auto stage_ids = [&](const Segment &sg) {
       const int p0 = (kChunk * sg.c0) >> p.log2_bs;
-      const int p1 = (kChunk * (sg.c0 + sg.n) - 1) >> p.log2_bs;
-      const int np = p1 - p0 + 1;
+      const int np = ((kChunk * (sg.c0 + sg.n) - 1) >> p.log2_bs) - p0 + 1;
       const int32_t *bt = p.block_tables + static_cast<int64_t>(sg.r) * p.max_blocks + p0;
       __syncwarp();                    // the previous segment's ids are no longer read
       for (int i = lane; i < np && i < kStMaxPages; i += 32) bt_s[i] = bt[i];
       __syncwarp();
+    };
+    stage_ids(locate(pre, N, hg, x_begin, x_end));
+    grid_dependency_wait();
+    for (int64_t x = x_begin; x < x_end && !stop;) {
+      const Segment sg = locate(pre, N, hg, x, x_end);
+      if (x != x_begin) stage_ids(sg);
+      const int p0 = (kChunk * sg.c0) >> p.log2_bs;
       if (lane == 0) {
         for (int k = 0; k < sg.n; ++k, ++u) {
           const int st = u % kStStages;
@@ -590,11 +596,11 @@ attn_combine_stream_kernel(const StCombineParams p) {
                        lane;
     float m_w = -INFINITY, lsum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q0 = 0; q0 < n; q0 += 4) {
-      float2 v[4];
-      float4 o[4];
+    for (int q0 = 0; q0 < n; q0 += 8) {      // eight pieces per memory round trip
+      float2 v[8];
+      float4 o[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         v[k] = make_float2(-INFINITY, 0.0f);
         o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q0 + k < n) {
@@ -603,7 +609,7 @@ attn_combine_stream_kernel(const StCombineParams p) {
         }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         if (v[k].x == -INFINITY) continue;        // a piece that saw no visible token
         const float mn = fmaxf(m_w, v[k].x);
         const float a = st_ex2(m_w - mn), b = st_ex2(v[k].x - mn);
