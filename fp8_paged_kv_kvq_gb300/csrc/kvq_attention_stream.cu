@@ -307,15 +307,9 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         uint32_t c1w = 0u, c2w = 0u;
         if (rx != 0.0f) {
           const float inv = __int_as_float((254u << 23) - __float_as_uint(rx));
-          const float xs[4] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y)};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float xv = xs[t] * inv;
-            const uint32_t c1 = e4m3_round(xv, xv);
-            const float res = xv - e4m3_to_f32(c1);
-            c1w |= c1 << (8 * t);
-            c2w |= e4m3_round(res, res) << (8 * t);
-          }
+          const float xs[4] = {bf16_lo(v.x) * inv, bf16_hi(v.x) * inv, bf16_lo(v.y) * inv,
+                               bf16_hi(v.y) * inv};
+          e4m3_pieces4(xs, c1w, c2w);
         }
         *reinterpret_cast<uint32_t *>(plane + m * kHeadDim + 4 * lane) = c1w;
         *reinterpret_cast<uint32_t *>(plane + kStRows * kHeadDim + m * kHeadDim + 4 * lane) = c2w;

@@ -163,6 +163,22 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __fmul_rn(__uint_as_float(bits), 0x1p120f);
 }
 
+// The two e4m3 pieces of four query elements: p1 = e4m3(x), p2 = e4m3(x - p1)
+// (the difference is exact in binary32), four codes per word, element t in
+// byte t.  Through the hardware conversions: e4m3x2_rn rounds as e4m3_round,
+// and every e4m3 value is an f16.  For x of at most 8 significant bits inside
+// e4m3's range, x = p1 + p2 exactly.
+__device__ __forceinline__ void e4m3_pieces4(const float (&x)[4], uint32_t &c1w, uint32_t &c2w) {
+  const uint32_t a = e4m3x2_rn(x[0], x[1]), b = e4m3x2_rn(x[2], x[3]);
+  float d[4];
+  asm("{\n .reg .b16 l0, h0, l1, h1;\n mov.b32 {l0, h0}, %4;\n mov.b32 {l1, h1}, %5;\n"
+      " cvt.f32.f16 %0, l0;\n cvt.f32.f16 %1, h0;\n cvt.f32.f16 %2, l1;\n cvt.f32.f16 %3, h1;\n}\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(e4m3x2_to_f16x2(a)), "r"(e4m3x2_to_f16x2(b)));
+  c1w = a | (b << 16);
+  c2w = e4m3x2_rn(x[0] - d[0], x[1] - d[1]) | (e4m3x2_rn(x[2] - d[2], x[3] - d[3]) << 16);
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
