@@ -330,7 +330,7 @@ class DeviceWorkload:
         sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         cmax = (self.max_ctx + 15) // 16
         hg = w.num_kv_heads // 4
-        per_cta = (w.num_requests * hg * cmax + 3 * sms - 1) // (3 * sms)
+        per_cta = (w.num_requests * hg * (cmax + 3) + 3 * sms - 1) // (3 * sms)
         b = max(per_cta, (cmax + 14) // 15)
         page_ctas = hg * self.n_parts * w.num_requests
         return (rows <= 8 and w.block_size >= 16 and w.num_kv_heads % 4 == 0

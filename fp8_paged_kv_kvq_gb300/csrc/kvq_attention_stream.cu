@@ -58,7 +58,7 @@ constexpr int kOffStQ = kStStages * kStStageBytes;                    // [head][
 constexpr int kOffStRowExp = kOffStQ + kStHeads * 2 * kStRows * kHeadDim;
 constexpr int kOffStPre = kOffStRowExp + kStHeads * kStRows * 4;      // [N + 1] int32
 constexpr int kOffStBt = kOffStPre + (kStreamMaxRequests + 1 + 3) / 4 * 16;
-constexpr int kOffStBar = kOffStBt + kStMaxPages * 4;
+constexpr int kOffStBar = kOffStBt + 2 * kStMaxPages * 4;     // two segments' block ids
 constexpr int kOffStAbort = kOffStBar + 2 * kStStages * 8;
 constexpr int kStSmem = kOffStAbort + 16 + 1024;
 
@@ -97,11 +97,17 @@ __device__ __forceinline__ bool st_wait(uint32_t bar, uint32_t parity, volatile 
   return false;
 }
 
-// The segment holding global chunk x: request r (the largest with
-// (H/4) pre[r] <= x, so C_r > 0), head group g, first chunk c0 within the
-// request, and how many of the CTA's chunks (up to x_end) it covers.
+// In the work sequence a segment (request r, head group g) spans
+// V_r = C_r + kStreamSwitchChunks positions: the charge for starting it, then
+// its C_r chunks; pre[r] is the sum of V over the requests before r.  The
+// CTA's part of the segment holding position x (x < x_end): request r (the
+// largest with (H/4) pre[r] <= x, so V_r > 0), head group g, its first chunk
+// c0 and chunk count n (0 when the range ends inside the charge), the
+// segment's C, the position of its first chunk, and the position where the
+// CTA's range continues.
 struct Segment {
   int r, g, c0, n, C;
+  int64_t base, next;
 };
 
 __device__ __forceinline__ Segment locate(const int32_t *pre, int N, int hg, int64_t x,
@@ -114,12 +120,22 @@ __device__ __forceinline__ Segment locate(const int32_t *pre, int N, int hg, int
   }
   Segment s;
   s.r = lo;
-  s.C = pre[lo + 1] - pre[lo];
+  const int V = pre[lo + 1] - pre[lo];
+  s.C = V - kStreamSwitchChunks;
   const int64_t off = x - static_cast<int64_t>(hg) * pre[lo];
-  s.g = static_cast<int>(off / s.C);
-  s.c0 = static_cast<int>(off - static_cast<int64_t>(s.g) * s.C);
-  const int64_t left = x_end - x;
-  s.n = static_cast<int>(left < s.C - s.c0 ? left : s.C - s.c0);
+  s.g = static_cast<int>(off / V);
+  const int64_t start = static_cast<int64_t>(hg) * pre[lo] + static_cast<int64_t>(s.g) * V;
+  s.base = start + kStreamSwitchChunks;
+  const int64_t end = start + V < x_end ? start + V : x_end;
+  const int64_t xs = x > s.base ? x : s.base;
+  s.next = end;
+  if (xs >= end) {
+    s.c0 = 0;
+    s.n = 0;
+  } else {
+    s.c0 = static_cast<int>(xs - s.base);
+    s.n = static_cast<int>(end - xs);
+  }
   return s;
 }
 
@@ -151,7 +167,8 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   allow_dependents_launch();
   const int N = p.N;
   if (warp == 0) {
-    // chunks per request and their prefix: pre[r] = sum_{r' < r} C_r'
+    // positions per request (its chunks plus the segment charge) and their
+    // prefix: pre[r] is the sum of V over the requests before r
     int carry = 0;
     for (int r0 = 0; r0 < N; r0 += 32) {
       const int r = r0 + lane;
@@ -160,7 +177,8 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         if (blockIdx.x == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
         L = L < 0 ? 0 : p.ctx_limit;
       }
-      int v = (L + kChunk - 1) / kChunk;
+      const int c = (L + kChunk - 1) / kChunk;
+      int v = (c > 0) ? c + kStreamSwitchChunks : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int t = __shfl_up_sync(0xFFFFFFFFu, v, off);
@@ -203,22 +221,32 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
     // ---------------------------------------------------------- producer
     uint32_t u = 0;                    // chunks issued (lane 0's count)
     bool bad = false, stop = false;
-    // a segment's block ids into shared memory (all lanes); the first
-    // segment's before the dependency wait (the tables are not written by
-    // the previous kernel)
-    auto stage_ids = [&](const Segment &sg) {
+    // a segment's block ids into one of two shared-memory buffers (all lanes,
+    // cp.async): the first segment's before the dependency wait (the tables
+    // are not written by the previous kernel), each next one's while the
+    // current segment is issued, so a segment change costs no memory round
+    // trip in the issue loop
+    auto stage_ids = [&](const Segment &sg, int buf) {
       const int p0 = (kChunk * sg.c0) >> p.log2_bs;
       const int np = ((kChunk * (sg.c0 + sg.n) - 1) >> p.log2_bs) - p0 + 1;
       const int32_t *bt = p.block_tables + static_cast<int64_t>(sg.r) * p.max_blocks + p0;
-      __syncwarp();                    // the previous segment's ids are no longer read
-      for (int i = lane; i < np && i < kStMaxPages; i += 32) bt_s[i] = bt[i];
-      __syncwarp();
+      for (int i = lane; i < np && i < kStMaxPages; i += 32)
+        cp_async_4(bt_s + buf * kStMaxPages + i, bt + i, 4u);
+      cp_async_commit();
     };
-    stage_ids(locate(pre, N, hg, x_begin, x_end));
+    stage_ids(locate(pre, N, hg, x_begin, x_end), 0);
     grid_dependency_wait();
-    for (int64_t x = x_begin; x < x_end && !stop;) {
+    int buf = 0;
+    for (int64_t x = x_begin; x < x_end && !stop; buf ^= 1) {
       const Segment sg = locate(pre, N, hg, x, x_end);
-      if (x != x_begin) stage_ids(sg);
+      if (sg.n == 0) break;
+      cp_async_wait<0>();              // this segment's ids (issued a segment ago)
+      __syncwarp();
+      if (sg.next < x_end) {
+        const Segment nx = locate(pre, N, hg, sg.next, x_end);
+        if (nx.n > 0) stage_ids(nx, buf ^ 1);
+      }
+      const int32_t *ids = bt_s + buf * kStMaxPages;
       const int p0 = (kChunk * sg.c0) >> p.log2_bs;
       if (lane == 0) {
         for (int k = 0; k < sg.n; ++k, ++u) {
@@ -232,7 +260,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
           const uint32_t fb = smem_addr(&full[st]);
           const int j = kChunk * (sg.c0 + k);        // chunks lie within a page (bs >= 16)
           const int pi = (j >> p.log2_bs) - p0;
-          const uint32_t blk = (pi < kStMaxPages) ? static_cast<uint32_t>(bt_s[pi]) : 0xFFFFFFFFu;
+          const uint32_t blk = (pi < kStMaxPages) ? static_cast<uint32_t>(ids[pi]) : 0xFFFFFFFFu;
           uint32_t bytes = 0;
           if (blk >= p.num_blocks) {                 // also every negative id
             bad = true;
@@ -249,7 +277,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         }
       }
       stop = __shfl_sync(0xFFFFFFFFu, stop ? 1 : 0, 0) != 0;
-      x += sg.n;
+      x = sg.next;
     }
     if (lane == 0) {
       if (bad && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
@@ -274,6 +302,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   bool timed_out = false;
   for (int64_t x = x_begin; x < x_end && !timed_out;) {
     const Segment sg = locate(pre, N, hg, x, x_end);
+    if (sg.n == 0) break;
     const int r = sg.r;
     const int h = kStHeads * sg.g + w;
     int L = p.context_lens[r];
@@ -315,6 +344,23 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         *reinterpret_cast<uint32_t *>(plane + kStRows * kHeadDim + m * kHeadDim + 4 * lane) = c2w;
       }
       __syncwarp();
+    }
+    // the next segment's query rows and context length into L1 while this
+    // segment runs (its preparation then hits L1): lanes 2m, 2m + 1 take the
+    // two 128-byte lines of row m, lane 31 the context length
+    if (sg.next < x_end) {
+      const Segment nx = locate(pre, N, hg, sg.next, x_end);
+      const int hn = kStHeads * nx.g + w;
+      const int m = lane >> 1;
+      const void *a = nullptr;
+      if (m < p.M) {
+        const int i = m / p.G, gq = m - i * p.G;
+        a = p.q + ((static_cast<int64_t>(nx.r) * p.R + i) * p.Hq + hn * p.G + gq) * kHeadDim +
+            64 * (lane & 1);
+      } else if (lane == 31) {
+        a = p.context_lens + nx.r;
+      }
+      if (a != nullptr) asm volatile("prefetch.global.L1 [%0];" :: "l"(a));
     }
     // B fragments for k-step s2: b0 = dims 32 s2 + 4c + 0..3, b1 = + 16, row g
     uint32_t qb[4][2][2];
@@ -523,8 +569,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
     const float vsc = (ev == -1000) ? 0.0f : __int_as_float((127 + ev) << 23);   // undo 2^-ev
     const bool direct = (sg.c0 == 0 && sg.n == sg.C);
-    const int64_t seg_base = static_cast<int64_t>(hg) * pre[r] + static_cast<int64_t>(sg.g) * sg.C;
-    const int slot = static_cast<int>(blockIdx.x - seg_base / B);
+    const int slot = static_cast<int>(blockIdx.x - sg.base / B);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int n = 2 * c4 + e;
@@ -549,7 +594,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         if (g8 == 0) p.ml_part[sl] = make_float2(m_run[e], l_run[e]);
       }
     }
-    x += sg.n;
+    x = sg.next;
   }
   if (timed_out && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
 }
@@ -579,10 +624,12 @@ attn_combine_stream_kernel(const StCombineParams p) {
   const int g = (qh / p.G) / kStHeads;
   const int64_t B = p.plan[0];
   const int32_t *pre = p.plan + 2;
-  const int C = pre[r + 1] - pre[r];
+  const int V = pre[r + 1] - pre[r];
   uint2 packed = make_uint2(0u, 0u);
-  if (C > 0) {
-    const int64_t base = static_cast<int64_t>(p.H / kStHeads) * pre[r] + static_cast<int64_t>(g) * C;
+  if (V > 0) {
+    const int C = V - kStreamSwitchChunks;
+    const int64_t base = static_cast<int64_t>(p.H / kStHeads) * pre[r] +
+                         static_cast<int64_t>(g) * V + kStreamSwitchChunks;
     const int n = static_cast<int>((base + C - 1) / B - base / B) + 1;
     if (n <= 1) return;                // written by the partials kernel
     const float2 *ml = p.ml_part + row * kStreamSlots;
@@ -635,7 +682,8 @@ bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s) {
   const int64_t cmax = (static_cast<int64_t>(s.max_context_len) + kChunk - 1) / kChunk;
   const int64_t hg = num_kv_heads / kStHeads;
   // chunks per CTA stay within the block-id window of one segment
-  const int64_t per_cta = (s.num_requests * hg * cmax + 3 * sms - 1) / (3 * sms);
+  const int64_t per_cta =
+      (s.num_requests * hg * (cmax + kStreamSwitchChunks) + 3 * sms - 1) / (3 * sms);
   const int64_t b_min = (cmax + kStreamSlots - 2) / (kStreamSlots - 1);
   const int64_t b = per_cta > b_min ? per_cta : b_min;
   return s.rows <= kStRows && bs >= kChunk && num_kv_heads % kStHeads == 0 &&

@@ -55,6 +55,11 @@ struct AttnShape {
 // requests, [2 ..] per-request chunk prefix) then partials in kStreamSlots
 // slots per output row.
 constexpr int32_t kStreamSlots = 16;
+// A segment (the chunks of one request and head group) is charged this many
+// extra chunks at its start, so a CTA whose range crosses into a new segment
+// (a second query preparation, during which its ring stands full) gets
+// correspondingly less work.
+constexpr int32_t kStreamSwitchChunks = 3;
 constexpr int32_t kStreamMaxRequests = 1024;
 size_t attn_stream_plan_bytes(int32_t num_requests);
 
