@@ -80,6 +80,16 @@ def _load():
             lib.kvqo_quantize_scatter.argtypes = [P, i64, P, i64, i64, ctypes.c_int,
                                                   ctypes.c_int, P, i64, P, P, P, P]
             lib.kvqo_dequant_rows.restype = None
+            lib.kvqo_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.kvqo_e2m1_decode.restype = ctypes.c_double
+            lib.kvqo_e2m1_encode.argtypes = [ctypes.c_double]
+            lib.kvqo_e2m1_encode.restype = ctypes.c_uint8
+            lib.kvqo_mxfp4_group_exponent.argtypes = [ctypes.c_double]
+            lib.kvqo_mxfp4_group_exponent.restype = ctypes.c_int
+            lib.kvqo_mxfp4_quantize_rows.argtypes = [P, i64, ctypes.c_int, P, P]
+            lib.kvqo_mxfp4_quantize_rows.restype = None
+            lib.kvqo_mxfp4_dequant_rows.argtypes = [P, P, i64, ctypes.c_int, P]
+            lib.kvqo_mxfp4_dequant_rows.restype = None
             lib.kvqo_dequant_rows.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P,
                                               i64, ctypes.c_int, P]
             lib.kvqo_paged_attention.restype = i32
@@ -175,6 +185,51 @@ def quantize_scatter(k_bits: np.ndarray, k_token_stride: int,
         _ptr(k), k_token_stride, _ptr(v), v_token_stride, num_tokens, H, D,
         _ptr(sid), S, _ptr(cache["k_codes"]), _ptr(cache["v_codes"]),
         _ptr(cache["k_scales"]), _ptr(cache["v_scales"])))
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """E2M1 code (low 4 bits) -> value, float64 (MXFP4 element format)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.kvqo_e2m1_decode(int(x)) for x in c.ravel()]).reshape(c.shape)
+
+
+def e2m1_encode(q) -> np.ndarray:
+    """Nearest E2M1 code to each value (ties to even), sign kept."""
+    lib = _load()
+    a = np.asarray(q, dtype=np.float64)
+    return np.array([lib.kvqo_e2m1_encode(float(x)) for x in a.ravel()],
+                    dtype=np.uint8).reshape(a.shape)
+
+
+def mxfp4_group_exponent(amax: float) -> int:
+    """Smallest X with amax <= 6 * 2^X, clamped to [-127, 127]."""
+    return int(_load().kvqo_mxfp4_group_exponent(float(amax)))
+
+
+def mxfp4_quantize_rows(x_bf16_bits: np.ndarray):
+    """MXFP4 rows: x [..., D] bf16 bit patterns (D a multiple of 32) ->
+    (codes uint8 [..., D/2] packed pairs, exps uint8 [..., D/32] E8M0)."""
+    lib = _load()
+    x = _c(x_bf16_bits, np.uint16)
+    D = x.shape[-1]
+    assert D % 32 == 0
+    rows = x.reshape(-1, D)
+    codes = np.empty((rows.shape[0], D // 2), dtype=np.uint8)
+    exps = np.empty((rows.shape[0], D // 32), dtype=np.uint8)
+    lib.kvqo_mxfp4_quantize_rows(_ptr(rows), rows.shape[0], D, _ptr(codes), _ptr(exps))
+    return codes.reshape(x.shape[:-1] + (D // 2,)), exps.reshape(x.shape[:-1] + (D // 32,))
+
+
+def mxfp4_dequant_rows(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    """codes [n, D/2], exps [n, D/32] -> float32 [n, D]."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    e = _c(exps, np.uint8)
+    n, half = c.shape
+    out = np.empty((n, 2 * half), dtype=np.float32)
+    lib.kvqo_mxfp4_dequant_rows(_ptr(c), _ptr(e), n, 2 * half, _ptr(out))
+    return out
 
 
 def empty_cache(num_slots: int, H: int, D: int) -> dict:

@@ -391,3 +391,116 @@ int32_t kvqo_paged_attention_units(const uint8_t *k_codes, const uint8_t *v_code
     free(scores);
     return err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Compressed index keys, [ATOM] PR description, index-key bullet: FP8 with a
+ * per-row FP32 scale (the rows above, one index head per token: H = 1), or
+ * MXFP4 -- packed E2M1 pairs and one E8M0 exponent per 32 dims, rounded up
+ * so that a group never clips; FP4 decodes with bit operations.
+ *
+ * Readings of what the bullet leaves open (each one is listed in the design doc):
+ *  - E2M1 is the OCP microscaling element format: 1 sign bit, 2 exponent bits
+ *    (bias 1), 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ *  - E8M0 is a biased exponent: byte X + 127 stands for the group scale 2^X.
+ *  - "rounded up so a group never clips": X is the smallest integer with
+ *    group amax <= 6 * 2^X (the largest E2M1 magnitude), clamped to
+ *    [-127, 127]; an all-zero group gets X = -127.
+ *  - Each element becomes the E2M1 value nearest to x / 2^X (exact: a power
+ *    of two), ties to the code with an even mantissa bit, with x's sign (so
+ *    -0.0 and negative values that round to zero keep the sign bit).
+ *  - Element 2i goes to the low nibble of byte i, element 2i + 1 to the high.
+ *  - Dequantisation is decode(code) * 2^X rounded once to binary32. */
+
+double kvqo_e2m1_decode(uint8_t c)
+{
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 3;
+    int m = c & 1;
+    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -mag : mag;
+}
+
+/* Nearest E2M1 magnitude code (0..7) to a >= 0, ties to the even code. */
+static uint8_t e2m1_round_mag(double a)
+{
+    if (a >= 6.0)
+        return 7;
+    int lo = 0;
+    while (lo < 7 && kvqo_e2m1_decode((uint8_t)(lo + 1)) <= a)
+        ++lo;
+    /* decode(lo) <= a < decode(lo + 1) */
+    double vlo = kvqo_e2m1_decode((uint8_t)lo);
+    double vhi = kvqo_e2m1_decode((uint8_t)(lo + 1));
+    double half = 0.5 * (vlo + vhi);
+    if (a < half)
+        return (uint8_t)lo;
+    if (a > half)
+        return (uint8_t)(lo + 1);
+    return (uint8_t)((lo & 1) ? lo + 1 : lo); /* the mantissa bit is the code LSB */
+}
+
+uint8_t kvqo_e2m1_encode(double q)
+{
+    uint8_t sign = signbit(q) ? 0x8 : 0x0;
+    return (uint8_t)(sign | e2m1_round_mag(fabs(q)));
+}
+
+/* The group exponent X: the smallest integer with amax <= 6 * 2^X, clamped to
+ * [-127, 127] (-127 for an all-zero group). */
+int kvqo_mxfp4_group_exponent(double amax)
+{
+    if (amax == 0.0)
+        return -127;
+    int k;
+    frexp(amax, &k);                        /* amax in [2^(k-1), 2^k) */
+    int X = k - 4;                          /* 6 * 2^(k-4) < 2^(k-1) <= amax */
+    while (6.0 * ldexp(1.0, X) < amax)
+        ++X;
+    if (X < -127)
+        X = -127;
+    if (X > 127)
+        X = 127;
+    return X;
+}
+
+/* One row of D bf16 values (D a multiple of 32): codes [D/2] bytes, exps
+ * [D/32] E8M0 bytes. */
+void kvqo_mxfp4_quantize_row(const uint16_t *x, int D, uint8_t *codes, uint8_t *exps)
+{
+    for (int g = 0; g < D / 32; ++g) {
+        double amax = 0.0;
+        for (int d = 32 * g; d < 32 * g + 32; ++d) {
+            double a = fabs((double)kvqo_bf16_to_float(x[d]));
+            if (a > amax)
+                amax = a;
+        }
+        int X = kvqo_mxfp4_group_exponent(amax);
+        exps[g] = (uint8_t)(X + 127);
+        for (int d = 32 * g; d < 32 * g + 32; d += 2) {
+            uint8_t c0 = kvqo_e2m1_encode(ldexp((double)kvqo_bf16_to_float(x[d]), -X));
+            uint8_t c1 = kvqo_e2m1_encode(ldexp((double)kvqo_bf16_to_float(x[d + 1]), -X));
+            codes[d / 2] = (uint8_t)(c0 | (c1 << 4));
+        }
+    }
+}
+
+void kvqo_mxfp4_quantize_rows(const uint16_t *x, int64_t n_rows, int D, uint8_t *codes,
+                              uint8_t *exps)
+{
+    for (int64_t i = 0; i < n_rows; ++i)
+        kvqo_mxfp4_quantize_row(x + i * D, D, codes + i * (D / 2), exps + i * (D / 32));
+}
+
+/* Rows [n, D] back to binary32: decode(code) * 2^X, one rounding. */
+void kvqo_mxfp4_dequant_rows(const uint8_t *codes, const uint8_t *exps, int64_t n_rows, int D,
+                             float *out)
+{
+    for (int64_t i = 0; i < n_rows; ++i) {
+        for (int d = 0; d < D; ++d) {
+            uint8_t byte = codes[i * (D / 2) + d / 2];
+            uint8_t c = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+            int X = (int)exps[i * (D / 32) + d / 32] - 127;
+            out[i * D + d] = (float)ldexp(kvqo_e2m1_decode(c), X);
+        }
+    }
+}
