@@ -28,12 +28,17 @@ __all__ = [
     "paged_decode", "paged_decode_partials", "paged_decode_combine",
     "paged_decode_workspace_size", "paged_decode_partition_tokens", "dequant_rows",
     "header_functions", "LIB_PATH", "HEADER_PATH",
+    "IndexCache", "INDEX_FP8", "INDEX_MXFP4", "index_cache_bytes", "index_quantize_scatter",
+    "index_dequant_rows",
     "ERRF_SLOT_RANGE", "ERRF_BLOCK_RANGE", "ERRF_CONTEXT_RANGE",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "kvq.h")
+
+INDEX_FP8 = 0
+INDEX_MXFP4 = 1
 
 ERRF_SLOT_RANGE = 1
 ERRF_BLOCK_RANGE = 2
@@ -55,6 +60,12 @@ class _CacheStruct(ctypes.Structure):
                 ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
                 ("num_slots", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32)]
+
+
+class _IndexCacheStruct(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("exponents", ctypes.c_void_p), ("num_slots", ctypes.c_int64),
+                ("format", ctypes.c_int32), ("dim", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -90,6 +101,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "kvq_paged_decode_combine": (ctypes.c_int, [CP, i32, i32, i32, i32, P, i32, i32,
                                                         P, P, sz, P]),
             "kvq_dequant_rows": (ctypes.c_int, [CP, P, i64, i32, P, P, P, P]),
+            "kvq_index_cache_bytes": (sz, [i64, i32, i32]),
+            "kvq_index_quantize_scatter": (ctypes.c_int, [ctypes.POINTER(_IndexCacheStruct), P,
+                                                          i64, i64, P, P, P]),
+            "kvq_index_dequant_rows": (ctypes.c_int, [ctypes.POINTER(_IndexCacheStruct), P, i64,
+                                                      i32, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -303,3 +319,82 @@ def dequant_rows(cache: Cache, slot_ids: torch.Tensor, out_dtype=torch.float32,
                                    _ptr(out_v), _ptr(err_flags), _stream(stream)),
            "kvq_dequant_rows")
     return out_k, out_v
+
+
+# ---------------------------------------------------------------------------
+# compressed index keys
+
+@dataclass
+class IndexCache:
+    """Device tensors of an index-key cache (one row of ``dim`` values per slot).
+
+    FP8:   codes uint8 [num_slots, dim], scales float32 [num_slots]
+    MXFP4: codes uint8 [num_slots, dim/2] (E2M1 pairs), exponents uint8
+           [num_slots, dim/32] (E8M0)"""
+    format: int
+    codes: torch.Tensor
+    scales: torch.Tensor | None = None
+    exponents: torch.Tensor | None = None
+
+    @staticmethod
+    def empty(num_slots: int, format: int, dim: int = 128, device="cuda") -> "IndexCache":
+        if format == INDEX_FP8:
+            return IndexCache(format,
+                              torch.zeros(num_slots, dim, dtype=torch.uint8, device=device),
+                              scales=torch.zeros(num_slots, dtype=torch.float32, device=device))
+        if format == INDEX_MXFP4:
+            return IndexCache(format,
+                              torch.zeros(num_slots, dim // 2, dtype=torch.uint8, device=device),
+                              exponents=torch.zeros(num_slots, dim // 32, dtype=torch.uint8,
+                                                    device=device))
+        raise ValueError("format must be INDEX_FP8 or INDEX_MXFP4")
+
+    @property
+    def num_slots(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def dim(self) -> int:
+        return self.codes.shape[1] * (1 if self.format == INDEX_FP8 else 2)
+
+    def struct(self) -> _IndexCacheStruct:
+        for t in (self.codes, self.scales, self.exponents):
+            if t is not None and not t.is_contiguous():
+                raise ValueError("index cache tensors must be contiguous")
+        return _IndexCacheStruct(self.codes.data_ptr(),
+                                 0 if self.scales is None else self.scales.data_ptr(),
+                                 0 if self.exponents is None else self.exponents.data_ptr(),
+                                 self.num_slots, self.format, self.dim)
+
+
+def index_cache_bytes(num_slots: int, format: int, dim: int = 128) -> int:
+    return load().kvq_index_cache_bytes(num_slots, format, dim)
+
+
+def index_quantize_scatter(cache: IndexCache, x: torch.Tensor, slot_ids: torch.Tensor,
+                           err_flags: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_index_quantize_scatter: bf16 rows [T, dim] (a view with unit inner
+    stride; any token stride) into ``cache`` at device int64 ``slot_ids``."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != cache.dim or x.stride(1) != 1:
+        raise ValueError(f"x: expected bf16 [T, {cache.dim}] with unit inner stride")
+    if slot_ids.dtype != torch.int64 or slot_ids.numel() != x.shape[0]:
+        raise ValueError("slot_ids must be int64 with one id per row")
+    st = cache.struct()
+    _check(load().kvq_index_quantize_scatter(ctypes.byref(st), _ptr(x), x.stride(0), x.shape[0],
+                                             _ptr(slot_ids), _ptr(err_flags), _stream(stream)),
+           "kvq_index_quantize_scatter")
+
+
+def index_dequant_rows(cache: IndexCache, slot_ids: torch.Tensor, out_dtype=torch.float32,
+                       err_flags: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvq_index_dequant_rows: fp32 or bf16 rows [n, dim] at ``slot_ids``."""
+    if slot_ids.dtype != torch.int64:
+        raise ValueError("slot_ids must be int64")
+    code = {torch.float32: 0, torch.bfloat16: 1}[out_dtype]
+    n = slot_ids.numel()
+    out = torch.empty((n, cache.dim), dtype=out_dtype, device=cache.codes.device)
+    st = cache.struct()
+    _check(load().kvq_index_dequant_rows(ctypes.byref(st), _ptr(slot_ids), n, code, _ptr(out),
+                                         _ptr(err_flags), _stream(stream)),
+           "kvq_index_dequant_rows")
+    return out

@@ -12,7 +12,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 1;
+constexpr int32_t kAbiVersion = 2;
 constexpr int32_t kMaxRowsPerKvHead = 128;
 constexpr int32_t kMaxPartitionTokens = 1 << 20;
 
@@ -317,6 +317,68 @@ kvq_status kvq_dequant_rows(const kvq_cache *cache, const int64_t *slot_ids, int
   if ((n + 7) / 8 > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
   return from_cuda(kvq::launch_dequant_rows(*cache, slot_ids, n, out_dtype, out_k, out_v,
                                             err_flags, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kvq_index_cache_bytes(int64_t num_slots, int32_t format, int32_t dim) {
+  if (num_slots < 0 || dim <= 0 || dim % 32 != 0) return 0;
+  if (format == KVQ_INDEX_FP8) return static_cast<size_t>(num_slots) * (dim + 4);
+  if (format == KVQ_INDEX_MXFP4) return static_cast<size_t>(num_slots) * (dim / 2 + dim / 32);
+  return 0;
+}
+
+}  // extern "C"
+
+namespace {
+
+kvq_status check_index_cache(const kvq_index_cache *c) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->num_slots < 0 || c->dim <= 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->format != KVQ_INDEX_FP8 && c->format != KVQ_INDEX_MXFP4) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->dim != kvq::kHeadDimAbi) return KVQ_ERR_UNSUPPORTED;
+  if (c->num_slots > 0) {
+    if (c->codes == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->format == KVQ_INDEX_FP8 && c->scales == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->format == KVQ_INDEX_MXFP4 && c->exponents == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  }
+  if (!aligned(c->codes, 16) || !aligned(c->scales, 4)) return KVQ_ERR_MISALIGNED;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_index_quantize_scatter(const kvq_index_cache *cache, const void *x,
+                                      int64_t x_token_stride, int64_t num_tokens,
+                                      const int64_t *slot_ids, int32_t *err_flags,
+                                      kvq_stream_t stream) {
+  kvq_status st = check_index_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (num_tokens < 0 || x_token_stride < 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;
+  if (x == nullptr || slot_ids == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(x, 16) || (x_token_stride % 8) != 0 || !aligned(slot_ids, 8) ||
+      !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  if ((num_tokens + 31) / 32 > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
+  return from_cuda(kvq::launch_index_quantize_scatter(*cache, x, x_token_stride, num_tokens,
+                                                      slot_ids, err_flags,
+                                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvq_status kvq_index_dequant_rows(const kvq_index_cache *cache, const int64_t *slot_ids,
+                                  int64_t n, int32_t out_dtype, void *out, int32_t *err_flags,
+                                  kvq_stream_t stream) {
+  kvq_status st = check_index_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n < 0 || (out_dtype != 0 && out_dtype != 1)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (n == 0) return KVQ_OK;
+  if (slot_ids == nullptr || out == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(slot_ids, 8) || !aligned(out, 16) || !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  if ((n + 3) / 4 > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
+  return from_cuda(kvq::launch_index_dequant_rows(*cache, slot_ids, n, out_dtype, out, err_flags,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

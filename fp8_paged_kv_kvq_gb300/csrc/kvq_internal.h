@@ -89,6 +89,15 @@ cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int
                                 int32_t out_dtype, void *out_k, void *out_v,
                                 int32_t *err_flags, cudaStream_t stream);
 
+cudaError_t launch_index_quantize_scatter(const kvq_index_cache &c, const void *x,
+                                          int64_t x_stride, int64_t num_tokens,
+                                          const int64_t *slot_ids, int32_t *err_flags,
+                                          cudaStream_t stream);
+
+cudaError_t launch_index_dequant_rows(const kvq_index_cache &c, const int64_t *slot_ids,
+                                      int64_t n, int32_t out_dtype, void *out,
+                                      int32_t *err_flags, cudaStream_t stream);
+
 cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const void *q,
                                  const int32_t *block_tables, const int32_t *context_lens,
                                  float sm_scale, void *out, void *workspace,

@@ -226,6 +226,181 @@ dequant_rows_kernel(const DequantParams p) {
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Compressed index keys (ATOM PR #2655, PR description, index-key bullet):
+// FP8 with one FP32 scale per row (the K/V row format), or MXFP4 -- packed
+// E2M1 pairs with one E8M0 exponent per 32 dims, rounded up so a group never
+// clips.  Rows of 128 values, one per token; each 4-lane group owns a row and
+// each lane 32 values, which for MXFP4 is exactly one exponent group.
+struct IndexParams {
+  const uint16_t *x;
+  int64_t x_stride;
+  int64_t num_tokens;
+  const int64_t *slot_ids;
+  uint8_t *codes;
+  float *scales;
+  uint8_t *exps;
+  int64_t num_slots;
+  int32_t *err_flags;
+};
+
+constexpr int kIdxWarps = 4;
+
+// Two E2M1 codes (round to nearest even, saturating; low nibble = lo).
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n mov.b16 %0, {t, 0};\n}\n"
+      : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The group exponent X from the bf16 bits of the group's largest magnitude:
+// the smallest integer with amax <= 6 * 2^X, clamped to [-127, 127].  With
+// amax = (1 + m/128) 2^(E-127): X = E - 129 when 1 + m/128 <= 1.5 (m <= 64),
+// else E - 128; zero and subnormal amax (below 2^-126) clamp to -127.
+__device__ __forceinline__ int mxfp4_group_exponent(uint32_t amax_bits) {
+  const int E = static_cast<int>((amax_bits >> 7) & 0xFFu);
+  if (E == 0) return -127;
+  int X = E - 129 + ((amax_bits & 0x7Fu) > 0x40u ? 1 : 0);
+  return X < -127 ? -127 : X;
+}
+
+// Four codes of elements (w0 lo, w0 hi, w1 lo, w1 hi) scaled by y = 2^-X:
+// two bytes, even element in the low nibble, each code with its element's
+// sign (bf16 bits 15 of the halves).
+__device__ __forceinline__ uint32_t mxfp4_encode4(uint32_t w0, uint32_t w1, float y) {
+  const uint32_t c = e2m1x2_rn(bf16_lo(w0) * y, bf16_hi(w0) * y) |
+                     (e2m1x2_rn(bf16_lo(w1) * y, bf16_hi(w1) * y) << 8);
+  const uint32_t signs = ((w0 >> 12) & 0x8u) | ((w0 >> 24) & 0x80u) | ((w1 >> 4) & 0x800u) |
+                         ((w1 >> 16) & 0x8000u);
+  return c | signs;
+}
+
+template <int kFormat>
+__global__ void __launch_bounds__(kIdxWarps * 32, 12)
+index_quantize_kernel(const IndexParams p) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 3;
+  const unsigned gmask = 0xFu << (lane & 28);
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (kIdxWarps * 8) + (threadIdx.x >> 2);
+  grid_dependency_wait();
+  allow_dependents_launch();
+  if (t >= p.num_tokens) return;
+  const uint16_t *src = p.x + t * p.x_stride + sub * 32;
+  uint4 a[2], b[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    a[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k));
+    b[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k + 8));
+  }
+  const int64_t slot = __ldg(p.slot_ids + t);
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (sub == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
+    return;
+  }
+  uint32_t m = __vmaxu2(max_mag_bf16x2(a[0], b[0]), max_mag_bf16x2(a[1], b[1]));
+  if (kFormat == KVQ_INDEX_FP8) {
+    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 1));
+    m = __vmaxu2(m, __shfl_xor_sync(gmask, m, 2));
+    const float amax = __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+    uint4 out0 = make_uint4(0u, 0u, 0u, 0u), out1 = out0;
+    float s = 0.0f;
+    if (amax != 0.0f) {
+      s = (amax >= kMarksteinMinScale) ? div_markstein(amax, 448.0f, kInv448)
+                                       : __fdiv_rn(amax, 448.0f);
+      if (s >= kMarksteinMinScale) {
+        const float y = __frcp_rn(s);
+        out0 = encode16<true>(a[0], b[0], s, y);
+        out1 = encode16<true>(a[1], b[1], s, y);
+      } else {
+        out0 = encode16<false>(a[0], b[0], s, 0.0f);
+        out1 = encode16<false>(a[1], b[1], s, 0.0f);
+      }
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(p.codes + slot * kHeadDim + sub * 32);
+    dst[0] = out0;
+    dst[1] = out1;
+    if (sub == 0) p.scales[slot] = s;
+  } else {
+    // this lane's 32 values are one group
+    const int X = mxfp4_group_exponent(max(m & 0xFFFFu, m >> 16));
+    const float y = (X == 127) ? __uint_as_float(0x00400000u)              // 2^-127
+                               : __uint_as_float(static_cast<uint32_t>(127 - X) << 23);
+    uint4 out;
+    out.x = mxfp4_encode4(a[0].x, a[0].y, y) | (mxfp4_encode4(a[0].z, a[0].w, y) << 16);
+    out.y = mxfp4_encode4(b[0].x, b[0].y, y) | (mxfp4_encode4(b[0].z, b[0].w, y) << 16);
+    out.z = mxfp4_encode4(a[1].x, a[1].y, y) | (mxfp4_encode4(a[1].z, a[1].w, y) << 16);
+    out.w = mxfp4_encode4(b[1].x, b[1].y, y) | (mxfp4_encode4(b[1].z, b[1].w, y) << 16);
+    *reinterpret_cast<uint4 *>(p.codes + slot * (kHeadDim / 2) + sub * 16) = out;
+    p.exps[slot * (kHeadDim / 32) + sub] = static_cast<uint8_t>(X + 127);
+  }
+}
+
+// Rows back to real values, one warp per row: FP8 fl32(e4m3(c) * scale); MXFP4
+// fl32(e2m1(c) * 2^X) (exact products but for overflow), optionally rounded
+// again to bf16.
+struct IndexDequantParams {
+  const uint8_t *codes;
+  const float *scales;
+  const uint8_t *exps;
+  int64_t num_slots;
+  const int64_t *slot_ids;
+  int64_t n;
+  int32_t out_bf16;
+  void *out;
+  int32_t *err_flags;
+};
+
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h2, float &lo, float &hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+}
+
+template <int kFormat>
+__global__ void __launch_bounds__(kIdxWarps * 32)
+index_dequant_kernel(const IndexDequantParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kIdxWarps + (threadIdx.x >> 5);
+  grid_dependency_wait();
+  allow_dependents_launch();
+  if (i >= p.n) return;
+  const int64_t slot = p.slot_ids[i];
+  const bool valid = slot >= 0 && slot < p.num_slots;
+  if (slot >= p.num_slots && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
+  float v[4] = {0.f, 0.f, 0.f, 0.f};                 // dims 4 lane .. 4 lane + 3
+  if (valid) {
+    if (kFormat == KVQ_INDEX_FP8) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(p.codes + slot * kHeadDim) + lane);
+      const float s = __ldg(p.scales + slot);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(e4m3_to_f32((w >> (8 * j)) & 0xFFu), s);
+    } else {
+      const uint16_t w = __ldg(reinterpret_cast<const uint16_t *>(p.codes + slot * (kHeadDim / 2)) + lane);
+      const int X = static_cast<int>(__ldg(p.exps + slot * (kHeadDim / 32) + lane / 8)) - 127;
+      const float sc = (X == -127) ? __uint_as_float(0x00400000u)
+                                   : __uint_as_float(static_cast<uint32_t>(127 + X) << 23);
+      uint32_t h01, h23;
+      asm("{\n .reg .b8 c0, c1;\n mov.b16 {c0, c1}, %2;\n cvt.rn.f16x2.e2m1x2 %0, c0;\n"
+          " cvt.rn.f16x2.e2m1x2 %1, c1;\n}\n" : "=r"(h01), "=r"(h23) : "h"(w));
+      f16x2_to_f32x2(h01, v[0], v[1]);
+      f16x2_to_f32x2(h23, v[2], v[3]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(v[j], sc);
+    }
+  }
+  const int64_t o = i * kHeadDim + 4 * lane;
+  if (p.out_bf16) {
+    uint2 pk;
+    pk.x = pack_bf16x2(v[0], v[1]);
+    pk.y = pack_bf16x2(v[2], v[3]);
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + o) = pk;
+  } else {
+    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k_stride,
@@ -280,6 +455,57 @@ cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int
   const int64_t blocks = (n + kQuantWarps - 1) / kQuantWarps;
   return launch_overlapped(dequant_rows_kernel, dim3(static_cast<unsigned>(blocks)),
                            dim3(kQuantWarps * 32), 0, stream, p);
+}
+
+}  // namespace kvq
+
+namespace kvq {
+
+cudaError_t launch_index_quantize_scatter(const kvq_index_cache &c, const void *x,
+                                          int64_t x_stride, int64_t num_tokens,
+                                          const int64_t *slot_ids, int32_t *err_flags,
+                                          cudaStream_t stream) {
+  IndexParams p;
+  p.x = static_cast<const uint16_t *>(x);
+  p.x_stride = x_stride;
+  p.num_tokens = num_tokens;
+  p.slot_ids = slot_ids;
+  p.codes = c.codes;
+  p.scales = c.scales;
+  p.exps = c.exponents;
+  p.num_slots = c.num_slots;
+  p.err_flags = err_flags;
+  const int64_t blocks = (num_tokens + kIdxWarps * 8 - 1) / (kIdxWarps * 8);
+  if (c.format == KVQ_INDEX_FP8)
+    return launch_overlapped(index_quantize_kernel<KVQ_INDEX_FP8>,
+                             dim3(static_cast<unsigned>(blocks)), dim3(kIdxWarps * 32), 0,
+                             stream, p);
+  return launch_overlapped(index_quantize_kernel<KVQ_INDEX_MXFP4>,
+                           dim3(static_cast<unsigned>(blocks)), dim3(kIdxWarps * 32), 0, stream,
+                           p);
+}
+
+cudaError_t launch_index_dequant_rows(const kvq_index_cache &c, const int64_t *slot_ids,
+                                      int64_t n, int32_t out_dtype, void *out,
+                                      int32_t *err_flags, cudaStream_t stream) {
+  IndexDequantParams p;
+  p.codes = c.codes;
+  p.scales = c.scales;
+  p.exps = c.exponents;
+  p.num_slots = c.num_slots;
+  p.slot_ids = slot_ids;
+  p.n = n;
+  p.out_bf16 = out_dtype == 1;
+  p.out = out;
+  p.err_flags = err_flags;
+  const int64_t blocks = (n + kIdxWarps - 1) / kIdxWarps;
+  if (c.format == KVQ_INDEX_FP8)
+    return launch_overlapped(index_dequant_kernel<KVQ_INDEX_FP8>,
+                             dim3(static_cast<unsigned>(blocks)), dim3(kIdxWarps * 32), 0,
+                             stream, p);
+  return launch_overlapped(index_dequant_kernel<KVQ_INDEX_MXFP4>,
+                           dim3(static_cast<unsigned>(blocks)), dim3(kIdxWarps * 32), 0, stream,
+                           p);
 }
 
 }  // namespace kvq

@@ -246,6 +246,60 @@ kvq_status kvq_dequant_rows(const kvq_cache *cache, const int64_t *slot_ids, int
                             int32_t out_dtype, void *out_k, void *out_v,
                             int32_t *err_flags, kvq_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Compressed index keys.  ATOM PR #2655, PR description, index-key bullet:
+ * index keys are cached either as FP8 with one FP32 scale per row -- the K/V
+ * row format above -- or as MXFP4: packed E2M1 pairs plus one E8M0 exponent
+ * per 32 dims, rounded up so a group never clips; FP4 decodes with bit
+ * operations.  One row of `dim` values per token (one index head):
+ *   FP8    codes uint8 [num_slots, dim] (e4m3) and scales fp32 [num_slots]:
+ *          scale = amax / 448, code_d = e4m3_rne(x_d / scale), as for K/V.
+ *   MXFP4  codes uint8 [num_slots, dim / 2]: element 2i in the low nibble of
+ *          byte i, element 2i + 1 in the high nibble, each an E2M1 code (1 sign,
+ *          2 exponent bits with bias 1, 1 mantissa bit; magnitudes 0, 0.5, 1,
+ *          1.5, 2, 3, 4, 6); exponents uint8 [num_slots, dim / 32]: byte X + 127
+ *          for the group scale 2^X, X the smallest integer with the group's
+ *          amax <= 6 * 2^X, clamped to [-127, 127] (-127 for an all-zero
+ *          group); code = the E2M1 value nearest x / 2^X, ties to the even
+ *          mantissa bit, carrying the sign of x.
+ * dim must be 128; alignment as for the K/V cache (codes 16 bytes, x rows 16
+ * bytes with a token stride of a multiple of 8 elements, slot ids 8). */
+#define KVQ_INDEX_FP8 0
+#define KVQ_INDEX_MXFP4 1
+
+typedef struct kvq_index_cache {
+    uint8_t *codes;                      /* see above, per format                   */
+    float *scales;                       /* FP8: [num_slots] fp32; MXFP4: unused    */
+    uint8_t *exponents;                  /* MXFP4: [num_slots, dim/32]; FP8: unused */
+    int64_t num_slots;
+    int32_t format;                      /* KVQ_INDEX_FP8 or KVQ_INDEX_MXFP4        */
+    int32_t dim;                         /* 128                                     */
+} kvq_index_cache;
+
+/* Bytes of an index-key cache: FP8 num_slots * (dim + 4); MXFP4 num_slots *
+ * (dim / 2 + dim / 32).  0 for an invalid argument. */
+size_t kvq_index_cache_bytes(int64_t num_slots, int32_t format, int32_t dim);
+
+/* Quantise index-key rows and scatter them to slots (one launch, capturable).
+ *   x               device bf16; token t's row starts at element t*x_token_stride
+ *   x_token_stride  in elements, a multiple of 8, >= 0
+ *   num_tokens      rows (0 launches nothing)
+ *   slot_ids        device int64 [num_tokens]: as for kvq_quantize_scatter
+ *   err_flags       device int32, optional */
+kvq_status kvq_index_quantize_scatter(const kvq_index_cache *cache, const void *x,
+                                      int64_t x_token_stride, int64_t num_tokens,
+                                      const int64_t *slot_ids, int32_t *err_flags,
+                                      kvq_stream_t stream);
+
+/* Index-key rows back to real values: FP8 fl32(e4m3(c) * scale); MXFP4
+ * fl32(e2m1(c) * 2^X); out_dtype 1 rounds that once more to bf16.
+ *   slot_ids  device int64 [n]; an id outside [0, num_slots) gives a zero row
+ *             (ids >= num_slots also set KVQ_ERRF_SLOT_RANGE)
+ *   out       device [n, dim] of out_dtype (0 = fp32, 1 = bf16) */
+kvq_status kvq_index_dequant_rows(const kvq_index_cache *cache, const int64_t *slot_ids,
+                                  int64_t n, int32_t out_dtype, void *out,
+                                  int32_t *err_flags, kvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
