@@ -74,9 +74,13 @@ DESCRIPTIONS = {
                 "head_dim 128, block 64"),
     "store": ("prefill store under CUDA graph: 16,384 tokens as strided K/V views of a fused "
               "qkv [16384, 6144], 1% outliers x50, zero rows, permuted int64 slot ids, block 64"),
+    "index": ("MXFP4 index-key store under CUDA graph: 262,144 rows of 128 bf16 values "
+              "(N(0,1) x a log-normal magnitude per 32-dim group) into E2M1 pairs + one E8M0 "
+              "exponent per 32 dims, permuted int64 slot ids"),
 }
 
-DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "verify": 1500, "longctx": 1500, "store": 5000}
+DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "verify": 1500, "longctx": 1500, "store": 5000,
+                 "index": 3000}
 
 
 def parse_args(argv=None):
@@ -820,11 +824,200 @@ def run_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------------------
+# the index-key store (MXFP4)
+
+INDEX_TOKENS = 262144
+INDEX_ROW_BYTES = 128 * 2 + 64 + 4 + 8      # bf16 row read, codes, exponents, slot id
+INDEX_METRIC = "MXFP4 index-key store: achieved HBM GB/s (% of 8 TB/s); rows quantized/s"
+
+
+def index_inputs():
+    """Seeded bf16 rows [262144, 128] (N(0,1) times exp(2 N(0,1)) per 32-dim
+    group) and a permutation of the slots, on the host."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(INDEX_TOKENS, 4, 32, generator=g) * torch.exp(
+        2.0 * torch.randn(INDEX_TOKENS, 4, 1, generator=g))
+    slots = torch.randperm(INDEX_TOKENS, generator=g).to(torch.int64)
+    return x.reshape(INDEX_TOKENS, 128).to(torch.bfloat16), slots
+
+
+def index_oracle_rate(budget_s: float, x=None):
+    """The oracle's MXFP4 quantisation on one host thread over a bounded
+    sample of the rows: (GB/s of algorithmic bytes, rows done, seconds)."""
+    import oracle
+    if x is None:
+        x, _ = index_inputs()
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    rows, elapsed, i = 0, 0.0, 0
+    while elapsed < budget_s and i < INDEX_TOKENS:
+        chunk = bits[i:i + 4096]
+        t0 = time.perf_counter()
+        oracle.mxfp4_quantize_rows(chunk)
+        elapsed += time.perf_counter() - t0
+        rows += chunk.shape[0]
+        i += chunk.shape[0]
+    return rows * INDEX_ROW_BYTES / elapsed / 1e9, rows, elapsed
+
+
+def run_index(args, rank, local, world):
+    import fp8_paged_kv_kvq_gb300 as kvq
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS["index"]
+    W = max(3, args.warmup if args.warmup is not None else min(50, max(3, K // 10)))
+    lib = kvq.load()
+    x_h, slots_h = index_inputs()
+    x, slots = x_h.to(dev), slots_h.to(dev)
+    cache = kvq.IndexCache.empty(INDEX_TOKENS, kvq.INDEX_MXFP4, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    st = cache.struct()
+    P = ctypes.c_void_p
+    qargs = (ctypes.byref(st), P(x.data_ptr()), x.stride(0), INDEX_TOKENS, P(slots.data_ptr()),
+             P(err.data_ptr()), P(stream.cuda_stream))
+
+    def quantize():
+        status = lib.kvq_index_quantize_scatter(*qargs)
+        if status:
+            raise RuntimeError(f"kvq_index_quantize_scatter: status {status}")
+
+    with torch.cuda.stream(stream):
+        quantize()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            quantize()
+        torch.cuda.synchronize(dev)
+        flush = None if args.profile else L2Flush(dev)
+        for i in range(W):
+            if flush is not None:
+                flush(i)
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        sampler = ClockSampler(local) if not args.profile else None
+        dist_barrier(world)
+        torch.cuda.synchronize(dev)
+        if sampler:
+            sampler.start()
+        wall0 = time.perf_counter()
+        torch.cuda.nvtx.range_push("kvq_timed")
+        for i in range(K):
+            if flush is not None:
+                flush(i + 7)
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+        wall1 = time.perf_counter()
+        if sampler:
+            sampler.stop()
+        dist_barrier(world)
+        ms = dist_max(sum(a.elapsed_time(b) for a, b in evs) / K, world)
+        if int(err.item()) != 0:
+            raise RuntimeError("device error flags set during the benchmark")
+        peak, peak_src = measured_peaks()
+        step_bytes = INDEX_TOKENS * INDEX_ROW_BYTES
+        value = world * step_bytes / (ms * 1e-3) / 1e9
+        res = {
+            "metric": INDEX_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS["index"], "name": "index",
+                       "l2": ("flushed before every timed step (256 MiB write, then a 256 MiB "
+                              "read)") if flush is not None else "not flushed (profile mode)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "storage": "E2M1 pairs (uint8) + E8M0 exponent per 32 dims"},
+            "pct_of_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+            "rows_quantized_per_s": round(world * INDEX_TOKENS / (ms * 1e-3), 1),
+            "kernels_us": {"index_quantize_scatter": round(1e3 * ms, 3)},
+            "gpu_launches": K,
+            "wall_s_timed_region": round(wall1 - wall0, 3),
+        }
+        achieved = step_bytes / (ms * 1e-3) / 1e9
+        res["roofline"] = {
+            "kernel": "index_quantize_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                            else "fallback 6.8 TB/s"),
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": step_bytes,
+            "traffic": ncu_traffic("index_quantize_kernel", "index",
+                                   "fp8_paged_kv_kvq_gb300/csrc/kvq_quantize.cu"),
+        }
+        if sampler:
+            res["clocks"] = sampler.summary(wall0, wall1)
+        if not args.profile and not args.no_e2e:
+            xp = x_h.pin_memory()
+            sp = slots_h.pin_memory()
+            ep = torch.empty(cache.exponents.shape, dtype=torch.uint8, pin_memory=True)
+
+            def body():
+                x.copy_(xp, non_blocking=True)
+                slots.copy_(sp, non_blocking=True)
+                quantize()
+                ep.copy_(cache.exponents, non_blocking=True)
+
+            for _ in range(3):
+                body()
+            torch.cuda.synchronize(dev)
+            n_e2e = max(20, min(K, 300))
+            ems = dist_max(_timed(stream, dev, n_e2e, body, L2Flush(dev)), world)
+            res["e2e"] = {"value": round(world * step_bytes / (ems * 1e-3) / 1e9, 2),
+                          "unit": "GB/s", "ms_per_step": round(ems, 5),
+                          "h2d_bytes_per_step": x_h.numel() * 2 + slots_h.numel() * 8,
+                          "d2h_bytes_per_step": ep.numel()}
+        if rank == 0 and world == 1 and not args.profile and not args.no_cpu_baseline:
+            v, rows, secs = index_oracle_rate(12.0, x_h)
+            res["cpu_baseline"] = {"value": round(v, 5), "unit": "GB/s", "cores": 1,
+                                   "kind": "oracle",
+                                   "sample": f"{rows} rows of the workload; {secs:.1f} s "
+                                             "single-thread CPU time"}
+    return res
+
+
+def run_index_reference(args, rank, world):
+    """--impl reference for the index workload: the oracle on the host."""
+    if rank != 0:
+        return None
+    K = args.steps if args.steps is not None else 60
+    W = max(3, args.warmup if args.warmup is not None else 3)
+    budget = min(2.0, 150.0 / (K + W))
+    x, _ = index_inputs()
+    for _ in range(W):
+        index_oracle_rate(budget / 4, x)
+    total_b, total_t = 0.0, 0.0
+    for _ in range(K):
+        _, rows, secs = index_oracle_rate(budget, x)
+        total_b += rows * INDEX_ROW_BYTES
+        total_t += secs
+    value = total_b / total_t / 1e9
+    return {
+        "impl": "reference", "metric": INDEX_METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(1e3 * total_t / K, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": DESCRIPTIONS["index"], "name": "index"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step a bounded run of 4096-row chunks of the workload"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, local, world = dist_init()
-    res = run_reference(args, rank, world) if args.impl == "reference" else \
-        run_kvq(args, rank, local, world)
+    if args.workload == "index":
+        res = run_index_reference(args, rank, world) if args.impl == "reference" else \
+            run_index(args, rank, local, world)
+    else:
+        res = run_reference(args, rank, world) if args.impl == "reference" else \
+            run_kvq(args, rank, local, world)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:
