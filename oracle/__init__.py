@@ -90,6 +90,10 @@ def _load():
             lib.kvqo_mxfp4_quantize_rows.restype = None
             lib.kvqo_mxfp4_dequant_rows.argtypes = [P, P, i64, ctypes.c_int, P]
             lib.kvqo_mxfp4_dequant_rows.restype = None
+            lib.kvqo_index_scores.argtypes = [ctypes.c_int, P, P, P, i64, ctypes.c_int,
+                                              ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P]
+            lib.kvqo_index_scores.restype = ctypes.c_int32
             lib.kvqo_dequant_rows.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P,
                                               i64, ctypes.c_int, P]
             lib.kvqo_paged_attention.restype = i32
@@ -301,4 +305,26 @@ def paged_attention_units(cache: dict, q_bits: np.ndarray, N: int, R: int, Hq: i
                                          _ptr(u), u.shape[0], _ptr(out))
     if err < 0:
         raise ValueError("oracle attention: bad unit or allocation failure")
+    return out, int(err)
+
+
+def index_scores(fmt: int, codes: np.ndarray, scales, exps, block_tables: np.ndarray,
+                 block_size: int, context_lens: np.ndarray, R: int, H: int,
+                 q_bits: np.ndarray, max_len: int):
+    """Index scores in float64 [N*R, max_len]: sum over heads of max(0, q . k),
+    -inf where a row does not see the token (format 0 FP8 keys with scales,
+    1 MXFP4 keys with exponents).  Returns (scores, error word)."""
+    lib = _load()
+    c = _c(codes, np.uint8)
+    S = c.shape[0]
+    D = c.shape[1] if fmt == 0 else 2 * c.shape[1]
+    sc = _c(scales if scales is not None else np.zeros(1, np.float32), np.float32)
+    ex = _c(exps if exps is not None else np.zeros(1, np.uint8), np.uint8)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    qb = _c(q_bits, np.uint16)
+    N = cl.size
+    out = np.empty((N * R, max_len), dtype=np.float64)
+    err = lib.kvqo_index_scores(fmt, _ptr(c), _ptr(sc), _ptr(ex), S, D, block_size, _ptr(bt),
+                                bt.shape[1], _ptr(cl), N, R, H, _ptr(qb), max_len, _ptr(out))
     return out, int(err)

@@ -504,3 +504,70 @@ void kvqo_mxfp4_dequant_rows(const uint8_t *codes, const uint8_t *exps, int64_t 
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Index scoring over the compressed index keys, [ATOM] PR description: the
+ * stacked decode scorer lets R query rows x H index heads of a request meet
+ * each cached key once, applies the per-head ReLU and sums the heads.  For
+ * request r, query row i and cached token t (slot from the block table):
+ *     score(r, i, t) = sum_h max(0, <q(r, i, h), khat_t>)
+ * with khat_t the dequantised key, computed in double.  Readings:
+ * no per-head weight (a caller folds one into q); row i sees the tokens
+ * t < L_r - R + 1 + i, as the attention rows do; every other position up to
+ * max_len gets -inf.
+ *   format 0: codes [S, D] e4m3, scales [S]; format 1: codes [S, D/2] E2M1
+ *   pairs, exps [S, D/32] E8M0.  q: bf16 [N*R, H, D]; out: double [N*R, max_len].
+ * Returns the error word (block or context range). */
+static double index_key_value(int format, const uint8_t *codes, const float *scales,
+                              const uint8_t *exps, int64_t slot, int D, int d)
+{
+    if (format == 0)
+        return kvqo_e4m3_decode(codes[slot * D + d]) * (double)scales[slot];
+    uint8_t byte = codes[slot * (D / 2) + d / 2];
+    uint8_t c = (d & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+    return ldexp(kvqo_e2m1_decode(c), (int)exps[slot * (D / 32) + d / 32] - 127);
+}
+
+int32_t kvqo_index_scores(int format, const uint8_t *codes, const float *scales,
+                          const uint8_t *exps, int64_t num_slots, int D, int bs,
+                          const int32_t *block_tables, int max_blocks,
+                          const int32_t *context_lens, int N, int R, int H,
+                          const uint16_t *q, int max_len, double *out)
+{
+    int32_t err = 0;
+    for (int r = 0; r < N; ++r) {
+        int L = context_lens[r];
+        if (L < 0 || L > max_len || (int64_t)L > (int64_t)max_blocks * bs) {
+            err |= KVQO_ERR_CONTEXT_RANGE;
+            L = L < 0 ? 0 : L;
+            if (L > max_len) L = max_len;
+            if ((int64_t)L > (int64_t)max_blocks * bs) L = max_blocks * bs;
+        }
+        for (int i = 0; i < R; ++i) {
+            double *o = out + (int64_t)(r * R + i) * max_len;
+            int visible = L - R + 1 + i;
+            for (int t = 0; t < max_len; ++t)
+                o[t] = -INFINITY;
+            for (int t = 0; t < visible; ++t) {
+                int64_t blk = block_tables[(int64_t)r * max_blocks + t / bs];
+                if (blk < 0 || (blk + 1) * bs > num_slots) {
+                    err |= KVQO_ERR_BLOCK_RANGE;
+                    continue;
+                }
+                int64_t slot = blk * bs + t % bs;
+                double score = 0.0;
+                for (int h = 0; h < H; ++h) {
+                    const uint16_t *qv = q + ((int64_t)(r * R + i) * H + h) * D;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dot += (double)kvqo_bf16_to_float(qv[d]) *
+                               index_key_value(format, codes, scales, exps, slot, D, d);
+                    if (dot > 0.0)
+                        score += dot;
+                }
+                o[t] = score;
+            }
+        }
+    }
+    return err;
+}
