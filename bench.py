@@ -15,7 +15,7 @@ Default workload: the decode batch -- 32 requests, context lengths uniform in
 log-normal row magnitudes, one query row per request.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
-                  [--workload decode|verify|longctx|store|tiny]
+                  [--workload decode|verify|longctx|store|tiny|index|scores]
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle (oracle/)
 on bounded samples of the same workload; it is a deliberately slow program, a
@@ -77,10 +77,13 @@ DESCRIPTIONS = {
     "index": ("MXFP4 index-key store under CUDA graph: 262,144 rows of 128 bf16 values "
               "(N(0,1) x a log-normal magnitude per 32-dim group) into E2M1 pairs + one E8M0 "
               "exponent per 32 dims, permuted int64 slot ids"),
+    "scores": ("stacked index scores under CUDA graph: 64 requests x 4 query rows x 4 index "
+               "heads (16 stacked vectors), context 32768, block 64, MXFP4 index keys, "
+               "fp32 scores out"),
 }
 
 DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "verify": 1500, "longctx": 1500, "store": 5000,
-                 "index": 3000}
+                 "index": 3000, "scores": 1500}
 
 
 def parse_args(argv=None):
@@ -96,6 +99,8 @@ def parse_args(argv=None):
                          "same shape, for profiler captures); 0 = all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--index-format", choices=["mxfp4", "fp8"], default="mxfp4",
+                    help="index-key format of the scores workload")
     ap.add_argument("--profile", action="store_true",
                     help="no L2 flush, clocks, e2e or CPU baseline: a short run for ncu")
     return ap.parse_args(argv)
@@ -1009,10 +1014,243 @@ def run_index_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------------------
+# stacked index scores over MXFP4 index keys
+
+SCORES_METRIC = ("stacked index scores over {} keys: achieved HBM GB/s (% of 8 TB/s); "
+                 "tokens scored/s")
+
+
+def scores_inputs(fmt: int = 1):
+    """Host inputs of the index-scoring workload: block tables, context
+    lengths, key codes with their scales (FP8, fmt 0) or exponents (MXFP4,
+    fmt 1), bf16 queries [N, R, H, 128]."""
+    import workloads
+    w = workloads.INDEX_SCORES
+    lens = np.full(w.num_requests, w.context, dtype=np.int32)
+    bt, nblk = workloads.block_tables(lens, w.block_size, w.seed)
+    codes, scales, exps = workloads.index_key_codes(fmt, nblk * w.block_size, w.seed)
+    q = workloads.index_queries(w.num_requests, w.rows, w.heads, w.seed)
+    return w, fmt, lens, bt, codes, scales, exps, q
+
+
+def scores_step_bytes(w, fmt: int = 1) -> int:
+    """Algorithmic bytes of one launch: every key read once (MXFP4: 64 code
+    bytes + 4 exponent bytes per token; FP8: 128 + a 4-byte scale), the block
+    tables, lengths and queries, and the fp32 scores of every (row, token)."""
+    T = w.num_requests * w.context
+    key = 64 + 4 if fmt == 1 else 128 + 4
+    return (T * key + w.num_requests * (w.context // w.block_size) * 4 +
+            w.num_requests * 4 + w.num_requests * w.rows * w.heads * 128 * 2 +
+            w.num_requests * w.rows * w.context * 4)
+
+
+def scores_oracle_rate(budget_s: float, inp=None):
+    """The oracle's index scorer on one host thread over whole requests of the
+    workload until the budget is spent: (tokens/s, requests done, seconds)."""
+    import oracle
+    w, fmt, lens, bt, codes, scales, exps, q = inp if inp is not None else scores_inputs()
+    qb = q.view(torch.int16).numpy().view(np.uint16)
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < w.num_requests:
+        r = done
+        t0 = time.perf_counter()
+        oracle.index_scores(fmt, codes, scales, exps, bt[r:r + 1], w.block_size, lens[r:r + 1],
+                            w.rows, w.heads, qb[r].reshape(-1, 128), w.context)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    return done * w.context / elapsed, done, elapsed
+
+
+def run_scores(args, rank, local, world):
+    import fp8_paged_kv_kvq_gb300 as kvq
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K = args.steps if args.steps is not None else DEFAULT_STEPS["scores"]
+    W = max(3, args.warmup if args.warmup is not None else min(50, max(3, K // 10)))
+    lib = kvq.load()
+    fmt = 1 if args.index_format == "mxfp4" else 0
+    inp = scores_inputs(fmt)
+    w, _, lens_h, bt_h, codes_h, scales_h, exps_h, q_h = inp
+    N = w.num_requests if args.requests <= 0 else min(args.requests, w.num_requests)
+    cache = kvq.IndexCache.empty(codes_h.shape[0], fmt, device=dev)
+    cache.codes.copy_(torch.from_numpy(codes_h))
+    if fmt == 1:
+        cache.exponents.copy_(torch.from_numpy(exps_h))
+    else:
+        cache.scales.copy_(torch.from_numpy(scales_h))
+    bt = torch.from_numpy(bt_h[:N]).contiguous().to(dev)
+    lens = torch.from_numpy(lens_h[:N]).to(dev)
+    q = q_h[:N].contiguous().to(dev)
+    out = torch.empty((N * w.rows, w.context), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    st = cache.struct()
+    P = ctypes.c_void_p
+    sargs = (ctypes.byref(st), w.block_size, P(q.data_ptr()), N, w.rows, w.heads,
+             P(bt.data_ptr()), bt.shape[1], P(lens.data_ptr()), w.context, P(out.data_ptr()),
+             P(err.data_ptr()), P(stream.cuda_stream))
+
+    def score():
+        status = lib.kvq_index_scores(*sargs)
+        if status:
+            raise RuntimeError(f"kvq_index_scores: status {status}")
+
+    wN = dataclasses.replace(w, num_requests=N)
+    step_bytes = scores_step_bytes(wN, fmt)
+    fmt_name = "MXFP4" if fmt == 1 else "FP8"
+    res = {}
+    with torch.cuda.stream(stream):
+        score()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            score()
+        torch.cuda.synchronize(dev)
+        flush = None if args.profile else L2Flush(dev)
+        for i in range(W):
+            if flush is not None:
+                flush(i)
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        sampler = ClockSampler(local) if not args.profile else None
+        dist_barrier(world)
+        torch.cuda.synchronize(dev)
+        if sampler:
+            sampler.start()
+        wall0 = time.perf_counter()
+        torch.cuda.nvtx.range_push("kvq_timed")
+        for i in range(K):
+            if flush is not None:
+                flush(i + 7)
+            evs[i][0].record(stream)
+            graph.replay()
+            evs[i][1].record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+        wall1 = time.perf_counter()
+        if sampler:
+            sampler.stop()
+        dist_barrier(world)
+        ms = dist_max(sum(a.elapsed_time(b) for a, b in evs) / K, world)
+        if int(err.item()) != 0:
+            raise RuntimeError("device error flags set during the benchmark")
+        peak, peak_src = measured_peaks()
+        value = world * step_bytes / (ms * 1e-3) / 1e9
+        tokens = N * w.context
+        res = {
+            "metric": SCORES_METRIC.format(fmt_name), "value": round(value, 2), "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS["scores"].replace("MXFP4", fmt_name),
+                       "name": "scores", "requests": N,
+                       "l2": ("flushed before every timed step (256 MiB write, then a 256 MiB "
+                              "read)") if flush is not None else "not flushed (profile mode)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "keys": ("E2M1 pairs (uint8) + E8M0 exponent per 32 dims"
+                                if fmt == 1 else "e4m3 codes + fp32 scale per row") +
+                               ", random codes"},
+            "pct_of_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+            "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+            "tokens_scored_per_s": round(world * tokens / (ms * 1e-3), 1),
+            "kernels_us": {"index_scores": round(1e3 * ms, 3)},
+            "gpu_launches": K,
+            "wall_s_timed_region": round(wall1 - wall0, 3),
+        }
+        achieved = step_bytes / (ms * 1e-3) / 1e9
+        res["roofline"] = {
+            "kernel": "index_scores_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                            else "fallback 6.8 TB/s"),
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": step_bytes,
+            "traffic": ncu_traffic("index_scores_kernel", "scores",
+                                   "fp8_paged_kv_kvq_gb300/csrc/kvq_index_scores.cu"),
+        }
+        if sampler:
+            res["clocks"] = sampler.summary(wall0, wall1)
+        if not args.profile and not args.no_e2e:
+            qp = torch.empty(q.shape, dtype=q.dtype, pin_memory=True).copy_(q_h[:N])
+            btp = torch.empty(bt.shape, dtype=bt.dtype, pin_memory=True).copy_(
+                torch.from_numpy(bt_h[:N]))
+            lp = torch.empty(lens.shape, dtype=lens.dtype, pin_memory=True).copy_(
+                torch.from_numpy(lens_h[:N]))
+            op = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+            def body():
+                q.copy_(qp, non_blocking=True)
+                bt.copy_(btp, non_blocking=True)
+                lens.copy_(lp, non_blocking=True)
+                score()
+                op.copy_(out, non_blocking=True)
+
+            for _ in range(3):
+                body()
+            torch.cuda.synchronize(dev)
+            n_e2e = max(20, min(K, 200))
+            ems = dist_max(_timed(stream, dev, n_e2e, body, L2Flush(dev)), world)
+            res["e2e"] = {"value": round(world * step_bytes / (ems * 1e-3) / 1e9, 2),
+                          "unit": "GB/s", "ms_per_step": round(ems, 5),
+                          "h2d_bytes_per_step": sum(t.numel() * t.element_size()
+                                                    for t in (qp, btp, lp)),
+                          "d2h_bytes_per_step": op.numel() * op.element_size()}
+        if rank == 0 and world == 1 and not args.profile and not args.no_cpu_baseline:
+            tps, done, secs = scores_oracle_rate(12.0, inp)
+            res["cpu_baseline"] = {"value": round(tps * step_bytes / tokens / 1e9, 5),
+                                   "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                   "tokens_per_s": round(tps, 1),
+                                   "sample": f"{done} whole requests of the workload; "
+                                             f"{secs:.1f} s single-thread CPU time"}
+    return res
+
+
+def run_scores_reference(args, rank, world):
+    """--impl reference for the index-scoring workload: the oracle on the host."""
+    if rank != 0:
+        return None
+    K = args.steps if args.steps is not None else 40
+    W = max(3, args.warmup if args.warmup is not None else 3)
+    budget = min(2.5, 150.0 / (K + W))
+    fmt = 1 if args.index_format == "mxfp4" else 0
+    fmt_name = "MXFP4" if fmt == 1 else "FP8"
+    inp = scores_inputs(fmt)
+    w = inp[0]
+    per_token = scores_step_bytes(w, fmt) / (w.num_requests * w.context)
+    for _ in range(W):
+        scores_oracle_rate(budget / 4, inp)
+    total_tok, total_t = 0.0, 0.0
+    for _ in range(K):
+        _, done, secs = scores_oracle_rate(budget, inp)
+        total_tok += done * w.context
+        total_t += secs
+    value = total_tok * per_token / total_t / 1e9
+    return {
+        "impl": "reference", "metric": SCORES_METRIC.format(fmt_name), "value": round(value, 5),
+        "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(1e3 * total_t / K, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS["scores"].replace("MXFP4", fmt_name), "name": "scores"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step whole requests of the workload until a bounded "
+                                   "CPU time is spent"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, local, world = dist_init()
-    if args.workload == "index":
+    if args.workload == "scores":
+        res = run_scores_reference(args, rank, world) if args.impl == "reference" else \
+            run_scores(args, rank, local, world)
+    elif args.workload == "index":
         res = run_index_reference(args, rank, world) if args.impl == "reference" else \
             run_index(args, rank, local, world)
     else:

@@ -106,6 +106,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                           i64, i64, P, P, P]),
             "kvq_index_dequant_rows": (ctypes.c_int, [ctypes.POINTER(_IndexCacheStruct), P, i64,
                                                       i32, P, P, P]),
+            "kvq_index_scores": (ctypes.c_int, [ctypes.POINTER(_IndexCacheStruct), i32, P, i32,
+                                                i32, i32, P, i32, P, i32, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(lib, name)
@@ -397,4 +399,34 @@ def index_dequant_rows(cache: IndexCache, slot_ids: torch.Tensor, out_dtype=torc
     _check(load().kvq_index_dequant_rows(ctypes.byref(st), _ptr(slot_ids), n, code, _ptr(out),
                                          _ptr(err_flags), _stream(stream)),
            "kvq_index_dequant_rows")
+    return out
+
+
+def index_scores(cache: IndexCache, block_size: int, q: torch.Tensor, block_tables: torch.Tensor,
+                 context_lens: torch.Tensor, max_context_len: int,
+                 out: torch.Tensor | None = None, err_flags: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """kvq_index_scores: stacked index scores fp32 [N * R, max_context_len] for
+    bf16 queries ``q`` [N, R, H, dim] over the paged index keys; -inf where a
+    row does not see a token."""
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 4 \
+            or q.shape[3] != cache.dim:
+        raise ValueError(f"q must be a contiguous bf16 [N, R, H, {cache.dim}] tensor")
+    if block_tables.dtype != torch.int32 or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be contiguous int32 [N, max_blocks]")
+    if context_lens.dtype != torch.int32 or not context_lens.is_contiguous():
+        raise ValueError("context_lens must be contiguous int32 [N]")
+    N, R, H = q.shape[0], q.shape[1], q.shape[2]
+    if block_tables.shape[0] != N or context_lens.numel() != N:
+        raise ValueError("block_tables / context_lens must have one entry per request")
+    if out is None:
+        out = torch.empty((N * R, max_context_len), dtype=torch.float32, device=q.device)
+    elif out.dtype != torch.float32 or not out.is_contiguous() \
+            or tuple(out.shape) != (N * R, max_context_len):
+        raise ValueError("out must be contiguous fp32 [N * R, max_context_len]")
+    st = cache.struct()
+    _check(load().kvq_index_scores(ctypes.byref(st), block_size, _ptr(q), N, R, H,
+                                   _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                   max_context_len, _ptr(out), _ptr(err_flags), _stream(stream)),
+           "kvq_index_scores")
     return out

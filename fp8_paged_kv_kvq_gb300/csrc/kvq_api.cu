@@ -381,4 +381,32 @@ kvq_status kvq_index_dequant_rows(const kvq_index_cache *cache, const int64_t *s
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+kvq_status kvq_index_scores(const kvq_index_cache *cache, int32_t block_size, const void *q,
+                            int32_t num_requests, int32_t rows_per_request,
+                            int32_t num_index_heads, const int32_t *block_tables,
+                            int32_t max_blocks_per_req, const int32_t *context_lens,
+                            int32_t max_context_len, float *out, int32_t *err_flags,
+                            kvq_stream_t stream) {
+  kvq_status st = check_index_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (block_size <= 0 || num_requests < 0 || rows_per_request < 1 || num_index_heads < 1 ||
+      max_blocks_per_req < 0 || max_context_len < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!is_pow2(block_size) || block_size < 16 ||
+      !kvq::index_scores_supported(rows_per_request, num_index_heads))
+    return KVQ_ERR_UNSUPPORTED;
+  if (num_requests > 65535) return KVQ_ERR_UNSUPPORTED;
+  if (num_requests == 0 || max_context_len == 0) return KVQ_OK;
+  if (q == nullptr || block_tables == nullptr || context_lens == nullptr || out == nullptr)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+      !aligned(out, 4) || !aligned(err_flags, 4) || !aligned(cache->scales, 16) ||
+      !aligned(cache->exponents, 16))
+    return KVQ_ERR_MISALIGNED;
+  return from_cuda(kvq::launch_index_scores(
+      *cache, log2_exact(block_size), q, num_requests, rows_per_request, num_index_heads,
+      block_tables, max_blocks_per_req, context_lens, max_context_len, out, err_flags,
+      current_sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

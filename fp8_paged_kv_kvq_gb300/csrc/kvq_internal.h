@@ -98,6 +98,15 @@ cudaError_t launch_index_dequant_rows(const kvq_index_cache &c, const int64_t *s
                                       int64_t n, int32_t out_dtype, void *out,
                                       int32_t *err_flags, cudaStream_t stream);
 
+// Stacked index scorer: R * H <= 16 query vectors per request, H in {1,2,4,8}.
+bool index_scores_supported(int32_t rows_per_request, int32_t num_index_heads);
+cudaError_t launch_index_scores(const kvq_index_cache &c, int32_t log2_block, const void *q,
+                                int32_t num_requests, int32_t rows_per_request,
+                                int32_t num_index_heads, const int32_t *block_tables,
+                                int32_t max_blocks_per_req, const int32_t *context_lens,
+                                int32_t max_context_len, float *out, int32_t *err_flags,
+                                int32_t sms, cudaStream_t stream);
+
 cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const void *q,
                                  const int32_t *block_tables, const int32_t *context_lens,
                                  float sm_scale, void *out, void *workspace,

@@ -300,6 +300,44 @@ kvq_status kvq_index_dequant_rows(const kvq_index_cache *cache, const int64_t *s
                                   int64_t n, int32_t out_dtype, void *out,
                                   int32_t *err_flags, kvq_stream_t stream);
 
+/* Stacked index scores over the compressed index keys (one launch, capturable).
+ * ATOM PR #2655, PR description: the stacked decode scorer puts a request's R
+ * query rows x H index heads into one operand so that every cached index key
+ * is read once per step and meets every head in one dot product; the ReLU of
+ * each head's dot comes before the heads are summed.  For request r, row i
+ * and token t < L_r - R + 1 + i (row i sees the context up to and including
+ * its own position, as in verify):
+ *     out[r*R + i][t] = sum_h max(0, sum_d q[r][i][h][d] * khat_t[d]),
+ * khat_t the dequantised key of token t (FP8: e4m3(c) * scale; MXFP4:
+ * e2m1(c) * 2^X), read through the request's block table.  Every other entry
+ * of the row, up to max_context_len, is -inf.
+ *   cache            index keys, paged in blocks of block_size slots; its scale
+ *                    (FP8) or exponent (MXFP4) plane 16-byte aligned
+ *   block_size       tokens per block, a power of two >= 16
+ *   q                device bf16 [num_requests, rows_per_request,
+ *                    num_index_heads, dim], 16-byte aligned
+ *   rows_per_request R >= 1;  num_index_heads H in {1, 2, 4, 8}; R * H <= 16
+ *   block_tables     device int32 [num_requests, max_blocks_per_req]
+ *   context_lens     device int32 [num_requests]: L_r, in [0, min(max_context_len,
+ *                    max_blocks_per_req * block_size)]; outside that range it is
+ *                    clamped and KVQ_ERRF_CONTEXT_RANGE set
+ *   out              device fp32 [num_requests * R, max_context_len]
+ *   err_flags        device int32, optional: KVQ_ERRF_BLOCK_RANGE for a block id
+ *                    outside [0, num_slots / block_size) (the scores of that
+ *                    block's tokens are then unspecified), KVQ_ERRF_CONTEXT_RANGE
+ *                    as above, KVQ_ERRF_WAIT_TIMEOUT if a bounded in-kernel wait
+ *                    for a copy gave up
+ * Accuracy: the dots are f16 products accumulated in fp32 (both key formats
+ * and the bf16 query, scaled by a power of two, are exact in f16 except for
+ * parts below 2^-24 of a vector's largest element); each score is within
+ * 1e-5 * sum_h sum_d |q_hd * khat_d| of the exact value. */
+kvq_status kvq_index_scores(const kvq_index_cache *cache, int32_t block_size, const void *q,
+                            int32_t num_requests, int32_t rows_per_request,
+                            int32_t num_index_heads, const int32_t *block_tables,
+                            int32_t max_blocks_per_req, const int32_t *context_lens,
+                            int32_t max_context_len, float *out, int32_t *err_flags,
+                            kvq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,3 +130,48 @@ def test_dequant_validation(lib):
     assert d(ctypes.byref(c), P(8), 4, 2, P(16), P(16), P(0), P(0)) == INVALID
     assert d(ctypes.byref(c), P(0), 4, 0, P(16), P(16), P(0), P(0)) == INVALID
     assert d(ctypes.byref(c), P(8), 4, 0, P(20), P(16), P(0), P(0)) == MISALIGNED
+
+
+def _index_cache(fmt=1, slots=64, ptr=0x10000):
+    return kvq._IndexCacheStruct(ptr, ptr + 0x100000 if fmt == 0 else 0,
+                                 ptr + 0x200000 if fmt == 1 else 0, slots, fmt, 128)
+
+
+def test_index_cache_bytes_and_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.kvq_index_cache_bytes(1000, 0, 128) == 1000 * 132
+    assert lib.kvq_index_cache_bytes(1000, 1, 128) == 1000 * 68
+    assert lib.kvq_index_cache_bytes(1000, 2, 128) == 0
+    c = _index_cache()
+    q = lib.kvq_index_quantize_scatter
+    assert q(ctypes.byref(c), P(16), 128, 0, P(8), P(0), P(0)) == OK
+    assert q(ctypes.byref(c), P(16), 129, 4, P(8), P(0), P(0)) == MISALIGNED
+    bad = _index_cache()
+    bad.format = 5
+    assert q(ctypes.byref(bad), P(16), 128, 4, P(8), P(0), P(0)) == INVALID
+    nodim = _index_cache()
+    nodim.dim = 64
+    assert q(ctypes.byref(nodim), P(16), 128, 4, P(8), P(0), P(0)) == UNSUPPORTED
+
+
+def test_index_scores_validation_happens_before_launch(lib):
+    """kvq_index_scores: R * H <= 16 with H in {1, 2, 4, 8}, a power-of-two
+    block size, a 16-byte aligned query; empty batches launch nothing."""
+    P = ctypes.c_void_p
+    s = lib.kvq_index_scores
+    c = _index_cache()
+
+    def call(bs=16, q=16, N=2, R=4, H=4, mb=8, maxc=128, out=16):
+        return s(ctypes.byref(c), bs, P(q), N, R, H, P(64), mb, P(128), maxc, P(out), P(0),
+                 P(0))
+    assert call(N=0) == OK and call(maxc=0) == OK
+    assert call(H=3) == UNSUPPORTED
+    assert call(R=5, H=4) == UNSUPPORTED
+    assert call(bs=24) == UNSUPPORTED
+    assert call(bs=8) == UNSUPPORTED
+    assert call(bs=0) == INVALID
+    assert call(R=0) == INVALID
+    assert call(N=70000) == UNSUPPORTED
+    assert call(q=24) == MISALIGNED
+    assert call(out=18) == MISALIGNED
+    assert call(q=0) == INVALID

@@ -24,6 +24,13 @@ projection output, MTP-style verify with 3 draft tokens, a 1M-token context):
   longctx    2 requests x 1,048,576 tokens, 32 q heads / 8 KV heads, block size
              64; K, V as in ``decode``; 1 query row per request.    (seed 4)
 
+One more workload feeds the stacked index scorer:
+
+  index_scores  64 requests x 4 query rows x 4 index heads, context 32,768,
+             block size 64, one 128-dim index key per token; the key codes are
+             drawn directly (every drawn byte a finite code of its format), the
+             queries N(0,1).                                          (seed 6)
+
 Large caches are generated chunk by chunk on the device with a generator seeded
 from (workload seed, request, chunk), so that any chunk can be drawn again on
 its own (the parity tests sample requests of the large workloads that way).
@@ -185,3 +192,42 @@ def scaled(w: Workload, **changes) -> Workload:
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (same shape)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclasses.dataclass(frozen=True)
+class IndexScoreWorkload:
+    num_requests: int = 64
+    rows: int = 4
+    heads: int = 4
+    context: int = 32768
+    block_size: int = 64
+    seed: int = 6
+
+
+INDEX_SCORES = IndexScoreWorkload()
+
+
+def index_key_codes(fmt: int, num_slots: int, seed: int, exp_spread: int = 8):
+    """Random index-key codes for ``num_slots`` tokens of 128 dims, as numpy.
+
+    fmt 0 (FP8): codes uint8 [S, 128] uniform over the 254 finite e4m3 codes
+    (0x7F and 0xFF left out), scales fp32 [S] = exp(N(0,1)) / 448.
+    fmt 1 (MXFP4): codes uint8 [S, 64] uniform over all bytes (every nibble is
+    an E2M1 code), exponent bytes uint8 [S, 4] uniform in 127 +- exp_spread.
+    Returns (codes, scales or None, exponents or None)."""
+    g = generator(seed, 7, fmt)
+    if fmt == 0:
+        c = torch.randint(0, 254, (num_slots, HEAD_DIM), generator=g, dtype=torch.int32)
+        c = c + (c >= 0x7F).to(torch.int32)                 # skip 0x7F; 0xFF never drawn
+        sc = torch.exp(torch.randn(num_slots, generator=g)) / 448.0
+        return c.to(torch.uint8).numpy(), sc.to(torch.float32).numpy(), None
+    c = torch.randint(0, 256, (num_slots, HEAD_DIM // 2), generator=g, dtype=torch.int32)
+    e = torch.randint(127 - exp_spread, 128 + exp_spread, (num_slots, HEAD_DIM // 32),
+                      generator=g, dtype=torch.int32)
+    return c.to(torch.uint8).numpy(), None, e.to(torch.uint8).numpy()
+
+
+def index_queries(num_requests: int, rows: int, heads: int, seed: int) -> torch.Tensor:
+    """bf16 query vectors [N, R, H, 128], N(0,1)."""
+    g = generator(seed, 8)
+    return torch.randn(num_requests, rows, heads, HEAD_DIM, generator=g).to(torch.bfloat16)
