@@ -228,10 +228,10 @@ index_scores_kernel(const ScParams p) {
   const int nq = p.R * kH;
   constexpr int kU = kH == 1 ? 2 : 1;
   uint32_t qb[2][8][2];
-  float cs[2][2];
+  float hcs[2][2];                                   // column scales / 2
   float *orow[2][kU];
   int vis[2][kU];
-  int L = 0;
+  int L = 0, vis_min = 0;
   // the request's query vectors as B fragments -- tile t (vector 8t + g),
   // k-step s: b0 = dims 32c + 4s + 0, 1; b1 = dims 32c + 4s + 2, 3 -- each
   // vector scaled by 2^-e so that its largest magnitude lies in [2^7, 2^8)
@@ -240,6 +240,7 @@ index_scores_kernel(const ScParams p) {
     if ((Lraw < 0 || Lraw > p.ctx_limit) && tid == 0 && p.err_flags)
       atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
     L = sc_context(p, r);
+    vis_min = L - p.R + 1;                           // row 0 sees the fewest tokens
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int n = 8 * t + g;
@@ -281,8 +282,8 @@ index_scores_kernel(const ScParams p) {
         qb[t][m >> 1][m & 1] = h2;
       }
       const float qsc = amax == 0.0f ? 0.0f : exp2i(e);
-      cs[t][0] = __shfl_sync(0xFFFFFFFFu, qsc, 4 * (2 * c));
-      cs[t][1] = __shfl_sync(0xFFFFFFFFu, qsc, 4 * (2 * c + 1));
+      hcs[t][0] = 0.5f * __shfl_sync(0xFFFFFFFFu, qsc, 4 * (2 * c));
+      hcs[t][1] = 0.5f * __shfl_sync(0xFFFFFFFFu, qsc, 4 * (2 * c + 1));
       // accumulator column 2c + u is vector 8t + 2c + u = row n / H, head
       // n % H.  With H = 1 a lane owns two rows per tile; otherwise a row's
       // heads sit on 1, 2 or 4 lanes and the lowest of them writes.
@@ -325,8 +326,11 @@ index_scores_kernel(const ScParams p) {
         for (int e = 0; e < 4; ++e) acc[t][e] = 0.0f;
       if (j0 < L) {
         // this lane's two token rows (g, g + 8), dims 32c .. 32c + 31 of
-        // each as 16 f16 pairs: pair m holds dims 32c + 2m, 32c + 2m + 1
-        uint32_t kp[2][16];
+        // each: raw code words, converted to f16 pairs one k-step at a time
+        // (pair m holds dims 32c + 2m, 32c + 2m + 1)
+        constexpr int kW = F::kRowBytes / 16;        // words of a row per lane
+        uint32_t rw[2][kW];
+        uint32_t f2[2] = {0u, 0u};                   // MXFP4 group factor, f16x2
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int tt = kScTile * tile + g + 8 * h;
@@ -335,37 +339,46 @@ index_scores_kernel(const ScParams p) {
             const uint4 w0 = *reinterpret_cast<const uint4 *>(sb + tt * F::kRowBytes + 32 * c);
             const uint4 w1 =
                 *reinterpret_cast<const uint4 *>(sb + tt * F::kRowBytes + 32 * c + 16);
-            const uint32_t b[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int m = 0; m < 16; ++m)
-              kp[h][m] = e4m3x2_to_f16x2(b[m >> 1] >> (16 * (m & 1)));
+            rw[h][0] = w0.x; rw[h][1] = w0.y; rw[h][2] = w0.z; rw[h][3] = w0.w;
+            rw[h][kW > 4 ? 4 : 0] = w1.x; rw[h][kW > 5 ? 5 : 0] = w1.y;
+            rw[h][kW > 6 ? 6 : 0] = w1.z; rw[h][kW > 7 ? 7 : 0] = w1.w;
             tok_scale[h] = __uint_as_float(side);
           } else {
             const uint4 w0 = *reinterpret_cast<const uint4 *>(sb + tt * F::kRowBytes + 16 * c);
-            // the token's groups brought to its largest exponent (a power
-            // of two <= 1 per group, exact down to f16's smallest subnormal)
-            const uint32_t m2 = __vmaxu2(side & 0x00FF00FFu, (side >> 8) & 0x00FF00FFu);
-            const int Xmax = static_cast<int>(max(m2 & 0xFFFFu, m2 >> 16)) - 127;
-            const int d = static_cast<int>((side >> (8 * c)) & 0xFFu) - 127 - Xmax;
-            const uint32_t f = d >= -14 ? static_cast<uint32_t>(15 + d) << 10
-                                        : (d >= -24 ? 1u << (d + 24) : 0u);
-            const uint32_t f2 = f | (f << 16);
-            const uint32_t b[4] = {w0.x, w0.y, w0.z, w0.w};
-#pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-              uint32_t lo, hi;
-              e2m1x4_to_f16x2x2(b[m >> 2] >> (8 * (m & 3)), lo, hi);
-              kp[h][m] = hmul2(lo, f2);
-              kp[h][m + 1] = hmul2(hi, f2);
-            }
-            tok_scale[h] = exp2i(Xmax);
+            rw[h][0] = w0.x; rw[h][1] = w0.y; rw[h][2] = w0.z; rw[h][3] = w0.w;
+            // the token's groups brought to its largest exponent: lane c
+            // holds group c, the quad the token.  2^(X_c - Xmax) as binary32
+            // (0 below 2^-126), then rounded to f16 -- exact down to f16's
+            // smallest subnormal 2^-24, 0 below it
+            const int xb = static_cast<int>((side >> (8 * c)) & 0xFFu);
+            int mb = max(xb, __shfl_xor_sync(0xFFFFFFFFu, xb, 1));
+            mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, 2));
+            const float fx = __uint_as_float(static_cast<uint32_t>(max(xb - mb + 127, 0)) << 23);
+            f2[h] = pack_f16x2(fx, fx);
+            // 2^Xmax: the largest exponent byte is the binary32 exponent
+            // field (byte 0: 2^-127, a subnormal)
+            tok_scale[h] = __uint_as_float(mb ? static_cast<uint32_t>(mb) << 23 : 1u << 22);
           }
         }
         // S^T = K Q^T over the 8 k-steps, both query tiles: a0/a2 = row g
         // pairs 2s / 2s + 1, a1/a3 = row g + 8
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t a[4] = {kp[0][2 * s], kp[1][2 * s], kp[0][2 * s + 1], kp[1][2 * s + 1]};
+          uint32_t a[4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (kFormat == KVQ_INDEX_FP8) {
+              // pairs 2s, 2s + 1 = bytes 4s .. 4s + 3 = word s
+              a[h] = e4m3x2_to_f16x2(rw[h][s]);
+              a[2 + h] = e4m3x2_to_f16x2(rw[h][s] >> 16);
+            } else {
+              // pairs 2s, 2s + 1 = bytes 2s, 2s + 1 = half s & 1 of word s / 2
+              uint32_t lo, hi;
+              e2m1x4_to_f16x2x2(rw[h][s >> 1] >> (16 * (s & 1)), lo, hi);
+              a[h] = hmul2(lo, f2[h]);
+              a[2 + h] = hmul2(hi, f2[h]);
+            }
+          }
           mma_f16_16816(acc[0], a, qb[0][s][0], qb[0][s][1]);
           mma_f16_16816(acc[1], a, qb[1][s][0], qb[1][s][1]);
         }
@@ -373,26 +386,40 @@ index_scores_kernel(const ScParams p) {
         tok_scale[0] = tok_scale[1] = 0.0f;          // past the context: every entry -inf
       }
       // acc[t] = (token g, col 2c), (g, 2c + 1), (g + 8, 2c), (g + 8, 2c + 1).
-      // The token and column scales are >= 0, so the ReLU goes first:
-      // score = tok * sum_h cs_h * max(0, acc_h)
+      // The token and column scales are >= 0, so the ReLU goes first, as
+      // (x + |x|) / 2: score = tok * sum_h cs_h * max(0, acc_h).  A tile that
+      // every row sees in full needs no mask.
+      const bool plain = j0 + kScTile <= vis_min && j0 + kScTile <= p.max_len;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int j = j0 + g + 8 * h;
-          const float r0 = fmaxf(acc[t][2 * h], 0.0f) * cs[t][0];
-          const float r1 = fmaxf(acc[t][2 * h + 1], 0.0f) * cs[t][1];
+          const float r0 = (acc[t][2 * h] + fabsf(acc[t][2 * h])) * hcs[t][0];
+          const float r1 = (acc[t][2 * h + 1] + fabsf(acc[t][2 * h + 1])) * hcs[t][1];
           if (kH == 1) {
 #pragma unroll
-            for (int u2 = 0; u2 < kU; ++u2)
-              if (orow[t][u2] != nullptr && j < p.max_len)
-                orow[t][u2][j] = j < vis[t][u2] ? (u2 ? r1 : r0) * tok_scale[h] : -INFINITY;
+            for (int u2 = 0; u2 < kU; ++u2) {
+              if (orow[t][u2] == nullptr) continue;
+              float v = (u2 ? r1 : r0) * tok_scale[h];
+              if (!plain) {
+                if (j >= p.max_len) continue;
+                v = j < vis[t][u2] ? v : -INFINITY;
+              }
+              orow[t][u2][j] = v;
+            }
           } else {
             float sum = r0 + r1;
             if (kH >= 4) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
             if (kH >= 8) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
-            if (orow[t][0] != nullptr && j < p.max_len)
-              orow[t][0][j] = j < vis[t][0] ? sum * tok_scale[h] : -INFINITY;
+            if (orow[t][0] != nullptr) {
+              float v = sum * tok_scale[h];
+              if (plain) {
+                orow[t][0][j] = v;
+              } else if (j < p.max_len) {
+                orow[t][0][j] = j < vis[t][0] ? v : -INFINITY;
+              }
+            }
           }
         }
     }
