@@ -80,6 +80,12 @@ def _load():
             lib.kvqo_quantize_scatter.argtypes = [P, i64, P, i64, i64, ctypes.c_int,
                                                   ctypes.c_int, P, i64, P, P, P, P]
             lib.kvqo_dequant_rows.restype = None
+            lib.kvqo_e5m2_decode.restype = f64
+            lib.kvqo_e5m2_decode.argtypes = [ctypes.c_uint8]
+            lib.kvqo_e5m2_encode.restype = ctypes.c_uint8
+            lib.kvqo_e5m2_encode.argtypes = [ctypes.c_float]
+            lib.kvqo_e5m2_encode_array.restype = None
+            lib.kvqo_e5m2_encode_array.argtypes = [P, i64, P]
             lib.kvqo_e2m1_decode.argtypes = [ctypes.c_uint8]
             lib.kvqo_e2m1_decode.restype = ctypes.c_double
             lib.kvqo_e2m1_encode.argtypes = [ctypes.c_double]
@@ -137,6 +143,25 @@ def e4m3_encode(q) -> np.ndarray:
     qa = _c(np.reshape(q, -1), np.float32)
     out = np.empty(qa.shape, dtype=np.uint8)
     lib.kvqo_e4m3_encode_array(_ptr(qa), qa.size, _ptr(out))
+    return out.reshape(shape)
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    """Exact value of each e5m2 code (float64; +-inf for 0x7C / 0xFC, NaN for
+    the other exponent-31 codes)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    table = np.array([lib.kvqo_e5m2_decode(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def e5m2_encode(q) -> np.ndarray:
+    """Round-to-nearest-even, saturating e5m2 code of each finite float32."""
+    lib = _load()
+    shape = np.shape(q)
+    qa = _c(np.reshape(q, -1), np.float32)
+    out = np.empty(qa.shape, dtype=np.uint8)
+    lib.kvqo_e5m2_encode_array(_ptr(qa), qa.size, _ptr(out))
     return out.reshape(shape)
 
 

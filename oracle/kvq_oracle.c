@@ -571,3 +571,70 @@ int32_t kvqo_index_scores(int format, const uint8_t *codes, const float *scales,
     }
     return err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* E5M2, for the unscaled-cache ablation.  [SGJ] design points: the fp8 cache
+ * of that page casts O(1) values to e4m3 or e5m2 with no scale at all, and
+ * prefers e4m3 for its extra mantissa bit.  E5M2: 1 sign, 5 exponent bits with
+ * bias 15, 2 mantissa bits; exponent field 0 is subnormal (m/4 * 2^-14),
+ * exponent field 31 holds infinity (m = 0) and NaN (m != 0).
+ * Reading: the cast rounds to nearest, ties to the even mantissa, and
+ * saturates at the largest finite magnitude 57344 (as the e4m3 encode does at
+ * 448), so no infinity or NaN code is produced from a finite input. */
+
+double kvqo_e5m2_decode(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int e = (c >> 2) & 0x1F;
+    int m = c & 0x3;
+    double mag;
+    if (e == 31)
+        mag = (m == 0) ? INFINITY : NAN;
+    else if (e == 0)
+        mag = ldexp((double)m / 4.0, -14);
+    else
+        mag = ldexp(1.0 + (double)m / 4.0, e - 15);
+    return sign ? -mag : mag;
+}
+
+/* The 124 finite nonnegative magnitudes, code 0 .. 0x7B, ascending. */
+static double grid52[0x7C];
+
+__attribute__((constructor)) static void fill_e5m2_table(void)
+{
+    for (int c = 0; c < 0x7C; ++c)
+        grid52[c] = kvqo_e5m2_decode((uint8_t)c);
+}
+
+/* Nearest e5m2 magnitude by bisection over the ascending grid, ties to the
+ * code with the even mantissa (the code's least significant bit). */
+uint8_t kvqo_e5m2_encode(float q)
+{
+    uint8_t sign = signbit(q) ? 0x80 : 0x00;
+    double a = fabs((double)q);
+    if (a >= 57344.0)
+        return (uint8_t)(sign | 0x7B);
+    int lo = 0, hi = 0x7B;                 /* grid52[lo] <= a < grid52[hi] */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (grid52[mid] <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double half = 0.5 * (grid52[lo] + grid52[hi]);
+    int pick;
+    if (a < half)
+        pick = lo;
+    else if (a > half)
+        pick = hi;
+    else
+        pick = (lo & 1) ? hi : lo;
+    return (uint8_t)(sign | pick);
+}
+
+void kvqo_e5m2_encode_array(const float *q, int64_t n, uint8_t *codes)
+{
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = kvqo_e5m2_encode(q[i]);
+}

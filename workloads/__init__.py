@@ -231,3 +231,11 @@ def index_queries(num_requests: int, rows: int, heads: int, seed: int) -> torch.
     """bf16 query vectors [N, R, H, 128], N(0,1)."""
     g = generator(seed, 8)
     return torch.randn(num_requests, rows, heads, HEAD_DIM, generator=g).to(torch.bfloat16)
+
+
+def unit_rms_rows(num_tokens: int, H: int, D: int, g: torch.Generator) -> torch.Tensor:
+    """bf16 rows [T, H, D] with unit RMS each (N(0,1) divided by the row's
+    RMS): the O(1) post-LayerNorm values an unscaled fp8 cache is meant for."""
+    x = torch.randn(num_tokens, H, D, generator=g, dtype=torch.float64)
+    x = x / torch.sqrt((x * x).mean(dim=-1, keepdim=True))
+    return x.to(torch.bfloat16)
