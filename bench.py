@@ -75,7 +75,7 @@ DESCRIPTIONS = {
     "store": ("prefill store under CUDA graph: 16,384 tokens as strided K/V views of a fused "
               "qkv [16384, 6144], 1% outliers x50, zero rows, permuted int64 slot ids, block 64"),
     "index": ("MXFP4 index-key store under CUDA graph: 262,144 rows of 128 bf16 values "
-              "(N(0,1) x a log-normal magnitude per 32-dim group) into E2M1 pairs + one E8M0 "
+              "(N(0,1) x a log-normal magnitude per 32-dim group) into E2M1 codes (two a byte) + an E8M0 "
               "exponent per 32 dims, permuted int64 slot ids"),
     "scores": ("stacked index scores under CUDA graph: 64 requests x 4 query rows x 4 index "
                "heads (16 stacked vectors), context 32768, block 64, MXFP4 index keys, "
@@ -935,7 +935,7 @@ def run_index(args, rank, local, world):
                        "l2": ("flushed before every timed step (256 MiB write, then a 256 MiB "
                               "read)") if flush is not None else "not flushed (profile mode)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "storage": "E2M1 pairs (uint8) + E8M0 exponent per 32 dims"},
+                       "storage": "E2M1 codes two per byte + an E8M0 exponent per 32 dims"},
             "pct_of_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
             "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
             "rows_quantized_per_s": round(world * INDEX_TOKENS / (ms * 1e-3), 1),
@@ -1150,7 +1150,7 @@ def run_scores(args, rank, local, world):
                        "l2": ("flushed before every timed step (256 MiB write, then a 256 MiB "
                               "read)") if flush is not None else "not flushed (profile mode)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "keys": ("E2M1 pairs (uint8) + E8M0 exponent per 32 dims"
+                       "keys": ("E2M1 codes two per byte + an E8M0 exponent per 32 dims"
                                 if fmt == 1 else "e4m3 codes + fp32 scale per row") +
                                ", random codes"},
             "pct_of_8tbs": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),

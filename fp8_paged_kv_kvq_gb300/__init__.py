@@ -9,9 +9,9 @@ a ``KvqError`` is raised.
 
 Row format (ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8 scale
 planes for KV offload", PR description; FlashML-org/FreeToken PR #354
-"feat(kvcache): store the KV cache as fp8 e4m3 codes", PR description): each
-(token, KV head) row of K and V is head_dim e4m3 codes in a uint8 buffer of the
-16-bit cache's geometry plus one fp32 scale = row amax / 448.
+"feat(kvcache): store the KV cache as fp8 e4m3 codes", PR description): every
+cached (token, KV head) row of K or V is head_dim e4m3 bytes, in a uint8 buffer
+shaped like the 16-bit cache, and one fp32 scale = row amax / 448.
 """
 from __future__ import annotations
 

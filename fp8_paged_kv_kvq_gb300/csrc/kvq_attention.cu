@@ -3,11 +3,12 @@
 //
 // ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for KV
 // offload", PR description:
-//  * K/V bullet: the attention reads E4M3 tiles, multiplies the key scale into
-//    its score column and folds the value scale into the probability before PV;
-//  * stacked decode scorer: the query rows of one verify (4 rows) and the heads
-//    that share the keys are stacked into one M operand, so a request's keys
-//    are read once per verify and meet every row in a single dot.
+//  * K/V bullet: attention runs on the E4M3 tiles themselves; a token's key
+//    scale is applied to its score after the code dot product, and its value
+//    scale to its probability ahead of the PV product;
+//  * stacked decode scorer: all query rows of a verify step (4 of them) and
+//    all heads reading the same keys go into one MMA operand, so each key tile
+//    is loaded once per step for every one of those rows.
 // sgl-project/sglang-jax #1776 "feat(dsa): implement fp8 KV cache (e4m3) with
 // a bf16 indexer cache", Modifications: the cached block is upcast to the query
 // dtype before the score dot, and P is never rounded to fp8.

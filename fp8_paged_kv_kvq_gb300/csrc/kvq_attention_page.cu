@@ -3,8 +3,8 @@
 //
 // Same method and per-chunk arithmetic as kvq_attention_skinny.cu (ROCm/ATOM
 // PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for KV offload",
-// PR description, K/V bullet: key scale into the score column, value scale
-// folded into the probability before PV; transposed tiles S^T = K Q^T on FP8
+// PR description, K/V bullet: per-token key scale on the score after the code
+// dot, per-token value scale on the probability ahead of PV; transposed tiles S^T = K Q^T on FP8
 // tensor cores with Q as two exact e4m3 pieces, O^T = V^T P^T on f16 tensor
 // cores), with the loads laid out page-major:
 //

@@ -2,9 +2,9 @@
 // rows per KV head (decode with GQA <= 8, or short verify), FP8 cache.
 //
 // Same method as kvq_attention.cu (ROCm/ATOM PR #2655 "fix(qwen4-exp): register
-// the QSA FP8 scale planes for KV offload", PR description, K/V bullet: key
-// scale into the score column, value scale folded into the probability before
-// PV), laid out for few rows:
+// the QSA FP8 scale planes for KV offload", PR description, K/V bullet:
+// per-token key scale on the score after the code dot, per-token value scale on
+// the probability ahead of PV), laid out for few rows:
 //
 //  * The tiles are transposed: S^T = K Q^T and O^T = V^T P^T, so the tokens (and
 //    the head dims) fill the MMA's 16-row M side and the <= 8 query rows the

@@ -3,9 +3,9 @@
 //
 // The method is the one of kvq_attention.cu (ROCm/ATOM PR #2655 "fix(qwen4-exp):
 // register the QSA FP8 scale planes for KV offload", PR description, K/V
-// bullet: the key scale multiplies its score column, the value scale folds
-// into the probability before PV; the R verify rows of a request that share a
-// KV head are stacked into one tile).  Laid out for sm_103a:
+// bullet: each token's key scale is applied to its score after the code dot
+// product and its value scale to its probability ahead of PV; the R verify rows
+// of a request that share a KV head are stacked into one tile).  Laid out for sm_103a:
 //
 //  * CTA = (KV head, partition, request), one per SM, 14 warps with fixed
 //    roles.  Warp 12 (one lane) streams 128-token stages through a 4-deep ring

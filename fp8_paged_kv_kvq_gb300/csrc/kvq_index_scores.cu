@@ -1,11 +1,12 @@
 // kvq_index_scores.cu -- stacked index scoring over the compressed index keys.
 //
 // ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for KV
-// offload", PR description: the stacked decode scorer puts R query rows x H
-// index heads of a request into one M operand so the request's compressed
-// index keys are read once per verify and meet every head in a single dot;
-// the per-head ReLU is applied before the heads are summed.  Keys are FP8 with
-// a per-row FP32 scale or MXFP4 (E2M1 pairs, one E8M0 exponent per 32 dims):
+// offload", PR description: the decode-time scorer there multiplies all R query
+// rows x H index heads of a request against each cached index key in a single
+// matrix product, so every key is loaded once per step; each head's dot product
+// is clipped at zero (ReLU) and the clipped values are added into the row's
+// score.  Keys are FP8 plus an FP32 scale for each row, or MXFP4 (two E2M1
+// codes per byte and an E8M0 exponent for every 32 dims):
 //     score(r, i, t) = sum_h max(0, <q(r, i, h), khat_t>),
 // -inf where row i does not see token t (t >= L - R + 1 + i).
 //

@@ -2,11 +2,11 @@
 // E4M3 paged cache, and the row dequantiser.
 //
 // FreeToken PR #354 "feat(kvcache): store the KV cache as fp8 e4m3 codes", PR
-// description: one (token, KV head) row of K and of V becomes head_dim e4m3
-// codes plus one fp32 symmetric scale (ROCm/ATOM PR #2655, PR description, K/V
-// bullet: scale = row amax / FP8 max), written by one launch for K and V to
-// slot ids held in device memory, so the launch can be captured in a CUDA
-// graph.  The fix commit "give the V tensor its own row pitch in the fp8 KV
+// description: every cached (token, KV head) row, of K as of V, is held as
+// head_dim e4m3 bytes and a single symmetric fp32 scale (ROCm/ATOM PR #2655, PR
+// description, K/V bullet: the scale is the row's largest magnitude over the
+// FP8 maximum); one launch handles K and V and takes its slot ids from device
+// memory, so it can be captured in a CUDA graph.  The fix commit "give the V tensor its own row pitch in the fp8 KV
 // store": K and V each carry their own token pitch.
 //
 // Layout of the work: each 4-lane group owns one 128-element row (32 elements,
@@ -229,9 +229,9 @@ dequant_rows_kernel(const DequantParams p) {
 
 // ---------------------------------------------------------------------------
 // Compressed index keys (ATOM PR #2655, PR description, index-key bullet):
-// FP8 with one FP32 scale per row (the K/V row format), or MXFP4 -- packed
-// E2M1 pairs with one E8M0 exponent per 32 dims, rounded up so a group never
-// clips.  Rows of 128 values, one per token; each 4-lane group owns a row and
+// FP8 with one FP32 scale per row (the K/V row format), or MXFP4 -- two E2M1
+// codes per byte and one E8M0 exponent per 32 dims, the exponent taken large
+// enough that no element of its group exceeds the E2M1 range.  Rows of 128 values, one per token; each 4-lane group owns a row and
 // each lane 32 values, which for MXFP4 is exactly one exponent group.
 struct IndexParams {
   const uint16_t *x;

@@ -7,19 +7,19 @@
  *  - Row format.  ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8
  *    scale planes for KV offload", PR description (K/V bullet), and
  *    FlashML-org/FreeToken PR #354 "feat(kvcache): store the KV cache as fp8
- *    e4m3 codes", PR description: each (token, KV head) row of K and of V is
- *    stored as head_dim E4M3 codes plus ONE fp32 symmetric scale,
+ *    e4m3 codes", PR description: every cached (token, KV head) row, of K as of
+ *    V, is held as head_dim E4M3 bytes and a single symmetric fp32 scale,
  *        scale = amax(|x|) / 448,   code_d = e4m3_rne(x_d / scale),
- *    so the row's largest element maps to +-448 and nothing saturates.  Codes
- *    live in a plain uint8 buffer with exactly the geometry of a 16-bit KV
- *    buffer ([num_slots, num_kv_heads, head_dim]); the scales in a sidecar
+ *    so the row's largest element maps to +-448 and nothing saturates.  The
+ *    code bytes sit in a plain uint8 buffer shaped like the 16-bit cache
+ *    ([num_slots, num_kv_heads, head_dim]); the scales in a sidecar
  *    [num_slots, num_kv_heads] fp32.  Division and rounding are IEEE binary32,
  *    round-to-nearest-even; |x / scale| >= 448 saturates to 448; an all-zero
  *    row stores scale 0 and codes 0x00; a NaN code is never written.
  *
- *  - Attention.  ATOM PR #2655, PR description (K/V bullet): the attention
- *    reads E4M3 tiles, multiplies the key scale into its score column and folds
- *    the value scale into the probability before PV.  With G = Hq / H query
+ *  - Attention.  ATOM PR #2655, PR description (K/V bullet): attention runs
+ *    on the E4M3 tiles; a token's key scale is applied to its score after the
+ *    code dot product and its value scale to its probability ahead of PV.  With G = Hq / H query
  *    heads per KV head (query head hq reads KV head hq / G), for request r with
  *    context length L and R query rows (R = 1: decode; R > 1: the rows of a
  *    multi-token verify whose last R tokens are already cached, as in the
@@ -249,9 +249,9 @@ kvq_status kvq_dequant_rows(const kvq_cache *cache, const int64_t *slot_ids, int
 /* ------------------------------------------------------------------------ */
 /* Compressed index keys.  ATOM PR #2655, PR description, index-key bullet:
  * index keys are cached either as FP8 with one FP32 scale per row -- the K/V
- * row format above -- or as MXFP4: packed E2M1 pairs plus one E8M0 exponent
- * per 32 dims, rounded up so a group never clips; FP4 decodes with bit
- * operations.  One row of `dim` values per token (one index head):
+ * row format above -- or as MXFP4: two E2M1 codes per byte plus one E8M0
+ * exponent per 32 dims, the exponent large enough that no element of the group
+ * overflows; the FP4 codes are decoded by bit manipulation.  One row of `dim` values per token (one index head):
  *   FP8    codes uint8 [num_slots, dim] (e4m3) and scales fp32 [num_slots]:
  *          scale = amax / 448, code_d = e4m3_rne(x_d / scale), as for K/V.
  *   MXFP4  codes uint8 [num_slots, dim / 2]: element 2i in the low nibble of
@@ -301,10 +301,10 @@ kvq_status kvq_index_dequant_rows(const kvq_index_cache *cache, const int64_t *s
                                   int32_t *err_flags, kvq_stream_t stream);
 
 /* Stacked index scores over the compressed index keys (one launch, capturable).
- * ATOM PR #2655, PR description: the stacked decode scorer puts a request's R
- * query rows x H index heads into one operand so that every cached index key
- * is read once per step and meets every head in one dot product; the ReLU of
- * each head's dot comes before the heads are summed.  For request r, row i
+ * ATOM PR #2655, PR description: the decode-time scorer there multiplies all
+ * R query rows x H index heads of a request against each cached index key in
+ * a single matrix product, so every key is loaded once per step; each head's
+ * dot product is clipped at zero (ReLU) and the clipped values are added.  For request r, row i
  * and token t < L_r - R + 1 + i (row i sees the context up to and including
  * its own position, as in verify):
  *     out[r*R + i][t] = sum_h max(0, sum_d q[r][i][h][d] * khat_t[d]),

@@ -11,7 +11,7 @@ only compiles the C file with gcc and marshals numpy arrays through ctypes.
 Pages followed (title and section):
   * ROCm/ATOM PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for
     KV offload" -- PR description, K/V bullet (per-row FP32 scale = amax / FP8
-    max; key scale into the score column, value scale into the probability).
+    max; key scale on the score, value scale on the probability).
   * FlashML-org/FreeToken PR #354 "feat(kvcache): store the KV cache as fp8 e4m3
     codes" -- PR description (uint8 codes + fp32 row-scale sidecar, fused
     quantize+scatter to device slot ids) and the fix commit "give the V tensor

@@ -5,9 +5,9 @@ bf16 indexer cache", design points and accuracy tests: the latent cache there
 is cast to e4m3 or e5m2 with no scale at all (its values are O(1), post-
 LayerNorm; fp8 precision is relative, so a power-of-two rescale would change
 nothing), e4m3 is preferred for its extra mantissa bit (worst-case relative
-rounding error about 6 % against about 12.5 % for e5m2), and the attention
-error against an otherwise identical bf16 cache comes out about twice as large
-for e5m2 (ratios 1.87-2.10 on that page).
+rounding error about 6 % against about 12.5 % for e5m2), and, measured as the
+attention error relative to the same cache kept in bf16, e5m2 does about twice
+as badly as e4m3 (ratios 1.87-2.10 on that page).
 
 This module states the caches the ablation compares and the attention it runs
 on them, in float64, in the plainest form:

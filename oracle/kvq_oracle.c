@@ -14,14 +14,15 @@
  * Sources (web pages; cited by title and section):
  *  [ATOM]   ROCm/ATOM PR #2655, "fix(qwen4-exp): register the QSA FP8 scale
  *           planes for KV offload" -- PR description, K/V bullet: E4M3 codes
- *           with one FP32 scale per (token, KV head) = row amax / FP8 max; the
- *           attention kernel multiplies the key scale into its score column and
- *           folds the value scale into the probability before PV.
+ *           and, per (token, KV head), an FP32 scale equal to the row's largest
+ *           magnitude over the FP8 maximum; the
+ *           attention applies a token's key scale to its score after the code
+ *           dot product and its value scale to its probability ahead of PV.
  *  [FT]     FlashML-org/FreeToken PR #354, "feat(kvcache): store the KV cache as
- *           fp8 e4m3 codes (--kv-cache-dtype fp8)" -- PR description: head_dim
- *           codes plus one fp32 symmetric scale per row, codes in a uint8 buffer
- *           with the geometry of the 16-bit KV buffer, fused quantize+scatter to
- *           device slot ids; review thread and fix commit "give the V tensor its
+ *           fp8 e4m3 codes (--kv-cache-dtype fp8)" -- PR description: a row is
+ *           head_dim code bytes and a single symmetric fp32 scale, the bytes in
+ *           a uint8 buffer shaped like the 16-bit cache, written by a fused
+ *           quantize-and-scatter to slot ids held on the device; review thread and fix commit "give the V tensor its
  *           own row pitch in the fp8 KV store": K and V each have their own row
  *           pitch; codes are checked against a round-to-nearest-even reference.
  *  [SGJ]    sgl-project/sglang-jax #1776, "feat(dsa): implement fp8 KV cache
@@ -158,7 +159,8 @@ void kvqo_float_to_bf16_array(const float *x, int64_t n, uint16_t *out)
 
 /* ------------------------------------------------------------------------ */
 /* One (token, KV head) row: [ATOM] PR description (K/V bullet) and [FT] PR
- * description: scale = row amax / FP8 max (448), codes = e4m3(x / scale). */
+ * description: the scale is the row's largest magnitude over 448, and each
+ * code is e4m3(x / scale). */
 
 void kvqo_quantize_row(const uint16_t *x, int D, uint8_t *codes, float *scale)
 {
@@ -260,9 +262,9 @@ void kvqo_dequant_rows(const uint8_t *codes, const float *scales, int64_t num_sl
  *
  * For each visible token: k_hat = decode(code) * k_scale, v_hat likewise
  * (exact in double); score = sm_scale * <q, k_hat>; p = softmax(score);
- * out = sum_j p_j * v_hat_j.  Multiplying the key scale into the score column
- * and folding the value scale into p before PV ([ATOM] PR description) is the
- * same quantity in exact arithmetic; the oracle takes the plain definition.
+ * out = sum_j p_j * v_hat_j.  Scaling the score by the key scale after the
+ * code dot and p by the value scale ahead of PV ([ATOM] PR description) gives
+ * the same quantity in exact arithmetic; the oracle takes the plain definition.
  *
  * q: bf16 [N*R, Hq, D]; out: double [N*R, Hq, D]. Returns the error word
  * (bit 1: a block id outside [0, num_slots/bs); bit 2: a context length
@@ -395,14 +397,15 @@ int32_t kvqo_paged_attention_units(const uint8_t *k_codes, const uint8_t *v_code
 /* ------------------------------------------------------------------------ */
 /* Compressed index keys, [ATOM] PR description, index-key bullet: FP8 with a
  * per-row FP32 scale (the rows above, one index head per token: H = 1), or
- * MXFP4 -- packed E2M1 pairs and one E8M0 exponent per 32 dims, rounded up
- * so that a group never clips; FP4 decodes with bit operations.
+ * MXFP4 -- two E2M1 codes per byte and one E8M0 exponent per 32 dims, the
+ * exponent rounded up until no element of the group overflows; the FP4 codes
+ * are decoded by bit manipulation.
  *
  * Readings of what the bullet leaves open (each one is listed in the design doc):
  *  - E2M1 is the OCP microscaling element format: 1 sign bit, 2 exponent bits
  *    (bias 1), 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
  *  - E8M0 is a biased exponent: byte X + 127 stands for the group scale 2^X.
- *  - "rounded up so a group never clips": X is the smallest integer with
+ *  - the exponent rounded up so no element overflows: X is the smallest integer with
  *    group amax <= 6 * 2^X (the largest E2M1 magnitude), clamped to
  *    [-127, 127]; an all-zero group gets X = -127.
  *  - Each element becomes the E2M1 value nearest to x / 2^X (exact: a power

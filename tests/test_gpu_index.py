@@ -1,7 +1,7 @@
 """kvq_index_quantize_scatter / kvq_index_dequant_rows on the GPU against the
 oracle (ROCm/ATOM PR #2655, PR description, index-key bullet: index keys as
-FP8 with a per-row FP32 scale, or MXFP4 with packed E2M1 pairs and one E8M0
-exponent per 32 dims, rounded up so a group never clips): codes, scales and
+FP8 plus an FP32 scale for each row, or MXFP4 -- two E2M1 codes per byte and
+an E8M0 exponent for every 32 dims, large enough that no element overflows): codes, scales and
 exponents bit-exact, dequantised rows exact, on random rows and on rows built
 to sit on every rounding decision."""
 import numpy as np

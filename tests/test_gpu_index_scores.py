@@ -1,7 +1,7 @@
 """kvq_index_scores on the GPU against the oracle (ATOM PR #2655, PR
-description: the stacked decode scorer puts a request's query rows x index
-heads into one operand, reads each cached index key once, and applies each
-head's ReLU before the heads are summed).
+description: the decode-time scorer multiplies a request's query rows x
+index heads against each cached index key in one product, loading each key
+once, and clips each head's dot at zero before adding the heads).
 
 Scores must lie within the bound the kernel's arithmetic gives (f16 products
 of exactly converted keys and power-of-two-scaled queries, fp32 accumulation;

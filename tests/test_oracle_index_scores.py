@@ -1,6 +1,7 @@
 """Pins for the oracle's index scorer (ROCm/ATOM PR #2655, PR description:
-the stacked decode scorer lets R query rows x H index heads meet each cached
-index key once; the per-head ReLU comes before the heads are summed), checked
+the decode-time scorer multiplies R query rows x H index heads against each
+cached index key in one product; each head's dot is clipped at zero before
+the heads are added), checked
 against scores worked by hand, a dense numpy evaluation on the dequantised
 keys, and the block-table indirection."""
 import numpy as np

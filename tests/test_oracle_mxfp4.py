@@ -1,6 +1,6 @@
 """Pins for the oracle's MXFP4 index-key codec (ROCm/ATOM PR #2655, PR
-description, index-key bullet: packed E2M1 pairs, one E8M0 exponent per 32
-dims, rounded up so a group never clips), checked against values worked by
+description, index-key bullet: two E2M1 codes per byte, an E8M0 exponent for
+every 32 dims, large enough that no element overflows), checked against values worked by
 hand from the format, brute force over all 16 codes, and properties that must
 hold for every input."""
 import numpy as np
