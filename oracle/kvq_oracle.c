@@ -29,7 +29,7 @@
  *           (e4m3) with a bf16 indexer cache" -- design points: e4m3 range 448,
  *           0.0156 floor of the normal range, ~6% worst-case relative error.
  *
- * Readings of points the pages leave open (each one is listed in the design doc):
+ * Readings of points the pages leave open:
  *  - the encode divides by the stored fp32 scale: q = fl32(x / s);
  *  - rounding is round-to-nearest-even onto the e4m3 grid, |q| >= 448 saturates
  *    to the largest finite code (0x7E magnitude); NaN codes are never produced;
@@ -401,7 +401,7 @@ int32_t kvqo_paged_attention_units(const uint8_t *k_codes, const uint8_t *v_code
  * exponent rounded up until no element of the group overflows; the FP4 codes
  * are decoded by bit manipulation.
  *
- * Readings of what the bullet leaves open (each one is listed in the design doc):
+ * Readings of what the bullet leaves open:
  *  - E2M1 is the OCP microscaling element format: 1 sign bit, 2 exponent bits
  *    (bias 1), 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
  *  - E8M0 is a biased exponent: byte X + 127 stands for the group scale 2^X.
@@ -514,7 +514,7 @@ void kvqo_mxfp4_dequant_rows(const uint8_t *codes, const uint8_t *exps, int64_t 
  * each cached key once, applies the per-head ReLU and sums the heads.  For
  * request r, query row i and cached token t (slot from the block table):
  *     score(r, i, t) = sum_h max(0, <q(r, i, h), khat_t>)
- * with khat_t the dequantised key, computed in double.  Readings (DESIGN.md):
+ * with khat_t the dequantised key, computed in double.  Readings:
  * no per-head weight (a caller folds one into q); row i sees the tokens
  * t < L_r - R + 1 + i, as the attention rows do; every other position up to
  * max_len gets -inf.
