@@ -63,6 +63,18 @@ def test_worst_case_relative_error_is_half_an_ulp(fmt, m, lo, hi):
     u = 2.0 ** -(m + 1)
     assert rel.max() <= u
     assert rel.max() >= 0.999 * u / (1 + u)
+    # the tight maximum, u / (1 + u), sits at 1 + u of a binade: 1/17 and 1/9
+    assert rel.max() <= u / (1 + u) + 1e-7
+
+
+def test_e5m2_bound_is_the_pages_number(golden_dir):
+    """The page's worst-case figure for e5m2 (golden fixture, about 12.5 %) is
+    the half-ulp bound 2^-3 of a 2-bit mantissa."""
+    import json
+    import os
+    facts = json.load(open(os.path.join(golden_dir, "pages_facts.json")))
+    w = facts["worst_case_rel_error"]
+    assert abs(w["e5m2"] - 2.0 ** -3) <= w["approx_rel"] * w["e5m2"]
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
@@ -115,7 +127,8 @@ def test_e5m2_error_is_about_twice_e4m3(R, L):
     err = {f: A.rel_l2(A.attention_fp64(q, A.cache_values(f, k), A.cache_values(f, v),
                                         D ** -0.5), ref)
            for f in ("e4m3", "e5m2", "e4m3_row")}
-    assert 1.6 <= err["e5m2"] / err["e4m3"] <= 2.6, err
+    # the page measured 1.87-2.10 on its model; seeds of this recipe give 1.95-2.11
+    assert 1.8 <= err["e5m2"] / err["e4m3"] <= 2.25, err
     assert err["e4m3"] < 0.1 and err["e4m3_row"] < 0.1
 
 
