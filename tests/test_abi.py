@@ -175,3 +175,24 @@ def test_index_scores_validation_happens_before_launch(lib):
     assert call(q=24) == MISALIGNED
     assert call(out=18) == MISALIGNED
     assert call(q=0) == INVALID
+
+
+def test_index_scores_binding_rejects_bad_tensors():
+    """The Python binding checks dtypes and shapes before it calls the library
+    (every call here raises before anything could be launched)."""
+    import torch
+    cache = kvq.IndexCache.empty(64, kvq.INDEX_MXFP4, device="cpu")
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    lens = torch.zeros(2, dtype=torch.int32)
+    q = torch.zeros(2, 4, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kvq.index_scores(cache, 16, q.float(), bt, lens, 64)                 # not bf16
+    with pytest.raises(ValueError):
+        kvq.index_scores(cache, 16, q[..., :64], bt, lens, 64)               # wrong dim
+    with pytest.raises(ValueError):
+        kvq.index_scores(cache, 16, q, bt.long(), lens, 64)                  # int64 table
+    with pytest.raises(ValueError):
+        kvq.index_scores(cache, 16, q, bt[:1], lens, 64)                     # one table row
+    with pytest.raises(ValueError):
+        kvq.index_scores(cache, 16, q, bt, lens, 64,
+                         out=torch.empty(8, 32, dtype=torch.float32))        # wrong out shape
