@@ -22,7 +22,9 @@
 // chunk a warp:
 //   1. runs S = Q K^T on the FP8 tensor cores (m16n8k32 e4m3, fp32
 //      accumulate) with the K code bytes themselves as B fragments -- no
-//      decode -- against Q split exactly into two e4m3 pieces per element;
+//      decode -- against Q split into two e4m3 pieces per element, q =
+//      2^e (p1 + p2), exact for elements >= 2^-9 of the row's largest and off
+//      by at most 2^-17 of it below that;
 //   2. multiplies each score column by its key scale and sm_scale*log2(e),
 //      masks causally (row i sees tokens j < L - R + 1 + i), and updates a
 //      running max per row, rescaling the accumulators only when the max grows
@@ -312,9 +314,12 @@ attn_partials_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tma
   // Row m is scaled by 2^-e_m (e_m from the row's largest |q|, so the largest
   // scaled element lies in [128, 256)); p1 = e4m3_rne(x) and p2 = e4m3_rne(x -
   // p1).  x has 8 significant bits and p1 keeps the top 4, so the residual is a
-  // multiple of x's ulp no larger than 8 ulps and p2 holds it exactly unless it
-  // falls below e4m3's 2^-9 grid (elements under 2^-17 of the row's largest).
-  // q = 2^e_m * (p1 + p2); 2^e_m multiplies the row's scores later.
+  // multiple of x's ulp no larger than 8 ulps, and p2 holds it exactly when
+  // that ulp is at least e4m3's smallest step 2^-9, i.e. for |x| >= 2^-2 (every
+  // element >= 2^-9 of the row's largest).  For smaller elements p2 rounds to
+  // the 2^-9 grid: q = 2^e_m (p1 + p2) is then off by at most 2^-10 2^e_m,
+  // which is at most 2^-17 of the row's largest.  2^e_m multiplies the row's
+  // scores later.
   float *row_exp = reinterpret_cast<float *>(smem + off_rowexp(MT));   // [MT * 16]
   const int rows_here = min(MT * 16, p.M - row_base);
   auto q_row = [&](int m) {   // m < rows_here
@@ -751,14 +756,12 @@ attn_combine_kernel(const CombineParams p) {
   const int warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
-  // the context length is not written by the partials kernel: read it while
-  // that kernel drains, and wait only before reading the partials
   allow_dependents_launch();
+  grid_dependency_wait();                         // before any global read
   int L = p.context_lens[r];
   L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
   const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
   if (n_parts <= 1) return;                       // written by the partials kernel
-  grid_dependency_wait();
   const float2 *ml = p.ml_part + row * p.n_parts_max;
   const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * p.n_parts_max * kHeadDim) +
                      lane;
@@ -836,13 +839,11 @@ attn_combine_rows_kernel(const CombineParams p) {
   allow_dependents_launch();
   if (row >= p.rows_total) return;
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
-  // the context length is not written by the partials kernel: read it while
-  // that kernel drains, and wait only before reading the partials
+  grid_dependency_wait();                         // before any global read
   int L = p.context_lens[r];
   L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
   const int n_parts = (L + p.part_tokens - 1) / p.part_tokens;
   if (n_parts <= 1) return;                       // written by the partials kernel
-  grid_dependency_wait();
   const float2 *ml = p.ml_part + row * p.n_parts_max;
   const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * p.n_parts_max * kHeadDim) +
                      lane;

@@ -5,7 +5,8 @@
 // PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for KV offload",
 // PR description, K/V bullet: per-token key scale on the score after the code
 // dot, per-token value scale on the probability ahead of PV; transposed tiles S^T = K Q^T on FP8
-// tensor cores with Q as two exact e4m3 pieces, O^T = V^T P^T on f16 tensor
+// tensor cores with Q as two e4m3 pieces (exact for elements >= 2^-9 of the row's
+// largest, off by <= 2^-17 of it below), O^T = V^T P^T on f16 tensor
 // cores), with the loads laid out page-major:
 //
 //  * CTA = (group of 4 KV heads, partition, request).  Warps 0-3 each own one
@@ -103,12 +104,11 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int part = blockIdx.y;
   const int r = blockIdx.z;
 
-  // Everything before the first cache read (context length, block table,
-  // query pieces) runs while the previous kernel of the stream -- the
-  // quantize-scatter that writes the cache -- may still be running: none of it
-  // reads what that kernel writes.  The producer waits before its first copy,
-  // the head warps before their first global write.
+  // The launch overlaps the previous kernel's drain; every global access
+  // (context lengths, block tables, queries, the cache, the outputs) comes
+  // after the wait, so whatever a previous kernel wrote is visible.
   allow_dependents_launch();
+  grid_dependency_wait();
   int L = p.context_lens[r];
   if (L < 0 || L > p.ctx_limit) {
     if (part == 0 && tid == 0 && h0 == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
@@ -147,7 +147,6 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
   if (warp == kPgHeads) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      grid_dependency_wait();
       int issued = 0;
       bool bad = false;
       for (int u = 0; u < n_chunks; ++u) {
@@ -414,7 +413,6 @@ attn_page_kernel(const PgParams p, const __grid_constant__ CUtensorMap tmap_k,
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
-  grid_dependency_wait();
   timed_out = __any_sync(0xFFFFFFFFu, timed_out);
   if (timed_out) {
     if (lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);

@@ -10,7 +10,9 @@
 //    the head dims) fill the MMA's 16-row M side and the <= 8 query rows the
 //    8-wide N side.  QK^T runs on FP8 tensor cores (m16n8k32 e4m3) with the K
 //    code bytes as the A operand as they sit in shared memory -- no decode --
-//    and Q as two exact e4m3 pieces per element (B operand, registers).  PV runs
+//    and Q as two e4m3 pieces per element (B operand, registers; q = 2^e (p1 +
+//    p2) exactly for elements >= 2^-9 of the row's largest, off by at most
+//    2^-17 of it below that).  PV runs
 //    on f16 tensor cores (m16n8k16) with V codes converted exactly to f16 by
 //    the hardware e4m3x2 conversion and P'' = p * v_scale * 2^-E <= 1 (E a
 //    running power-of-two bound on the value scales) moved from the S^T
@@ -97,11 +99,11 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int part = blockIdx.y;
   const int r = blockIdx.z;
 
-  // Everything before the first cache read (context length, block table,
-  // query pieces) runs while the previous kernel of the stream -- the
-  // quantize-scatter that writes the cache -- may still be running: none of it
-  // reads what that kernel writes.
+  // The launch overlaps the previous kernel's drain; every global access
+  // (context lengths, block tables, queries, the cache, the outputs) comes
+  // after the wait, so whatever a previous kernel wrote is visible.
   allow_dependents_launch();
+  grid_dependency_wait();
   int L = p.context_lens[r];
   if (L < 0 || L > p.ctx_limit) {
     if (part == 0 && tid == 0 && h == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
@@ -222,7 +224,6 @@ attn_skinny_kernel(const SkParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
     cp_async_commit();
   };
-  grid_dependency_wait();     // the cache (codes and scales) from here on
 #pragma unroll
   for (int u = 0; u < kSkStages; ++u) issue(u);
 

@@ -6,7 +6,8 @@
 // PR #2655 "fix(qwen4-exp): register the QSA FP8 scale planes for KV offload",
 // PR description, K/V bullet: per-token key scale on the score after the code
 // dot, per-token value scale on the probability ahead of PV; transposed tiles S^T = K Q^T on FP8
-// tensor cores with Q as two exact e4m3 pieces, O^T = V^T P^T on f16 tensor
+// tensor cores with Q as two e4m3 pieces (exact for elements >= 2^-9 of the row's
+// largest, off by <= 2^-17 of it below), O^T = V^T P^T on f16 tensor
 // cores) and the page-major loads of kvq_attention_page.cu (one TMA box of 16
 // slots x 4 KV heads per K and V chunk, 4-head scale boxes, a producer warp and
 // a 3-deep ring), with the work split by tokens instead of fixed partitions:
@@ -160,11 +161,12 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   volatile int *abort_s = reinterpret_cast<volatile int *>(smem + kOffStAbort);
   float *row_exp = reinterpret_cast<float *>(smem + kOffStRowExp);
 
-  // Everything before the first cache read and the first global write
-  // (context lengths, block tables, query pieces) runs while the previous
-  // kernel of the stream -- the quantize-scatter that writes the cache -- may
-  // still be running: none of it reads what that kernel writes.
+  // The launch overlaps the previous kernel's drain; every global access
+  // (context lengths, block tables, queries, the cache, the workspace, the
+  // outputs) comes after the wait, so whatever a previous kernel wrote is
+  // visible and whatever it still reads is not overwritten.
   allow_dependents_launch();
+  grid_dependency_wait();
   const int N = p.N;
   if (warp == 0) {
     // positions per request (its chunks plus the segment charge) and their
@@ -208,7 +210,6 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int64_t x_begin = static_cast<int64_t>(blockIdx.x) * B;
   const int64_t x_end = total < x_begin + B ? total : x_begin + B;
   if (blockIdx.x == 0) {
-    grid_dependency_wait();            // the plan's previous reader has finished
     if (tid == 0) {
       p.plan[0] = static_cast<int32_t>(B);
       p.plan[1] = N;
@@ -222,8 +223,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
     uint32_t u = 0;                    // chunks issued (lane 0's count)
     bool bad = false, stop = false;
     // a segment's block ids into one of two shared-memory buffers (all lanes,
-    // cp.async): the first segment's before the dependency wait (the tables
-    // are not written by the previous kernel), each next one's while the
+    // cp.async): the first segment's up front, each next one's while the
     // current segment is issued, so a segment change costs no memory round
     // trip in the issue loop
     auto stage_ids = [&](const Segment &sg, int buf) {
@@ -235,7 +235,6 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       cp_async_commit();
     };
     stage_ids(locate(pre, N, hg, x_begin, x_end), 0);
-    grid_dependency_wait();
     int buf = 0;
     for (int64_t x = x_begin; x < x_end && !stop; buf ^= 1) {
       const Segment sg = locate(pre, N, hg, x, x_end);
@@ -558,7 +557,6 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
     if (timed_out) break;
 
     // ---- the segment's (max, denominator, O) for this head's rows
-    grid_dependency_wait();            // before the first global write
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float l = l_run[e];
@@ -618,7 +616,7 @@ attn_combine_stream_kernel(const StCombineParams p) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kStCombineRows + (threadIdx.x >> 5);
   allow_dependents_launch();
   if (row >= p.rows_total) return;
-  grid_dependency_wait();              // the plan and the partials
+  grid_dependency_wait();              // the plan and the partials (any global read)
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
   const int qh = static_cast<int>(row % p.Hq);
   const int g = (qh / p.G) / kStHeads;

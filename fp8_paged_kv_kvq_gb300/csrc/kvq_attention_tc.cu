@@ -13,8 +13,9 @@
 //    rows) and one of each scale plane.
 //  * Warp 13 (one lane) issues the MMAs.  S^T = K Q^T is one M=128 (tokens) x
 //    N=64 x K=128 product on e4m3 operands (kind::f8f6f4): the K code tile
-//    straight from shared memory as A (K-major), and as B the two exact e4m3
-//    pieces of Q stacked as 64 rows (piece 1 of the 32 rows, then piece 2), so
+//    straight from shared memory as A (K-major), and as B the two e4m3 pieces
+//    of Q (exact for elements >= 2^-9 of the row's largest, off by at most
+//    2^-17 of it below) stacked as 64 rows (piece 1 of the 32 rows, then piece 2), so
 //    each K step is one instruction; the softmax adds the two column halves.
 //    (A tcgen05 MMA costs about the same for N = 32 as for N = 128.)  O^T += V^T P^T is M=128 (dims) x N=32 x K=128
 //    (tokens) on f16 operands (kind::f16), both MN-major from shared memory,
@@ -27,11 +28,11 @@
 //    exceeds the running power-of-two bound 2^E).  The rows that moved are
 //    agreed CTA-wide behind one named barrier, and only they are reduced.  A change rescales the running
 //    denominators in registers and moves the PV accumulation on to a fresh
-//    TMEM buffer (14 of them; the epilogue merges the buffers with the ratios
+//    TMEM buffer (12 of them; the epilogue merges the buffers with the ratios
 //    of their references), so it never waits for the tensor cores; only
-//    after the 14th change does a change rescale the live buffer in place.
+//    after the 12th change does a change rescale the live buffer in place.
 //    They write P''^T =
-//    p * v_scale * 2^-E (f16, <= 256) in the MMA's canonical swizzled layout,
+//    p * v_scale * 2^-E (f16, <= 2^14) in the MMA's canonical swizzled layout,
 //    and at the end each thread reads one dim of O^T back from TMEM.
 //  * Warps 8-11 own one token each and convert its V codes exactly to f16 (the
 //    V^T operand, also in its canonical layout) while the softmax runs.

@@ -131,7 +131,10 @@ index_scores_kernel(const ScParams p) {
   const int64_t x_end = (blockIdx.x + 1) * p.total / gridDim.x;
   const int n_units = static_cast<int>(x_end - x_begin);
 
+  // The launch overlaps the previous kernel's drain; every global access comes
+  // after the wait, so whatever a previous kernel wrote is visible.
   allow_dependents_launch();
+  grid_dependency_wait();
   if (tid == 0) {
     for (int s = 0; s < kScStages; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
@@ -164,7 +167,6 @@ index_scores_kernel(const ScParams p) {
     int L = sc_context(p, r);
     bool has;
     uint32_t blk = fetch(r, k, L, has);
-    grid_dependency_wait();                          // the keys
     int u = 0;
     for (; u < n_units; ++u) {
       // the next chunk's block id is read before this chunk's stage frees up
@@ -302,7 +304,6 @@ index_scores_kernel(const ScParams p) {
 
   int r = r_begin, k = k_begin, cur_r = r_begin;
   setup(r_begin);
-  grid_dependency_wait();                            // the previous kernel's writes to out
   for (int u = 0; u < n_units; ++u) {
     if (r != cur_r) {
       setup(r);

@@ -13,8 +13,10 @@ namespace kvq {
 
 // Launches `kernel` with programmatic stream serialization, so that its launch
 // overlaps the drain of the previous kernel in the stream; every kernel
-// launched this way calls grid_dependency_wait() before its first read of
-// global memory another kernel may have written.
+// launched this way calls grid_dependency_wait() before its first access to
+// global memory (read or write), so it sees everything earlier work on the
+// stream wrote -- also when that work let its dependents launch early -- and
+// overwrites nothing that work still reads.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args &&...args) {

@@ -36,6 +36,16 @@
  *    allocates, never synchronises and never reads device data on the host, so
  *    each call is asynchronous on `stream` and can be captured in a CUDA graph.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - Ordering on the stream.  Every kernel of the library is launched with
+ *    programmatic stream serialization, so it may start while the previous
+ *    kernel on `stream` is still draining; before its first access to global
+ *    memory (inputs, cache, workspace, outputs, err_flags) each kernel waits
+ *    until that kernel has completed and its writes are visible
+ *    (griddepcontrol.wait).  Only the launch and the shared-memory set-up
+ *    overlap.  Inputs written by earlier work on the stream -- also by a
+ *    kernel of the caller's that lets its dependents launch early -- are
+ *    therefore read after that work has finished; no extra synchronisation is
+ *    needed.
  *  - Arguments are validated on the host before anything is launched; a
  *    violation returns a status and launches nothing.  A launch failure returns
  *    KVQ_ERR_CUDA.  Unsupported shapes are refused, never silently handled by

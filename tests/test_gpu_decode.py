@@ -1,7 +1,8 @@
 """kvq_paged_decode on the GPU against the fp64 oracle (the oracle quantises
 the same seeded bf16 rows itself): decode and multi-row verify shapes,
 single-partition and split-K paths, ragged tails, edge cases, and the large
-workloads at full size on sampled outputs."""
+workloads at full size on every output (verify: every request of one KV
+head)."""
 import numpy as np
 import pytest
 import torch
@@ -222,10 +223,16 @@ def test_graph_capture_of_decode():
     assert_attention_close(out, ref, "graph replay")
 
 
-def _full_size(name, sample_requests, heads):
+def _full_size(name, one_head=None):
     """The named workload at full size, in the configuration the benchmark
-    times (default partition size), checked on sampled (request, KV head)
-    units: the oracle quantises those requests' rows for that KV head itself."""
+    times (default partition size, hence the same kernels and split), checked
+    against the oracle on every (request, KV head) unit -- or, with `one_head`,
+    on every request for that KV head.  The oracle quantises each unit's bf16
+    rows itself (codes and both scale planes compared bit for bit) and computes
+    its attention in fp64; the units run on all host cores (the oracle's C
+    calls release the GIL)."""
+    import concurrent.futures
+    import os
     w = workloads.WORKLOADS[name]
     lens = workloads.context_lengths(w)
     bt, nblk = workloads.block_tables(lens, w.block_size, w.seed)
@@ -246,42 +253,76 @@ def _full_size(name, sample_requests, heads):
                            int(lens.max()), w.sm_scale, rows_per_request=R, err_flags=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    out_h = out.cpu()
-    for r, h in zip(sample_requests, heads):
+    out_h = out.float().cpu().numpy().astype(np.float64)
+    q_h = workloads.bf16_bits(q.cpu())
+    heads = list(range(H)) if one_head is None else [one_head]
+
+    def unit(r, h, kb, vb, got_codes, got_scales):
+        """Oracle side of one (request, KV head): its own one-head cache."""
         L = int(lens[r])
         slots = workloads.token_slots(bt, r, L, w.block_size)
-        oc = oracle.empty_cache(S, 1, D)          # the oracle's own cache, KV head h only
-        kall, vall = [], []
-        for c0 in range(0, L, ct):
-            n = min(ct, L - c0)
-            k, v = workloads.request_kv(w, r, c0, n, device="cuda")
-            kall.append(workloads.bf16_bits(k[:, h:h + 1]))
-            vall.append(workloads.bf16_bits(v[:, h:h + 1]))
-        kb = np.concatenate(kall).reshape(-1)
-        vb = np.concatenate(vall).reshape(-1)
+        oc = oracle.empty_cache(S, 1, D)
         oracle.quantize_scatter(kb, D, vb, D, L, 1, D, slots, oc)
-        sl = torch.from_numpy(slots).cuda()
-        assert np.array_equal(cache.k_codes[sl, h].cpu().numpy(), oc["k_codes"][slots, 0])
-        assert np.array_equal(cache.v_codes[sl, h].cpu().numpy(), oc["v_codes"][slots, 0])
-        assert np.array_equal(cache.v_scales[sl, h].cpu().numpy().view(np.uint32),
-                              oc["v_scales"][slots, 0].view(np.uint32))
-        qh = workloads.bf16_bits(q[r * R:(r + 1) * R, h * G:(h + 1) * G].cpu())
-        ref, _ = oracle.paged_attention(oc, qh, 1, R, G, bt[r:r + 1], lens[r:r + 1],
+        for nm in ("k_codes", "v_codes"):
+            assert np.array_equal(got_codes[nm], oc[nm][slots, 0]), f"{name} r={r} h={h} {nm}"
+        for nm in ("k_scales", "v_scales"):
+            assert np.array_equal(got_scales[nm].view(np.uint32),
+                                  oc[nm][slots, 0].view(np.uint32)), f"{name} r={r} h={h} {nm}"
+        qh = np.ascontiguousarray(q_h[r * R:(r + 1) * R, h * G:(h + 1) * G])
+        ref, e = oracle.paged_attention(oc, qh, 1, R, G, bt[r:r + 1], lens[r:r + 1],
                                         w.block_size, w.sm_scale)
-        gpu = out_h[r * R:(r + 1) * R, h * G:(h + 1) * G]
-        assert_attention_close(gpu, ref, f"{name} r={r} h={h}")
+        assert e == 0
+        return r, h, ref
+
+    workers = max(1, len(os.sched_getaffinity(0)))
+    gpu_all, ref_all, pending = [], [], []
+
+    def collect(fut):
+        r, h, ref = fut.result()
+        gpu_all.append(out_h[r * R:(r + 1) * R, h * G:(h + 1) * G].reshape(-1))
+        ref_all.append(ref.reshape(-1))
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        for r in range(w.num_requests):
+            L = int(lens[r])
+            sl = torch.from_numpy(workloads.token_slots(bt, r, L, w.block_size)).cuda()
+            for h in heads:
+                # the unit's rows, redrawn on the device chunk by chunk (one
+                # head at a time keeps the host memory in flight small)
+                kparts, vparts = [], []
+                for c0 in range(0, L, ct):
+                    n = min(ct, L - c0)
+                    k, v = workloads.request_kv(w, r, c0, n, device="cuda")
+                    kparts.append(workloads.bf16_bits(k[:, h]))
+                    vparts.append(workloads.bf16_bits(v[:, h]))
+                got_codes = {"k_codes": cache.k_codes[sl, h].cpu().numpy(),
+                             "v_codes": cache.v_codes[sl, h].cpu().numpy()}
+                got_scales = {"k_scales": cache.k_scales[sl, h].cpu().numpy(),
+                              "v_scales": cache.v_scales[sl, h].cpu().numpy()}
+                kb = np.concatenate(kparts).reshape(-1)
+                vb = np.concatenate(vparts).reshape(-1)
+                pending.append(ex.submit(unit, r, h, kb, vb, got_codes, got_scales))
+                while len(pending) >= 2 * workers:      # bound the host memory in flight
+                    collect(pending.pop(0))
+        while pending:
+            collect(pending.pop(0))
+    n_units = len(ref_all)
+    assert n_units == w.num_requests * len(heads)
+    assert_attention_close(np.concatenate(gpu_all), np.concatenate(ref_all),
+                           f"{name} full size, {n_units} (request, KV head) units, "
+                           f"{workers} host threads")
 
 
 def test_decode_batch_full_size():
-    _full_size("decode", [0, 17, 31], [0, 5, 7])
+    _full_size("decode")
 
 
 def test_verify_full_size():
-    _full_size("verify", [0, 63], [3, 7])
+    _full_size("verify", one_head=5)
 
 
 def test_long_context_full_size():
-    _full_size("longctx", [1], [6])
+    _full_size("longctx")
 
 
 def _constructed_cache(L, bs, k_code_fn, v_code_fn, ks_fn, vs_fn):
@@ -346,3 +387,77 @@ def test_scores_with_extreme_key_scales():
     out = gpu_decode(built, q, 1, 1.0 / np.sqrt(128))
     ref, _ = oracle_decode(built, q, 1, 1, 1.0 / np.sqrt(128))
     assert_attention_close(out, ref, "extreme key scales")
+
+
+def _split_case(tiny: bool, R: int, G: int, H: int = 4, L: int = 96, bs: int = 16, seed=0):
+    """Query rows whose element 0 is the row maximum 1.0 and whose other 127
+    elements are bf16 values of 8 significant bits and random sign, either in
+    [2^-16, 2^-10) (below the split's exactness threshold amax * 2^-9) or in
+    [2^-9, 2^-1) (above it).  Every cached key holds, in dims 1..127, the code
+    of 448 with the sign of the query element in even tokens and the opposite
+    sign in odd tokens, so the scores come from those elements alone: s_even =
+    +s, s_odd = -s, s near 0.5.  Values are +1 (even tokens) and -1 (odd).  The
+    attention output is then a convex mix of +-1 whose derivative with respect
+    to any score is at most 2 in magnitude."""
+    rng = np.random.default_rng(seed)
+    D = 128
+    Hq = G * H
+    mant = rng.integers(128, 256, size=(R * Hq, D - 1)).astype(np.float64) / 128.0
+    ex = rng.integers(-16, -10, size=(R * Hq, D - 1)) if tiny else \
+        rng.integers(-9, -1, size=(R * Hq, D - 1))
+    sign = np.where(rng.random((R * Hq, D - 1)) < 0.5, -1.0, 1.0)
+    qv = np.concatenate([np.ones((R * Hq, 1)), sign * mant * np.exp2(ex)], axis=1)
+    q = torch.from_numpy(qv).to(torch.bfloat16).reshape(R, Hq, D)
+    assert torch.equal(q.double(), torch.from_numpy(qv).reshape(R, Hq, D))   # exact in bf16
+    # one KV head's query rows must agree on the key sign pattern: use the
+    # pattern of the head's first row for every row of the head (the other
+    # rows' scores are then smaller, never larger)
+    lens = np.array([L], dtype=np.int32)
+    bt, nblk = workloads.block_tables(lens, bs, 321, spare_blocks=2)
+    S = nblk * bs
+    oc = oracle.empty_cache(S, H, D)
+    slots = workloads.token_slots(bt, 0, L, bs)
+    c448 = 0x7E
+    for h in range(H):
+        sg = np.sign(qv[h * G, 1:])
+        for j in range(L):
+            pos = (sg > 0) if j % 2 == 0 else (sg < 0)
+            oc["k_codes"][slots[j], h, 1:] = np.where(pos, c448, c448 | 0x80)
+            oc["k_codes"][slots[j], h, 0] = 0
+            oc["v_codes"][slots[j], h, :] = 0x38 if j % 2 == 0 else 0xB8   # +-1.0
+    sm = 1.0 / np.sqrt(128.0)
+    sum_abs = np.abs(qv[:, 1:]).sum(axis=1).max() * 448.0
+    ks = np.float32(0.5 / (sm * sum_abs))
+    oc["k_scales"][slots, :] = ks
+    oc["v_scales"][slots, :] = np.float32(1.0)
+    cache = kvq.Cache(*(torch.from_numpy(oc[n]).cuda() for n in
+                        ("k_codes", "v_codes", "k_scales", "v_scales")), bs)
+    built = {"cache": cache, "ocache": oc, "bt": bt, "lens": lens, "S": S}
+    # the split's bound: an element below amax 2^-9 carries an absolute error
+    # of at most 2^-10 2^e = 2^-17 (amax = 1, 2^e = 2^-7), so a score moves by
+    # at most sm * ks * 127 * 448 * 2^-17
+    ds = sm * float(ks) * 127 * 448 * 2.0 ** -17
+    return built, q, sm, ds
+
+
+@pytest.mark.parametrize("R,G", [(1, 4), (4, 8)])
+def test_query_split_error_bound(R, G):
+    """The two-piece e4m3 query split q = 2^e (p1 + p2): exact for every element
+    of magnitude >= amax * 2^-9, and off by at most 2^-10 * 2^e (amax * 2^-17
+    here) for smaller ones.  Scores built only from such elements move the
+    output by at most twice the score error (plus f16-P and bf16 rounding);
+    scores built from elements above the threshold are exact."""
+    H = 4
+    for tiny in (False, True):
+        built, q, sm, ds = _split_case(tiny, R, G, H)
+        out = gpu_decode(built, q, R, sm)
+        ref, e = oracle_decode(built, q, R, G * H, sm)
+        assert e == 0
+        g = out.float().cpu().numpy().astype(np.float64)
+        err = np.abs(g - ref)
+        rounding = 2.0 ** -9 * np.abs(ref) + 2.0 ** -10
+        bound = rounding + (2.0 * ds if tiny else 0.0)
+        worst = float((err / bound).max())
+        print(f"split R={R} G={G} tiny={tiny}: worst err / bound {worst:.3f}, "
+              f"max err {err.max():.3e}, score bound {ds:.3e}")
+        assert worst <= 1.0, (tiny, worst)

@@ -2,7 +2,10 @@
 allocate device memory (it uses a fixed scratch array inside the library
 instead of a caller workspace).  Called through the C ABI and checked against
 kvq_paged_decode on the same inputs, twice in a row, with shapes that need the
-split-K scratch; plus the refusal of a shape larger than the array.
+split-K scratch; with the default partition choice (the load-balanced kernel,
+which keeps its plan and piece slots in the array) against the oracle, twice
+in a row with different lengths; plus the refusal of a shape larger than the
+array.
 
 This file is collected last so that a run stopping at its first failure has
 already run every other test; it builds its own inputs and passes alone."""
@@ -15,7 +18,8 @@ import torch
 import fp8_paged_kv_kvq_gb300 as kvq
 import workloads
 from fp8_paged_kv_kvq_gb300 import build as kbuild
-from kvq_testlib import attention_errors, MAX_ABS, REL_L2, build_paged
+from kvq_testlib import (REL_L2, assert_attention_close, attention_errors, build_paged,
+                         oracle_decode)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +65,39 @@ def test_noalloc_decode_matches_the_workspace_decode_twice_in_a_row():
         ref = kvq.paged_decode(cache, q, bt, cl, 3000, w.sm_scale, partition_tokens=P)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
-        mx, rel, _ = attention_errors(out, ref.float().cpu().numpy().astype(np.float64))
-        assert mx <= MAX_ABS and rel <= REL_L2, (call, mx, rel)
+        mx, rel, _, _ = attention_errors(out, ref.float().cpu().numpy().astype(np.float64))
+        assert mx <= 1.0 and rel <= REL_L2, (call, mx, rel)
+
+
+def test_noalloc_default_partition_against_the_oracle():
+    """partition_tokens = 0 on a small decode batch: the library picks its
+    load-balanced kernel, which keeps its plan and its piece slots in the
+    scratch array.  Two calls in a row with different context lengths (and a
+    different number of pieces per request) are checked against the oracle, so
+    nothing the first call left in the array leaks into the second."""
+    fn = _noalloc_fn()
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=5)
+    lens = np.array([4096, 300, 1, 2000, 777], dtype=np.int32)
+    built = build_paged(w, lens, oracle_side=True)
+    cache = built["cache"]
+    bt = torch.from_numpy(built["bt"]).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for call, (seed, ln) in enumerate([(3, lens), (4, np.array([1500, 299, 0, 2000, 20]))]):
+        ln = ln.astype(np.int32)
+        need = kvq.paged_decode_workspace_size(5, 1, w.num_q_heads, w.num_kv_heads, 128,
+                                               w.block_size, 4096, 0)
+        assert 0 < need <= SCRATCH_BYTES
+        g = workloads.generator(seed, 56)
+        q = torch.randn(5, w.num_q_heads, 128, generator=g).to(torch.bfloat16)
+        out = torch.full((5, w.num_q_heads, 128), float("nan"), dtype=torch.bfloat16,
+                         device="cuda")
+        assert _call(fn, cache, q.cuda(), bt, torch.from_numpy(ln).cuda(), 4096, w.sm_scale, 1,
+                     0, out, err) == 0
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        ref, e = oracle_decode(built, q, 1, w.num_q_heads, w.sm_scale, lens=ln)
+        assert e == 0
+        assert_attention_close(out, ref, f"noalloc default partition, call {call}")
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
