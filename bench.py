@@ -292,9 +292,13 @@ class DeviceWorkload:
             w.num_requests, R, w.num_q_heads, H, w.block_size, self.max_ctx)
         self.n_parts = (self.max_ctx + self.P - 1) // self.P
         self.balanced = self.P_arg == 0 and self._balanced_mode()
+        # more than 8 stacked rows per KV head, partition left to the library:
+        # the rows-on-M tensor-core kernel, which merges its pieces itself
+        self.rows_kernel = (self.P_arg == 0 and R * w.group > 8 and w.block_size >= 16
+                            and H % 4 == 0 and w.num_requests <= 1024)
         need = kvq.paged_decode_workspace_size(w.num_requests, R, w.num_q_heads, H, D,
                                                w.block_size, self.max_ctx, self.P_arg)
-        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
         self.out = torch.empty_like(self.q)
         torch.cuda.synchronize(device)
         assert int(self.err.item()) == 0, "setup store reported an error"
@@ -377,6 +381,8 @@ class DeviceWorkload:
         if self.balanced:
             return "attn_stream_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_stream.cu"
         rows = w.rows_per_request * w.group
+        if self.rows_kernel:
+            return "attn_rows_kernel", "fp8_paged_kv_kvq_gb300/csrc/kvq_attention_rows.cu"
         page_ctas = (w.num_kv_heads // 4) * self.n_parts * w.num_requests
         sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         if (rows <= 8 and w.block_size >= 16 and w.num_kv_heads % 4 == 0
@@ -414,6 +420,8 @@ class DeviceWorkload:
     def launches_per_step(self):
         if self.name == "store":
             return self.layers
+        if self.rows_kernel:
+            return 2
         return 2 + (1 if self.n_parts > 1 else 0)
 
     # algorithmic bytes: attention = codes + scales + q + out + block tables +
@@ -607,6 +615,10 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         if wl.balanced:
             res["config"]["split"] = ("load-balanced: the batch's 16-token chunks split evenly "
                                       "over a persistent grid (3 CTAs per SM)")
+        elif wl.rows_kernel:
+            res["config"]["split"] = ("load-balanced: the batch's 128-token chunks split evenly "
+                                      "over a persistent grid (1 CTA per SM), cut units merged "
+                                      "in the same launch")
         else:
             res["config"]["partition_tokens"] = wl.P
             res["config"]["partitions"] = wl.n_parts

@@ -3,6 +3,7 @@
 // allocates, synchronises or reads device memory.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -111,7 +112,13 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
     return KVQ_ERR_INVALID_ARGUMENT;
   const int32_t G = num_q_heads / cache->num_kv_heads;
   const int64_t M = static_cast<int64_t>(rows_per_request) * G;
-  if (M > kMaxRowsPerKvHead) return KVQ_ERR_UNSUPPORTED;
+  // more than 8 stacked rows per KV head with the partition size left to the
+  // library: the rows-on-M tensor-core kernel (no partitions, up to
+  // kRowsMaxRows rows: verify and chunked prefill)
+  const bool rows_path = partition_tokens == 0 && M > 8 && M <= kvq::kRowsMaxRows &&
+                         cache->block_size >= 16 && cache->num_kv_heads % 4 == 0 &&
+                         num_requests <= kvq::kRowsMaxRequests;
+  if (M > kMaxRowsPerKvHead && !rows_path) return KVQ_ERR_UNSUPPORTED;
   if (num_requests > 65535) return KVQ_ERR_UNSUPPORTED;
   s->num_requests = num_requests;
   s->rows_per_request = rows_per_request;
@@ -134,6 +141,12 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
   s->log2_block = log2_exact(cache->block_size);
   s->sms = current_sm_count();
   s->stream = 0;
+  s->num_kv_heads = cache->num_kv_heads;
+  s->rows_kernel = rows_path ? 1 : 0;
+  if (rows_path) {
+    s->num_partitions = 1;
+    return KVQ_OK;
+  }
   // With the partition size left to the library, batches of <= 8 stacked rows
   // whose page-major partition grid would be small (under ~3 waves) go to the
   // load-balanced kernel, which splits the batch's tokens evenly over a
@@ -163,6 +176,7 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
 }
 
 size_t workspace_for(const kvq::AttnShape &s) {
+  if (s.rows_kernel) return kvq::attn_rows_workspace_bytes(s, s.num_kv_heads);
   const int64_t rows_total =
       static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
   if (s.stream)
@@ -261,6 +275,15 @@ kvq_status kvq_paged_decode_partials(const kvq_cache *cache, const void *q, int3
   const size_t need = workspace_for(s);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need))
     return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  // the rows-on-M kernel loads the scale planes by TMA (16-byte aligned) and
+  // numbers slots in 32 bits; other caches of <= 128 stacked rows run the
+  // partitioned kernels with one partition per request (no workspace)
+  if (s.rows_kernel && !kvq::attn_rows_supported(*cache, s)) {
+    if (s.rows > kMaxRowsPerKvHead) return KVQ_ERR_UNSUPPORTED;
+    s.rows_kernel = 0;
+    s.partition_tokens = std::max<int32_t>(64, (max_context_len + 63) / 64 * 64);
+    s.num_partitions = 1;
+  }
   return from_cuda(kvq::launch_attn_partials(*cache, s, q, block_tables, context_lens, sm_scale,
                                              out, workspace, err_flags,
                                              reinterpret_cast<cudaStream_t>(stream)));
@@ -276,7 +299,7 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
   kvq_status st = make_shape(cache, num_requests, rows_per_request, num_q_heads,
                              max_blocks_per_req, max_context_len, partition_tokens, &s);
   if (st != KVQ_OK) return st;
-  if (num_requests == 0 || s.num_partitions <= 1) return KVQ_OK;
+  if (num_requests == 0 || s.rows_kernel || s.num_partitions <= 1) return KVQ_OK;
   if (out == nullptr || context_lens == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned(out, 16) || !aligned(context_lens, 4) || !aligned(workspace, 16))
     return KVQ_ERR_MISALIGNED;

@@ -1033,6 +1033,9 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
   p.ml_part = nullptr;
   if (s.num_partitions > 1)
     carve_workspace(workspace, rows_total, s.num_partitions, &p.o_part, &p.ml_part);
+  if (s.rows_kernel)
+    return launch_attn_rows(c, s, q, block_tables, context_lens, sm_scale, out, workspace,
+                            err_flags, stream);
   if (s.stream)
     return launch_attn_partials_stream(c, s, q, block_tables, context_lens, sm_scale, out,
                                        workspace, err_flags, stream);
@@ -1073,6 +1076,7 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
 
 cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,
                                 void *workspace, cudaStream_t stream) {
+  if (s.rows_kernel) return cudaSuccess;       // pieces merged by the partials kernel
   if (s.stream) return launch_attn_combine_stream(s, out, workspace, stream);
   if (s.num_partitions <= 1) return cudaSuccess;
   CombineParams p;

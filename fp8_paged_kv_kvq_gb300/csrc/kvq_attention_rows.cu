@@ -1,0 +1,1027 @@
+// kvq_attention_rows.cu -- paged attention over the FP8 cache for many stacked
+// query rows per KV head (multi-token verify, chunked prefill) on the
+// 5th-generation tensor cores, with the query rows on the MMA's M side.
+//
+// The method is the one of the other attention kernels (ROCm/ATOM PR #2655
+// "fix(qwen4-exp): register the QSA FP8 scale planes for KV offload", PR
+// description, K/V bullet: each token's key scale multiplies its score after
+// the code dot product and its value scale its probability ahead of PV; the
+// verify rows of a request that share a KV head are stacked so its codes are
+// read once per verify).  sgl-project/sglang-jax #1776 "feat(dsa): implement
+// fp8 KV cache (e4m3) with a bf16 indexer cache", Modifications: a prefill
+// chunk attends causally over the cached blocks, the probabilities are never
+// rounded to fp8.  Laid out for sm_103a:
+//
+//  * A unit of work is (request, KV head, tile of up to 128 stacked rows) over
+//    the tokens its last row sees, in 128-token chunks.  The batch's chunks,
+//    ordered (request, head, tile, chunk) with a small charge per unit start,
+//    are split into equal contiguous ranges over a persistent grid of one CTA
+//    per SM, so every CTA streams the same bytes whatever the lengths.  A
+//    unit cut by a range boundary is finished by the CTA whose piece lands
+//    last (an atomic ticket per unit), which merges the pieces' (max,
+//    denominator, output) from the workspace; no second launch.
+//  * The stacked rows fill the 128 TMEM lanes.  With RC rows per tile (32, 64
+//    or 128) the tile is replicated 128 / RC times on M; copy c takes the
+//    tokens [c RC, c RC + RC) of each chunk, so every softmax thread owns one
+//    (row, token slice) with its own running max, denominator and value bound
+//    -- no cross-thread reduction per chunk -- and the copies' partial results
+//    are merged once per unit in shared memory.
+//  * S = Q K^T: M = 128 rows x N = 128 tokens x K = 128, kind::f8f6f4, A = the
+//    query tile as two e4m3 pieces (q = 2^e (p1 + p2), exact for elements >=
+//    2^-9 of the row's largest, off by at most 2^-17 of it below), the second
+//    piece accumulating onto the first, B = the K code tile straight from the
+//    TMA ring (K-major, 128-byte swizzle).  O += P V: M = 128 x N = 128 dims x
+//    K = 128 tokens, kind::f16, A = P'' = p v_scale 2^-E read from TMEM (the
+//    softmax writes it there as f16), B = the V codes converted exactly to f16
+//    (MN-major, 128-byte swizzle) by four converter warps.
+//  * Warp roles (320 threads): 0-3 softmax (TMEM lane quarters 0-3), 4-7 V
+//    conversion, 8 TMA (block ids fetched ahead by cp.async, one 3-D box per
+//    page and plane, one 2-D box of 4 heads' scales per page and plane), 9 MMA
+//    (one lane).  TMEM: two S buffers, O, two P buffers (512 columns).
+//  * Every wait is bounded; a role that gives up raises a shared abort flag,
+//    the softmax warps agree on it at their barriers, copies and MMAs in
+//    flight complete, the CTA frees its tensor memory (KVQ_ERRF_WAIT_TIMEOUT).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kRwTok = 128;                  // tokens per chunk
+constexpr int kRwStages = 3;                 // code ring depth
+constexpr int kRwSoftWarps = 4;
+constexpr int kRwConvWarps = 4;
+constexpr int kRwWarpTma = kRwSoftWarps + kRwConvWarps;
+constexpr int kRwWarpMma = kRwWarpTma + 1;
+constexpr int kRwThreads = (kRwWarpMma + 1) * 32;
+constexpr int kRwIdAhead = 4;                // chunks whose block ids are in flight
+constexpr int kRwMaxPagesPerChunk = 8;       // block size >= 16
+constexpr float kRwLazy = 14.0f;             // log2 of the largest unnormalised p
+constexpr float kRwOvershoot = 4.0f;         // a moved reference sits this far above the max
+
+constexpr uint32_t kColS = 0;                // S buffer b: columns 128 b .. 128 b + 127
+constexpr uint32_t kColO = 256;              // O: 256 .. 383
+constexpr uint32_t kColP = 384;              // P buffer b (f16 pairs): 384 + 64 b .. + 63
+constexpr uint32_t kRwTmemCols = 512;
+
+// shared memory, offsets from a 1024-byte aligned base
+constexpr int kCodeBytes = kRwTok * kHeadDim;                 // one plane of a chunk
+constexpr int kStageBytes = 2 * kCodeBytes;                   // K codes | V codes
+constexpr int kScBytes = kRwTok * 16;                         // [token][4 heads] fp32
+constexpr int kVfBytes = kRwTok * kHeadDim * 2;               // f16 V operand
+constexpr int kQBytes = 128 * kHeadDim;                       // one e4m3 piece, 128 rows
+constexpr int kOffSc = kRwStages * kStageBytes;
+constexpr int kOffVf = kOffSc + kRwStages * 2 * kScBytes;
+constexpr int kOffQ = kOffVf + 2 * kVfBytes;                  // also the merge scratch
+constexpr int kOffTs = kOffQ + 2 * kQBytes;                   // [warp][K | V][128] fp32
+constexpr int kOffIds = kOffTs + kRwSoftWarps * 2 * kRwTok * 4;
+constexpr int kOffRowf = kOffIds + (kRwIdAhead + 1) * kRwMaxPagesPerChunk * 4;
+constexpr int kOffMl = kOffRowf + 128 * 4;                    // [128 lanes] (m, l, E, -)
+constexpr int kOffPre = kOffMl + 128 * 16;
+constexpr int kOffBar = kOffPre + (kRowsMaxRequests + 4) * 4;
+constexpr int kBarKvFull = 0;
+constexpr int kBarKvEmpty = kBarKvFull + kRwStages;
+constexpr int kBarSFull = kBarKvEmpty + kRwStages;
+constexpr int kBarSFree = kBarSFull + 2;
+constexpr int kBarPReady = kBarSFree + 2;
+constexpr int kBarVfReady = kBarPReady + 2;
+constexpr int kBarPvDone = kBarVfReady + 2;
+constexpr int kBarQReady = kBarPvDone + 2;
+constexpr int kBarOFree = kBarQReady + 1;
+constexpr int kNumBars = kBarOFree + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort, ticket
+constexpr int kRwSmem = kOffMisc + 64 + 1024;
+
+static_assert(kOffSc % 1024 == 0 && kOffVf % 1024 == 0 && kOffQ % 1024 == 0,
+              "operand buffers need 1024-byte alignment");
+static_assert(kOffBar % 8 == 0, "barrier alignment");
+static_assert(kRwSmem <= 227 * 1024, "shared memory budget");
+
+// S = Q K^T: M = 128 rows, N = 128 tokens, both operands K-major
+constexpr uint32_t kIdescQK = mma_idesc(128, kRwTok, false, false);
+// O = P V: M = 128 rows, N = 128 dims, A (TMEM) K-major, B MN-major
+constexpr uint32_t kIdescPV = mma_idesc(128, kHeadDim, false, true);
+
+struct RwParams {
+  uint32_t num_blocks;       // < 2^31
+  int32_t H;
+  int32_t log2_bs;
+  int32_t box;               // rows of a TMA box: min(block size, 128)
+  const uint16_t *q;
+  uint16_t *out;
+  const int32_t *block_tables;
+  int32_t max_blocks;
+  const int32_t *context_lens;
+  int32_t ctx_limit;
+  int32_t N, R, Hq, G, M;
+  int32_t T;                 // row tiles per (request, KV head)
+  float qk_scale;            // sm_scale * log2(e)
+  float *o_part;             // [grid][2][rows per tile][128]
+  float2 *ml_part;           // [grid][2][rows per tile]
+  int32_t *tickets;          // [N * H * T], zero between calls
+  int32_t *err_flags;
+};
+
+__device__ __forceinline__ float rw_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Bounded wait that also gives up once another role raised the abort flag.
+__device__ __forceinline__ bool rw_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  for (int i = 0; i < (1 << 19); ++i) {
+    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+    if ((i & 15) == 15 && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+// Barrier over the softmax warps that also ORs a flag across them.
+__device__ __forceinline__ bool soft_barrier_or(bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r) : "r"(flag ? 1u : 0u), "n"(kRwSoftWarps * 32) : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void soft_barrier() { named_barrier(1, kRwSoftWarps * 32); }
+
+// Smallest e in [-126, 126] with 2^e >= v (v >= 0 given as its bits).
+__device__ __forceinline__ int rw_pow2_ceil(uint32_t bits) {
+  const int ex = static_cast<int>((bits >> 23) & 0xFFu);
+  int e = (ex == 0) ? -126 : ex - 127 + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
+  return e > 126 ? 126 : e;
+}
+
+__device__ __forceinline__ float pow2f(int e) {    // e in [-126, 127]
+  return __int_as_float((127 + e) << 23);
+}
+
+__device__ __forceinline__ float pow2f_down(int d) {   // 2^d for d <= 0, 0 below 2^-126
+  return d < -126 ? 0.0f : pow2f(d);
+}
+
+// ---------------------------------------------------------------------------
+// Work layout.  Unit (r, h, t): the rows [128 t, 128 t + 128) of the stacked
+// rows m = i G + g (query row i, query head h G + g) of request r; it reads the
+// tokens its last row sees.  In the work sequence it spans V = C + kRowsSwitch
+// positions (C its chunks) or none when C = 0; request r's units take
+// W_r = H sum_t V_rt positions from pre[r] on, ordered (h, t).
+
+struct Geo {
+  int32_t R, G, M, T, H, ctx_limit;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int lim) { return L < 0 ? 0 : (L > lim ? lim : L); }
+
+// Tokens the last row of tile t sees, and the tile's chunk count.
+__device__ __forceinline__ int tile_tokens(const Geo &g, int L, int t) {
+  const int m_last = min(g.M, 128 * (t + 1)) - 1;
+  const int v = L - g.R + 1 + m_last / g.G;
+  return v < 0 ? 0 : (v > L ? L : v);
+}
+
+__device__ __forceinline__ int tile_positions(const Geo &g, int L, int t) {
+  const int c = (tile_tokens(g, L, t) + kRwTok - 1) / kRwTok;
+  return c > 0 ? c + kRowsSwitch : 0;
+}
+
+struct Seg {
+  int r, h, t, L;
+  int C, c0, n;          // the unit's chunks, the CTA's first chunk and count
+  int vis;               // tokens the unit reads
+  int64_t first;         // position of the unit's first chunk
+  int64_t next;          // where the CTA's range continues
+};
+
+__device__ __forceinline__ Seg locate_rows(const int32_t *pre, const int32_t *context_lens, const Geo &g, int N,
+                           int64_t x, int64_t x_end) {
+  int lo = 0, hi = N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  Seg s;
+  s.r = lo;
+  s.L = clamp_len(context_lens[lo], g.ctx_limit);
+  int S = 0;
+  for (int t = 0; t < g.T; ++t) S += tile_positions(g, s.L, t);
+  const int64_t off = x - pre[lo];
+  s.h = static_cast<int>(off / S);
+  int rem = static_cast<int>(off - static_cast<int64_t>(s.h) * S);
+  int acc = 0, t = 0;
+  for (; t < g.T - 1; ++t) {
+    const int v = tile_positions(g, s.L, t);
+    if (rem < acc + v) break;
+    acc += v;
+  }
+  s.t = t;
+  s.vis = tile_tokens(g, s.L, t);
+  s.C = (s.vis + kRwTok - 1) / kRwTok;
+  const int64_t start = pre[lo] + static_cast<int64_t>(s.h) * S + acc;
+  s.first = start + kRowsSwitch;
+  const int64_t uend = start + (s.C > 0 ? s.C + kRowsSwitch : 0);
+  const int64_t end = uend < x_end ? uend : x_end;
+  const int64_t xs = x > s.first ? x : s.first;
+  s.next = end > x ? end : x + 1;
+  if (xs >= end) {
+    s.c0 = 0;
+    s.n = 0;
+  } else {
+    s.c0 = static_cast<int>(xs - s.first);
+    s.n = static_cast<int>(end - xs);
+  }
+  return s;
+}
+
+// Walks the chunks of a CTA's range in order.
+struct ChunkWalk {
+  Seg sg;
+  int k;                 // chunk within the segment
+  int seg;               // segment index
+  int64_t x, x_end;
+  bool valid;
+  __device__ __forceinline__ void start(const int32_t *pre, const int32_t *cl, const Geo &g, int N, int64_t xb,
+                        int64_t xe) {
+    x = xb;
+    x_end = xe;
+    seg = -1;
+    valid = false;
+    k = 0;
+    advance_segment(pre, cl, g, N);
+  }
+  __device__ __forceinline__ void advance_segment(const int32_t *pre, const int32_t *cl, const Geo &g, int N) {
+    while (x < x_end) {
+      sg = locate_rows(pre, cl, g, N, x, x_end);
+      x = sg.next;
+      if (sg.n > 0) {
+        ++seg;
+        k = 0;
+        valid = true;
+        return;
+      }
+    }
+    valid = false;
+  }
+  __device__ __forceinline__ void next(const int32_t *pre, const int32_t *cl, const Geo &g, int N) {
+    if (!valid) return;
+    if (++k < sg.n) return;
+    advance_segment(pre, cl, g, N);
+  }
+};
+
+template <int RC>
+__global__ void __launch_bounds__(kRwThreads, 1)
+attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
+                 const __grid_constant__ CUtensorMap tm_vc,
+                 const __grid_constant__ CUtensorMap tm_ks,
+                 const __grid_constant__ CUtensorMap tm_vs) {
+  constexpr int kCopies = 128 / RC;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+
+  int32_t *pre = reinterpret_cast<int32_t *>(smem + kOffPre);
+  const uint32_t bar0 = smem_addr(smem + kOffBar);
+  auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+  volatile int *abort_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+  int *ticket_s = reinterpret_cast<int *>(smem + kOffMisc + 8);
+  float *rowf_s = reinterpret_cast<float *>(smem + kOffRowf);
+
+  // The launch overlaps the previous kernel's drain; every global access comes
+  // after the wait.
+  allow_dependents_launch();
+  grid_dependency_wait();
+
+  const Geo geo{p.R, p.G, p.M, p.T, p.H, p.ctx_limit};
+  const int N = p.N;
+  if (warp == 0) {
+    int carry = 0;
+    for (int r0 = 0; r0 < N; r0 += 32) {
+      const int r = r0 + lane;
+      int W = 0;
+      if (r < N) {
+        int L = p.context_lens[r];
+        if (L < 0 || L > p.ctx_limit) {
+          if (blockIdx.x == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_CONTEXT_RANGE);
+          L = clamp_len(L, p.ctx_limit);
+        }
+        for (int t = 0; t < p.T; ++t) W += tile_positions(geo, L, t);
+        W *= p.H;
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, W, off);
+        if (lane >= off) W += v;
+      }
+      if (r < N) pre[r + 1] = carry + W;
+      carry += __shfl_sync(0xFFFFFFFFu, W, 31);
+    }
+    if (lane == 0) pre[0] = 0;
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kRwStages; ++s) {
+      mbar_init(BAR(kBarKvFull + s), 1);
+      mbar_init(BAR(kBarKvEmpty + s), 1 + kRwConvWarps + kRwSoftWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(kBarSFull + b), 1);
+      mbar_init(BAR(kBarSFree + b), kRwSoftWarps);
+      mbar_init(BAR(kBarPReady + b), kRwSoftWarps);
+      mbar_init(BAR(kBarVfReady + b), kRwConvWarps);
+      mbar_init(BAR(kBarPvDone + b), 1);
+    }
+    mbar_init(BAR(kBarQReady), kRwSoftWarps);
+    mbar_init(BAR(kBarOFree), kRwSoftWarps);
+    *abort_s = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kRwWarpTma) {
+    tmem_alloc(smem_addr(tmem_slot), kRwTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int64_t total = pre[N];
+  const int64_t B = total > 0 ? (total + gridDim.x - 1) / gridDim.x : 1;
+  const int64_t x_begin = static_cast<int64_t>(blockIdx.x) * B;
+  const int64_t x_end = total < x_begin + B ? total : x_begin + B;
+
+  if (warp == kRwWarpTma) {
+    // ---------------------------------------------------------------- TMA
+    // Block ids of chunk u + kRwIdAhead are fetched (lanes < pages, cp.async,
+    // one commit group per chunk) while chunk u is issued.
+    int32_t *ids = reinterpret_cast<int32_t *>(smem + kOffIds);
+    const int npg = p.box < kRwTok ? kRwTok / p.box : 1;
+    ChunkWalk fw, iw;
+    fw.start(pre, p.context_lens, geo, N, x_begin, x_end);
+    iw = fw;
+    auto fetch = [&](const ChunkWalk &w, int slot) {
+      if (w.valid && lane < npg) {
+        const int j = (w.sg.c0 + w.k) * kRwTok + lane * p.box;     // first token of the box
+        const bool need = j < w.sg.vis;
+        const int32_t *src = p.block_tables + static_cast<int64_t>(w.sg.r) * p.max_blocks +
+                             (need ? (j >> p.log2_bs) : 0);
+        cp_async_4(ids + slot * kRwMaxPagesPerChunk + lane, src, need ? 4u : 0u);
+      }
+      cp_async_commit();
+    };
+    for (int a = 0; a < kRwIdAhead; ++a) {
+      fetch(fw, a % (kRwIdAhead + 1));
+      fw.next(pre, p.context_lens, geo, N);
+    }
+    uint32_t u = 0;
+    bool bad = false, stop = false;
+    for (; iw.valid && !stop; ++u) {
+      fetch(fw, (u + kRwIdAhead) % (kRwIdAhead + 1));
+      fw.next(pre, p.context_lens, geo, N);
+      cp_async_wait<kRwIdAhead>();
+      __syncwarp();
+      if (lane == 0) {
+        const int b = u % kRwStages;
+        if (u >= kRwStages && !rw_wait(BAR(kBarKvEmpty + b), ((u / kRwStages) - 1) & 1, abort_s)) {
+          stop = true;
+        } else {
+          const uint32_t kdst = smem_addr(smem + b * kStageBytes);
+          const uint32_t vdst = kdst + kCodeBytes;
+          const uint32_t ksd = smem_addr(smem + kOffSc + b * 2 * kScBytes);
+          const uint32_t vsd = ksd + kScBytes;
+          const uint32_t fb = BAR(kBarKvFull + b);
+          const int32_t *cid = ids + (u % (kRwIdAhead + 1)) * kRwMaxPagesPerChunk;
+          const int j0 = (iw.sg.c0 + iw.k) * kRwTok;
+          const int h = iw.sg.h;
+          uint32_t bytes = 0;
+          for (int i = 0; i < npg; ++i) {
+            const int j = j0 + i * p.box;
+            if (j >= iw.sg.vis) break;
+            const uint32_t blk = static_cast<uint32_t>(cid[i]);
+            if (blk >= p.num_blocks) {
+              bad = true;
+              continue;
+            }
+            const int z = static_cast<int>((blk << p.log2_bs) | (j & ((1 << p.log2_bs) - 1)));
+            tma_load_3d(kdst + i * p.box * kHeadDim, &tm_kc, 0, h, z, fb);
+            tma_load_3d(vdst + i * p.box * kHeadDim, &tm_vc, 0, h, z, fb);
+            tma_load_2d(ksd + i * p.box * 16, &tm_ks, h & ~3, z, fb);
+            tma_load_2d(vsd + i * p.box * 16, &tm_vs, h & ~3, z, fb);
+            bytes += 2u * p.box * kHeadDim + 2u * p.box * 16u;
+          }
+          mbar_arrive_expect_tx(fb, bytes);
+        }
+      }
+      stop = __shfl_sync(0xFFFFFFFFu, stop ? 1 : 0, 0) != 0;
+      iw.next(pre, p.context_lens, geo, N);
+    }
+    cp_async_wait<0>();
+    if (lane == 0) {
+      if (bad && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
+      // copies still in flight (after an abort) land before the CTA leaves
+      const uint32_t issued = stop ? u - 1 : u;
+      for (uint32_t v = (issued > kRwStages ? issued - kRwStages : 0); v < issued; ++v)
+        mbar_wait_sleep_bounded(BAR(kBarKvFull + v % kRwStages), (v / kRwStages) & 1);
+    }
+  } else if (warp == kRwWarpMma) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t q0 = smem_addr(smem + kOffQ);
+      const uint32_t vf0 = smem_addr(smem + kOffVf);
+      uint32_t last_bar = 0, last_par = 0;
+      bool any = false, ok = true;
+      int pend = -1, pend_first = 0, pend_seg = 0;          // the chunk whose PV is due
+      auto issue_pv = [&]() -> bool {
+        const int c = pend, cb = c & 1;
+        if (!rw_wait(BAR(kBarPReady + cb), (c >> 1) & 1, abort_s)) return false;
+        if (!rw_wait(BAR(kBarVfReady + cb), (c >> 1) & 1, abort_s)) return false;
+        if (pend_first && pend_seg >= 1 && !rw_wait(BAR(kBarOFree), (pend_seg - 1) & 1, abort_s))
+          return false;
+        tc_fence_after();
+        const uint64_t bd = smem_desc(vf0 + cb * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
+#pragma unroll
+        for (int kk = 0; kk < kRwTok / 16; ++kk)
+          tc_mma_f16_tmem_a(tmem + kColO, tmem + kColP + 64 * cb + 8 * kk, bd + (2048 >> 4) * kk,
+                            kIdescPV, (pend_first && kk == 0) ? 0u : 1u);
+        tc_commit(BAR(kBarPvDone + cb));
+        last_bar = BAR(kBarPvDone + cb);
+        last_par = (c >> 1) & 1;
+        any = true;
+        pend = -1;
+        return true;
+      };
+      ChunkWalk w;
+      w.start(pre, p.context_lens, geo, N, x_begin, x_end);
+      int s = 0;
+      for (; w.valid && ok; ++s) {
+        const int b = s % kRwStages, sb = s & 1;
+        if (w.k == 0) {
+          // a new unit: its query tile replaces the last one once the
+          // previous unit's final PV is issued (its softmax needs it first)
+          if (pend >= 0 && !issue_pv()) { ok = false; break; }
+          if (!rw_wait(BAR(kBarQReady), w.seg & 1, abort_s)) { ok = false; break; }
+        }
+        if (!rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) { ok = false; break; }
+        if (s >= 2 && !rw_wait(BAR(kBarSFree + sb), ((s >> 1) - 1) & 1, abort_s)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t kd = smem_desc(smem_addr(smem + b * kStageBytes), 16, 1024, kSmemSwizzle128);
+        const uint64_t qa = smem_desc(q0, 16, 1024, kSmemSwizzle128);
+        const uint64_t qb = smem_desc(q0 + kQBytes, 16, 1024, kSmemSwizzle128);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_e4m3(tmem + kColS + 128 * sb, qa + 2 * kk, kd + 2 * kk, kIdescQK, kk != 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_e4m3(tmem + kColS + 128 * sb, qb + 2 * kk, kd + 2 * kk, kIdescQK, 1u);
+        tc_commit(BAR(kBarSFull + sb));
+        tc_commit(BAR(kBarKvEmpty + b));
+        last_bar = BAR(kBarSFull + sb);
+        last_par = (s >> 1) & 1;
+        any = true;
+        if (pend >= 0 && !issue_pv()) { ok = false; break; }
+        pend = s;
+        pend_first = (w.k == 0);
+        pend_seg = w.seg;
+        w.next(pre, p.context_lens, geo, N);
+      }
+      if (ok && pend >= 0) issue_pv();
+      // every MMA issued has completed before the tensor memory is freed
+      if (any) mbar_wait_sleep_bounded(last_bar, last_par);
+    }
+  } else if (warp >= kRwSoftWarps) {
+    // ------------------------------------------------ V codes -> f16 operand
+    // Token t's codes -> f16, MN-major, 128-byte swizzle: dims 64j.. in block j
+    // (16 KiB apart), token t at (t/8)*1024 + (t%8)*128, the chunk of dims
+    // 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's range get zeros: their
+    // stage rows hold stale codes, and a NaN code would poison the product
+    // even at p = 0.
+    const int t = 32 * (warp - kRwSoftWarps) + lane;
+    ChunkWalk w;
+    w.start(pre, p.context_lens, geo, N, x_begin, x_end);
+    for (int s = 0; w.valid; ++s) {
+      const int b = s % kRwStages, vb = s & 1;
+      const bool valid = (w.sg.c0 + w.k) * kRwTok + t < w.sg.vis;
+      bool ok = rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
+      if (s >= 2) ok = rw_wait(BAR(kBarPvDone + vb), ((s >> 1) - 1) & 1, abort_s) && ok;
+      if (__any_sync(0xFFFFFFFFu, !ok)) break;
+      const uint8_t *vrow = smem + b * kStageBytes + kCodeBytes + t * kHeadDim;
+      uint8_t *vf = smem + kOffVf + vb * kVfBytes + (t >> 3) * 1024 + (t & 7) * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) w4 = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (t & 7)) << 4));
+        const uint4 lo = make_uint4(e4m3x2_to_f16x2(w4.x), e4m3x2_to_f16x2(w4.x >> 16),
+                                    e4m3x2_to_f16x2(w4.y), e4m3x2_to_f16x2(w4.y >> 16));
+        const uint4 hi = make_uint4(e4m3x2_to_f16x2(w4.z), e4m3x2_to_f16x2(w4.z >> 16),
+                                    e4m3x2_to_f16x2(w4.w), e4m3x2_to_f16x2(w4.w >> 16));
+        uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
+        const int c0 = (2 * c) & 7;
+        *reinterpret_cast<uint4 *>(blk + ((c0 ^ (t & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(BAR(kBarVfReady + vb));
+        mbar_arrive(BAR(kBarKvEmpty + b));
+      }
+      w.next(pre, p.context_lens, geo, N);
+    }
+  } else {
+    // ----------------------------------------------------------- softmax
+    const int L32 = 32 * warp + lane;           // this thread's TMEM lane
+    const int copy = L32 / RC;                  // its token slice [copy RC, copy RC + RC)
+    const int mrow = L32 % RC;                  // its row within the tile
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    float *ts = reinterpret_cast<float *>(smem + kOffTs) + warp * 2 * kRwTok;
+    float4 *ml_s = reinterpret_cast<float4 *>(smem + kOffMl);
+    bool aborted = false;
+    {
+      // P columns outside this thread's slice stay zero for the whole kernel
+      uint32_t z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+      for (int c = 0; c < 128; c += 16) tmem_st16u(tl + kColP + c, z);
+      tmem_wait_st();
+    }
+    ChunkWalk w;
+    w.start(pre, p.context_lens, geo, N, x_begin, x_end);
+    int s = 0;                                  // chunks consumed
+    while (w.valid) {
+      const Seg sg = w.sg;
+      const int seg = w.seg;
+      const int r = sg.r, h = sg.h;
+      const int row0 = 128 * sg.t;              // the tile's first stacked row
+      const int rows_here = min(p.M - row0, RC);
+      // ---- the unit's query tile: rows m < rows_here of the tile, every copy
+      //      (the previous unit's MMAs reading Q and its merge are finished)
+      constexpr int kQRows = RC / kRwSoftWarps;          // rows per warp, loaded at once
+      uint2 qv[kQRows];
+#pragma unroll
+      for (int i = 0; i < kQRows; ++i) {
+        const int m = warp + kRwSoftWarps * i;
+        qv[i] = make_uint2(0u, 0u);
+        if (m < rows_here) {
+          const int ma = row0 + m, ir = ma / p.G, gq = ma - ir * p.G;
+          qv[i] = *reinterpret_cast<const uint2 *>(
+              p.q + ((static_cast<int64_t>(r) * p.R + ir) * p.Hq + h * p.G + gq) * kHeadDim +
+              4 * lane);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kQRows; ++i) {
+        const int m = warp + kRwSoftWarps * i;
+        const uint2 v = qv[i];
+        float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                           fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+        int e = (ex == 0) ? -126 : ex - 127 - 7;
+        e = e < -126 ? -126 : (e > 126 ? 126 : e);
+        const float rx = (amax == 0.0f) ? 0.0f : pow2f(e);          // 2^e
+        uint32_t c1w = 0u, c2w = 0u;
+        if (rx != 0.0f) {
+          const float inv = pow2f(-e);
+          const float xs[4] = {bf16_lo(v.x) * inv, bf16_hi(v.x) * inv, bf16_lo(v.y) * inv,
+                               bf16_hi(v.y) * inv};
+          e4m3_pieces4(xs, c1w, c2w);
+        }
+        if (lane == 0) rowf_s[m] = rx * p.qk_scale;
+#pragma unroll
+        for (int c = 0; c < kCopies; ++c) {
+          const int row = c * RC + m;
+          const int off = row * kHeadDim + (((lane >> 2) ^ (row & 7)) << 4) + 4 * (lane & 3);
+          *reinterpret_cast<uint32_t *>(smem + kOffQ + off) = c1w;
+          *reinterpret_cast<uint32_t *>(smem + kOffQ + kQBytes + off) = c2w;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(kBarQReady));
+      if (soft_barrier_or(aborted || *abort_s)) {
+        aborted = true;
+        break;
+      }
+      // ---- this thread's row
+      const bool row_ok = mrow < rows_here;
+      const int ma = row0 + mrow;
+      const int vis = row_ok ? min(sg.L, sg.L - p.R + 1 + ma / p.G) : 0;   // tokens it sees
+      const float rowf = rowf_s[mrow];
+      float m_ref = -INFINITY, lsum = 0.0f;
+      int E = -126;
+      bool have_o = false;                      // a PV of this unit has been issued
+      const int s_first = s;
+      for (int k = 0; k < sg.n; ++k, ++s) {
+        const int b = s % kRwStages, sb = s & 1;
+        const int j0 = (sg.c0 + k) * kRwTok + copy * RC;   // this slice's first token
+        bool ok = rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
+        ok = ok && rw_wait(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s);
+        if (__any_sync(0xFFFFFFFFu, !ok)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        // scales of head h for the chunk's 128 tokens, into this warp's buffer
+        {
+          const float *sc = reinterpret_cast<const float *>(smem + kOffSc + b * 2 * kScBytes);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = lane + 32 * i;
+            ts[tk] = sc[4 * tk + (h & 3)];
+            ts[kRwTok + tk] = sc[kRwTok * 4 + 4 * tk + (h & 3)];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));
+        const float4 *ks4 = reinterpret_cast<const float4 *>(ts + copy * RC);
+        const float4 *vs4 = reinterpret_cast<const float4 *>(ts + kRwTok + copy * RC);
+        const int lim = vis - j0;               // tokens jj < lim of the slice are seen
+        const uint32_t scol = tl + kColS + 128 * sb + copy * RC;
+        // One piece of 32 scores: x_j = s_j k_scale_j 2^e sm_scale log2(e), -inf
+        // where the row does not see the token.
+        auto load_piece = [&](int pc, float (&x)[32]) {
+          tmem_ld32(scol + 32 * pc, x);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 k4 = ks4[8 * pc + q4];
+            const int jj = 32 * pc + 4 * q4;
+            x[4 * q4] = (jj < lim) ? x[4 * q4] * (k4.x * rowf) : -INFINITY;
+            x[4 * q4 + 1] = (jj + 1 < lim) ? x[4 * q4 + 1] * (k4.y * rowf) : -INFINITY;
+            x[4 * q4 + 2] = (jj + 2 < lim) ? x[4 * q4 + 2] * (k4.z * rowf) : -INFINITY;
+            x[4 * q4 + 3] = (jj + 3 < lim) ? x[4 * q4 + 3] * (k4.w * rowf) : -INFINITY;
+          }
+        };
+        // P'' = p v_scale 2^-E of one piece (f16 pairs) and its share of the
+        // denominator; flags a score above the reference's headroom or a value
+        // scale above the bound (the piece then has to be redone).
+        uint32_t pk[RC / 2];
+        auto p_piece = [&](int pc, const float (&x)[32], float &lpart) -> bool {
+          const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
+          const float thr = m_ref + kRwLazy;
+          const float vbound = pow2f(E), vnorm = pow2f(-E);
+          bool over = false;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            // scales of unseen tokens may be stale shared memory: weight 0
+            const float4 v4 = vs4[8 * pc + q4];
+            const int jj = 32 * pc + 4 * q4;
+            const float va = (jj < lim) ? v4.x : 0.0f, vb = (jj + 1 < lim) ? v4.y : 0.0f;
+            const float vc = (jj + 2 < lim) ? v4.z : 0.0f, vd = (jj + 3 < lim) ? v4.w : 0.0f;
+            over |= (x[4 * q4] > thr) | (x[4 * q4 + 1] > thr) | (x[4 * q4 + 2] > thr) |
+                    (x[4 * q4 + 3] > thr);
+            over |= (fmaxf(fmaxf(va, vb), fmaxf(vc, vd)) > vbound);
+            const float pa = rw_ex2(x[4 * q4] - ms), pb = rw_ex2(x[4 * q4 + 1] - ms);
+            const float pc2 = rw_ex2(x[4 * q4 + 2] - ms), pd = rw_ex2(x[4 * q4 + 3] - ms);
+            lpart += (pa + pb) + (pc2 + pd);
+            pk[16 * pc + 2 * q4] = pack_f16x2(pa * (va * vnorm), pb * (vb * vnorm));
+            pk[16 * pc + 2 * q4 + 1] = pack_f16x2(pc2 * (vc * vnorm), pd * (vd * vnorm));
+          }
+          return over;
+        };
+        // fast path: every piece under the present references
+        float lchunk = 0.0f;
+        bool over = false;
+#pragma unroll
+        for (int pc = 0; pc < RC / 32; ++pc) {
+          float x[32];
+          load_piece(pc, x);
+          over |= p_piece(pc, x, lchunk);
+        }
+        if (__any_sync(0xFFFFFFFFu, over)) {
+          // ---- slow path (rare): new references for the rows that need them,
+          //      the O rows so far rescaled, the chunk redone
+          float mx = -INFINITY, vmax = 0.0f;
+#pragma unroll
+          for (int pc = 0; pc < RC / 32; ++pc) {
+            float x[32];
+            load_piece(pc, x);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) mx = fmaxf(mx, x[jj]);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 v4 = vs4[8 * pc + q4];
+              const int jj = 32 * pc + 4 * q4;
+              vmax = fmaxf(vmax, fmaxf(fmaxf((jj < lim) ? v4.x : 0.0f, (jj + 1 < lim) ? v4.y : 0.0f),
+                                       fmaxf((jj + 2 < lim) ? v4.z : 0.0f, (jj + 3 < lim) ? v4.w : 0.0f)));
+            }
+          }
+          float f = 1.0f;
+          const float m_new = (mx > m_ref + kRwLazy) ? mx + kRwOvershoot : m_ref;
+          const int e_new = max(E, rw_pow2_ceil(__float_as_uint(vmax)));
+          if (m_ref != -INFINITY) {
+            const float fm = rw_ex2(m_ref - m_new);
+            lsum *= fm;
+            f = fm * pow2f_down(E - e_new);
+          }
+          m_ref = m_new;
+          E = e_new;
+          // the O rows accumulated so far follow the new references
+          if (have_o && __any_sync(0xFFFFFFFFu, f != 1.0f)) {
+            const int sp = s - 1;
+            if (!rw_wait(BAR(kBarPvDone + (sp & 1)), (sp >> 1) & 1, abort_s)) aborted = true;
+            if (__any_sync(0xFFFFFFFFu, aborted)) {
+              aborted = true;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+              float o[32];
+              tmem_ld32(tl + kColO + c, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= f;
+              tmem_st32(tl + kColO + c, o);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          }
+          lchunk = 0.0f;
+#pragma unroll
+          for (int pc = 0; pc < RC / 32; ++pc) {
+            float x[32];
+            load_piece(pc, x);
+            p_piece(pc, x, lchunk);
+          }
+        }
+        lsum += lchunk;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(kBarSFree + sb));
+        // the P buffer of chunk s - 2 is free once its PV has completed
+        if (s >= 2 && !rw_wait(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) aborted = true;
+        if (__any_sync(0xFFFFFFFFu, aborted)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < RC / 2; c += 16) {
+          uint32_t w16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w16[i] = pk[c + i];
+          tmem_st16u(tl + kColP + 64 * sb + copy * (RC / 2) + c, w16);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(kBarPReady + sb));
+        have_o = true;
+      }
+      // ---- the unit's piece: wait for its last PV
+      if (!aborted && sg.n > 0) {
+        const int se = s_first + sg.n - 1;
+        if (!rw_wait(BAR(kBarPvDone + (se & 1)), (se >> 1) & 1, abort_s)) aborted = true;
+      }
+      if (soft_barrier_or(aborted || *abort_s)) {
+        aborted = true;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(kBarOFree));
+        break;
+      }
+      tc_fence_after();
+      // ---- merge the copies (token slices) of each row: exchange (m, l, E),
+      //      then add the scaled O rows copy after copy in shared memory; the
+      //      last copy's threads end up with the unit's rows
+      ml_s[L32] = make_float4(m_ref, lsum, static_cast<float>(E), 0.0f);
+      soft_barrier();
+      float m_all = -INFINITY;
+      int e_all = -126;
+#pragma unroll
+      for (int c = 0; c < kCopies; ++c) {
+        const float4 v = ml_s[c * RC + mrow];
+        m_all = fmaxf(m_all, v.x);
+        if (v.x != -INFINITY) e_all = max(e_all, static_cast<int>(v.z));
+      }
+      float l_all = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kCopies; ++c) {
+        const float4 v = ml_s[c * RC + mrow];
+        if (v.x != -INFINITY) l_all += rw_ex2(v.x - m_all) * v.y;
+      }
+      const float f_me = (m_ref == -INFINITY) ? 0.0f
+                                              : rw_ex2(m_ref - m_all) * pow2f_down(E - e_all);
+      const bool writer = (copy == kCopies - 1) && row_ok;
+      const bool direct = (sg.c0 == 0 && sg.n == sg.C);
+      const float vsc = pow2f(e_all);           // undo the 2^-E of P''
+      const int ir = ma / p.G, gq = ma - ir * p.G;
+      const int64_t orow = (static_cast<int64_t>(r) * p.R + ir) * p.Hq + h * p.G + gq;
+      const int b_first = static_cast<int>(sg.first / B);
+      const int slot = 2 * static_cast<int>(blockIdx.x) +
+                       (static_cast<int>(blockIdx.x) == b_first ? 1 : 0);
+      const float inv = (l_all > 0.0f) ? vsc / l_all : 0.0f;
+      float *acc = reinterpret_cast<float *>(smem + kOffQ);    // [dim][RC]
+      for (int c = 0; c < kCopies; ++c) {
+        if (copy == c) {
+#pragma unroll 1
+          for (int pc = 0; pc < 4; ++pc) {
+            float o[32];
+            tmem_ld32(tl + kColO + 32 * pc, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              o[i] *= f_me;
+              if (c > 0) o[i] += acc[(32 * pc + i) * RC + mrow];
+              if (c < kCopies - 1) acc[(32 * pc + i) * RC + mrow] = o[i];
+            }
+            if (c == kCopies - 1 && writer) {
+              if (direct) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + 32 * pc);
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8)
+                  dst[c8] = make_uint4(pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv),
+                                       pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv),
+                                       pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv),
+                                       pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv));
+              } else {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.o_part + (static_cast<int64_t>(slot) * RC + mrow) * kHeadDim + 32 * pc);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                  dst[c4] = make_float4(o[4 * c4] * vsc, o[4 * c4 + 1] * vsc,
+                                        o[4 * c4 + 2] * vsc, o[4 * c4 + 3] * vsc);
+              }
+            }
+          }
+        }
+        if (kCopies > 1) soft_barrier();
+      }
+      // the O rows have been read: the next unit's PVs may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(kBarOFree));
+      if (!direct) {
+        // a piece: slot 1 of this CTA if the unit continues past its range
+        // (its first CTA), else slot 0; the piece that lands last merges
+        if (writer) {
+          p.ml_part[static_cast<int64_t>(slot) * RC + mrow] = make_float2(m_all, l_all);
+          __threadfence();
+        }
+        soft_barrier();
+        const int b_last = static_cast<int>((sg.first + sg.C - 1) / B);
+        const int64_t unit = (static_cast<int64_t>(r) * p.H + h) * p.T + sg.t;
+        if (tid == 0) {
+          const int old = atomicAdd(p.tickets + unit, 1);
+          *ticket_s = (old == b_last - b_first) ? 1 : 0;
+          if (old == b_last - b_first) p.tickets[unit] = 0;     // ready for the next call
+          __threadfence();
+        }
+        soft_barrier();
+        if (*ticket_s) {
+          // every piece of the unit: warp per row, lane per 4 dims, running
+          // log-sum-exp over the pieces
+          for (int m = warp; m < rows_here; m += kRwSoftWarps) {
+            float mw = -INFINITY, ls = 0.0f;
+            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int bb = b_first; bb <= b_last; ++bb) {
+              const int sl = 2 * bb + (bb == b_first ? 1 : 0);
+              const float2 v = __ldcg(p.ml_part + static_cast<int64_t>(sl) * RC + m);
+              const float4 o4 = __ldcg(reinterpret_cast<const float4 *>(
+                  p.o_part + (static_cast<int64_t>(sl) * RC + m) * kHeadDim) + lane);
+              if (v.x == -INFINITY) continue;
+              const float mn = fmaxf(mw, v.x);
+              const float fa = rw_ex2(mw - mn), fb = rw_ex2(v.x - mn);
+              ls = ls * fa + v.y * fb;
+              a4.x = a4.x * fa + o4.x * fb;
+              a4.y = a4.y * fa + o4.y * fb;
+              a4.z = a4.z * fa + o4.z * fb;
+              a4.w = a4.w * fa + o4.w * fb;
+              mw = mn;
+            }
+            const float iv = (ls > 0.0f) ? 1.0f / ls : 0.0f;
+            const int mab = row0 + m, i2 = mab / p.G, g2 = mab - i2 * p.G;
+            const int64_t orw = (static_cast<int64_t>(r) * p.R + i2) * p.Hq + h * p.G + g2;
+            *reinterpret_cast<uint2 *>(p.out + orw * kHeadDim + 4 * lane) =
+                make_uint2(pack_bf16x2(a4.x * iv, a4.y * iv), pack_bf16x2(a4.z * iv, a4.w * iv));
+          }
+        }
+      }
+      soft_barrier();                           // the merge scratch is free again
+      w.advance_segment(pre, p.context_lens, geo, N);
+    }
+    if (aborted && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
+    if (aborted) *abort_s = 1;
+    // units whose rows see no token: zero rows, spread over the grid
+    if (!aborted) {
+      const int n_units = N * p.H * p.T;
+      for (int u = blockIdx.x * kRwSoftWarps + warp; u < n_units;
+           u += gridDim.x * kRwSoftWarps) {
+        const int t = u % p.T, rh = u / p.T, h = rh % p.H, r = rh / p.H;
+        const int L = clamp_len(p.context_lens[r], p.ctx_limit);
+        if (tile_tokens(geo, L, t) > 0) continue;
+        const int rows = min(p.M - 128 * t, 128);
+        for (int m = 0; m < rows; ++m) {
+          const int ma = 128 * t + m, ir = ma / p.G, gq = ma - ir * p.G;
+          const int64_t orow = (static_cast<int64_t>(r) * p.R + ir) * p.Hq + h * p.G + gq;
+          *reinterpret_cast<uint2 *>(p.out + orow * kHeadDim + 4 * lane) = make_uint2(0u, 0u);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kRwWarpTma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kRwTmemCols);
+  }
+}
+
+}  // namespace
+
+int32_t attn_rows_per_tile(int32_t rows) { return rows <= 32 ? 32 : (rows <= 64 ? 64 : 128); }
+
+bool attn_rows_supported(const kvq_cache &c, const AttnShape &s) {
+  const int bs = 1 << s.log2_block;
+  return s.rows > 8 && bs >= 16 && c.num_kv_heads % 4 == 0 && c.num_slots > 0 &&
+         c.num_slots < (int64_t(1) << 31) && s.num_requests <= kRowsMaxRequests &&
+         (reinterpret_cast<uintptr_t>(c.k_scales) & 15u) == 0 &&
+         (reinterpret_cast<uintptr_t>(c.v_scales) & 15u) == 0;
+}
+
+size_t attn_rows_workspace_bytes(const AttnShape &s, int32_t num_kv_heads) {
+  const int64_t T = (s.rows + 127) / 128;
+  const int64_t units = static_cast<int64_t>(s.num_requests) * num_kv_heads * T;
+  const int64_t rc = attn_rows_per_tile(s.rows);
+  const int64_t grid = s.sms > 0 ? s.sms : 152;
+  const size_t tickets = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
+  const size_t o = static_cast<size_t>(grid) * 2 * rc * kHeadDim * sizeof(float);
+  const size_t ml = static_cast<size_t>(grid) * 2 * rc * sizeof(float2);
+  return tickets + (o + 255) / 256 * 256 + (ml + 255) / 256 * 256;
+}
+
+cudaError_t launch_attn_rows(const kvq_cache &c, const AttnShape &s, const void *q,
+                             const int32_t *block_tables, const int32_t *context_lens,
+                             float sm_scale, void *out, void *workspace, int32_t *err_flags,
+                             cudaStream_t stream) {
+  RwParams p;
+  p.num_blocks = static_cast<uint32_t>(c.num_slots >> s.log2_block);
+  p.H = c.num_kv_heads;
+  p.log2_bs = s.log2_block;
+  p.box = (1 << s.log2_block) < kRwTok ? (1 << s.log2_block) : kRwTok;
+  p.q = static_cast<const uint16_t *>(q);
+  p.out = static_cast<uint16_t *>(out);
+  p.block_tables = block_tables;
+  p.max_blocks = s.max_blocks_per_req;
+  p.context_lens = context_lens;
+  const int64_t cap = static_cast<int64_t>(s.max_blocks_per_req) << s.log2_block;
+  p.ctx_limit = static_cast<int32_t>(cap < s.max_context_len ? cap : s.max_context_len);
+  p.N = s.num_requests;
+  p.R = s.rows_per_request;
+  p.Hq = s.num_q_heads;
+  p.G = s.group;
+  p.M = s.rows;
+  p.T = (s.rows + 127) / 128;
+  p.qk_scale = sm_scale * 1.4426950408889634f;
+  const int64_t units = static_cast<int64_t>(s.num_requests) * c.num_kv_heads * p.T;
+  const int rc = attn_rows_per_tile(s.rows);
+  const int grid = s.sms > 0 ? s.sms : 152;
+  char *ws = static_cast<char *>(workspace);
+  p.tickets = reinterpret_cast<int32_t *>(ws);
+  ws += (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
+  p.o_part = reinterpret_cast<float *>(ws);
+  ws += (static_cast<size_t>(grid) * 2 * rc * kHeadDim * sizeof(float) + 255) / 256 * 256;
+  p.ml_part = reinterpret_cast<float2 *>(ws);
+  p.err_flags = err_flags;
+  CUtensorMap mkc, mvc, mks, mvs;
+  if (!encode_code_tensor_map(&mkc, c.k_codes, c.num_slots, c.num_kv_heads, p.box) ||
+      !encode_code_tensor_map(&mvc, c.v_codes, c.num_slots, c.num_kv_heads, p.box) ||
+      !encode_scale_tensor_map(&mks, c.k_scales, c.num_slots, c.num_kv_heads, p.box) ||
+      !encode_scale_tensor_map(&mvs, c.v_scales, c.num_slots, c.num_kv_heads, p.box))
+    return cudaErrorInvalidValue;
+  void (*kernel)(RwParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) =
+      rc == 32 ? attn_rows_kernel<32> : (rc == 64 ? attn_rows_kernel<64> : attn_rows_kernel<128>);
+  static std::atomic<uint64_t> configured[3];
+  const int which = rc == 32 ? 0 : (rc == 64 ? 1 : 2);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit == 0 || !(configured[which].load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRwSmem);
+    if (e != cudaSuccess) return e;
+    configured[which].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return launch_overlapped(kernel, dim3(grid), dim3(kRwThreads), kRwSmem, stream, p, mkc, mvc,
+                           mks, mvs);
+}
+
+}  // namespace kvq

@@ -51,6 +51,8 @@ struct AttnShape {
   int32_t log2_block;
   int32_t sms;                // SMs of the current device
   int32_t stream;             // 1: the load-balanced kernel (partials in stream slots)
+  int32_t rows_kernel;        // 1: the rows-on-M tcgen05 kernel (no combine launch)
+  int32_t num_kv_heads;
 };
 
 // The load-balanced decode kernel's layout: a plan ([0] chunks per CTA, [1]
@@ -136,6 +138,22 @@ cudaError_t launch_attn_partials_page(const kvq_cache &c, const AttnShape &s, co
                                       const int32_t *block_tables, const int32_t *context_lens,
                                       float sm_scale, void *out, float *o_part, float2 *ml_part,
                                       int32_t *err_flags, cudaStream_t stream);
+
+// The rows-on-M tcgen05 kernel for more than 8 stacked rows per KV head
+// (verify, chunked prefill): a persistent grid of one CTA per SM over the
+// batch's 128-token chunks, units cut by a range boundary merged by their last
+// piece.  Its workspace: a zeroed ticket per (request, KV head, 128-row tile),
+// then the pieces' partials, two slots per CTA.
+constexpr int32_t kRowsMaxRequests = 1024;
+constexpr int32_t kRowsSwitch = 3;          // chunk charge per unit start
+constexpr int32_t kRowsMaxRows = 4096;      // stacked rows per KV head
+int32_t attn_rows_per_tile(int32_t rows);
+bool attn_rows_supported(const kvq_cache &c, const AttnShape &s);
+size_t attn_rows_workspace_bytes(const AttnShape &s, int32_t num_kv_heads);
+cudaError_t launch_attn_rows(const kvq_cache &c, const AttnShape &s, const void *q,
+                             const int32_t *block_tables, const int32_t *context_lens,
+                             float sm_scale, void *out, void *workspace, int32_t *err_flags,
+                             cudaStream_t stream);
 
 // The tcgen05 partials kernel for 9..32 stacked rows per KV head.
 bool attn_tc_supported(const kvq_cache &c, const AttnShape &s);

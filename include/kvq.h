@@ -139,20 +139,27 @@ kvq_status kvq_quantize_scatter(const kvq_cache *cache,
                                 int64_t num_tokens, const int64_t *slot_ids,
                                 int32_t *err_flags, kvq_stream_t stream);
 
-/* Tokens per split-K partition that kvq_paged_decode uses when passed 0: a
- * power of two in [256, 8192] (up to 32768 when 9..32 query rows per KV head,
- * rows_per_request * num_q_heads / num_kv_heads, go to the tensor-core verify
- * kernel) chosen from the batch shape and the current device's SM count (152
- * is assumed when no device is visible); always a multiple of 64. */
+/* Tokens per split-K partition that kvq_paged_decode uses when passed 0 and
+ * the shape takes a partitioned kernel: a power of two in [256, 8192] (up to
+ * 32768 for 9..32 stacked rows per KV head) chosen from the batch shape and
+ * the current device's SM count (152 is assumed when no device is visible);
+ * always a multiple of 64.  With 0, shapes of <= 8 stacked rows per KV head
+ * whose partition grid would be small, and every shape of more than 8 stacked
+ * rows per KV head (rows_per_request * num_q_heads / num_kv_heads; pages of
+ * >= 16 tokens, KV heads a multiple of 4), instead split the batch's tokens
+ * evenly over a persistent grid and use no fixed partitions. */
 int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t rows_per_request,
                                           int32_t num_q_heads, int32_t num_kv_heads,
                                           int32_t block_size, int32_t max_context_len);
 
 /* Workspace bytes kvq_paged_decode needs for this shape (0 when every request
- * fits one partition): num_requests*rows_per_request*num_q_heads *
- * ceil(max_context_len / partition) * (head_dim + 2) * 4, each of the two
- * parts rounded up to 256.  partition_tokens 0 means the value
- * kvq_paged_decode_partition_tokens gives.  Returns 0 for invalid arguments. */
+ * fits one partition).  With fixed partitions: num_requests*rows_per_request*
+ * num_q_heads * ceil(max_context_len / partition) * (head_dim + 2) * 4, each
+ * of the two parts rounded up to 256.  With partition_tokens 0 the library's
+ * own split decides (see kvq_paged_decode_partition_tokens); for more than 8
+ * stacked rows per KV head that is one int32 counter per (request, KV head,
+ * 128-row tile) plus two pieces of partial results per SM.  Returns 0 for
+ * invalid arguments. */
 size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,
                                        int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size,
@@ -164,9 +171,12 @@ size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_re
  *   q               device bf16 [num_requests*rows_per_request, num_q_heads,
  *                   head_dim], contiguous; row r*rows_per_request + i is query
  *                   row i of request r.
- *   rows_per_request R >= 1; R * (num_q_heads/num_kv_heads) <= 128 (the rows
- *                   of one KV head are processed in groups of at most 32 that
- *                   each read the head's codes once).
+ *   rows_per_request R >= 1; the stacked rows per KV head, R * (num_q_heads /
+ *                   num_kv_heads), at most 128 with a fixed partition size and
+ *                   at most 4096 with partition_tokens 0 (a verify step, a
+ *                   chunk of prefill: tiles of up to 128 rows each read the
+ *                   head's codes once; more than 128 need a cache whose scale
+ *                   planes are 16-byte aligned and fewer than 2^31 slots).
  *   num_q_heads     a multiple of cache->num_kv_heads
  *   block_tables    device int32 [num_requests, max_blocks_per_req]: physical
  *                   block of each logical block of the request
@@ -179,7 +189,13 @@ size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_re
  *                   [64, 1<<20]; 0 = kvq_paged_decode_partition_tokens()
  *   out             device bf16, same shape as q (written, round-to-nearest)
  *   workspace       device, >= kvq_paged_decode_workspace_size(...) bytes
- *                   (may be NULL when that size is 0)
+ *                   (may be NULL when that size is 0), zero-filled before its
+ *                   first use (e.g. one cudaMemset after allocating it).  The
+ *                   load-balanced split for more than 8 stacked rows keeps
+ *                   per-unit counters in it that each call returns to zero, so
+ *                   a workspace stays reusable without clearing -- unless a
+ *                   call sets KVQ_ERRF_WAIT_TIMEOUT, after which it must be
+ *                   zero-filled again.
  *   err_flags       device int32, optional
  * Calls that share a workspace must not run concurrently. */
 kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q,
@@ -229,10 +245,13 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
  *    device, with that device current) and caches it; make that first call
  *    before any stream capture on the device.
  *  - All calls share the one array and it keeps the last call's contents.
- *    Nothing in it needs to start at zero: every byte the combine reads is
- *    written by the same call's first launch.  Calls that overlap on the GPU
- *    (on different streams, or from several host threads) race on the array
- *    and give wrong results; order them on one stream or with events. */
+ *    The array starts zero-filled when the library loads, and every call
+ *    leaves the counters the load-balanced split keeps in it back at zero (a
+ *    call that sets KVQ_ERRF_WAIT_TIMEOUT may not; the array cannot be cleared
+ *    from outside, so decode on such a device afterwards through
+ *    kvq_paged_decode).  Calls that overlap on the GPU (on different streams,
+ *    or from several host threads) race on the array and give wrong results;
+ *    order them on one stream or with events. */
 kvq_status kvq_paged_decode_noalloc(const kvq_cache *cache, const void *q,
                                     int32_t num_requests, int32_t rows_per_request,
                                     int32_t num_q_heads, const int32_t *block_tables,

@@ -89,7 +89,8 @@ def test_decode_validation_happens_before_launch(lib):
     assert _decode(lib, c, R=0) == INVALID
     assert _decode(lib, c, part=100) == INVALID                # not a multiple of 64
     assert _decode(lib, c, sm=float("nan")) == INVALID
-    assert _decode(lib, c, R=5, Hq=256) == UNSUPPORTED         # 5*32 rows per KV head
+    assert _decode(lib, c, R=5, Hq=256, part=64) == UNSUPPORTED   # 160 rows, fixed partitions
+    assert _decode(lib, c, R=200, Hq=256) == UNSUPPORTED       # 6400 rows per KV head
     assert _decode(lib, _cache(head_dim=256)) == UNSUPPORTED
     assert _decode(lib, _cache(block_size=24)) == UNSUPPORTED  # not a power of two
     assert _decode(lib, _cache(block_size=0)) == INVALID
@@ -99,6 +100,23 @@ def test_decode_validation_happens_before_launch(lib):
     assert _decode(lib, c, maxc=128, part=64) == WS_SMALL      # two partitions need a workspace
     need = lib.kvq_paged_decode_workspace_size(2, 1, 32, 8, 128, 16, 128, 64)
     assert _decode(lib, c, maxc=128, part=64, ws=256, wsb=need - 1) == WS_SMALL
+
+
+def test_workspace_size_of_the_rows_split(lib):
+    """More than 8 stacked rows per KV head with partition_tokens 0: one int32
+    ticket per (request, KV head, 128-row tile), rounded to 256 bytes, then two
+    pieces per SM of rows-per-tile (32, 64 or 128) partial rows of 128 fp32 and
+    their (max, denominator) pairs, each part rounded to 256 bytes."""
+    sms = lib.kvq_test_sm_count() if hasattr(lib, "kvq_test_sm_count") else 152
+
+    def expect(N, H, rows):
+        T = (rows + 127) // 128
+        rc = 32 if rows <= 32 else (64 if rows <= 64 else 128)
+        r256 = lambda x: (x + 255) // 256 * 256
+        return r256(N * H * T * 4) + r256(sms * 2 * rc * 128 * 4) + r256(sms * 2 * rc * 8)
+    assert lib.kvq_paged_decode_workspace_size(64, 4, 64, 8, 128, 64, 32768, 0) == expect(64, 8, 32)
+    assert lib.kvq_paged_decode_workspace_size(3, 3, 48, 4, 128, 16, 500, 0) == expect(3, 4, 36)
+    assert lib.kvq_paged_decode_workspace_size(1, 512, 32, 8, 128, 64, 4096, 0) == expect(1, 8, 2048)
 
 
 def test_workspace_size_formula(lib):

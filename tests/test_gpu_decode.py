@@ -203,7 +203,7 @@ def test_graph_capture_of_decode():
     P = 128
     need = kvq.paged_decode_workspace_size(3, 1, w.num_q_heads, w.num_kv_heads, 128,
                                            w.block_size, 1024, P)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(q)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
