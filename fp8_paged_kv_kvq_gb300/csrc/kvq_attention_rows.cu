@@ -89,10 +89,10 @@ constexpr int kOffBar = kOffPre + (kRowsMaxRequests + 4) * 4;
 constexpr int kBarKvFull = 0;
 constexpr int kBarKvEmpty = kBarKvFull + kRwStages;
 constexpr int kBarSFull = kBarKvEmpty + kRwStages;
-constexpr int kBarSFree = kBarSFull + 2;
-constexpr int kBarPReady = kBarSFree + 2;
-constexpr int kBarVfReady = kBarPReady + 2;
-constexpr int kBarPvDone = kBarVfReady + 2;
+// chunk s is ready for its PV once its P'' is in TMEM (softmax warps, which
+// have also finished reading its S) and its V operand converted (converters)
+constexpr int kBarReady = kBarSFull + 2;
+constexpr int kBarPvDone = kBarReady + 2;
 constexpr int kBarQReady = kBarPvDone + 2;
 constexpr int kBarOFree = kBarQReady + 1;
 constexpr int kNumBars = kBarOFree + 1;
@@ -136,7 +136,11 @@ __device__ __forceinline__ float rw_ex2(float x) {
 }
 
 // Bounded wait that also gives up once another role raised the abort flag.
-__device__ __forceinline__ bool rw_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+// One out-of-line copy for the whole kernel: inlined (and unrolled) at every
+// wait it would multiply the code the warps' loops have to keep in the
+// instruction cache.
+__device__ __noinline__ bool rw_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+#pragma unroll 1
   for (int i = 0; i < (1 << 19); ++i) {
     if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
     if ((i & 15) == 15 && *abort) return false;
@@ -205,7 +209,7 @@ struct Seg {
   int64_t next;          // where the CTA's range continues
 };
 
-__device__ __forceinline__ Seg locate_rows(const int32_t *pre, const int32_t *context_lens, const Geo &g, int N,
+__device__ __forceinline__ Seg locate_rows(const int32_t *pre, const int32_t *context_lens, const Geo g, int N,
                            int64_t x, int64_t x_end) {
   int lo = 0, hi = N - 1;
   while (lo < hi) {
@@ -246,41 +250,213 @@ __device__ __forceinline__ Seg locate_rows(const int32_t *pre, const int32_t *co
   return s;
 }
 
-// Walks the chunks of a CTA's range in order.
+// The first segment with chunks at or after position x (n = 0 when the range
+// has none left).  Out of line: it runs once per segment, and its code stays
+// out of the roles' hot loops.
+__device__ __noinline__ Seg next_segment(const int32_t *pre, const int32_t *cl, const Geo g, int N,
+                                         int64_t x, int64_t x_end) {
+  while (x < x_end) {
+    const Seg sg = locate_rows(pre, cl, g, N, x, x_end);
+    if (sg.n > 0) return sg;
+    x = sg.next;
+  }
+  Seg e;
+  e.r = e.h = e.t = e.L = e.C = e.c0 = e.n = e.vis = 0;
+  e.first = e.next = x_end;
+  return e;
+}
+
+// Walks the chunks of a CTA's range in order (its state in registers).
 struct ChunkWalk {
   Seg sg;
   int k;                 // chunk within the segment
   int seg;               // segment index
-  int64_t x, x_end;
+  int64_t x_end;
   bool valid;
-  __device__ __forceinline__ void start(const int32_t *pre, const int32_t *cl, const Geo &g, int N, int64_t xb,
-                        int64_t xe) {
-    x = xb;
+  __device__ __forceinline__ void start(const int32_t *pre, const int32_t *cl, const Geo g, int N,
+                                        int64_t xb, int64_t xe) {
     x_end = xe;
-    seg = -1;
-    valid = false;
+    seg = 0;
     k = 0;
-    advance_segment(pre, cl, g, N);
+    sg = next_segment(pre, cl, g, N, xb, xe);
+    valid = sg.n > 0;
   }
-  __device__ __forceinline__ void advance_segment(const int32_t *pre, const int32_t *cl, const Geo &g, int N) {
-    while (x < x_end) {
-      sg = locate_rows(pre, cl, g, N, x, x_end);
-      x = sg.next;
-      if (sg.n > 0) {
-        ++seg;
-        k = 0;
-        valid = true;
-        return;
-      }
-    }
-    valid = false;
+  __device__ __forceinline__ void advance_segment(const int32_t *pre, const int32_t *cl,
+                                                  const Geo g, int N) {
+    sg = next_segment(pre, cl, g, N, sg.next, x_end);
+    valid = sg.n > 0;
+    k = 0;
+    ++seg;
   }
-  __device__ __forceinline__ void next(const int32_t *pre, const int32_t *cl, const Geo &g, int N) {
+  __device__ __forceinline__ void next(const int32_t *pre, const int32_t *cl, const Geo g, int N) {
     if (!valid) return;
     if (++k < sg.n) return;
     advance_segment(pre, cl, g, N);
   }
 };
+
+// ---------------------------------------------------------------------------
+// Softmax pieces.  A softmax thread owns TMEM lane L (row L % RC of the tile,
+// copy L / RC) and the chunk's token slice [copy RC, copy RC + RC).  The hot
+// loop below is kept compact (16 tokens per trip, not unrolled over the
+// slice) and the rare or once-per-unit steps live in functions of their own:
+// the kernel's warps run four different loops side by side, and their code
+// has to stay in the SM's instruction cache.
+
+// P'' = p v_scale 2^-E of this thread's slice under the present references,
+// written to TMEM 16 tokens at a time, and its share of the denominator.
+// True if a score passed the reference's headroom or a value scale the bound
+// 2^E: the chunk then has to be redone under new references.
+template <int RC>
+__device__ __forceinline__ bool rows_chunk_p(uint32_t scol, uint32_t pcol, const float *ks,
+                                            const float *vs, int lim, float rowf, float m_ref,
+                                            int E, float &lchunk) {
+  const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
+  const float thr = m_ref + kRwLazy;
+  const float vbound = pow2f(E), vnorm = pow2f(-E);
+  bool over = false;
+#pragma unroll 1
+  for (int g = 0; g < RC / 16; ++g) {
+    float x[16];
+    tmem_ld16(scol + 16 * g, x);
+    uint32_t pk[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 k4 = reinterpret_cast<const float4 *>(ks)[4 * g + q];
+      const float4 v4 = reinterpret_cast<const float4 *>(vs)[4 * g + q];
+      const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+      float pw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // unseen tokens: -inf score, value weight 0 (their scales may be stale)
+        const bool seen = 16 * g + 4 * q + e < lim;
+        const float xe = seen ? x[4 * q + e] * (kk[e] * rowf) : -INFINITY;
+        const float ve = seen ? vv[e] : 0.0f;
+        over |= (xe > thr) | (ve > vbound);
+        const float pe = rw_ex2(xe - ms);
+        lchunk += pe;
+        pw[e] = pe * (ve * vnorm);
+      }
+      pk[2 * q] = pack_f16x2(pw[0], pw[1]);
+      pk[2 * q + 1] = pack_f16x2(pw[2], pw[3]);
+    }
+    tmem_st8u(pcol + 8 * g, pk);
+  }
+  return over;
+}
+
+// The rare case (a row's scores passed its reference's headroom or a value
+// scale the bound): new references, the denominator and the O rows so far
+// rescaled (once the previous chunk's PV has completed), the chunk redone.
+// False if a wait gave up.
+template <int RC>
+__device__ __noinline__ bool rows_chunk_redo(uint32_t scol, uint32_t pcol, uint32_t ocol,
+                                             const float *ks, const float *vs, int lim,
+                                             float rowf, float &m_ref, int &E, float &lsum,
+                                             float &lchunk, bool have_o, uint32_t pv_bar,
+                                             uint32_t pv_par, volatile int *abort_s) {
+  float mx = -INFINITY, vmax = 0.0f;
+#pragma unroll 1
+  for (int g = 0; g < RC / 16; ++g) {
+    float x[16];
+    tmem_ld16(scol + 16 * g, x);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const bool seen = 16 * g + i < lim;
+      mx = fmaxf(mx, seen ? x[i] * (ks[16 * g + i] * rowf) : -INFINITY);
+      vmax = fmaxf(vmax, seen ? vs[16 * g + i] : 0.0f);
+    }
+  }
+  float f = 1.0f;
+  const float m_new = (mx > m_ref + kRwLazy) ? mx + kRwOvershoot : m_ref;
+  // a new value bound keeps two binades of headroom (fewer redos as the
+  // scales grow; P'' then stays <= p / 4)
+  const int e_need = rw_pow2_ceil(__float_as_uint(vmax));
+  const int e_new = e_need > E ? min(e_need + 2, 126) : E;
+  if (m_ref != -INFINITY) {
+    const float fm = rw_ex2(m_ref - m_new);
+    lsum *= fm;
+    f = fm * pow2f_down(E - e_new);
+  }
+  m_ref = m_new;
+  E = e_new;
+  if (have_o && __any_sync(0xFFFFFFFFu, f != 1.0f)) {
+    const bool ok = rw_wait(pv_bar, pv_par, abort_s);
+    if (__any_sync(0xFFFFFFFFu, !ok)) return false;
+    tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      float o[32];
+      tmem_ld32(ocol + c, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] *= f;
+      tmem_st32(ocol + c, o);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+  }
+  lchunk = 0.0f;
+  rows_chunk_p<RC>(scol, pcol, ks, vs, lim, rowf, m_ref, E, lchunk);
+  return true;
+}
+
+// The unit's query tile (rows m < rows_here of tile row0, every copy) as two
+// e4m3 pieces per element in the K-major 128-byte swizzled layout, and each
+// row's factor 2^e sm_scale log2(e); each softmax warp takes every 4th row.
+struct QArgs {
+  const uint16_t *q;
+  int32_t R, Hq, G;
+  float qk_scale;
+};
+
+template <int RC>
+__device__ __noinline__ void rows_load_q(const QArgs p, int r, int h, int row0, int rows_here,
+                                         uint8_t *smem, float *rowf_s, int warp, int lane) {
+  constexpr int kCopies = 128 / RC;
+  constexpr int kQRows = RC / kRwSoftWarps;          // rows per warp, loaded at once
+  uint2 qv[kQRows];
+#pragma unroll
+  for (int i = 0; i < kQRows; ++i) {
+    const int m = warp + kRwSoftWarps * i;
+    qv[i] = make_uint2(0u, 0u);
+    if (m < rows_here) {
+      const int ma = row0 + m, ir = ma / p.G, gq = ma - ir * p.G;
+      qv[i] = *reinterpret_cast<const uint2 *>(
+          p.q + ((static_cast<int64_t>(r) * p.R + ir) * p.Hq + h * p.G + gq) * kHeadDim +
+          4 * lane);
+    }
+  }
+#pragma unroll 1
+  for (int i = 0; i < kQRows; ++i) {
+    const int m = warp + kRwSoftWarps * i;
+    const uint2 v = qv[i];
+    float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                       fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+    int e = (ex == 0) ? -126 : ex - 127 - 7;
+    e = e < -126 ? -126 : (e > 126 ? 126 : e);
+    const float rx = (amax == 0.0f) ? 0.0f : pow2f(e);          // 2^e
+    uint32_t c1w = 0u, c2w = 0u;
+    if (rx != 0.0f) {
+      const float inv = pow2f(-e);
+      const float xs[4] = {bf16_lo(v.x) * inv, bf16_hi(v.x) * inv, bf16_lo(v.y) * inv,
+                           bf16_hi(v.y) * inv};
+      e4m3_pieces4(xs, c1w, c2w);
+    }
+    if (lane == 0) rowf_s[m] = rx * p.qk_scale;
+#pragma unroll
+    for (int c = 0; c < kCopies; ++c) {
+      const int row = c * RC + m;
+      const int off = row * kHeadDim + (((lane >> 2) ^ (row & 7)) << 4) + 4 * (lane & 3);
+      *reinterpret_cast<uint32_t *>(smem + kOffQ + off) = c1w;
+      *reinterpret_cast<uint32_t *>(smem + kOffQ + kQBytes + off) = c2w;
+    }
+  }
+}
 
 template <int RC>
 __global__ void __launch_bounds__(kRwThreads, 1)
@@ -342,9 +518,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(kBarSFull + b), 1);
-      mbar_init(BAR(kBarSFree + b), kRwSoftWarps);
-      mbar_init(BAR(kBarPReady + b), kRwSoftWarps);
-      mbar_init(BAR(kBarVfReady + b), kRwConvWarps);
+      mbar_init(BAR(kBarReady + b), kRwSoftWarps + kRwConvWarps);
       mbar_init(BAR(kBarPvDone + b), 1);
     }
     mbar_init(BAR(kBarQReady), kRwSoftWarps);
@@ -449,8 +623,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       int pend = -1, pend_first = 0, pend_seg = 0;          // the chunk whose PV is due
       auto issue_pv = [&]() -> bool {
         const int c = pend, cb = c & 1;
-        if (!rw_wait(BAR(kBarPReady + cb), (c >> 1) & 1, abort_s)) return false;
-        if (!rw_wait(BAR(kBarVfReady + cb), (c >> 1) & 1, abort_s)) return false;
+        if (!rw_wait(BAR(kBarReady + cb), (c >> 1) & 1, abort_s)) return false;
         if (pend_first && pend_seg >= 1 && !rw_wait(BAR(kBarOFree), (pend_seg - 1) & 1, abort_s))
           return false;
         tc_fence_after();
@@ -478,7 +651,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           if (!rw_wait(BAR(kBarQReady), w.seg & 1, abort_s)) { ok = false; break; }
         }
         if (!rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) { ok = false; break; }
-        if (s >= 2 && !rw_wait(BAR(kBarSFree + sb), ((s >> 1) - 1) & 1, abort_s)) { ok = false; break; }
+        // S buffer s & 1 was read by chunk s - 2's softmax, which this thread
+        // saw ready before issuing that chunk's PV
         tc_fence_after();
         const uint64_t kd = smem_desc(smem_addr(smem + b * kStageBytes), 16, 1024, kSmemSwizzle128);
         const uint64_t qa = smem_desc(q0, 16, 1024, kSmemSwizzle128);
@@ -538,7 +712,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(BAR(kBarVfReady + vb));
+        mbar_arrive(BAR(kBarReady + vb));
         mbar_arrive(BAR(kBarKvEmpty + b));
       }
       w.next(pre, p.context_lens, geo, N);
@@ -572,48 +746,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       const int rows_here = min(p.M - row0, RC);
       // ---- the unit's query tile: rows m < rows_here of the tile, every copy
       //      (the previous unit's MMAs reading Q and its merge are finished)
-      constexpr int kQRows = RC / kRwSoftWarps;          // rows per warp, loaded at once
-      uint2 qv[kQRows];
-#pragma unroll
-      for (int i = 0; i < kQRows; ++i) {
-        const int m = warp + kRwSoftWarps * i;
-        qv[i] = make_uint2(0u, 0u);
-        if (m < rows_here) {
-          const int ma = row0 + m, ir = ma / p.G, gq = ma - ir * p.G;
-          qv[i] = *reinterpret_cast<const uint2 *>(
-              p.q + ((static_cast<int64_t>(r) * p.R + ir) * p.Hq + h * p.G + gq) * kHeadDim +
-              4 * lane);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kQRows; ++i) {
-        const int m = warp + kRwSoftWarps * i;
-        const uint2 v = qv[i];
-        float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                           fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-        int e = (ex == 0) ? -126 : ex - 127 - 7;
-        e = e < -126 ? -126 : (e > 126 ? 126 : e);
-        const float rx = (amax == 0.0f) ? 0.0f : pow2f(e);          // 2^e
-        uint32_t c1w = 0u, c2w = 0u;
-        if (rx != 0.0f) {
-          const float inv = pow2f(-e);
-          const float xs[4] = {bf16_lo(v.x) * inv, bf16_hi(v.x) * inv, bf16_lo(v.y) * inv,
-                               bf16_hi(v.y) * inv};
-          e4m3_pieces4(xs, c1w, c2w);
-        }
-        if (lane == 0) rowf_s[m] = rx * p.qk_scale;
-#pragma unroll
-        for (int c = 0; c < kCopies; ++c) {
-          const int row = c * RC + m;
-          const int off = row * kHeadDim + (((lane >> 2) ^ (row & 7)) << 4) + 4 * (lane & 3);
-          *reinterpret_cast<uint32_t *>(smem + kOffQ + off) = c1w;
-          *reinterpret_cast<uint32_t *>(smem + kOffQ + kQBytes + off) = c2w;
-        }
-      }
+      rows_load_q<RC>(QArgs{p.q, p.R, p.Hq, p.G, p.qk_scale}, r, h, row0, rows_here, smem,
+                      rowf_s, warp, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(kBarQReady));
@@ -640,150 +774,43 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           break;
         }
         tc_fence_after();
-        // scales of head h for the chunk's 128 tokens, into this warp's buffer
+        // scales of head h for this warp's token slice, into its buffer [K | V]
         {
           const float *sc = reinterpret_cast<const float *>(smem + kOffSc + b * 2 * kScBytes);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int tk = lane + 32 * i;
-            ts[tk] = sc[4 * tk + (h & 3)];
-            ts[kRwTok + tk] = sc[kRwTok * 4 + 4 * tk + (h & 3)];
+          for (int i = 0; i < RC / 32; ++i) {
+            const int tk = copy * RC + lane + 32 * i;
+            ts[lane + 32 * i] = sc[4 * tk + (h & 3)];
+            ts[RC + lane + 32 * i] = sc[kRwTok * 4 + 4 * tk + (h & 3)];
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));
-        const float4 *ks4 = reinterpret_cast<const float4 *>(ts + copy * RC);
-        const float4 *vs4 = reinterpret_cast<const float4 *>(ts + kRwTok + copy * RC);
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
         const uint32_t scol = tl + kColS + 128 * sb + copy * RC;
-        // One piece of 32 scores: x_j = s_j k_scale_j 2^e sm_scale log2(e), -inf
-        // where the row does not see the token.
-        auto load_piece = [&](int pc, float (&x)[32]) {
-          tmem_ld32(scol + 32 * pc, x);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 k4 = ks4[8 * pc + q4];
-            const int jj = 32 * pc + 4 * q4;
-            x[4 * q4] = (jj < lim) ? x[4 * q4] * (k4.x * rowf) : -INFINITY;
-            x[4 * q4 + 1] = (jj + 1 < lim) ? x[4 * q4 + 1] * (k4.y * rowf) : -INFINITY;
-            x[4 * q4 + 2] = (jj + 2 < lim) ? x[4 * q4 + 2] * (k4.z * rowf) : -INFINITY;
-            x[4 * q4 + 3] = (jj + 3 < lim) ? x[4 * q4 + 3] * (k4.w * rowf) : -INFINITY;
-          }
-        };
-        // P'' = p v_scale 2^-E of one piece (f16 pairs) and its share of the
-        // denominator; flags a score above the reference's headroom or a value
-        // scale above the bound (the piece then has to be redone).
-        uint32_t pk[RC / 2];
-        auto p_piece = [&](int pc, const float (&x)[32], float &lpart) -> bool {
-          const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
-          const float thr = m_ref + kRwLazy;
-          const float vbound = pow2f(E), vnorm = pow2f(-E);
-          bool over = false;
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            // scales of unseen tokens may be stale shared memory: weight 0
-            const float4 v4 = vs4[8 * pc + q4];
-            const int jj = 32 * pc + 4 * q4;
-            const float va = (jj < lim) ? v4.x : 0.0f, vb = (jj + 1 < lim) ? v4.y : 0.0f;
-            const float vc = (jj + 2 < lim) ? v4.z : 0.0f, vd = (jj + 3 < lim) ? v4.w : 0.0f;
-            over |= (x[4 * q4] > thr) | (x[4 * q4 + 1] > thr) | (x[4 * q4 + 2] > thr) |
-                    (x[4 * q4 + 3] > thr);
-            over |= (fmaxf(fmaxf(va, vb), fmaxf(vc, vd)) > vbound);
-            const float pa = rw_ex2(x[4 * q4] - ms), pb = rw_ex2(x[4 * q4 + 1] - ms);
-            const float pc2 = rw_ex2(x[4 * q4 + 2] - ms), pd = rw_ex2(x[4 * q4 + 3] - ms);
-            lpart += (pa + pb) + (pc2 + pd);
-            pk[16 * pc + 2 * q4] = pack_f16x2(pa * (va * vnorm), pb * (vb * vnorm));
-            pk[16 * pc + 2 * q4 + 1] = pack_f16x2(pc2 * (vc * vnorm), pd * (vd * vnorm));
-          }
-          return over;
-        };
-        // fast path: every piece under the present references
+        const uint32_t pcol = tl + kColP + 64 * sb + copy * (RC / 2);
+        // the P buffer of chunk s - 2 is free: this thread issued PV(s - 2)
+        // before QK(s), and the commit that signalled S(s) covers every MMA
+        // issued before it
         float lchunk = 0.0f;
-        bool over = false;
-#pragma unroll
-        for (int pc = 0; pc < RC / 32; ++pc) {
-          float x[32];
-          load_piece(pc, x);
-          over |= p_piece(pc, x, lchunk);
-        }
+        // the unit's first chunk sets the references: straight to the redo
+        const bool over =
+            k == 0 || rows_chunk_p<RC>(scol, pcol, ts, ts + RC, lim, rowf, m_ref, E, lchunk);
         if (__any_sync(0xFFFFFFFFu, over)) {
-          // ---- slow path (rare): new references for the rows that need them,
-          //      the O rows so far rescaled, the chunk redone
-          float mx = -INFINITY, vmax = 0.0f;
-#pragma unroll
-          for (int pc = 0; pc < RC / 32; ++pc) {
-            float x[32];
-            load_piece(pc, x);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) mx = fmaxf(mx, x[jj]);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 v4 = vs4[8 * pc + q4];
-              const int jj = 32 * pc + 4 * q4;
-              vmax = fmaxf(vmax, fmaxf(fmaxf((jj < lim) ? v4.x : 0.0f, (jj + 1 < lim) ? v4.y : 0.0f),
-                                       fmaxf((jj + 2 < lim) ? v4.z : 0.0f, (jj + 3 < lim) ? v4.w : 0.0f)));
-            }
-          }
-          float f = 1.0f;
-          const float m_new = (mx > m_ref + kRwLazy) ? mx + kRwOvershoot : m_ref;
-          const int e_new = max(E, rw_pow2_ceil(__float_as_uint(vmax)));
-          if (m_ref != -INFINITY) {
-            const float fm = rw_ex2(m_ref - m_new);
-            lsum *= fm;
-            f = fm * pow2f_down(E - e_new);
-          }
-          m_ref = m_new;
-          E = e_new;
-          // the O rows accumulated so far follow the new references
-          if (have_o && __any_sync(0xFFFFFFFFu, f != 1.0f)) {
-            const int sp = s - 1;
-            if (!rw_wait(BAR(kBarPvDone + (sp & 1)), (sp >> 1) & 1, abort_s)) aborted = true;
-            if (__any_sync(0xFFFFFFFFu, aborted)) {
-              aborted = true;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 128; c += 32) {
-              float o[32];
-              tmem_ld32(tl + kColO + c, o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= f;
-              tmem_st32(tl + kColO + c, o);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-          }
-          lchunk = 0.0f;
-#pragma unroll
-          for (int pc = 0; pc < RC / 32; ++pc) {
-            float x[32];
-            load_piece(pc, x);
-            p_piece(pc, x, lchunk);
+          tmem_wait_st();
+          const int sp = s - 1;
+          if (!rows_chunk_redo<RC>(scol, pcol, tl + kColO, ts, ts + RC, lim, rowf, m_ref, E,
+                                   lsum, lchunk,
+                                   have_o, BAR(kBarPvDone + (sp & 1)), (sp >> 1) & 1, abort_s)) {
+            aborted = true;
+            break;
           }
         }
         lsum += lchunk;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(kBarSFree + sb));
-        // the P buffer of chunk s - 2 is free once its PV has completed
-        if (s >= 2 && !rw_wait(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) aborted = true;
-        if (__any_sync(0xFFFFFFFFu, aborted)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < RC / 2; c += 16) {
-          uint32_t w16[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w16[i] = pk[c + i];
-          tmem_st16u(tl + kColP + 64 * sb + copy * (RC / 2) + c, w16);
-        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(kBarPReady + sb));
+        if (lane == 0) mbar_arrive(BAR(kBarReady + sb));
         have_o = true;
       }
       // ---- the unit's piece: wait for its last PV
