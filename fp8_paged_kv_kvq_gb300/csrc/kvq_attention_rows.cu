@@ -34,10 +34,12 @@
 //    K = 128 tokens, kind::f16, A = P'' = p v_scale 2^-E read from TMEM (the
 //    softmax writes it there as f16), B = the V codes converted exactly to f16
 //    (MN-major, 128-byte swizzle) by four converter warps.
-//  * Warp roles (320 threads): 0-3 softmax (TMEM lane quarters 0-3), 4-7 V
+//  * Warp roles (352 threads): 0-3 softmax (TMEM lane quarters 0-3), 4-7 V
 //    conversion, 8 TMA (block ids fetched ahead by cp.async, one 3-D box per
-//    page and plane, one 2-D box of 4 heads' scales per page and plane), 9 MMA
-//    (one lane).  TMEM: two S buffers, O, two P buffers (512 columns).
+//    page and plane, one 2-D box of 4 heads' scales per page and plane), 9
+//    QK^T MMAs and 10 PV MMAs (one lane each: the two chains of tensor-core
+//    work run side by side).  TMEM: two S buffers, O, two P buffers (512
+//    columns).
 //  * Every wait is bounded; a role that gives up raises a shared abort flag,
 //    the softmax warps agree on it at their barriers, copies and MMAs in
 //    flight complete, the CTA frees its tensor memory (KVQ_ERRF_WAIT_TIMEOUT).
@@ -59,8 +61,9 @@ constexpr int kRwStages = 3;                 // code ring depth
 constexpr int kRwSoftWarps = 4;
 constexpr int kRwConvWarps = 4;
 constexpr int kRwWarpTma = kRwSoftWarps + kRwConvWarps;
-constexpr int kRwWarpMma = kRwWarpTma + 1;
-constexpr int kRwThreads = (kRwWarpMma + 1) * 32;
+constexpr int kRwWarpMma = kRwWarpTma + 1;       // QK^T issuer
+constexpr int kRwWarpPv = kRwWarpMma + 1;        // PV issuer
+constexpr int kRwThreads = (kRwWarpPv + 1) * 32;
 constexpr int kRwIdAhead = 4;                // chunks whose block ids are in flight
 constexpr int kRwMaxPagesPerChunk = 8;       // block size >= 16
 constexpr float kRwLazy = 14.0f;             // log2 of the largest unnormalised p
@@ -614,45 +617,20 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         mbar_wait_sleep_bounded(BAR(kBarKvFull + v % kRwStages), (v / kRwStages) & 1);
     }
   } else if (warp == kRwWarpMma) {
-    // ---------------------------------------------------------------- MMA
+    // ------------------------------------------------------------ QK^T MMA
     if (lane == 0) {
       const uint32_t q0 = smem_addr(smem + kOffQ);
-      const uint32_t vf0 = smem_addr(smem + kOffVf);
       uint32_t last_bar = 0, last_par = 0;
-      bool any = false, ok = true;
-      int pend = -1, pend_first = 0, pend_seg = 0;          // the chunk whose PV is due
-      auto issue_pv = [&]() -> bool {
-        const int c = pend, cb = c & 1;
-        if (!rw_wait(BAR(kBarReady + cb), (c >> 1) & 1, abort_s)) return false;
-        if (pend_first && pend_seg >= 1 && !rw_wait(BAR(kBarOFree), (pend_seg - 1) & 1, abort_s))
-          return false;
-        tc_fence_after();
-        const uint64_t bd = smem_desc(vf0 + cb * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
-#pragma unroll
-        for (int kk = 0; kk < kRwTok / 16; ++kk)
-          tc_mma_f16_tmem_a(tmem + kColO, tmem + kColP + 64 * cb + 8 * kk, bd + (2048 >> 4) * kk,
-                            kIdescPV, (pend_first && kk == 0) ? 0u : 1u);
-        tc_commit(BAR(kBarPvDone + cb));
-        last_bar = BAR(kBarPvDone + cb);
-        last_par = (c >> 1) & 1;
-        any = true;
-        pend = -1;
-        return true;
-      };
+      bool any = false;
       ChunkWalk w;
       w.start(pre, p.context_lens, geo, N, x_begin, x_end);
-      int s = 0;
-      for (; w.valid && ok; ++s) {
+      for (int s = 0; w.valid; ++s) {
         const int b = s % kRwStages, sb = s & 1;
-        if (w.k == 0) {
-          // a new unit: its query tile replaces the last one once the
-          // previous unit's final PV is issued (its softmax needs it first)
-          if (pend >= 0 && !issue_pv()) { ok = false; break; }
-          if (!rw_wait(BAR(kBarQReady), w.seg & 1, abort_s)) { ok = false; break; }
-        }
-        if (!rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) { ok = false; break; }
-        // S buffer s & 1 was read by chunk s - 2's softmax, which this thread
-        // saw ready before issuing that chunk's PV
+        // a new unit's query tile (written once the last unit's softmax and
+        // merge are done); S buffer s & 1 once chunk s - 2's softmax read it
+        if (w.k == 0 && !rw_wait(BAR(kBarQReady), w.seg & 1, abort_s)) break;
+        if (!rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) break;
+        if (s >= 2 && !rw_wait(BAR(kBarReady + sb), ((s >> 1) - 1) & 1, abort_s)) break;
         tc_fence_after();
         const uint64_t kd = smem_desc(smem_addr(smem + b * kStageBytes), 16, 1024, kSmemSwizzle128);
         const uint64_t qa = smem_desc(q0, 16, 1024, kSmemSwizzle128);
@@ -668,17 +646,41 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         last_bar = BAR(kBarSFull + sb);
         last_par = (s >> 1) & 1;
         any = true;
-        if (pend >= 0 && !issue_pv()) { ok = false; break; }
-        pend = s;
-        pend_first = (w.k == 0);
-        pend_seg = w.seg;
         w.next(pre, p.context_lens, geo, N);
       }
-      if (ok && pend >= 0) issue_pv();
       // every MMA issued has completed before the tensor memory is freed
       if (any) mbar_wait_sleep_bounded(last_bar, last_par);
     }
-  } else if (warp >= kRwSoftWarps) {
+  } else if (warp == kRwWarpPv) {
+    // -------------------------------------------------------------- PV MMA
+    if (lane == 0) {
+      const uint32_t vf0 = smem_addr(smem + kOffVf);
+      uint32_t last_bar = 0, last_par = 0;
+      bool any = false;
+      ChunkWalk w;
+      w.start(pre, p.context_lens, geo, N, x_begin, x_end);
+      for (int s = 0; w.valid; ++s) {
+        const int cb = s & 1;
+        const bool first = w.k == 0;
+        // P'' and the V operand of chunk s; a new unit's O once the last
+        // unit's rows have been read back
+        if (!rw_wait(BAR(kBarReady + cb), (s >> 1) & 1, abort_s)) break;
+        if (first && w.seg >= 1 && !rw_wait(BAR(kBarOFree), (w.seg - 1) & 1, abort_s)) break;
+        tc_fence_after();
+        const uint64_t bd = smem_desc(vf0 + cb * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
+#pragma unroll
+        for (int kk = 0; kk < kRwTok / 16; ++kk)
+          tc_mma_f16_tmem_a(tmem + kColO, tmem + kColP + 64 * cb + 8 * kk, bd + (2048 >> 4) * kk,
+                            kIdescPV, (first && kk == 0) ? 0u : 1u);
+        tc_commit(BAR(kBarPvDone + cb));
+        last_bar = BAR(kBarPvDone + cb);
+        last_par = (s >> 1) & 1;
+        any = true;
+        w.next(pre, p.context_lens, geo, N);
+      }
+      if (any) mbar_wait_sleep_bounded(last_bar, last_par);
+    }
+  } else if (warp >= kRwSoftWarps && warp < kRwWarpTma) {
     // ------------------------------------------------ V codes -> f16 operand
     // Token t's codes -> f16, MN-major, 128-byte swizzle: dims 64j.. in block j
     // (16 KiB apart), token t at (t/8)*1024 + (t%8)*128, the chunk of dims
@@ -789,9 +791,13 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
         const uint32_t scol = tl + kColS + 128 * sb + copy * RC;
         const uint32_t pcol = tl + kColP + 64 * sb + copy * (RC / 2);
-        // the P buffer of chunk s - 2 is free: this thread issued PV(s - 2)
-        // before QK(s), and the commit that signalled S(s) covers every MMA
-        // issued before it
+        // the P buffer of chunk s - 2 is free once its PV has completed
+        if (s >= 2 && !rw_wait(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) aborted = true;
+        if (__any_sync(0xFFFFFFFFu, aborted)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
         float lchunk = 0.0f;
         // the unit's first chunk sets the references: straight to the redo
         const bool over =
