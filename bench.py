@@ -73,6 +73,9 @@ DESCRIPTIONS = {
                "head_dim 128, block 64, 32 stacked rows per KV head"),
     "longctx": ("long-context split-K: 2 requests x 1,048,576 tokens, 32 q heads / 8 KV heads, "
                 "head_dim 128, block 64"),
+    "prefill": ("chunked prefill: 4 requests, each a 2,048-token chunk at the end of an "
+                "8,192-token context (causal), 32 q heads / 8 KV heads, head_dim 128, block 64, "
+                "log-normal rows"),
     "store": ("prefill store under CUDA graph: 16,384 tokens as strided K/V views of a fused "
               "qkv [16384, 6144], 1% outliers x50, zero rows, permuted int64 slot ids, block 64; "
               "one step stores 8 layers (8 qkv tensors into 8 caches, one launch each)"),
@@ -85,6 +88,7 @@ DESCRIPTIONS = {
 }
 
 DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "verify": 1500, "longctx": 1500, "store": 5000,
+                 "prefill": 300,
                  "index": 3000, "scores": 1500}
 
 
@@ -152,6 +156,19 @@ def measured_peaks():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor TFLOP/s measured on this machine (sustained: the kernels
+    run inside a long loop of steps), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -294,8 +311,10 @@ class DeviceWorkload:
         self.balanced = self.P_arg == 0 and self._balanced_mode()
         # more than 8 stacked rows per KV head, partition left to the library:
         # the rows-on-M tensor-core kernel, which merges its pieces itself
-        self.rows_kernel = (self.P_arg == 0 and R * w.group > 8 and w.block_size >= 16
-                            and H % 4 == 0 and w.num_requests <= 1024)
+        rows = R * w.group
+        self.rows_kernel = (self.P_arg == 0 and rows > 8 and rows <= 8192
+                            and not (rows <= 32 and w.block_size <= 128)
+                            and w.block_size >= 16 and H % 4 == 0 and w.num_requests <= 1024)
         need = kvq.paged_decode_workspace_size(w.num_requests, R, w.num_q_heads, H, D,
                                                w.block_size, self.max_ctx, self.P_arg)
         self.ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
@@ -445,6 +464,17 @@ class DeviceWorkload:
         bt = sum((int(L) + w.block_size - 1) // w.block_size for L in self.lens) * 4
         return tok * H * 2 * (D + 4) + 2 * self.q.numel() * 2 + bt + 4 * w.num_requests
 
+    def attn_flops(self):
+        """Useful flops of the attention: 2 D for q.k and 2 D for p v per
+        (query row, query head, token it sees)."""
+        if self.name == "store":
+            return 0
+        w = self.w
+        R, D = w.rows_per_request, w.head_dim
+        seen = sum(sum(max(0, min(int(L), int(L) - R + 1 + i)) for i in range(R))
+                   for L in self.lens)
+        return seen * w.num_q_heads * 4 * D
+
     def rows_quantized(self):
         return self.store_launches * self.new_k.shape[0] * self.w.num_kv_heads * 2
 
@@ -456,7 +486,7 @@ class DeviceWorkload:
 # the GPU arm
 
 # the other configurations the default (decode) run also times, with their steps
-PER_CONFIG_STEPS = {"store": 600, "verify": 200, "longctx": 300}
+PER_CONFIG_STEPS = {"store": 600, "verify": 200, "longctx": 300, "prefill": 100}
 
 
 def run_kvq(args, rank, local, world):
@@ -635,18 +665,38 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         res["kernels_us"]["quantize_scatter_note"] = (
             f"per launch: the {wl.layers}-launch graph replay divided by {wl.layers}")
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    res["roofline"] = {
-        "kernel": dom_name,
-        "bound": "hbm",
-        "achieved": round(achieved, 2),
-        "peak": peak,
-        "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                        else "fallback 6.8 TB/s"),
-        "unit": "GB/s",
-        "frac": round(achieved / peak, 4),
-        "algorithmic_bytes_per_launch": dom_bytes,
-        "traffic": ncu_traffic(dom_name, args.workload, dom_src),
-    }
+    if args.workload == "prefill":
+        # compute-bound: many rows share each KV byte.  q.k runs as two e4m3
+        # pieces at twice the bf16 rate, p v on f16 at the bf16 rate, so the
+        # useful flops at the bf16 peak take the time of the executed ones
+        tpeak, tsrc = measured_tensor_peak()
+        flops = wl.attn_flops()
+        tf = flops / (dom_ms * 1e-3) / 1e12
+        res["attn_tflops"] = round(tf, 2)
+        res["roofline"] = {
+            "kernel": dom_name, "bound": "tensor", "achieved": round(tf, 2), "peak": tpeak,
+            "peak_source": ("measured (MEASURED_PEAKS.json bf16_tflops_sustained; the q.k "
+                            "pieces on e4m3 at twice the bf16 rate and p.v on f16 make the "
+                            "useful flops' peak the bf16 one)" if tsrc == "measured"
+                            else "fallback 1.7 PFLOP/s"),
+            "unit": "TFLOP/s", "frac": round(tf / tpeak, 4),
+            "algorithmic_flops_per_launch": flops,
+            "hbm_gbs_of_algorithmic_bytes": round(achieved, 2),
+            "traffic": ncu_traffic(dom_name, args.workload, dom_src),
+        }
+    else:
+        res["roofline"] = {
+            "kernel": dom_name,
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_source": ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                            else "fallback 6.8 TB/s"),
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "traffic": ncu_traffic(dom_name, args.workload, dom_src),
+        }
     if sampler:
         res["clocks"] = sampler.summary(wall0, wall1)
     if not args.profile and not args.no_e2e:

@@ -146,7 +146,7 @@ cudaError_t launch_attn_partials_page(const kvq_cache &c, const AttnShape &s, co
 // then the pieces' partials, two slots per CTA.
 constexpr int32_t kRowsMaxRequests = 1024;
 constexpr int32_t kRowsSwitch = 3;          // chunk charge per unit start
-constexpr int32_t kRowsMaxRows = 4096;      // stacked rows per KV head
+constexpr int32_t kRowsMaxRows = 8192;      // stacked rows per KV head
 int32_t attn_rows_per_tile(int32_t rows);
 bool attn_rows_supported(const kvq_cache &c, const AttnShape &s);
 size_t attn_rows_workspace_bytes(const AttnShape &s, int32_t num_kv_heads);

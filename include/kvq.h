@@ -173,7 +173,7 @@ size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_re
  *                   row i of request r.
  *   rows_per_request R >= 1; the stacked rows per KV head, R * (num_q_heads /
  *                   num_kv_heads), at most 128 with a fixed partition size and
- *                   at most 4096 with partition_tokens 0 (a verify step, a
+ *                   at most 8192 with partition_tokens 0 (a verify step, a
  *                   chunk of prefill: tiles of up to 128 rows each read the
  *                   head's codes once; more than 128 need a cache whose scale
  *                   planes are 16-byte aligned and fewer than 2^31 slots).

@@ -90,7 +90,7 @@ def test_decode_validation_happens_before_launch(lib):
     assert _decode(lib, c, part=100) == INVALID                # not a multiple of 64
     assert _decode(lib, c, sm=float("nan")) == INVALID
     assert _decode(lib, c, R=5, Hq=256, part=64) == UNSUPPORTED   # 160 rows, fixed partitions
-    assert _decode(lib, c, R=200, Hq=256) == UNSUPPORTED       # 6400 rows per KV head
+    assert _decode(lib, c, R=300, Hq=256) == UNSUPPORTED       # 9600 rows per KV head
     assert _decode(lib, _cache(head_dim=256)) == UNSUPPORTED
     assert _decode(lib, _cache(block_size=24)) == UNSUPPORTED  # not a power of two
     assert _decode(lib, _cache(block_size=0)) == INVALID
@@ -103,7 +103,8 @@ def test_decode_validation_happens_before_launch(lib):
 
 
 def test_workspace_size_of_the_rows_split(lib):
-    """More than 8 stacked rows per KV head with partition_tokens 0: one int32
+    """More than 32 stacked rows per KV head (or 9..32 on pages of more than 128
+    tokens) with partition_tokens 0: one int32
     ticket per (request, KV head, 128-row tile), rounded to 256 bytes, then two
     pieces per SM of rows-per-tile (32, 64 or 128) partial rows of 128 fp32 and
     their (max, denominator) pairs, each part rounded to 256 bytes."""
@@ -114,7 +115,9 @@ def test_workspace_size_of_the_rows_split(lib):
         rc = 32 if rows <= 32 else (64 if rows <= 64 else 128)
         r256 = lambda x: (x + 255) // 256 * 256
         return r256(N * H * T * 4) + r256(sms * 2 * rc * 128 * 4) + r256(sms * 2 * rc * 8)
-    assert lib.kvq_paged_decode_workspace_size(64, 4, 64, 8, 128, 64, 32768, 0) == expect(64, 8, 32)
+    # 9..32 rows on pages of <= 128 tokens keep the partitioned tcgen05 kernel
+    assert lib.kvq_paged_decode_workspace_size(64, 4, 64, 8, 128, 64, 32768, 0) != expect(64, 8, 32)
+    assert lib.kvq_paged_decode_workspace_size(4, 4, 32, 8, 128, 256, 4096, 0) == expect(4, 8, 16)
     assert lib.kvq_paged_decode_workspace_size(3, 3, 48, 4, 128, 16, 500, 0) == expect(3, 4, 36)
     assert lib.kvq_paged_decode_workspace_size(1, 512, 32, 8, 128, 64, 4096, 0) == expect(1, 8, 2048)
 

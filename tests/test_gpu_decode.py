@@ -60,6 +60,8 @@ def test_decode_batch_scaled(partition_tokens):
     (1, 32, 8, 4),     # block size 4: cp.async staging
     (2, 16, 4, 8),     # block size 8: smallest TMA page box
     (4, 64, 8, 128),   # block larger than a 64-token stage
+    (4, 32, 8, 256),   # 16 rows on 256-token pages: the rows-on-M kernel, 32-row tiles
+    (4, 96, 8, 32),    # 48 rows: the rows-on-M kernel, 64-row tiles
 ])
 @pytest.mark.parametrize("partition_tokens", [0, 128])
 def test_verify_shapes(R, Hq, H, bs, partition_tokens):

@@ -23,6 +23,10 @@ projection output, MTP-style verify with 3 draft tokens, a 1M-token context):
              32,768, block size 64; K, V as in ``decode``.          (seed 3)
   longctx    2 requests x 1,048,576 tokens, 32 q heads / 8 KV heads, block size
              64; K, V as in ``decode``; 1 query row per request.    (seed 4)
+  prefill    4 requests, each a chunk of 2,048 new tokens at the end of an
+             8,192-token context (chunked prefill: the chunk's rows attend
+             causally to everything cached before them and to each other), 32 q
+             heads / 8 KV heads, block size 64; K, V as in ``decode``.  (seed 7)
 
 One more workload feeds the stacked index scorer:
 
@@ -76,6 +80,7 @@ WORKLOADS = {
     "store": Workload("store", 2, 0, 1, 32, 8, HEAD_DIM, 64, 0, 0, "normal", store_tokens=16384),
     "verify": Workload("verify", 3, 64, 4, 64, 8, HEAD_DIM, 64, 32768, 32768, "lognormal_rows"),
     "longctx": Workload("longctx", 4, 2, 1, 32, 8, HEAD_DIM, 64, 1 << 20, 1 << 20, "lognormal_rows"),
+    "prefill": Workload("prefill", 7, 4, 2048, 32, 8, HEAD_DIM, 64, 8192, 8192, "lognormal_rows"),
 }
 
 
