@@ -51,8 +51,8 @@ def _oracle_by_head(built, q_bits, R, G, H, sm_scale, lens):
     (256, [256], 8, 4, 64),                 # pure prefill of a 256-token prompt
     (256, [1000, 256, 700], 8, 4, 16),      # chunks after cached contexts, 16-token pages
     (512, [2048, 777], 4, 4, 64),           # 2048 rows per KV head, ragged context
-    (1000, [1500], 2, 8, 32),               # a chunk that is not a multiple of the tile
-    (2048, [2048, 4096], 2, 4, 64),         # 2,048-token chunks: 8,192 rows per KV head
+    (1000, [1500], 4, 8, 32),               # a chunk that is not a multiple of the tile
+    (2048, [2048, 4096], 4, 4, 64),         # 2,048-token chunks: 8,192 rows per KV head
 ])
 def test_prefill_chunks_match_the_oracle(R, lens, H, G, bs):
     w = workloads.scaled(workloads.WORKLOADS["prefill"], num_requests=len(lens),
