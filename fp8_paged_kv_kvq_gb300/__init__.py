@@ -257,9 +257,8 @@ def paged_decode(cache: Cache, q: torch.Tensor, block_tables: torch.Tensor,
                  out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                  err_flags: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """kvq_paged_decode: paged GQA decode / verify attention; returns ``out``
-    (bf16, shape of q).  ``workspace`` (uint8, >= paged_decode_workspace_size,
-    zero-filled before its first use; the library leaves it ready for reuse)
-    is allocated here, zeroed, by PyTorch, when not given."""
+    (bf16, shape of q).  ``workspace`` (uint8, >= paged_decode_workspace_size;
+    no initialisation needed) is allocated here, by PyTorch, when not given."""
     N, Hq, mb = _decode_args(cache, q, block_tables, context_lens, rows_per_request)
     if out is None:
         out = torch.empty_like(q)
@@ -267,7 +266,7 @@ def paged_decode(cache: Cache, q: torch.Tensor, block_tables: torch.Tensor,
         need = paged_decode_workspace_size(N, rows_per_request, Hq, cache.num_kv_heads,
                                            cache.head_dim, cache.block_size, max_context_len,
                                            partition_tokens)
-        workspace = torch.zeros(max(need, 1), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = cache.struct()
     _check(load().kvq_paged_decode(ctypes.byref(st), _ptr(q), N, rows_per_request, Hq,
                                    _ptr(block_tables), mb, _ptr(context_lens), max_context_len,

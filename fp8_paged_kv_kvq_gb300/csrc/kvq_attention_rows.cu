@@ -18,7 +18,7 @@
 //    are split into equal contiguous ranges over a persistent grid of one CTA
 //    per SM, so every CTA streams the same bytes whatever the lengths.  A
 //    unit cut by a range boundary is finished by the CTA whose piece lands
-//    last (an atomic ticket per unit), which merges the pieces' (max,
+//    last (a tagged ticket per unit), which merges the pieces' (max,
 //    denominator, output) from the workspace; no second launch.
 //  * The stacked rows fill the 128 TMEM lanes.  With RC rows per tile (32, 64
 //    or 128) the tile is replicated 128 / RC times on M; copy c takes the
@@ -128,7 +128,8 @@ struct RwParams {
   float qk_scale;            // sm_scale * log2(e)
   float *o_part;             // [grid][2][rows per tile][128]
   float2 *ml_part;           // [grid][2][rows per tile]
-  int32_t *tickets;          // [N * H * T], zero between calls
+  unsigned long long *tickets;  // [N * H * T]: (call tag, pieces landed)
+  uint32_t tag;              // this call's tag (nonzero)
   int32_t *err_flags;
 };
 
@@ -912,9 +913,11 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         const int b_last = static_cast<int>((sg.first + sg.C - 1) / B);
         const int64_t unit = (static_cast<int64_t>(r) * p.H + h) * p.T + sg.t;
         if (tid == 0) {
-          const int old = atomicAdd(p.tickets + unit, 1);
-          *ticket_s = (old == b_last - b_first) ? 1 : 0;
-          if (old == b_last - b_first) p.tickets[unit] = 0;     // ready for the next call
+          const uint32_t landed = ticket_take(p.tickets + unit, p.tag);
+          const bool last = landed == static_cast<uint32_t>(b_last - b_first + 1);
+          *ticket_s = last ? 1 : 0;
+          if (last) p.tickets[unit] = 0ull;
+          if (landed == 0u && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
           __threadfence();
         }
         soft_barrier();
@@ -995,7 +998,7 @@ size_t attn_rows_workspace_bytes(const AttnShape &s, int32_t num_kv_heads) {
   const int64_t units = static_cast<int64_t>(s.num_requests) * num_kv_heads * T;
   const int64_t rc = attn_rows_per_tile(s.rows);
   const int64_t grid = s.sms > 0 ? s.sms : 152;
-  const size_t tickets = (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
+  const size_t tickets = (static_cast<size_t>(units) * 8 + 255) / 256 * 256;
   const size_t o = static_cast<size_t>(grid) * 2 * rc * kHeadDim * sizeof(float);
   const size_t ml = static_cast<size_t>(grid) * 2 * rc * sizeof(float2);
   return tickets + (o + 255) / 256 * 256 + (ml + 255) / 256 * 256;
@@ -1028,8 +1031,9 @@ cudaError_t launch_attn_rows(const kvq_cache &c, const AttnShape &s, const void 
   const int rc = attn_rows_per_tile(s.rows);
   const int grid = s.sms > 0 ? s.sms : 152;
   char *ws = static_cast<char *>(workspace);
-  p.tickets = reinterpret_cast<int32_t *>(ws);
-  ws += (static_cast<size_t>(units) * 4 + 255) / 256 * 256;
+  p.tickets = reinterpret_cast<unsigned long long *>(ws);
+  p.tag = next_call_tag();
+  ws += (static_cast<size_t>(units) * 8 + 255) / 256 * 256;
   p.o_part = reinterpret_cast<float *>(ws);
   ws += (static_cast<size_t>(grid) * 2 * rc * kHeadDim * sizeof(float) + 255) / 256 * 256;
   p.ml_part = reinterpret_cast<float2 *>(ws);

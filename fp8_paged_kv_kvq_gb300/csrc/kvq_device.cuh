@@ -289,6 +289,26 @@ __device__ __forceinline__ void allow_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// Piece counter of a unit of work cut into pieces by CTA range boundaries.
+// The 64-bit word holds (call tag << 32) | pieces landed; a piece that finds
+// another call's tag -- or whatever the workspace held before -- starts the
+// count for this call, so the word needs no initialisation.  Returns the
+// pieces landed including this one (0 if the word could not be claimed).  The
+// piece that completes the count resets the word to 0, so a graph replay that
+// reuses the tag starts from zero too.
+__device__ __forceinline__ uint32_t ticket_take(unsigned long long *t, uint32_t tag) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long *>(t);
+  for (int i = 0; i < 4096; ++i) {
+    const unsigned long long want = (static_cast<uint32_t>(cur >> 32) == tag)
+                                        ? cur + 1ull
+                                        : ((static_cast<unsigned long long>(tag) << 32) | 1ull);
+    const unsigned long long prev = atomicCAS(t, cur, want);
+    if (prev == cur) return static_cast<uint32_t>(want & 0xFFFFFFFFull);
+    cur = prev;
+  }
+  return 0u;
+}
+
 // Makes barrier initialisation visible to the copy engine.
 __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");

@@ -55,9 +55,13 @@ struct AttnShape {
   int32_t num_kv_heads;
 };
 
-// The load-balanced decode kernel's layout: a plan ([0] chunks per CTA, [1]
-// requests, [2 ..] per-request chunk prefix) then partials in kStreamSlots
-// slots per output row.
+// A nonzero tag per launch of a kernel that counts pieces with tagged
+// tickets (ticket_take): a ticket word left by another call, or any other
+// content of the workspace, carries another tag and is restarted.
+uint32_t next_call_tag();
+
+// The load-balanced decode kernel's workspace: a ticket per (request, group
+// of 4 KV heads), then partials in kStreamSlots slots per output row.
 constexpr int32_t kStreamSlots = 16;
 // A segment (the chunks of one request and head group) is charged this many
 // extra chunks at its start, so a CTA whose range crosses into a new segment
@@ -65,7 +69,7 @@ constexpr int32_t kStreamSlots = 16;
 // correspondingly less work.
 constexpr int32_t kStreamSwitchChunks = 3;
 constexpr int32_t kStreamMaxRequests = 1024;
-size_t attn_stream_plan_bytes(int32_t num_requests);
+size_t attn_stream_ticket_bytes(int32_t num_requests, int32_t num_kv_heads);
 
 // Whether a shape suits the load-balanced kernel (apart from the cache's
 // scale alignment): at most 8 stacked rows, pages of >= 16 tokens, KV heads in
@@ -77,8 +81,6 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
                                         const int32_t *context_lens, float sm_scale, void *out,
                                         void *workspace, int32_t *err_flags,
                                         cudaStream_t stream);
-cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
-                                       cudaStream_t stream);
 
 // Workspace carve-up: partial outputs [rows_total][num_partitions][128] fp32,
 // then (max, denominator) pairs [rows_total][num_partitions][2] fp32.
@@ -142,8 +144,8 @@ cudaError_t launch_attn_partials_page(const kvq_cache &c, const AttnShape &s, co
 // The rows-on-M tcgen05 kernel for more than 8 stacked rows per KV head
 // (verify, chunked prefill): a persistent grid of one CTA per SM over the
 // batch's 128-token chunks, units cut by a range boundary merged by their last
-// piece.  Its workspace: a zeroed ticket per (request, KV head, 128-row tile),
-// then the pieces' partials, two slots per CTA.
+// piece.  Its workspace: a ticket per (request, KV head, 128-row tile), then
+// the pieces' partials, two slots per CTA.
 constexpr int32_t kRowsMaxRequests = 1024;
 constexpr int32_t kRowsSwitch = 3;          // chunk charge per unit start
 constexpr int32_t kRowsMaxRows = 8192;      // stacked rows per KV head

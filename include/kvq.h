@@ -156,10 +156,11 @@ int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t rows_per
  * fits one partition).  With fixed partitions: num_requests*rows_per_request*
  * num_q_heads * ceil(max_context_len / partition) * (head_dim + 2) * 4, each
  * of the two parts rounded up to 256.  With partition_tokens 0 the library's
- * own split decides (see kvq_paged_decode_partition_tokens); for more than 8
- * stacked rows per KV head that is one int32 counter per (request, KV head,
- * 128-row tile) plus two pieces of partial results per SM.  Returns 0 for
- * invalid arguments. */
+ * own split decides (see kvq_paged_decode_partition_tokens): for <= 8 stacked
+ * rows per KV head one 64-bit counter per (request, group of 4 KV heads) plus
+ * 16 pieces of partial results per output row; for the rows-on-M kernel one
+ * 64-bit counter per (request, KV head, 128-row tile) plus two pieces of
+ * partial results per SM.  Returns 0 for invalid arguments. */
 size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,
                                        int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size,
@@ -189,13 +190,10 @@ size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_re
  *                   [64, 1<<20]; 0 = kvq_paged_decode_partition_tokens()
  *   out             device bf16, same shape as q (written, round-to-nearest)
  *   workspace       device, >= kvq_paged_decode_workspace_size(...) bytes
- *                   (may be NULL when that size is 0), zero-filled before its
- *                   first use (e.g. one cudaMemset after allocating it).  The
- *                   load-balanced split for more than 8 stacked rows keeps
- *                   per-unit counters in it that each call returns to zero, so
- *                   a workspace stays reusable without clearing -- unless a
- *                   call sets KVQ_ERRF_WAIT_TIMEOUT, after which it must be
- *                   zero-filled again.
+ *                   (may be NULL when that size is 0); needs no
+ *                   initialisation.  The library's own split keeps per-unit
+ *                   piece counters in it, tagged with the call that writes
+ *                   them, so whatever the buffer held before is ignored.
  *   err_flags       device int32, optional
  * Calls that share a workspace must not run concurrently. */
 kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q,
@@ -245,13 +243,11 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
  *    device, with that device current) and caches it; make that first call
  *    before any stream capture on the device.
  *  - All calls share the one array and it keeps the last call's contents.
- *    The array starts zero-filled when the library loads, and every call
- *    leaves the counters the load-balanced split keeps in it back at zero (a
- *    call that sets KVQ_ERRF_WAIT_TIMEOUT may not; the array cannot be cleared
- *    from outside, so decode on such a device afterwards through
- *    kvq_paged_decode).  Calls that overlap on the GPU (on different streams,
- *    or from several host threads) race on the array and give wrong results;
- *    order them on one stream or with events. */
+ *    Nothing in it needs to start at zero: every byte a call reads was
+ *    written by the same call, and its piece counters carry the call's tag.
+ *    Calls that overlap on the GPU (on different streams, or from several
+ *    host threads) race on the array and give wrong results; order them on
+ *    one stream or with events. */
 kvq_status kvq_paged_decode_noalloc(const kvq_cache *cache, const void *q,
                                     int32_t num_requests, int32_t rows_per_request,
                                     int32_t num_q_heads, const int32_t *block_tables,

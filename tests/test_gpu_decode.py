@@ -463,3 +463,50 @@ def test_query_split_error_bound(R, G):
         print(f"split R={R} G={G} tiny={tiny}: worst err / bound {worst:.3f}, "
               f"max err {err.max():.3e}, score bound {ds:.3e}")
         assert worst <= 1.0, (tiny, worst)
+
+
+@pytest.mark.parametrize("R,Hq,H,bs,lens", [
+    (1, 32, 8, 16, [5000, 300, 0, 2000]),      # the load-balanced decode kernel, cut groups
+    (4, 128, 8, 64, [3000, 900]),              # 64 rows: the rows-on-M kernel, cut units
+])
+def test_workspace_needs_no_initialisation(R, Hq, H, bs, lens):
+    """The library's own split counts a cut unit's pieces in tagged words in
+    the workspace: a workspace full of arbitrary bytes (here 0xA5 and random)
+    and calls in a row on it, also from a captured CUDA graph replayed three
+    times, all give the oracle's result."""
+    w = workloads.scaled(workloads.WORKLOADS["verify"], num_requests=len(lens), rows_per_request=R,
+                         num_q_heads=Hq, num_kv_heads=H, block_size=bs)
+    lens = np.array(lens, dtype=np.int32)
+    built = build_paged(w, lens)
+    q = _queries(w, len(lens), R, 21)
+    ref, _ = oracle_decode(built, q, R, Hq, w.sm_scale)
+    bt = torch.from_numpy(built["bt"]).cuda()
+    cl = torch.from_numpy(lens).cuda()
+    maxc = int(lens.max())
+    need = kvq.paged_decode_workspace_size(len(lens), R, Hq, H, 128, bs, maxc, 0)
+    assert need > 0
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for fill in ("a5", "random"):
+        ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda") if fill == "a5" else \
+            torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=g)
+        for call in range(2):
+            out = kvq.paged_decode(built["cache"], q.cuda(), bt, cl, maxc, w.sm_scale,
+                                   rows_per_request=R, workspace=ws)
+            torch.cuda.synchronize()
+            assert_attention_close(out, ref, f"workspace {fill}, call {call}")
+    qd = q.cuda()
+    out = torch.empty_like(qd)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        kvq.paged_decode(built["cache"], qd, bt, cl, maxc, w.sm_scale, rows_per_request=R,
+                         out=out, workspace=ws)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        kvq.paged_decode(built["cache"], qd, bt, cl, maxc, w.sm_scale, rows_per_request=R,
+                         out=out, workspace=ws)
+    for rep in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_attention_close(out, ref, f"graph replay {rep}")
