@@ -185,7 +185,7 @@ size_t workspace_for(const kvq::AttnShape &s) {
   const int64_t rows_total =
       static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
   if (s.stream)
-    return kvq::attn_stream_ticket_bytes(s.num_requests, s.num_kv_heads) +
+    return kvq::attn_stream_plan_bytes(s.num_requests) +
            kvq::attn_workspace_bytes(rows_total, kvq::kStreamSlots);
   return kvq::attn_workspace_bytes(rows_total, s.num_partitions);
 }
@@ -314,7 +314,7 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
   kvq_status st = make_shape(cache, num_requests, rows_per_request, num_q_heads,
                              max_blocks_per_req, max_context_len, partition_tokens, &s);
   if (st != KVQ_OK) return st;
-  if (num_requests == 0 || s.rows_kernel || s.stream || s.num_partitions <= 1) return KVQ_OK;
+  if (num_requests == 0 || s.rows_kernel || s.num_partitions <= 1) return KVQ_OK;
   if (out == nullptr || context_lens == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned(out, 16) || !aligned(context_lens, 4) || !aligned(workspace, 16))
     return KVQ_ERR_MISALIGNED;

@@ -1077,7 +1077,7 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
 cudaError_t launch_attn_combine(const AttnShape &s, const int32_t *context_lens, void *out,
                                 void *workspace, cudaStream_t stream) {
   if (s.rows_kernel) return cudaSuccess;       // pieces merged by the partials kernel
-  if (s.stream) return cudaSuccess;            // pieces merged by the partials kernel
+  if (s.stream) return launch_attn_combine_stream(s, out, workspace, stream);
   if (s.num_partitions <= 1) return cudaSuccess;
   CombineParams p;
   p.context_lens = context_lens;

@@ -27,11 +27,9 @@
 //    runs the chunks and writes either the final row (a segment that is the
 //    whole request) or its (max, denominator, output) to partial slot
 //    b - first CTA of the (request, group).
-//  * A (request, head group) cut into pieces is finished by the CTA whose
-//    piece lands last (a tagged ticket per group in the workspace): its head
-//    warps merge the pieces' (max, denominator, output) with a running
-//    log-sum-exp and write the rows -- no second launch.  Requests with no
-//    cached token get zero rows.
+//  * CTA 0 writes B and the per-request chunk prefix into the workspace; the
+//    combine kernel (one warp per output row) reads them to find each row's
+//    slots.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -80,8 +78,7 @@ struct StParams {
   int32_t cmax;               // ceil(max context / 16)
   float *o_part;              // [rows][kStreamSlots][128]
   float2 *ml_part;            // [rows][kStreamSlots]
-  unsigned long long *tickets;  // [N][H / 4]: (call tag, pieces landed)
-  uint32_t tag;               // this call's tag (nonzero)
+  int32_t *plan;              // [0] B, [1] N, [2 ..] chunk prefix [N + 1]
   int32_t *err_flags;
 };
 
@@ -99,16 +96,6 @@ __device__ __forceinline__ bool st_wait(uint32_t bar, uint32_t parity, volatile 
   }
   *abort = 1;
   return false;
-}
-
-// Barrier over the four head warps that also ORs a flag across them.
-__device__ __forceinline__ bool heads_barrier_or(bool flag) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r) : "r"(flag ? 1u : 0u), "n"(kStHeads * 32) : "memory");
-  return r != 0;
 }
 
 // In the work sequence a segment (request r, head group g) spans
@@ -172,7 +159,6 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffStBar);
   uint64_t *empty = full + kStStages;
   volatile int *abort_s = reinterpret_cast<volatile int *>(smem + kOffStAbort);
-  volatile int *merge_s = abort_s + 1;
   float *row_exp = reinterpret_cast<float *>(smem + kOffStRowExp);
 
   // The launch overlaps the previous kernel's drain; every global access
@@ -223,12 +209,12 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   B = B > 0 ? B : 1;
   const int64_t x_begin = static_cast<int64_t>(blockIdx.x) * B;
   const int64_t x_end = total < x_begin + B ? total : x_begin + B;
-  // requests with no cached token get zero rows (spread over the grid)
-  for (int r = blockIdx.x; r < N; r += gridDim.x) {
-    if (pre[r + 1] != pre[r]) continue;
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out + static_cast<int64_t>(r) * p.R * p.Hq * kHeadDim);
-    for (int i = tid; i < p.R * p.Hq * (kHeadDim / 8); i += kStThreads)
-      dst[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (blockIdx.x == 0) {
+    if (tid == 0) {
+      p.plan[0] = static_cast<int32_t>(B);
+      p.plan[1] = N;
+    }
+    for (int i = tid; i <= N; i += kStThreads) p.plan[2 + i] = pre[i];
   }
   if (x_begin >= x_end) return;
 
@@ -567,8 +553,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
     }
-    // the four head warps agree on a time-out before any of them writes
-    timed_out = heads_barrier_or(timed_out);
+    timed_out = __any_sync(0xFFFFFFFFu, timed_out);
     if (timed_out) break;
 
     // ---- the segment's (max, denominator, O) for this head's rows
@@ -607,74 +592,86 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         if (g8 == 0) p.ml_part[sl] = make_float2(m_run[e], l_run[e]);
       }
     }
-    if (!direct) {
-      // a piece of the (request, head group): the CTA whose piece lands last
-      // merges every piece of the group's rows (running log-sum-exp, one warp
-      // per KV head, lane per 4 dims) -- no second launch
-      __threadfence();
-      named_barrier(1, kStHeads * 32);
-      const int n_pieces = static_cast<int>((sg.base + sg.C - 1) / B - sg.base / B) + 1;
-      unsigned long long *ticket = p.tickets + static_cast<int64_t>(r) * hg + sg.g;
-      int last = 0;
-      if (w == 0 && lane == 0) {
-        const uint32_t landed = ticket_take(ticket, p.tag);
-        last = (landed == static_cast<uint32_t>(n_pieces)) ? 1 : 0;
-        if (last) *ticket = 0ull;
-        if (landed == 0u && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
-        __threadfence();
-        *merge_s = last;
-      }
-      named_barrier(1, kStHeads * 32);
-      last = *merge_s;
-      if (last) {
-        for (int m = 0; m < p.M; ++m) {
-          const int i = m / p.G, gq = m - i * p.G;
-          const int64_t orow = (static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq;
-          const float2 *ml = p.ml_part + orow * kStreamSlots;
-          const float4 *op =
-              reinterpret_cast<const float4 *>(p.o_part + orow * kStreamSlots * kHeadDim) + lane;
-          float m_w = -INFINITY, lsum = 0.0f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int q0 = 0; q0 < n_pieces; q0 += 8) {      // eight pieces per round trip
-            float2 v[8];
-            float4 o4[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              v[k] = make_float2(-INFINITY, 0.0f);
-              o4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (q0 + k < n_pieces) {
-                v[k] = __ldcg(ml + q0 + k);
-                o4[k] = __ldcg(op + static_cast<int64_t>(q0 + k) * (kHeadDim / 4));
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              if (v[k].x == -INFINITY) continue;      // a piece that saw no visible token
-              const float mn = fmaxf(m_w, v[k].x);
-              const float a = st_ex2(m_w - mn), bb = st_ex2(v[k].x - mn);
-              lsum = lsum * a + v[k].y * bb;
-              acc.x = acc.x * a + o4[k].x * bb;
-              acc.y = acc.y * a + o4[k].y * bb;
-              acc.z = acc.z * a + o4[k].z * bb;
-              acc.w = acc.w * a + o4[k].w * bb;
-              m_w = mn;
-            }
-          }
-          const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-          *reinterpret_cast<uint2 *>(p.out + orow * kHeadDim + 4 * lane) =
-              make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-        }
-      }
-    }
     x = sg.next;
   }
   if (timed_out && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// Combine for the stream layout: one warp per output row, eight rows per CTA.
+struct StCombineParams {
+  int32_t R, Hq, G, H;
+  int64_t rows_total;
+  const int32_t *plan;
+  const float *o_part;
+  const float2 *ml_part;
+  uint16_t *out;
+};
+
+constexpr int kStCombineRows = 8;
+
+__global__ void __launch_bounds__(kStCombineRows * 32)
+attn_combine_stream_kernel(const StCombineParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kStCombineRows + (threadIdx.x >> 5);
+  allow_dependents_launch();
+  if (row >= p.rows_total) return;
+  grid_dependency_wait();              // the plan and the partials (any global read)
+  const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
+  const int qh = static_cast<int>(row % p.Hq);
+  const int g = (qh / p.G) / kStHeads;
+  const int64_t B = p.plan[0];
+  const int32_t *pre = p.plan + 2;
+  const int V = pre[r + 1] - pre[r];
+  uint2 packed = make_uint2(0u, 0u);
+  if (V > 0) {
+    const int C = V - kStreamSwitchChunks;
+    const int64_t base = static_cast<int64_t>(p.H / kStHeads) * pre[r] +
+                         static_cast<int64_t>(g) * V + kStreamSwitchChunks;
+    const int n = static_cast<int>((base + C - 1) / B - base / B) + 1;
+    if (n <= 1) return;                // written by the partials kernel
+    const float2 *ml = p.ml_part + row * kStreamSlots;
+    const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * kStreamSlots * kHeadDim) +
+                       lane;
+    float m_w = -INFINITY, lsum = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < n; q0 += 8) {      // eight pieces per memory round trip
+      float2 v[8];
+      float4 o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[k] = make_float2(-INFINITY, 0.0f);
+        o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q0 + k < n) {
+          v[k] = ml[q0 + k];
+          o[k] = op[static_cast<int64_t>(q0 + k) * (kHeadDim / 4)];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (v[k].x == -INFINITY) continue;        // a piece that saw no visible token
+        const float mn = fmaxf(m_w, v[k].x);
+        const float a = st_ex2(m_w - mn), b = st_ex2(v[k].x - mn);
+        lsum = lsum * a + v[k].y * b;
+        acc.x = acc.x * a + o[k].x * b;
+        acc.y = acc.y * a + o[k].y * b;
+        acc.z = acc.z * a + o[k].z * b;
+        acc.w = acc.w * a + o[k].w * b;
+        m_w = mn;
+      }
+    }
+    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  }
+  // a request with no cached token gets a zero row
+  *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
+}
+
 }  // namespace
 
-size_t attn_stream_ticket_bytes(int32_t num_requests, int32_t num_kv_heads) {
-  return (static_cast<size_t>(num_requests) * (num_kv_heads / kStHeads) * 8 + 255) / 256 * 256;
+size_t attn_stream_plan_bytes(int32_t num_requests) {
+  return (static_cast<size_t>(num_requests + 3) * 4 + 255) / 256 * 256;
 }
 
 bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s) {
@@ -717,10 +714,8 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
   p.M = s.rows;
   p.qk_scale = sm_scale * 1.4426950408889634f;
   p.cmax = static_cast<int32_t>((static_cast<int64_t>(p.ctx_limit) + kChunk - 1) / kChunk);
-  p.tickets = static_cast<unsigned long long *>(workspace);
-  p.tag = next_call_tag();
-  char *parts = static_cast<char *>(workspace) +
-                attn_stream_ticket_bytes(s.num_requests, c.num_kv_heads);
+  p.plan = static_cast<int32_t *>(workspace);
+  char *parts = static_cast<char *>(workspace) + attn_stream_plan_bytes(s.num_requests);
   const size_t o = static_cast<size_t>(rows_total) * kStreamSlots * kHeadDim * sizeof(float);
   p.o_part = reinterpret_cast<float *>(parts);
   p.ml_part = reinterpret_cast<float2 *>(parts + (o + 255) / 256 * 256);
@@ -746,6 +741,25 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
   const int grid = 3 * (s.sms > 0 ? s.sms : 152);
   return launch_overlapped(attn_stream_kernel, dim3(grid), dim3(kStThreads), kStSmem, stream,
                            p, mk, mv, mks, mvs);
+}
+
+cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
+                                       cudaStream_t stream) {
+  StCombineParams p;
+  p.R = s.rows_per_request;
+  p.Hq = s.num_q_heads;
+  p.G = s.group;
+  p.H = s.num_q_heads / s.group;
+  p.rows_total = static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
+  p.plan = static_cast<const int32_t *>(workspace);
+  const char *parts = static_cast<const char *>(workspace) + attn_stream_plan_bytes(s.num_requests);
+  const size_t o = static_cast<size_t>(p.rows_total) * kStreamSlots * kHeadDim * sizeof(float);
+  p.o_part = reinterpret_cast<const float *>(parts);
+  p.ml_part = reinterpret_cast<const float2 *>(parts + (o + 255) / 256 * 256);
+  p.out = static_cast<uint16_t *>(out);
+  const int64_t ctas = (p.rows_total + kStCombineRows - 1) / kStCombineRows;
+  return launch_overlapped(attn_combine_stream_kernel, dim3(static_cast<unsigned>(ctas)),
+                           dim3(kStCombineRows * 32), 0, stream, p);
 }
 
 }  // namespace kvq

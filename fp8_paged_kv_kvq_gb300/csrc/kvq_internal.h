@@ -60,8 +60,9 @@ struct AttnShape {
 // content of the workspace, carries another tag and is restarted.
 uint32_t next_call_tag();
 
-// The load-balanced decode kernel's workspace: a ticket per (request, group
-// of 4 KV heads), then partials in kStreamSlots slots per output row.
+// The load-balanced decode kernel's layout: a plan ([0] chunks per CTA, [1]
+// requests, [2 ..] per-request chunk prefix) then partials in kStreamSlots
+// slots per output row.
 constexpr int32_t kStreamSlots = 16;
 // A segment (the chunks of one request and head group) is charged this many
 // extra chunks at its start, so a CTA whose range crosses into a new segment
@@ -69,7 +70,7 @@ constexpr int32_t kStreamSlots = 16;
 // correspondingly less work.
 constexpr int32_t kStreamSwitchChunks = 3;
 constexpr int32_t kStreamMaxRequests = 1024;
-size_t attn_stream_ticket_bytes(int32_t num_requests, int32_t num_kv_heads);
+size_t attn_stream_plan_bytes(int32_t num_requests);
 
 // Whether a shape suits the load-balanced kernel (apart from the cache's
 // scale alignment): at most 8 stacked rows, pages of >= 16 tokens, KV heads in
@@ -81,6 +82,8 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
                                         const int32_t *context_lens, float sm_scale, void *out,
                                         void *workspace, int32_t *err_flags,
                                         cudaStream_t stream);
+cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
+                                       cudaStream_t stream);
 
 // Workspace carve-up: partial outputs [rows_total][num_partitions][128] fp32,
 // then (max, denominator) pairs [rows_total][num_partitions][2] fp32.

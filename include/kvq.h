@@ -157,10 +157,10 @@ int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t rows_per
  * num_q_heads * ceil(max_context_len / partition) * (head_dim + 2) * 4, each
  * of the two parts rounded up to 256.  With partition_tokens 0 the library's
  * own split decides (see kvq_paged_decode_partition_tokens): for <= 8 stacked
- * rows per KV head one 64-bit counter per (request, group of 4 KV heads) plus
- * 16 pieces of partial results per output row; for the rows-on-M kernel one
- * 64-bit counter per (request, KV head, 128-row tile) plus two pieces of
- * partial results per SM.  Returns 0 for invalid arguments. */
+ * rows per KV head the split's plan (the request prefix) plus 16 pieces of
+ * partial results per output row; for the rows-on-M kernel one 64-bit
+ * counter per (request, KV head, 128-row tile) plus two pieces of partial
+ * results per SM.  Returns 0 for invalid arguments. */
 size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,
                                        int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size,
@@ -191,9 +191,10 @@ size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_re
  *   out             device bf16, same shape as q (written, round-to-nearest)
  *   workspace       device, >= kvq_paged_decode_workspace_size(...) bytes
  *                   (may be NULL when that size is 0); needs no
- *                   initialisation.  The library's own split keeps per-unit
- *                   piece counters in it, tagged with the call that writes
- *                   them, so whatever the buffer held before is ignored.
+ *                   initialisation: every byte a call reads was written by
+ *                   the same call, and the piece counters of the rows-on-M
+ *                   kernel carry the tag of the call that wrote them, so
+ *                   whatever the buffer held before is ignored.
  *   err_flags       device int32, optional
  * Calls that share a workspace must not run concurrently. */
 kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q,

@@ -466,14 +466,15 @@ def test_query_split_error_bound(R, G):
 
 
 @pytest.mark.parametrize("R,Hq,H,bs,lens", [
-    (1, 32, 8, 16, [5000, 300, 0, 2000]),      # the load-balanced decode kernel, cut groups
+    (1, 32, 8, 16, [5000, 300, 0, 2000]),      # the load-balanced decode kernel and its combine
     (4, 128, 8, 64, [3000, 900]),              # 64 rows: the rows-on-M kernel, cut units
 ])
 def test_workspace_needs_no_initialisation(R, Hq, H, bs, lens):
-    """The library's own split counts a cut unit's pieces in tagged words in
-    the workspace: a workspace full of arbitrary bytes (here 0xA5 and random)
-    and calls in a row on it, also from a captured CUDA graph replayed three
-    times, all give the oracle's result."""
+    """A workspace full of arbitrary bytes (here 0xA5 and random) needs no
+    clearing: the load-balanced decode writes its plan every call, and the
+    rows-on-M kernel counts a cut unit's pieces in words tagged with the call.
+    Calls in a row on it, and a captured CUDA graph replayed three times, all
+    give the oracle's result."""
     w = workloads.scaled(workloads.WORKLOADS["verify"], num_requests=len(lens), rows_per_request=R,
                          num_q_heads=Hq, num_kv_heads=H, block_size=bs)
     lens = np.array(lens, dtype=np.int32)
