@@ -31,6 +31,8 @@ __all__ = [
     "IndexCache", "INDEX_FP8", "INDEX_MXFP4", "index_cache_bytes", "index_quantize_scatter",
     "index_dequant_rows",
     "ERRF_SLOT_RANGE", "ERRF_BLOCK_RANGE", "ERRF_CONTEXT_RANGE",
+    "CODES_E4M3", "CODES_E5M2", "quantize_scatter_unscaled", "paged_decode_codes",
+    "paged_decode_codes_workspace_size",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -39,6 +41,9 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "kvq.h")
 
 INDEX_FP8 = 0
 INDEX_MXFP4 = 1
+
+CODES_E4M3 = 0
+CODES_E5M2 = 1
 
 ERRF_SLOT_RANGE = 1
 ERRF_BLOCK_RANGE = 2
@@ -101,6 +106,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
             "kvq_paged_decode_combine": (ctypes.c_int, [CP, i32, i32, i32, i32, P, i32, i32,
                                                         P, P, sz, P]),
             "kvq_dequant_rows": (ctypes.c_int, [CP, P, i64, i32, P, P, P, P]),
+            "kvq_quantize_scatter_unscaled": (ctypes.c_int, [CP, i32, P, i64, P, i64, i64, P,
+                                                             P, P]),
+            "kvq_paged_decode_codes_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+            "kvq_paged_decode_codes": (ctypes.c_int, [CP, i32, P, i32, i32, i32, P, i32, P, i32,
+                                                      ctypes.c_float, P, P, sz, P, P]),
             "kvq_index_cache_bytes": (sz, [i64, i32, i32]),
             "kvq_index_quantize_scatter": (ctypes.c_int, [ctypes.POINTER(_IndexCacheStruct), P,
                                                           i64, i64, P, P, P]),
@@ -301,6 +311,57 @@ def paged_decode_combine(cache: Cache, num_requests: int, rows_per_request: int,
         _ptr(context_lens), max_context_len, partition_tokens, _ptr(out), _ptr(workspace),
         0 if workspace is None else workspace.numel(), _stream(stream)),
         "kvq_paged_decode_combine")
+
+
+def quantize_scatter_unscaled(cache: Cache, k: torch.Tensor, v: torch.Tensor,
+                              slot_ids: torch.Tensor, code_format: int = CODES_E4M3,
+                              err_flags: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_quantize_scatter_unscaled: cast bf16 K/V rows to e4m3 or e5m2 codes
+    with no scale (scale planes set to 1) -- the codec ablation's caches."""
+    H, D = cache.num_kv_heads, cache.head_dim
+    ks = _rows_view(k, H, D, "k")
+    vs = _rows_view(v, H, D, "v")
+    T = k.shape[0]
+    if v.shape[0] != T or slot_ids.numel() != T or slot_ids.dtype != torch.int64:
+        raise ValueError("k, v and slot_ids (int64) must have the same token count")
+    st = cache.struct()
+    _check(load().kvq_quantize_scatter_unscaled(ctypes.byref(st), code_format, _ptr(k), ks,
+                                                _ptr(v), vs, T, _ptr(slot_ids), _ptr(err_flags),
+                                                _stream(stream)),
+           "kvq_quantize_scatter_unscaled")
+
+
+def paged_decode_codes_workspace_size(num_requests: int, rows_per_request: int,
+                                      num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                      block_size: int, max_context_len: int) -> int:
+    return load().kvq_paged_decode_codes_workspace_size(num_requests, rows_per_request,
+                                                        num_q_heads, num_kv_heads, head_dim,
+                                                        block_size, max_context_len)
+
+
+def paged_decode_codes(cache: Cache, code_format: int, q: torch.Tensor,
+                       block_tables: torch.Tensor, context_lens: torch.Tensor,
+                       max_context_len: int, sm_scale: float, rows_per_request: int = 1,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       err_flags: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvq_paged_decode_codes: paged attention over a cache of e4m3 or e5m2
+    codes (the rows-on-M kernel for every shape); returns ``out``."""
+    N, Hq, mb = _decode_args(cache, q, block_tables, context_lens, rows_per_request)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        need = paged_decode_codes_workspace_size(N, rows_per_request, Hq, cache.num_kv_heads,
+                                                 cache.head_dim, cache.block_size,
+                                                 max_context_len)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = cache.struct()
+    _check(load().kvq_paged_decode_codes(ctypes.byref(st), code_format, _ptr(q), N,
+                                         rows_per_request, Hq, _ptr(block_tables), mb,
+                                         _ptr(context_lens), max_context_len, float(sm_scale),
+                                         _ptr(out), _ptr(workspace), workspace.numel(),
+                                         _ptr(err_flags), _stream(stream)),
+           "kvq_paged_decode_codes")
+    return out
 
 
 def dequant_rows(cache: Cache, slot_ids: torch.Tensor, out_dtype=torch.float32,

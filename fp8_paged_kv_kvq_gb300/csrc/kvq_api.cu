@@ -341,6 +341,109 @@ kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q, int32_t num_r
                                   partition_tokens, out, workspace, workspace_bytes, stream);
 }
 
+kvq_status kvq_quantize_scatter_unscaled(const kvq_cache *cache, int32_t code_format,
+                                         const void *k, int64_t k_token_stride, const void *v,
+                                         int64_t v_token_stride, int64_t num_tokens,
+                                         const int64_t *slot_ids, int32_t *err_flags,
+                                         kvq_stream_t stream) {
+  if (code_format != KVQ_CODES_E4M3 && code_format != KVQ_CODES_E5M2)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  kvq_status st = check_cache(cache, false);
+  if (st != KVQ_OK) return st;
+  if (num_tokens < 0 || k_token_stride < 0 || v_token_stride < 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;
+  if (k == nullptr || v == nullptr || slot_ids == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(k, 16) || !aligned(v, 16) || (k_token_stride % 8) != 0 ||
+      (v_token_stride % 8) != 0 || !aligned(slot_ids, 8) || !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  if (num_tokens > (int64_t(1) << 31) / (2 * cache->num_kv_heads) - 32) return KVQ_ERR_UNSUPPORTED;
+  return from_cuda(kvq::launch_quantize_unscaled(*cache, code_format, k, k_token_stride, v,
+                                                 v_token_stride, num_tokens, slot_ids, err_flags,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The shape of a kvq_paged_decode_codes call: the rows-on-M kernel for every
+// row count.
+kvq_status make_codes_shape(const kvq_cache *cache, int32_t num_requests,
+                            int32_t rows_per_request, int32_t num_q_heads,
+                            int32_t max_blocks_per_req, int32_t max_context_len,
+                            kvq::AttnShape *s) {
+  if (cache != nullptr && cache->num_kv_heads > 0 && num_q_heads > 0 && rows_per_request > 0 &&
+      num_q_heads % cache->num_kv_heads == 0 &&
+      static_cast<int64_t>(rows_per_request) * (num_q_heads / cache->num_kv_heads) > kvq::kRowsMaxRows)
+    return KVQ_ERR_UNSUPPORTED;
+  // the common checks (cache, sizes, GQA) as for one query row with a fixed
+  // partition size; then the shape is switched to the rows-on-M kernel
+  if (rows_per_request < 1) return KVQ_ERR_INVALID_ARGUMENT;
+  kvq_status st = make_shape(cache, num_requests, 1, num_q_heads, max_blocks_per_req,
+                             max_context_len, 64, s);
+  if (st != KVQ_OK) return st;
+  if (cache->block_size < 16 || cache->num_kv_heads % 4 != 0 ||
+      num_requests > kvq::kRowsMaxRequests)
+    return KVQ_ERR_UNSUPPORTED;
+  const int64_t M = static_cast<int64_t>(rows_per_request) * s->group;
+  s->rows_per_request = rows_per_request;
+  s->rows = static_cast<int32_t>(M);
+  s->row_groups = static_cast<int32_t>((M + 31) / 32);
+  s->rows_kernel = 1;
+  s->stream = 0;
+  s->num_partitions = 1;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_paged_decode_codes_workspace_size(int32_t num_requests, int32_t rows_per_request,
+                                             int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t block_size,
+                                             int32_t max_context_len) {
+  kvq_cache c{};
+  c.num_slots = 0;
+  c.num_kv_heads = num_kv_heads;
+  c.head_dim = head_dim;
+  c.block_size = block_size;
+  kvq::AttnShape s;
+  if (make_codes_shape(&c, num_requests, rows_per_request, num_q_heads, 1, max_context_len, &s) !=
+      KVQ_OK)
+    return 0;
+  return kvq::attn_rows_workspace_bytes(s, num_kv_heads);
+}
+
+kvq_status kvq_paged_decode_codes(const kvq_cache *cache, int32_t code_format, const void *q,
+                                  int32_t num_requests, int32_t rows_per_request,
+                                  int32_t num_q_heads, const int32_t *block_tables,
+                                  int32_t max_blocks_per_req, const int32_t *context_lens,
+                                  int32_t max_context_len, float sm_scale, void *out,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_flags,
+                                  kvq_stream_t stream) {
+  if (code_format != KVQ_CODES_E4M3 && code_format != KVQ_CODES_E5M2)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  kvq::AttnShape s;
+  kvq_status st = make_codes_shape(cache, num_requests, rows_per_request, num_q_heads,
+                                   max_blocks_per_req, max_context_len, &s);
+  if (st != KVQ_OK) return st;
+  if (!std::isfinite(sm_scale)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_requests == 0) return KVQ_OK;
+  if (q == nullptr || out == nullptr || block_tables == nullptr || context_lens == nullptr)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(block_tables, 4) ||
+      !aligned(context_lens, 4) || !aligned(workspace, 16) || !aligned(err_flags, 4))
+    return KVQ_ERR_MISALIGNED;
+  if (!kvq::attn_rows_supported(*cache, s)) return KVQ_ERR_UNSUPPORTED;
+  const size_t need = kvq::attn_rows_workspace_bytes(s, cache->num_kv_heads);
+  if (workspace == nullptr || workspace_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  return from_cuda(kvq::launch_attn_rows(*cache, s, q, block_tables, context_lens, sm_scale, out,
+                                         workspace, err_flags,
+                                         reinterpret_cast<cudaStream_t>(stream), code_format));
+}
+
 kvq_status kvq_dequant_rows(const kvq_cache *cache, const int64_t *slot_ids, int64_t n,
                             int32_t out_dtype, void *out_k, void *out_v, int32_t *err_flags,
                             kvq_stream_t stream) {

@@ -107,8 +107,11 @@ static_assert(kOffSc % 1024 == 0 && kOffVf % 1024 == 0 && kOffQ % 1024 == 0,
 static_assert(kOffBar % 8 == 0, "barrier alignment");
 static_assert(kRwSmem <= 227 * 1024, "shared memory budget");
 
-// S = Q K^T: M = 128 rows, N = 128 tokens, both operands K-major
+// S = Q K^T: M = 128 rows, N = 128 tokens, both operands K-major; A (the
+// query pieces) e4m3, B (the key codes) e4m3 or, for a cache of e5m2 codes,
+// e5m2 (B format field, bits 10-12: 1)
 constexpr uint32_t kIdescQK = mma_idesc(128, kRwTok, false, false);
+constexpr uint32_t kIdescQK_e5m2 = kIdescQK | (1u << 10);
 // O = P V: M = 128 rows, N = 128 dims, A (TMEM) K-major, B MN-major
 constexpr uint32_t kIdescPV = mma_idesc(128, kHeadDim, false, true);
 
@@ -462,7 +465,15 @@ __device__ __noinline__ void rows_load_q(const QArgs p, int r, int h, int row0, 
   }
 }
 
-template <int RC>
+// Two codes (bytes 0 and 1 of w16) to their exact f16 values: e4m3 through
+// the hardware conversion; e5m2 is the top byte of an f16, so a byte shift.
+template <int kFmt>
+__device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w16) {
+  if (kFmt == KVQ_CODES_E5M2) return prmt(w16, 0u, 0x1404u);
+  return e4m3x2_to_f16x2(w16);
+}
+
+template <int RC, int kFmt>
 __global__ void __launch_bounds__(kRwThreads, 1)
 attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
                  const __grid_constant__ CUtensorMap tm_vc,
@@ -620,6 +631,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
   } else if (warp == kRwWarpMma) {
     // ------------------------------------------------------------ QK^T MMA
     if (lane == 0) {
+      constexpr uint32_t kQK = kFmt == KVQ_CODES_E5M2 ? kIdescQK_e5m2 : kIdescQK;
       const uint32_t q0 = smem_addr(smem + kOffQ);
       uint32_t last_bar = 0, last_par = 0;
       bool any = false;
@@ -638,10 +650,10 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         const uint64_t qb = smem_desc(q0 + kQBytes, 16, 1024, kSmemSwizzle128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_e4m3(tmem + kColS + 128 * sb, qa + 2 * kk, kd + 2 * kk, kIdescQK, kk != 0);
+          tc_mma_e4m3(tmem + kColS + 128 * sb, qa + 2 * kk, kd + 2 * kk, kQK, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_e4m3(tmem + kColS + 128 * sb, qb + 2 * kk, kd + 2 * kk, kIdescQK, 1u);
+          tc_mma_e4m3(tmem + kColS + 128 * sb, qb + 2 * kk, kd + 2 * kk, kQK, 1u);
         tc_commit(BAR(kBarSFull + sb));
         tc_commit(BAR(kBarKvEmpty + b));
         last_bar = BAR(kBarSFull + sb);
@@ -703,10 +715,10 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       for (int c = 0; c < 8; ++c) {
         uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
         if (valid) w4 = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (t & 7)) << 4));
-        const uint4 lo = make_uint4(e4m3x2_to_f16x2(w4.x), e4m3x2_to_f16x2(w4.x >> 16),
-                                    e4m3x2_to_f16x2(w4.y), e4m3x2_to_f16x2(w4.y >> 16));
-        const uint4 hi = make_uint4(e4m3x2_to_f16x2(w4.z), e4m3x2_to_f16x2(w4.z >> 16),
-                                    e4m3x2_to_f16x2(w4.w), e4m3x2_to_f16x2(w4.w >> 16));
+        const uint4 lo = make_uint4(codes2_to_f16x2<kFmt>(w4.x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.x >> 16),
+                                    codes2_to_f16x2<kFmt>(w4.y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.y >> 16));
+        const uint4 hi = make_uint4(codes2_to_f16x2<kFmt>(w4.z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.z >> 16),
+                                    codes2_to_f16x2<kFmt>(w4.w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.w >> 16));
         uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
         const int c0 = (2 * c) & 7;
         *reinterpret_cast<uint4 *>(blk + ((c0 ^ (t & 7)) << 4)) = lo;
@@ -987,7 +999,7 @@ int32_t attn_rows_per_tile(int32_t rows) { return rows <= 32 ? 32 : (rows <= 64 
 
 bool attn_rows_supported(const kvq_cache &c, const AttnShape &s) {
   const int bs = 1 << s.log2_block;
-  return s.rows > 8 && bs >= 16 && c.num_kv_heads % 4 == 0 && c.num_slots > 0 &&
+  return s.rows >= 1 && bs >= 16 && c.num_kv_heads % 4 == 0 && c.num_slots > 0 &&
          c.num_slots < (int64_t(1) << 31) && s.num_requests <= kRowsMaxRequests &&
          (reinterpret_cast<uintptr_t>(c.k_scales) & 15u) == 0 &&
          (reinterpret_cast<uintptr_t>(c.v_scales) & 15u) == 0;
@@ -1007,7 +1019,7 @@ size_t attn_rows_workspace_bytes(const AttnShape &s, int32_t num_kv_heads) {
 cudaError_t launch_attn_rows(const kvq_cache &c, const AttnShape &s, const void *q,
                              const int32_t *block_tables, const int32_t *context_lens,
                              float sm_scale, void *out, void *workspace, int32_t *err_flags,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int32_t code_format) {
   RwParams p;
   p.num_blocks = static_cast<uint32_t>(c.num_slots >> s.log2_block);
   p.H = c.num_kv_heads;
@@ -1044,10 +1056,15 @@ cudaError_t launch_attn_rows(const kvq_cache &c, const AttnShape &s, const void 
       !encode_scale_tensor_map(&mks, c.k_scales, c.num_slots, c.num_kv_heads, p.box) ||
       !encode_scale_tensor_map(&mvs, c.v_scales, c.num_slots, c.num_kv_heads, p.box))
     return cudaErrorInvalidValue;
-  void (*kernel)(RwParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) =
-      rc == 32 ? attn_rows_kernel<32> : (rc == 64 ? attn_rows_kernel<64> : attn_rows_kernel<128>);
-  static std::atomic<uint64_t> configured[3];
-  const int which = rc == 32 ? 0 : (rc == 64 ? 1 : 2);
+  using Kernel = void (*)(RwParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap);
+  const bool e5 = code_format == KVQ_CODES_E5M2;
+  const Kernel kernel =
+      rc == 32 ? (e5 ? attn_rows_kernel<32, KVQ_CODES_E5M2> : attn_rows_kernel<32, KVQ_CODES_E4M3>)
+      : rc == 64 ? (e5 ? attn_rows_kernel<64, KVQ_CODES_E5M2> : attn_rows_kernel<64, KVQ_CODES_E4M3>)
+                 : (e5 ? attn_rows_kernel<128, KVQ_CODES_E5M2>
+                       : attn_rows_kernel<128, KVQ_CODES_E4M3>);
+  static std::atomic<uint64_t> configured[6];
+  const int which = (rc == 32 ? 0 : (rc == 64 ? 1 : 2)) + (e5 ? 3 : 0);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

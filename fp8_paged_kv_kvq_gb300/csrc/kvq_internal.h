@@ -158,7 +158,14 @@ size_t attn_rows_workspace_bytes(const AttnShape &s, int32_t num_kv_heads);
 cudaError_t launch_attn_rows(const kvq_cache &c, const AttnShape &s, const void *q,
                              const int32_t *block_tables, const int32_t *context_lens,
                              float sm_scale, void *out, void *workspace, int32_t *err_flags,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int32_t code_format = KVQ_CODES_E4M3);
+
+// The unscaled store of the codec ablation: codes = e4m3 or e5m2 cast of each
+// value, scales 1.
+cudaError_t launch_quantize_unscaled(const kvq_cache &c, int32_t code_format, const void *k,
+                                     int64_t k_stride, const void *v, int64_t v_stride,
+                                     int64_t num_tokens, const int64_t *slot_ids,
+                                     int32_t *err_flags, cudaStream_t stream);
 
 // The tcgen05 partials kernel for 9..32 stacked rows per KV head.
 bool attn_tc_supported(const kvq_cache &c, const AttnShape &s);

@@ -159,6 +159,65 @@ quantize_scatter_kernel(const QuantParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// The unscaled store of the codec ablation (sgl-project/sglang-jax #1776, design
+// points: an O(1) cache cast to fp8 with no scale): each bf16 value is cast
+// to e4m3 (saturating at 448) or e5m2 (saturating at 57344) with round-to-
+// nearest-even by the hardware conversion, the sign of a zero code taken from
+// its input, and both scale planes are set to 1 so the attention kernels read
+// the codes' own values.  Same row layout and lanes as the scaled store.
+__device__ __forceinline__ uint32_t e5m2x2_rn(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int kFormat>   // KVQ_CODES_E4M3 or KVQ_CODES_E5M2
+__device__ __forceinline__ uint32_t cast4(uint32_t w0, uint32_t w1) {
+  const float q0 = bf16_lo(w0), q1 = bf16_hi(w0), q2 = bf16_lo(w1), q3 = bf16_hi(w1);
+  const uint32_t signs = prmt(w0, w1, 0x7531u) & 0x80808080u;
+  if (kFormat == KVQ_CODES_E5M2) return e5m2x2_rn(q0, q1) | (e5m2x2_rn(q2, q3) << 16) | signs;
+  return e4m3x2_rn(q0, q1) | (e4m3x2_rn(q2, q3) << 16) | signs;
+}
+
+template <int kFormat>
+__global__ void __launch_bounds__(kQuantWarps * 32, 12)
+quantize_unscaled_kernel(const QuantParams p) {
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & (kLanesPerRow - 1);
+  const uint32_t rid = blockIdx.x * (kQuantWarps * kRowsPerWarp) + (threadIdx.x / kLanesPerRow);
+  const int H = p.num_kv_heads;
+  const uint32_t t32 =
+      static_cast<uint32_t>((static_cast<uint64_t>(rid) * p.rows_per_token_magic) >> p.rows_per_token_shift);
+  grid_dependency_wait();
+  allow_dependents_launch();
+  if (t32 >= p.num_tokens) return;
+  const int64_t t = t32;
+  const int rem = static_cast<int>(rid - t32 * static_cast<uint32_t>(2 * H));
+  const bool is_v = rem >= H;
+  const int h = is_v ? rem - H : rem;
+  const uint16_t *src = (is_v ? p.v + t * p.v_stride : p.k + t * p.k_stride) + h * kHeadDim + sub * kPerLane;
+  uint4 a[kVec], b[kVec];
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    a[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k));
+    b[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k + 8));
+  }
+  const int64_t slot = __ldg(p.slot_ids + t);
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (sub == 0 && rem == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
+    return;
+  }
+  const int64_t row = slot * H + h;
+  uint4 *dst = reinterpret_cast<uint4 *>((is_v ? p.v_codes : p.k_codes) + row * kHeadDim + sub * kPerLane);
+#pragma unroll
+  for (int k = 0; k < kVec; ++k)
+    dst[k] = make_uint4(cast4<kFormat>(a[k].x, a[k].y), cast4<kFormat>(a[k].z, a[k].w),
+                        cast4<kFormat>(b[k].x, b[k].y), cast4<kFormat>(b[k].z, b[k].w));
+  if (sub == 0) (is_v ? p.v_scales : p.k_scales)[row] = 1.0f;
+}
+
+// ---------------------------------------------------------------------------
 struct DequantParams {
   const uint8_t *k_codes;
   const uint8_t *v_codes;
@@ -403,10 +462,11 @@ index_dequant_kernel(const IndexDequantParams p) {
 
 }  // namespace
 
-cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k_stride,
-                                    const void *v, int64_t v_stride, int64_t num_tokens,
-                                    const int64_t *slot_ids, int32_t *err_flags,
-                                    cudaStream_t stream) {
+namespace {
+
+QuantParams quant_params(const kvq_cache &c, const void *k, int64_t k_stride, const void *v,
+                         int64_t v_stride, int64_t num_tokens, const int64_t *slot_ids,
+                         int32_t *err_flags) {
   QuantParams p;
   p.k = static_cast<const uint16_t *>(k);
   p.v = static_cast<const uint16_t *>(v);
@@ -430,10 +490,36 @@ cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k
     p.rows_per_token_shift = 32 + l;
     p.rows_per_token_magic = ((uint64_t(1) << (32 + l)) + d - 1) / d;
   }
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k_stride,
+                                    const void *v, int64_t v_stride, int64_t num_tokens,
+                                    const int64_t *slot_ids, int32_t *err_flags,
+                                    cudaStream_t stream) {
+  const QuantParams p = quant_params(c, k, k_stride, v, v_stride, num_tokens, slot_ids, err_flags);
   const int64_t rows = num_tokens * 2 * c.num_kv_heads;
   const int64_t blocks = (rows + kQuantWarps * kRowsPerWarp - 1) / (kQuantWarps * kRowsPerWarp);
   return launch_overlapped(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks)),
                            dim3(kQuantWarps * 32), 0, stream, p);
+}
+
+cudaError_t launch_quantize_unscaled(const kvq_cache &c, int32_t code_format, const void *k,
+                                     int64_t k_stride, const void *v, int64_t v_stride,
+                                     int64_t num_tokens, const int64_t *slot_ids,
+                                     int32_t *err_flags, cudaStream_t stream) {
+  const QuantParams p = quant_params(c, k, k_stride, v, v_stride, num_tokens, slot_ids, err_flags);
+  const int64_t rows = num_tokens * 2 * c.num_kv_heads;
+  const int64_t blocks = (rows + kQuantWarps * kRowsPerWarp - 1) / (kQuantWarps * kRowsPerWarp);
+  if (code_format == KVQ_CODES_E5M2)
+    return launch_overlapped(quantize_unscaled_kernel<KVQ_CODES_E5M2>,
+                             dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
+                             stream, p);
+  return launch_overlapped(quantize_unscaled_kernel<KVQ_CODES_E4M3>,
+                           dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
+                           stream, p);
 }
 
 cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int64_t n,

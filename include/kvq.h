@@ -257,6 +257,56 @@ kvq_status kvq_paged_decode_noalloc(const kvq_cache *cache, const void *q,
                                     int32_t partition_tokens, void *out, int32_t *err_flags,
                                     kvq_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* The codec ablation.  sgl-project/sglang-jax #1776 "feat(dsa): implement fp8
+ * KV cache (e4m3) with a bf16 indexer cache", design points and accuracy
+ * tests: a cache of O(1) values cast to fp8 with no scale at all, e4m3
+ * preferred to e5m2 for its extra mantissa bit (worst-case relative rounding
+ * error about 6 % against 12.5 %; attention error against a bf16 cache about
+ * twice as large for e5m2).  These two calls store and read such caches, so
+ * the three (per-row-scaled e4m3, unscaled e4m3, unscaled e5m2) can be
+ * compared on the same kernels. */
+#define KVQ_CODES_E4M3 0                 /* 1 sign, 4 exponent (bias 7), 3 mantissa */
+#define KVQ_CODES_E5M2 1                 /* 1 sign, 5 exponent (bias 15), 2 mantissa */
+
+/* Quantize + scatter with no scale: code_d = cast(x_d), round-to-nearest-even,
+ * saturating at the format's largest finite magnitude (448 for e4m3, 57344 for
+ * e5m2; no infinity or NaN code from a finite input), the sign of a zero code
+ * taken from its input.  Both scale planes of every stored row are set to 1, so
+ * kvq_paged_decode_codes (and, for e4m3, kvq_paged_decode and
+ * kvq_dequant_rows) read the codes' own values.  Arguments and errors as for
+ * kvq_quantize_scatter; code_format KVQ_CODES_E4M3 or KVQ_CODES_E5M2, anything
+ * else KVQ_ERR_INVALID_ARGUMENT. */
+kvq_status kvq_quantize_scatter_unscaled(const kvq_cache *cache, int32_t code_format,
+                                         const void *k, int64_t k_token_stride,
+                                         const void *v, int64_t v_token_stride,
+                                         int64_t num_tokens, const int64_t *slot_ids,
+                                         int32_t *err_flags, kvq_stream_t stream);
+
+/* Workspace bytes kvq_paged_decode_codes needs (the rows-on-M split: one
+ * 64-bit counter per (request, KV head, 128-row tile) plus two pieces of
+ * partial results per SM); 0 for invalid arguments. */
+size_t kvq_paged_decode_codes_workspace_size(int32_t num_requests, int32_t rows_per_request,
+                                             int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_dim, int32_t block_size,
+                                             int32_t max_context_len);
+
+/* kvq_paged_decode over a cache whose codes are in `code_format`: scores use
+ * e4m3(kc) or e5m2(kc) times the key scale, values e4m3(vc) or e5m2(vc) times
+ * the value scale (1 for the unscaled caches).  Always the rows-on-M
+ * tensor-core kernel (1 to 8192 stacked rows per KV head), so both formats run
+ * the same code; it needs KV heads in groups of 4, pages of >= 16 tokens,
+ * 16-byte aligned scale planes and fewer than 2^31 slots (else
+ * KVQ_ERR_UNSUPPORTED).  Other arguments as for kvq_paged_decode with
+ * partition_tokens 0; the workspace needs no initialisation. */
+kvq_status kvq_paged_decode_codes(const kvq_cache *cache, int32_t code_format, const void *q,
+                                  int32_t num_requests, int32_t rows_per_request,
+                                  int32_t num_q_heads, const int32_t *block_tables,
+                                  int32_t max_blocks_per_req, const int32_t *context_lens,
+                                  int32_t max_context_len, float sm_scale, void *out,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_flags,
+                                  kvq_stream_t stream);
+
 /* Dequantise whole rows back to real values: out = fl32(e4m3(c) * scale), one
  * IEEE multiply, or that value rounded once more to bf16 (nearest-even).
  * sglang-jax #1776 "feat(dsa): implement fp8 KV cache (e4m3) with a bf16
