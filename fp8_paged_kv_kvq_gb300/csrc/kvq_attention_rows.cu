@@ -69,9 +69,15 @@ constexpr int kRwMaxPagesPerChunk = 8;       // block size >= 16
 constexpr float kRwLazy = 14.0f;             // log2 of the largest unnormalised p
 constexpr float kRwOvershoot = 4.0f;         // a moved reference sits this far above the max
 
-constexpr uint32_t kColS = 0;                // S buffer b: columns 128 b .. 128 b + 127
-constexpr uint32_t kColO = 256;              // O: 256 .. 383
-constexpr uint32_t kColP = 384;              // P buffer b (f16 pairs): 384 + 64 b .. + 63
+// TMEM: S buffer b at columns 128 b .. 128 b + 127; once the softmax has read
+// S of chunk s it writes P'' of chunk s into the first 64 columns of the same
+// buffer (f16 pairs, the PV MMA's A operand).  O buffer b at 256 + 128 b: the
+// PV of chunk s accumulates into O buffer s & 1, so a reference move at
+// chunk s rescales buffer s & 1 -- last written by PV(s - 2), complete before
+// QK(s) was issued -- and buffer (s + 1) & 1 at chunk s + 1: neither waits for
+// an MMA in flight.  The epilogue adds the two with their references.
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 256;
 constexpr uint32_t kRwTmemCols = 512;
 
 // shared memory, offsets from a 1024-byte aligned base
@@ -311,22 +317,25 @@ struct ChunkWalk {
 // has to stay in the SM's instruction cache.
 
 // P'' = p v_scale 2^-E of this thread's slice under the present references,
-// written to TMEM 16 tokens at a time, and its share of the denominator.
-// True if a score passed the reference's headroom or a value scale the bound
-// 2^E: the chunk then has to be redone under new references.
+// packed as f16 pairs into pk (kept in registers: the slice's S columns may
+// share TMEM columns with P, so P is stored only once the chunk is settled),
+// its share of the denominator, and the slice's largest score and value
+// scale.  True if a score passed the reference's headroom or a value scale
+// the bound 2^E: the chunk then has to be redone under new references.
 template <int RC>
-__device__ __forceinline__ bool rows_chunk_p(uint32_t scol, uint32_t pcol, const float *ks,
-                                            const float *vs, int lim, float rowf, float m_ref,
-                                            int E, float &lchunk) {
+__device__ __forceinline__ bool rows_chunk_p(uint32_t scol, const float *ks, const float *vs,
+                                            int lim, float rowf, float m_ref, int E,
+                                            float &lchunk, float &mx, float &vmax,
+                                            uint32_t (&pk)[RC / 2]) {
   const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
   const float thr = m_ref + kRwLazy;
   const float vbound = pow2f(E), vnorm = pow2f(-E);
-  bool over = false;
-#pragma unroll 1
+  mx = -INFINITY;
+  vmax = 0.0f;
+#pragma unroll
   for (int g = 0; g < RC / 16; ++g) {
     float x[16];
     tmem_ld16(scol + 16 * g, x);
-    uint32_t pk[8];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float4 k4 = reinterpret_cast<const float4 *>(ks)[4 * g + q];
@@ -340,72 +349,138 @@ __device__ __forceinline__ bool rows_chunk_p(uint32_t scol, uint32_t pcol, const
         const bool seen = 16 * g + 4 * q + e < lim;
         const float xe = seen ? x[4 * q + e] * (kk[e] * rowf) : -INFINITY;
         const float ve = seen ? vv[e] : 0.0f;
-        over |= (xe > thr) | (ve > vbound);
+        mx = fmaxf(mx, xe);
+        vmax = fmaxf(vmax, ve);
         const float pe = rw_ex2(xe - ms);
         lchunk += pe;
         pw[e] = pe * (ve * vnorm);
       }
-      pk[2 * q] = pack_f16x2(pw[0], pw[1]);
-      pk[2 * q + 1] = pack_f16x2(pw[2], pw[3]);
+      pk[8 * g + 2 * q] = pack_f16x2(pw[0], pw[1]);
+      pk[8 * g + 2 * q + 1] = pack_f16x2(pw[2], pw[3]);
     }
-    tmem_st8u(pcol + 8 * g, pk);
   }
-  return over;
+  return (mx > thr) || (vmax > vbound);
+}
+
+// The O rows of one buffer brought to this thread's present references
+// (factor 2^(ref_o - m) 2^(e_o - E); rows of the warp already there multiply
+// by 1).  The buffer must have no MMA in flight.
+__device__ __forceinline__ void rows_rescale_o(uint32_t ocol, float f) {
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    float o[32];
+    tmem_ld32(ocol + c, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] *= f;
+    tmem_st32(ocol + c, o);
+  }
+  tmem_wait_st();
 }
 
 // The rare case (a row's scores passed its reference's headroom or a value
-// scale the bound): new references, the denominator and the O rows so far
-// rescaled (once the previous chunk's PV has completed), the chunk redone.
-// False if a wait gave up.
-template <int RC>
-__device__ __noinline__ bool rows_chunk_redo(uint32_t scol, uint32_t pcol, uint32_t ocol,
-                                             const float *ks, const float *vs, int lim,
-                                             float rowf, float &m_ref, int &E, float &lsum,
-                                             float &lchunk, bool have_o, uint32_t pv_bar,
-                                             uint32_t pv_par, volatile int *abort_s) {
-  float mx = -INFINITY, vmax = 0.0f;
-#pragma unroll 1
-  for (int g = 0; g < RC / 16; ++g) {
-    float x[16];
-    tmem_ld16(scol + 16 * g, x);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const bool seen = 16 * g + i < lim;
-      mx = fmaxf(mx, seen ? x[i] * (ks[16 * g + i] * rowf) : -INFINITY);
-      vmax = fmaxf(vmax, seen ? vs[16 * g + i] : 0.0f);
-    }
-  }
-  float f = 1.0f;
+// scale the bound): new references from the chunk's maxima and the
+// denominator brought under them; the chunk is then redone.  Rows whose
+// references stay put keep them (their redo repeats the same values).
+__device__ __forceinline__ void rows_new_refs(float mx, float vmax, float &m_ref, int &E,
+                                              float &lsum) {
   const float m_new = (mx > m_ref + kRwLazy) ? mx + kRwOvershoot : m_ref;
   // a new value bound keeps two binades of headroom (fewer redos as the
   // scales grow; P'' then stays <= p / 4)
   const int e_need = rw_pow2_ceil(__float_as_uint(vmax));
   const int e_new = e_need > E ? min(e_need + 2, 126) : E;
-  if (m_ref != -INFINITY) {
-    const float fm = rw_ex2(m_ref - m_new);
-    lsum *= fm;
-    f = fm * pow2f_down(E - e_new);
-  }
+  if (m_ref != -INFINITY) lsum *= rw_ex2(m_ref - m_new);
   m_ref = m_new;
   E = e_new;
-  if (have_o && __any_sync(0xFFFFFFFFu, f != 1.0f)) {
-    const bool ok = rw_wait(pv_bar, pv_par, abort_s);
-    if (__any_sync(0xFFFFFFFFu, !ok)) return false;
-    tc_fence_after();
+}
+
+// A move of one thread's references in the middle of a chunk (one token
+// slice per row, RC = 128): the new references, the factor that takes
+// exponentials under the old score reference to the new (the denominator's
+// terms) and the one for P'' (which also carries 2^-E).
+struct RwMove {
+  float m;
+  int e;
+  float fl, fp;
+};
+__device__ __noinline__ RwMove rows_move(float gmx, float gvmax, float m_ref, int E) {
+  RwMove r;
+  r.m = (gmx > m_ref + kRwLazy) ? gmx + kRwOvershoot : m_ref;
+  const int e_need = rw_pow2_ceil(__float_as_uint(gvmax));
+  r.e = e_need > E ? min(e_need + 2, 126) : E;
+  r.fl = (m_ref == -INFINITY) ? 0.0f : rw_ex2(m_ref - r.m);
+  r.fp = r.fl * pow2f_down(E - r.e);
+  return r;
+}
+
+// The P'' columns [pcol, pcol + ncols) of this thread's lane times f (the
+// warp's rows whose references stayed put have f = 1).
+__device__ __noinline__ void rows_rescale_p(uint32_t pcol, int ncols, float f) {
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
-      float o[32];
-      tmem_ld32(ocol + c, o);
+  for (int c = 0; c < ncols; c += 8) {
+    uint32_t w[8];
+    tmem_ld8u(pcol + c, w);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] *= f;
-      tmem_st32(ocol + c, o);
+    for (int i = 0; i < 8; ++i) {
+      float lo, hi;
+      asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n"
+          " cvt.f32.f16 %1, h;\n}\n" : "=f"(lo), "=f"(hi) : "r"(w[i]));
+      w[i] = pack_f16x2(lo * f, hi * f);
     }
-    tmem_wait_st();
-    tc_fence_before();
+    tmem_st8u(pcol + c, w);
   }
-  lchunk = 0.0f;
-  rows_chunk_p<RC>(scol, pcol, ks, vs, lim, rowf, m_ref, E, lchunk);
-  return true;
+}
+
+// P'' of a whole 128-token chunk for one row (RC = 128, one copy), stored
+// 8 columns at a time over the S columns of tokens already read (group g's
+// P'' goes to columns [8 g, 8 g + 8), whose S values the groups up to g have
+// consumed).  A row that outgrows its references moves them before the
+// group's exponentials and brings the P'' already stored, the chunk's
+// denominator share and the running denominator under the new ones, so no
+// S value is needed twice and nothing is held in registers across the chunk.
+__device__ __forceinline__ void rows_chunk_p_direct(uint32_t scol, const float *ks,
+                                                    const float *vs, int lim, float rowf,
+                                                    float &m_ref, int &E, float &lchunk,
+                                                    float &lsum) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    float x[16], vv[16];
+    tmem_ld16(scol + 16 * g, x);
+    float gmx = -INFINITY, gvm = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 k4 = reinterpret_cast<const float4 *>(ks)[4 * g + q];
+      const float4 v4 = reinterpret_cast<const float4 *>(vs)[4 * g + q];
+      const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+      const float vq[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // unseen tokens: -inf score, value weight 0 (their scales may be stale)
+        const bool seen = 16 * g + 4 * q + e < lim;
+        x[4 * q + e] = seen ? x[4 * q + e] * (kk[e] * rowf) : -INFINITY;
+        vv[4 * q + e] = seen ? vq[e] : 0.0f;
+        gmx = fmaxf(gmx, x[4 * q + e]);
+        gvm = fmaxf(gvm, vv[4 * q + e]);
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, gmx > m_ref + kRwLazy || gvm > pow2f(E))) {
+      const RwMove mv = rows_move(gmx, gvm, m_ref, E);
+      lsum *= mv.fl;
+      lchunk *= mv.fl;
+      if (g > 0) rows_rescale_p(scol, 8 * g, mv.fp);
+      m_ref = mv.m;
+      E = mv.e;
+    }
+    const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
+    const float vnorm = pow2f(-E);
+    uint32_t w8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float p0 = rw_ex2(x[2 * i] - ms), p1 = rw_ex2(x[2 * i + 1] - ms);
+      lchunk += p0 + p1;
+      w8[i] = pack_f16x2(p0 * (vv[2 * i] * vnorm), p1 * (vv[2 * i + 1] * vnorm));
+    }
+    tmem_st8u(scol + 8 * g, w8);
+  }
 }
 
 // The unit's query tile (rows m < rows_here of tile row0, every copy) as two
@@ -640,10 +715,11 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       for (int s = 0; w.valid; ++s) {
         const int b = s % kRwStages, sb = s & 1;
         // a new unit's query tile (written once the last unit's softmax and
-        // merge are done); S buffer s & 1 once chunk s - 2's softmax read it
+        // merge are done)
         if (w.k == 0 && !rw_wait(BAR(kBarQReady), w.seg & 1, abort_s)) break;
         if (!rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) break;
-        if (s >= 2 && !rw_wait(BAR(kBarReady + sb), ((s >> 1) - 1) & 1, abort_s)) break;
+        // S buffer s & 1 holds P of chunk s - 2 until that chunk's PV is done
+        if (s >= 2 && !rw_wait(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) break;
         tc_fence_after();
         const uint64_t kd = smem_desc(smem_addr(smem + b * kStageBytes), 16, 1024, kSmemSwizzle128);
         const uint64_t qa = smem_desc(q0, 16, 1024, kSmemSwizzle128);
@@ -675,6 +751,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       for (int s = 0; w.valid; ++s) {
         const int cb = s & 1;
         const bool first = w.k == 0;
+        const bool fresh = w.k < 2;              // the unit's first PV into O buffer cb
         // P'' and the V operand of chunk s; a new unit's O once the last
         // unit's rows have been read back
         if (!rw_wait(BAR(kBarReady + cb), (s >> 1) & 1, abort_s)) break;
@@ -683,8 +760,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         const uint64_t bd = smem_desc(vf0 + cb * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
 #pragma unroll
         for (int kk = 0; kk < kRwTok / 16; ++kk)
-          tc_mma_f16_tmem_a(tmem + kColO, tmem + kColP + 64 * cb + 8 * kk, bd + (2048 >> 4) * kk,
-                            kIdescPV, (first && kk == 0) ? 0u : 1u);
+          tc_mma_f16_tmem_a(tmem + kColO + 128 * cb, tmem + kColS + 128 * cb + 8 * kk,
+                            bd + (2048 >> 4) * kk, kIdescPV, (fresh && kk == 0) ? 0u : 1u);
         tc_commit(BAR(kBarPvDone + cb));
         last_bar = BAR(kBarPvDone + cb);
         last_par = (s >> 1) & 1;
@@ -741,21 +818,11 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     float *ts = reinterpret_cast<float *>(smem + kOffTs) + warp * 2 * kRwTok;
     float4 *ml_s = reinterpret_cast<float4 *>(smem + kOffMl);
     bool aborted = false;
-    {
-      // P columns outside this thread's slice stay zero for the whole kernel
-      uint32_t z[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = 0u;
-#pragma unroll
-      for (int c = 0; c < 128; c += 16) tmem_st16u(tl + kColP + c, z);
-      tmem_wait_st();
-    }
     ChunkWalk w;
     w.start(pre, p.context_lens, geo, N, x_begin, x_end);
     int s = 0;                                  // chunks consumed
     while (w.valid) {
       const Seg sg = w.sg;
-      const int seg = w.seg;
       const int r = sg.r, h = sg.h;
       const int row0 = 128 * sg.t;              // the tile's first stacked row
       const int rows_here = min(p.M - row0, RC);
@@ -777,7 +844,10 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       const float rowf = rowf_s[mrow];
       float m_ref = -INFINITY, lsum = 0.0f;
       int E = -126;
-      bool have_o = false;                      // a PV of this unit has been issued
+      // the references O buffer b holds its rows under (written once chunk
+      // s_first + b has been issued)
+      float ref_o[2] = {-INFINITY, -INFINITY};
+      int e_o[2] = {-126, -126};
       const int s_first = s;
       for (int k = 0; k < sg.n; ++k, ++s) {
         const int b = s % kRwStages, sb = s & 1;
@@ -803,34 +873,60 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
         const uint32_t scol = tl + kColS + 128 * sb + copy * RC;
-        const uint32_t pcol = tl + kColP + 64 * sb + copy * (RC / 2);
-        // the P buffer of chunk s - 2 is free once its PV has completed
-        if (s >= 2 && !rw_wait(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) aborted = true;
-        if (__any_sync(0xFFFFFFFFu, aborted)) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
+        const uint32_t ocol = tl + kColO + 128 * sb;
+        // P'' of the slice; redone (once: the new references cover the
+        // chunk) if a row of the warp outgrew its references
         float lchunk = 0.0f;
-        // the unit's first chunk sets the references: straight to the redo
-        const bool over =
-            k == 0 || rows_chunk_p<RC>(scol, pcol, ts, ts + RC, lim, rowf, m_ref, E, lchunk);
-        if (__any_sync(0xFFFFFFFFu, over)) {
-          tmem_wait_st();
-          const int sp = s - 1;
-          if (!rows_chunk_redo<RC>(scol, pcol, tl + kColO, ts, ts + RC, lim, rowf, m_ref, E,
-                                   lsum, lchunk,
-                                   have_o, BAR(kBarPvDone + (sp & 1)), (sp >> 1) & 1, abort_s)) {
-            aborted = true;
-            break;
+        uint32_t pk[RC < 128 ? RC / 2 : 1];
+        if constexpr (RC == 128) {
+          rows_chunk_p_direct(scol, ts, ts + RC, lim, rowf, m_ref, E, lchunk, lsum);
+        } else {
+          bool redone = false;
+          for (;;) {
+            float mx, vmax;
+            lchunk = 0.0f;
+            const bool over = rows_chunk_p<RC>(scol, ts, ts + RC, lim, rowf, m_ref, E, lchunk,
+                                               mx, vmax, pk);
+            if (!__any_sync(0xFFFFFFFFu, over) || redone) break;
+            rows_new_refs(mx, vmax, m_ref, E, lsum);
+            redone = true;
           }
         }
+        // O buffer s & 1 (no MMA in flight: PV(s - 2) completed before QK(s)
+        // was issued, and PV(s) waits for this chunk's Ready) follows the
+        // present references if a move left it behind; the two references are
+        // kept in registers: selected, not indexed
+        if (k >= 2) {
+          const float rb = sb ? ref_o[1] : ref_o[0];
+          const int eb = sb ? e_o[1] : e_o[0];
+          if (__any_sync(0xFFFFFFFFu, rb != m_ref || eb != E))
+            rows_rescale_o(ocol, (rb == -INFINITY) ? 0.0f : rw_ex2(rb - m_ref) * pow2f_down(eb - E));
+        }
+        if (sb) {
+          ref_o[1] = m_ref;
+          e_o[1] = E;
+        } else {
+          ref_o[0] = m_ref;
+          e_o[0] = E;
+        }
         lsum += lchunk;
+        // P'' into the first 64 columns of the S buffer: this slice's columns,
+        // zeros in the other slices' (their S values are there)
+        if constexpr (RC < 128) {
+          const uint32_t pbase = tl + kColS + 128 * sb;
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            const int sl = c / (RC / 2);          // the slice these columns belong to
+            uint32_t w8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w8[i] = (sl == copy) ? pk[(c % (RC / 2)) + i] : 0u;
+            tmem_st8u(pbase + c, w8);
+          }
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(kBarReady + sb));
-        have_o = true;
       }
       // ---- the unit's piece: wait for its last PV
       if (!aborted && sg.n > 0) {
@@ -875,16 +971,40 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       const int slot = 2 * static_cast<int>(blockIdx.x) +
                        (static_cast<int>(blockIdx.x) == b_first ? 1 : 0);
       const float inv = (l_all > 0.0f) ? vsc / l_all : 0.0f;
+      // the two O buffers under this thread's final references (a buffer the
+      // unit never wrote -- one chunk -- is not read)
+      const int bf = s_first & 1;
+      const bool both = sg.n > 1;
+      float fo0 = (ref_o[0] == -INFINITY) ? 0.0f
+                                          : f_me * rw_ex2(ref_o[0] - m_ref) * pow2f_down(e_o[0] - E);
+      float fo1 = (ref_o[1] == -INFINITY) ? 0.0f
+                                          : f_me * rw_ex2(ref_o[1] - m_ref) * pow2f_down(e_o[1] - E);
+      if (bf) {                                 // fo0: the first chunk's buffer
+        const float t = fo0;
+        fo0 = fo1;
+        fo1 = t;
+      }
+      const uint32_t ob0 = tl + kColO + 128 * bf, ob1 = tl + kColO + 128 * (bf ^ 1);
       float *acc = reinterpret_cast<float *>(smem + kOffQ);    // [dim][RC]
       for (int c = 0; c < kCopies; ++c) {
         if (copy == c) {
 #pragma unroll 1
           for (int pc = 0; pc < 4; ++pc) {
             float o[32];
-            tmem_ld32(tl + kColO + 32 * pc, o);
+            tmem_ld32(ob0 + 32 * pc, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= fo0;
+            if (both) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                float o2[16];
+                tmem_ld16(ob1 + 32 * pc + 16 * hh, o2);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[16 * hh + i] = fmaf(o2[i], fo1, o[16 * hh + i]);
+              }
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              o[i] *= f_me;
               if (c > 0) o[i] += acc[(32 * pc + i) * RC + mrow];
               if (c < kCopies - 1) acc[(32 * pc + i) * RC + mrow] = o[i];
             }

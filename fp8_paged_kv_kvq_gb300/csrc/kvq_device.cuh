@@ -507,6 +507,16 @@ __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&r)[8]
                   "r"(r[6]), "r"(r[7]) : "memory");
 }
 
+// 8 consecutive 32-bit columns of this thread's TMEM lane as raw words, the
+// wait for the load in the same statement.
+__device__ __forceinline__ void tmem_ld8u(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+               "tcgen05.wait::ld.sync.aligned;\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
