@@ -79,6 +79,18 @@ constexpr float kRwOvershoot = 4.0f;         // a moved reference sits this far 
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kRwTmemCols = 512;
+// Tiles of at most 64 rows read only their own slice's S columns, which they
+// can take in before computing P'': there S is one buffer (columns 0 .. 127)
+// and P'' has two of its own (b at 128 + 64 b), whose columns outside a lane's
+// slice stay zero for the whole launch.  QK(s + 1) then waits only for the
+// softmax to have read S(s) -- not for PV(s) -- and a chunk's P'' store
+// writes just its slice's columns.
+template <int RC>
+struct RwCols {
+  static constexpr bool kSplitP = RC < 128;
+  __device__ static uint32_t S(int sb) { return kSplitP ? kColS : kColS + 128u * sb; }
+  __device__ static uint32_t P(int sb) { return kSplitP ? 128u + 64u * sb : kColS + 128u * sb; }
+};
 
 // shared memory, offsets from a 1024-byte aligned base
 constexpr int kCodeBytes = kRwTok * kHeadDim;                 // one plane of a chunk
@@ -100,7 +112,9 @@ constexpr int kBarKvEmpty = kBarKvFull + kRwStages;
 constexpr int kBarSFull = kBarKvEmpty + kRwStages;
 // chunk s is ready for its PV once its P'' is in TMEM (softmax warps, which
 // have also finished reading its S) and its V operand converted (converters)
-constexpr int kBarReady = kBarSFull + 2;
+// tiles of at most 64 rows: S(s) has been read (the single S buffer is free)
+constexpr int kBarSFree = kBarSFull + 2;
+constexpr int kBarReady = kBarSFree + 2;
 constexpr int kBarPvDone = kBarReady + 2;
 constexpr int kBarQReady = kBarPvDone + 2;
 constexpr int kBarOFree = kBarQReady + 1;
@@ -160,6 +174,13 @@ __device__ __noinline__ bool rw_wait(uint32_t bar, uint32_t parity, volatile int
   }
   *abort = 1;
   return false;
+}
+
+// The same with the common case inline: a phase already complete costs one
+// try_wait, not a call (which, at this kernel's register load, saves and
+// restores live registers around it).
+__device__ __forceinline__ bool rw_wait_fast(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return mbar_try_wait(bar, parity) || rw_wait(bar, parity, abort);
 }
 
 // Barrier over the softmax warps that also ORs a flag across them.
@@ -316,50 +337,168 @@ struct ChunkWalk {
 // the kernel's warps run four different loops side by side, and their code
 // has to stay in the SM's instruction cache.
 
-// P'' = p v_scale 2^-E of this thread's slice under the present references,
-// packed as f16 pairs into pk (kept in registers: the slice's S columns may
-// share TMEM columns with P, so P is stored only once the chunk is settled),
-// its share of the denominator, and the slice's largest score and value
-// scale.  True if a score passed the reference's headroom or a value scale
-// the bound 2^E: the chunk then has to be redone under new references.
-template <int RC>
-__device__ __forceinline__ bool rows_chunk_p(uint32_t scol, const float *ks, const float *vs,
-                                            int lim, float rowf, float m_ref, int E,
-                                            float &lchunk, float &mx, float &vmax,
-                                            uint32_t (&pk)[RC / 2]) {
+// A move of one thread's references in the middle of a chunk: the new
+// references, the factor that takes exponentials under the old score
+// reference to the new (the denominator's terms) and the one for P'' (which
+// also carries 2^-E).
+struct RwMove {
+  float m;
+  int e;
+  float fl, fp;
+};
+__device__ __forceinline__ RwMove rows_move(float gmx, float gvmax, float m_ref, int E) {
+  RwMove r;
+  r.m = (gmx > m_ref + kRwLazy) ? gmx + kRwOvershoot : m_ref;
+  const int e_need = rw_pow2_ceil(__float_as_uint(gvmax));
+  r.e = e_need > E ? min(e_need + 2, 126) : E;
+  r.fl = (m_ref == -INFINITY) ? 0.0f : rw_ex2(m_ref - r.m);
+  r.fp = r.fl * pow2f_down(E - r.e);
+  return r;
+}
+
+// An f16 pair times f, through f32 (f may lie below the f16 range).
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t w, float f) {
+  float lo, hi;
+  asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n"
+      " cvt.f32.f16 %1, h;\n}\n" : "=f"(lo), "=f"(hi) : "r"(w));
+  return pack_f16x2(lo * f, hi * f);
+}
+
+// One 16-token group of a row's slice.  Scores in log2 units relative to the
+// present reference, u = S k_scale rowf - m (pairs of f32: the arithmetic
+// runs on the f32x2 path), the value scales beside them, unseen tokens
+// (j >= lim; only a unit's last chunk has them, hence the warp-uniform
+// `masked`) at -inf with weight 0, and the group's maxima.
+struct RwGroup {
+  uint64_t u[8], vw[8];
+  float gmx, gvm;
+};
+__device__ __forceinline__ void rows_group_u(const float (&x)[16], const float *ks,
+                                             const float *vs, int g, float rowf, float ms,
+                                             int lim, bool masked, RwGroup &gr) {
+  const uint64_t rf = pack_f32x2(rowf, rowf), nms = pack_f32x2(-ms, -ms);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 k4 = reinterpret_cast<const float4 *>(ks)[4 * g + q];
+    const float4 v4 = reinterpret_cast<const float4 *>(vs)[4 * g + q];
+    gr.u[2 * q] = fma_f32x2(mul_f32x2(pack_f32x2(x[4 * q], x[4 * q + 1]), pack_f32x2(k4.x, k4.y)),
+                            rf, nms);
+    gr.u[2 * q + 1] = fma_f32x2(
+        mul_f32x2(pack_f32x2(x[4 * q + 2], x[4 * q + 3]), pack_f32x2(k4.z, k4.w)), rf, nms);
+    gr.vw[2 * q] = pack_f32x2(v4.x, v4.y);
+    gr.vw[2 * q + 1] = pack_f32x2(v4.z, v4.w);
+  }
+  if (masked) {
+    // (their scales may be stale: the selects also drop a NaN product)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float a, b, va, vb;
+      unpack_f32x2(gr.u[i], a, b);
+      unpack_f32x2(gr.vw[i], va, vb);
+      const bool s0 = 16 * g + 2 * i < lim, s1 = 16 * g + 2 * i + 1 < lim;
+      gr.u[i] = pack_f32x2(s0 ? a : -INFINITY, s1 ? b : -INFINITY);
+      gr.vw[i] = pack_f32x2(s0 ? va : 0.0f, s1 ? vb : 0.0f);
+    }
+  }
+  float mx = -INFINITY, vm = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a, b, va, vb;
+    unpack_f32x2(gr.u[i], a, b);
+    unpack_f32x2(gr.vw[i], va, vb);
+    mx = fmaxf(mx, fmaxf(a, b));
+    vm = fmaxf(vm, fmaxf(va, vb));
+  }
+  gr.gmx = mx;
+  gr.gvm = vm;
+}
+
+// Whether a row of the warp has to move its references before the group's
+// exponentials (a score past the headroom, or a value scale past 2^E).
+__device__ __forceinline__ bool rows_group_over(const RwGroup &gr, float m_ref, int E) {
+  const float thr = (m_ref == -INFINITY) ? -INFINITY : kRwLazy;
+  return __any_sync(0xFFFFFFFFu, gr.gmx > thr || gr.gvm > pow2f(E));
+}
+
+// Moves this thread's references for the group (rows whose references hold
+// get factor 1) and shifts the group's u to the new score reference; returns
+// the factor for P'' already produced, after scaling the denominators.
+__device__ __forceinline__ float rows_group_move(RwGroup &gr, float &m_ref, int &E, float &lsum,
+                                                 float &lchunk) {
   const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
-  const float thr = m_ref + kRwLazy;
-  const float vbound = pow2f(E), vnorm = pow2f(-E);
-  mx = -INFINITY;
-  vmax = 0.0f;
+  const RwMove mv = rows_move(gr.gmx + ms, gr.gvm, m_ref, E);
+  lsum *= mv.fl;
+  lchunk *= mv.fl;
+  m_ref = mv.m;
+  E = mv.e;
+  const float ms_new = (m_ref == -INFINITY) ? 0.0f : m_ref;
+  const uint64_t d = pack_f32x2(ms - ms_new, ms - ms_new), one = pack_f32x2(1.0f, 1.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) gr.u[i] = fma_f32x2(gr.u[i], one, d);
+  return mv.fp;
+}
+
+// The group's P'' = 2^u v_scale 2^-E as f16 pairs, and its share of the
+// denominator added to lchunk.
+__device__ __forceinline__ void rows_group_p(const RwGroup &gr, int E, float &lchunk,
+                                             uint32_t *w8) {
+  const uint64_t vn = pack_f32x2(pow2f(-E), pow2f(-E));
+  uint64_t lc = pack_f32x2(0.0f, 0.0f);
+  const uint64_t one = pack_f32x2(1.0f, 1.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a, b;
+    unpack_f32x2(gr.u[i], a, b);
+    const uint64_t pp = pack_f32x2(rw_ex2(a), rw_ex2(b));
+    lc = fma_f32x2(pp, one, lc);
+    float w0, w1;
+    unpack_f32x2(mul_f32x2(pp, mul_f32x2(gr.vw[i], vn)), w0, w1);
+    w8[i] = pack_f16x2(w0, w1);
+  }
+  float l0, l1;
+  unpack_f32x2(lc, l0, l1);
+  lchunk += l0 + l1;
+}
+
+// P'' = p v_scale 2^-E of this thread's slice (RC <= 64 tokens), packed as f16
+// pairs into pk, and its share of the denominator.  The slice's S columns are
+// read first and the warp announces it on sfree (the next chunk's QK^T may
+// then overwrite them).  The slice goes 16 tokens at a time; a row whose
+// scores pass its reference's headroom, or whose value scales pass the bound
+// 2^E, moves its references before the group's exponentials and brings the
+// P'' already packed and the denominators under the new ones, so no
+// exponential is computed twice.
+template <int RC>
+__device__ __forceinline__ void rows_chunk_p(uint32_t scol, uint32_t sfree, int lane,
+                                            const float *ks, const float *vs, int lim, float rowf,
+                                            float &m_ref, int &E, float &lchunk, float &lsum,
+                                            uint32_t (&pk)[RC / 2]) {
+  float xs[RC];
+#pragma unroll
+  for (int c = 0; c < RC; c += 32) {
+    float x32[32];
+    tmem_ld32(scol + c, x32);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) xs[c + i] = x32[i];
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sfree);
+  const bool masked = __any_sync(0xFFFFFFFFu, lim < RC);
 #pragma unroll
   for (int g = 0; g < RC / 16; ++g) {
     float x[16];
-    tmem_ld16(scol + 16 * g, x);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 k4 = reinterpret_cast<const float4 *>(ks)[4 * g + q];
-      const float4 v4 = reinterpret_cast<const float4 *>(vs)[4 * g + q];
-      const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-      const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-      float pw[4];
+    for (int i = 0; i < 16; ++i) x[i] = xs[16 * g + i];
+    RwGroup gr;
+    rows_group_u(x, ks, vs, g, rowf, (m_ref == -INFINITY) ? 0.0f : m_ref, lim, masked, gr);
+    if (rows_group_over(gr, m_ref, E)) {
+      const float f = rows_group_move(gr, m_ref, E, lsum, lchunk);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // unseen tokens: -inf score, value weight 0 (their scales may be stale)
-        const bool seen = 16 * g + 4 * q + e < lim;
-        const float xe = seen ? x[4 * q + e] * (kk[e] * rowf) : -INFINITY;
-        const float ve = seen ? vv[e] : 0.0f;
-        mx = fmaxf(mx, xe);
-        vmax = fmaxf(vmax, ve);
-        const float pe = rw_ex2(xe - ms);
-        lchunk += pe;
-        pw[e] = pe * (ve * vnorm);
-      }
-      pk[8 * g + 2 * q] = pack_f16x2(pw[0], pw[1]);
-      pk[8 * g + 2 * q + 1] = pack_f16x2(pw[2], pw[3]);
+      for (int i = 0; i < 8 * g; ++i) pk[i] = scale_f16x2(pk[i], f);
     }
+    rows_group_p(gr, E, lchunk, &pk[8 * g]);
   }
-  return (mx > thr) || (vmax > vbound);
 }
 
 // The O rows of one buffer brought to this thread's present references
@@ -377,41 +516,6 @@ __device__ __forceinline__ void rows_rescale_o(uint32_t ocol, float f) {
   tmem_wait_st();
 }
 
-// The rare case (a row's scores passed its reference's headroom or a value
-// scale the bound): new references from the chunk's maxima and the
-// denominator brought under them; the chunk is then redone.  Rows whose
-// references stay put keep them (their redo repeats the same values).
-__device__ __forceinline__ void rows_new_refs(float mx, float vmax, float &m_ref, int &E,
-                                              float &lsum) {
-  const float m_new = (mx > m_ref + kRwLazy) ? mx + kRwOvershoot : m_ref;
-  // a new value bound keeps two binades of headroom (fewer redos as the
-  // scales grow; P'' then stays <= p / 4)
-  const int e_need = rw_pow2_ceil(__float_as_uint(vmax));
-  const int e_new = e_need > E ? min(e_need + 2, 126) : E;
-  if (m_ref != -INFINITY) lsum *= rw_ex2(m_ref - m_new);
-  m_ref = m_new;
-  E = e_new;
-}
-
-// A move of one thread's references in the middle of a chunk (one token
-// slice per row, RC = 128): the new references, the factor that takes
-// exponentials under the old score reference to the new (the denominator's
-// terms) and the one for P'' (which also carries 2^-E).
-struct RwMove {
-  float m;
-  int e;
-  float fl, fp;
-};
-__device__ __noinline__ RwMove rows_move(float gmx, float gvmax, float m_ref, int E) {
-  RwMove r;
-  r.m = (gmx > m_ref + kRwLazy) ? gmx + kRwOvershoot : m_ref;
-  const int e_need = rw_pow2_ceil(__float_as_uint(gvmax));
-  r.e = e_need > E ? min(e_need + 2, 126) : E;
-  r.fl = (m_ref == -INFINITY) ? 0.0f : rw_ex2(m_ref - r.m);
-  r.fp = r.fl * pow2f_down(E - r.e);
-  return r;
-}
-
 // The P'' columns [pcol, pcol + ncols) of this thread's lane times f (the
 // warp's rows whose references stayed put have f = 1).
 __device__ __noinline__ void rows_rescale_p(uint32_t pcol, int ncols, float f) {
@@ -420,12 +524,7 @@ __device__ __noinline__ void rows_rescale_p(uint32_t pcol, int ncols, float f) {
     uint32_t w[8];
     tmem_ld8u(pcol + c, w);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float lo, hi;
-      asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n"
-          " cvt.f32.f16 %1, h;\n}\n" : "=f"(lo), "=f"(hi) : "r"(w[i]));
-      w[i] = pack_f16x2(lo * f, hi * f);
-    }
+    for (int i = 0; i < 8; ++i) w[i] = scale_f16x2(w[i], f);
     tmem_st8u(pcol + c, w);
   }
 }
@@ -441,44 +540,19 @@ __device__ __forceinline__ void rows_chunk_p_direct(uint32_t scol, const float *
                                                     const float *vs, int lim, float rowf,
                                                     float &m_ref, int &E, float &lchunk,
                                                     float &lsum) {
+  const bool masked = __any_sync(0xFFFFFFFFu, lim < 128);
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    float x[16], vv[16];
+    float x[16];
     tmem_ld16(scol + 16 * g, x);
-    float gmx = -INFINITY, gvm = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 k4 = reinterpret_cast<const float4 *>(ks)[4 * g + q];
-      const float4 v4 = reinterpret_cast<const float4 *>(vs)[4 * g + q];
-      const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-      const float vq[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // unseen tokens: -inf score, value weight 0 (their scales may be stale)
-        const bool seen = 16 * g + 4 * q + e < lim;
-        x[4 * q + e] = seen ? x[4 * q + e] * (kk[e] * rowf) : -INFINITY;
-        vv[4 * q + e] = seen ? vq[e] : 0.0f;
-        gmx = fmaxf(gmx, x[4 * q + e]);
-        gvm = fmaxf(gvm, vv[4 * q + e]);
-      }
+    RwGroup gr;
+    rows_group_u(x, ks, vs, g, rowf, (m_ref == -INFINITY) ? 0.0f : m_ref, lim, masked, gr);
+    if (rows_group_over(gr, m_ref, E)) {
+      const float f = rows_group_move(gr, m_ref, E, lsum, lchunk);
+      if (g > 0) rows_rescale_p(scol, 8 * g, f);
     }
-    if (__any_sync(0xFFFFFFFFu, gmx > m_ref + kRwLazy || gvm > pow2f(E))) {
-      const RwMove mv = rows_move(gmx, gvm, m_ref, E);
-      lsum *= mv.fl;
-      lchunk *= mv.fl;
-      if (g > 0) rows_rescale_p(scol, 8 * g, mv.fp);
-      m_ref = mv.m;
-      E = mv.e;
-    }
-    const float ms = (m_ref == -INFINITY) ? 0.0f : m_ref;
-    const float vnorm = pow2f(-E);
     uint32_t w8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float p0 = rw_ex2(x[2 * i] - ms), p1 = rw_ex2(x[2 * i + 1] - ms);
-      lchunk += p0 + p1;
-      w8[i] = pack_f16x2(p0 * (vv[2 * i] * vnorm), p1 * (vv[2 * i + 1] * vnorm));
-    }
+    rows_group_p(gr, E, lchunk, w8);
     tmem_st8u(scol + 8 * g, w8);
   }
 }
@@ -608,6 +682,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(kBarSFull + b), 1);
+      mbar_init(BAR(kBarSFree + b), kRwSoftWarps);
       mbar_init(BAR(kBarReady + b), kRwSoftWarps + kRwConvWarps);
       mbar_init(BAR(kBarPvDone + b), 1);
     }
@@ -662,7 +737,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       __syncwarp();
       if (lane == 0) {
         const int b = u % kRwStages;
-        if (u >= kRwStages && !rw_wait(BAR(kBarKvEmpty + b), ((u / kRwStages) - 1) & 1, abort_s)) {
+        if (u >= kRwStages &&
+            !rw_wait_fast(BAR(kBarKvEmpty + b), ((u / kRwStages) - 1) & 1, abort_s)) {
           stop = true;
         } else {
           const uint32_t kdst = smem_addr(smem + b * kStageBytes);
@@ -716,20 +792,27 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         const int b = s % kRwStages, sb = s & 1;
         // a new unit's query tile (written once the last unit's softmax and
         // merge are done)
-        if (w.k == 0 && !rw_wait(BAR(kBarQReady), w.seg & 1, abort_s)) break;
-        if (!rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) break;
-        // S buffer s & 1 holds P of chunk s - 2 until that chunk's PV is done
-        if (s >= 2 && !rw_wait(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) break;
+        if (w.k == 0 && !rw_wait_fast(BAR(kBarQReady), w.seg & 1, abort_s)) break;
+        if (!rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s)) break;
+        if constexpr (RwCols<RC>::kSplitP) {
+          // the one S buffer is free once the softmax has read S(s - 1)
+          if (s >= 1 &&
+              !rw_wait_fast(BAR(kBarSFree + ((s - 1) & 1)), ((s - 1) >> 1) & 1, abort_s))
+            break;
+        } else {
+          // S buffer s & 1 holds P of chunk s - 2 until that chunk's PV is done
+          if (s >= 2 && !rw_wait_fast(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s)) break;
+        }
         tc_fence_after();
         const uint64_t kd = smem_desc(smem_addr(smem + b * kStageBytes), 16, 1024, kSmemSwizzle128);
         const uint64_t qa = smem_desc(q0, 16, 1024, kSmemSwizzle128);
         const uint64_t qb = smem_desc(q0 + kQBytes, 16, 1024, kSmemSwizzle128);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_e4m3(tmem + kColS + 128 * sb, qa + 2 * kk, kd + 2 * kk, kQK, kk != 0);
+          tc_mma_e4m3(tmem + RwCols<RC>::S(sb), qa + 2 * kk, kd + 2 * kk, kQK, kk != 0);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_e4m3(tmem + kColS + 128 * sb, qb + 2 * kk, kd + 2 * kk, kQK, 1u);
+          tc_mma_e4m3(tmem + RwCols<RC>::S(sb), qb + 2 * kk, kd + 2 * kk, kQK, 1u);
         tc_commit(BAR(kBarSFull + sb));
         tc_commit(BAR(kBarKvEmpty + b));
         last_bar = BAR(kBarSFull + sb);
@@ -754,13 +837,13 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         const bool fresh = w.k < 2;              // the unit's first PV into O buffer cb
         // P'' and the V operand of chunk s; a new unit's O once the last
         // unit's rows have been read back
-        if (!rw_wait(BAR(kBarReady + cb), (s >> 1) & 1, abort_s)) break;
-        if (first && w.seg >= 1 && !rw_wait(BAR(kBarOFree), (w.seg - 1) & 1, abort_s)) break;
+        if (!rw_wait_fast(BAR(kBarReady + cb), (s >> 1) & 1, abort_s)) break;
+        if (first && w.seg >= 1 && !rw_wait_fast(BAR(kBarOFree), (w.seg - 1) & 1, abort_s)) break;
         tc_fence_after();
         const uint64_t bd = smem_desc(vf0 + cb * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
 #pragma unroll
         for (int kk = 0; kk < kRwTok / 16; ++kk)
-          tc_mma_f16_tmem_a(tmem + kColO + 128 * cb, tmem + kColS + 128 * cb + 8 * kk,
+          tc_mma_f16_tmem_a(tmem + kColO + 128 * cb, tmem + RwCols<RC>::P(cb) + 8 * kk,
                             bd + (2048 >> 4) * kk, kIdescPV, (fresh && kk == 0) ? 0u : 1u);
         tc_commit(BAR(kBarPvDone + cb));
         last_bar = BAR(kBarPvDone + cb);
@@ -783,8 +866,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     for (int s = 0; w.valid; ++s) {
       const int b = s % kRwStages, vb = s & 1;
       const bool valid = (w.sg.c0 + w.k) * kRwTok + t < w.sg.vis;
-      bool ok = rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
-      if (s >= 2) ok = rw_wait(BAR(kBarPvDone + vb), ((s >> 1) - 1) & 1, abort_s) && ok;
+      bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
+      if (s >= 2) ok = rw_wait_fast(BAR(kBarPvDone + vb), ((s >> 1) - 1) & 1, abort_s) && ok;
       if (__any_sync(0xFFFFFFFFu, !ok)) break;
       const uint8_t *vrow = smem + b * kStageBytes + kCodeBytes + t * kHeadDim;
       uint8_t *vf = smem + kOffVf + vb * kVfBytes + (t >> 3) * 1024 + (t & 7) * 128;
@@ -809,7 +892,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       }
       w.next(pre, p.context_lens, geo, N);
     }
-  } else {
+  } else if (warp < kRwSoftWarps) {
     // ----------------------------------------------------------- softmax
     const int L32 = 32 * warp + lane;           // this thread's TMEM lane
     const int copy = L32 / RC;                  // its token slice [copy RC, copy RC + RC)
@@ -818,6 +901,16 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     float *ts = reinterpret_cast<float *>(smem + kOffTs) + warp * 2 * kRwTok;
     float4 *ml_s = reinterpret_cast<float4 *>(smem + kOffMl);
     bool aborted = false;
+    if constexpr (RwCols<RC>::kSplitP) {
+      // both P'' buffers of this lane zero: a chunk writes only its slice's
+      // columns
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) tmem_st32(tl + RwCols<RC>::P(0) + c, z);
+      tmem_wait_st();
+    }
     ChunkWalk w;
     w.start(pre, p.context_lens, geo, N, x_begin, x_end);
     int s = 0;                                  // chunks consumed
@@ -852,8 +945,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       for (int k = 0; k < sg.n; ++k, ++s) {
         const int b = s % kRwStages, sb = s & 1;
         const int j0 = (sg.c0 + k) * kRwTok + copy * RC;   // this slice's first token
-        bool ok = rw_wait(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
-        ok = ok && rw_wait(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s);
+        bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
+        ok = ok && rw_wait_fast(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s);
         if (__any_sync(0xFFFFFFFFu, !ok)) {
           aborted = true;
           break;
@@ -872,28 +965,32 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
-        const uint32_t scol = tl + kColS + 128 * sb + copy * RC;
+        const uint32_t scol = tl + RwCols<RC>::S(sb) + copy * RC;
         const uint32_t ocol = tl + kColO + 128 * sb;
-        // P'' of the slice; redone (once: the new references cover the
-        // chunk) if a row of the warp outgrew its references
+        // P'' of the slice (references moved on the way where needed)
         float lchunk = 0.0f;
         uint32_t pk[RC < 128 ? RC / 2 : 1];
         if constexpr (RC == 128) {
           rows_chunk_p_direct(scol, ts, ts + RC, lim, rowf, m_ref, E, lchunk, lsum);
         } else {
-          bool redone = false;
-          for (;;) {
-            float mx, vmax;
-            lchunk = 0.0f;
-            const bool over = rows_chunk_p<RC>(scol, ts, ts + RC, lim, rowf, m_ref, E, lchunk,
-                                               mx, vmax, pk);
-            if (!__any_sync(0xFFFFFFFFu, over) || redone) break;
-            rows_new_refs(mx, vmax, m_ref, E, lsum);
-            redone = true;
+          rows_chunk_p<RC>(scol, BAR(kBarSFree + sb), lane, ts, ts + RC, lim, rowf, m_ref, E,
+                           lchunk, lsum, pk);
+          // P'' buffer s & 1 and O buffer s & 1 were last read and written by
+          // PV(s - 2)
+          bool pv_ok = true;
+          if (s >= 2) {
+            const uint32_t pb = BAR(kBarPvDone + sb), ph = ((s >> 1) - 1) & 1;
+            pv_ok = rw_wait_fast(pb, ph, abort_s);
           }
+          if (__any_sync(0xFFFFFFFFu, !pv_ok)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
         }
-        // O buffer s & 1 (no MMA in flight: PV(s - 2) completed before QK(s)
-        // was issued, and PV(s) waits for this chunk's Ready) follows the
+        // O buffer s & 1 (no MMA in flight: PV(s - 2) has completed -- tiles
+        // of 128 rows: before QK(s) was issued -- and PV(s) waits for this
+        // chunk's Ready) follows the
         // present references if a move left it behind; the two references are
         // kept in registers: selected, not indexed
         if (k >= 2) {
@@ -910,17 +1007,15 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           e_o[0] = E;
         }
         lsum += lchunk;
-        // P'' into the first 64 columns of the S buffer: this slice's columns,
-        // zeros in the other slices' (their S values are there)
-        if constexpr (RC < 128) {
-          const uint32_t pbase = tl + kColS + 128 * sb;
+        // this slice's P'' columns of buffer s & 1 (the others stay zero)
+        if constexpr (RwCols<RC>::kSplitP) {
+          const uint32_t pbase = tl + RwCols<RC>::P(sb) + copy * (RC / 2);
 #pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            const int sl = c / (RC / 2);          // the slice these columns belong to
-            uint32_t w8[8];
+          for (int c = 0; c < RC / 2; c += 16) {
+            uint32_t w16[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w8[i] = (sl == copy) ? pk[(c % (RC / 2)) + i] : 0u;
-            tmem_st8u(pbase + c, w8);
+            for (int i = 0; i < 16; ++i) w16[i] = pk[c + i];
+            tmem_st16u(pbase + c, w16);
           }
         }
         tmem_wait_st();
@@ -931,7 +1026,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       // ---- the unit's piece: wait for its last PV
       if (!aborted && sg.n > 0) {
         const int se = s_first + sg.n - 1;
-        if (!rw_wait(BAR(kBarPvDone + (se & 1)), (se >> 1) & 1, abort_s)) aborted = true;
+        if (!rw_wait_fast(BAR(kBarPvDone + (se & 1)), (se >> 1) & 1, abort_s)) aborted = true;
       }
       if (soft_barrier_or(aborted || *abort_s)) {
         aborted = true;
