@@ -313,7 +313,6 @@ class DeviceWorkload:
         # the rows-on-M tensor-core kernel, which merges its pieces itself
         rows = R * w.group
         self.rows_kernel = (self.P_arg == 0 and rows > 8 and rows <= 8192
-                            and not (rows <= 32 and w.block_size <= 128)
                             and w.block_size >= 16 and H % 4 == 0 and w.num_requests <= 1024)
         need = kvq.paged_decode_workspace_size(w.num_requests, R, w.num_q_heads, H, D,
                                                w.block_size, self.max_ctx, self.P_arg)
@@ -393,7 +392,8 @@ class DeviceWorkload:
         the load-balanced kernel when the library picks it (see _stream_mode);
         for at most 8 stacked rows per KV head the page-major kernel when its
         grid (4 heads per CTA) is at least 9 CTAs per SM, else the skinny one
-        (pages of at least 8 tokens); the tcgen05 kernel for 9..32 rows (pages
+        (pages of at least 8 tokens); with an explicit partition the tcgen05
+        kernel for 9..32 rows (pages
         of 16..128 tokens, KV heads a multiple of 4, partitions a multiple of
         128 tokens); else the general one."""
         w = self.w

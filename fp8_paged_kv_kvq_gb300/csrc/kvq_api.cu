@@ -114,13 +114,11 @@ kvq_status make_shape(const kvq_cache *cache, int32_t num_requests, int32_t rows
     return KVQ_ERR_INVALID_ARGUMENT;
   const int32_t G = num_q_heads / cache->num_kv_heads;
   const int64_t M = static_cast<int64_t>(rows_per_request) * G;
-  // more than 32 stacked rows per KV head (9..32 on pages of more than 128
-  // tokens) with the partition size left to the library: the rows-on-M
-  // tensor-core kernel (no partitions, up to kRowsMaxRows rows: wide verify
-  // and chunked prefill).  9..32 rows keep the partitioned tcgen05 kernel,
-  // which is the faster of the two there.
+  // more than 8 stacked rows per KV head with the partition size left to the
+  // library: the rows-on-M tensor-core kernel (no partitions, up to
+  // kRowsMaxRows rows: verify and chunked prefill).  An explicit partition
+  // size keeps 9..32 rows on the partitioned tcgen05 kernel.
   const bool rows_path = partition_tokens == 0 && M > 8 && M <= kvq::kRowsMaxRows &&
-                         !(M <= 32 && cache->block_size <= 128) &&
                          cache->block_size >= 16 && cache->num_kv_heads % 4 == 0 &&
                          num_requests <= kvq::kRowsMaxRequests;
   if (M > kMaxRowsPerKvHead && !rows_path) return KVQ_ERR_UNSUPPORTED;

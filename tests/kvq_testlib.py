@@ -88,6 +88,26 @@ def build_paged(w: workloads.Workload, lens, device="cuda", spare_blocks=3, orac
     return {"cache": cache, "ocache": ocache, "bt": bt, "lens": lens, "S": S}
 
 
+def build_custom(w, kv_per_request, spare_blocks=3):
+    """GPU and oracle caches from given bf16 K/V rows [L, H, D] per request."""
+    lens = np.array([k.shape[0] for k, _ in kv_per_request], dtype=np.int32)
+    bt, nblk = workloads.block_tables(lens, w.block_size, w.seed, spare_blocks=spare_blocks)
+    S = nblk * w.block_size
+    H, D = w.num_kv_heads, w.head_dim
+    cache = kvq.Cache.empty(S, H, D, w.block_size)
+    ocache = oracle.empty_cache(S, H, D)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for r, (k, v) in enumerate(kv_per_request):
+        L = k.shape[0]
+        slots = workloads.token_slots(bt, r, L, w.block_size)
+        kvq.quantize_scatter(cache, k.cuda(), v.cuda(), torch.from_numpy(slots).cuda(), err)
+        oracle.quantize_scatter(workloads.bf16_bits(k).reshape(-1), H * D,
+                                workloads.bf16_bits(v).reshape(-1), H * D, L, H, D, slots, ocache)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return {"cache": cache, "ocache": ocache, "bt": bt, "lens": lens, "S": S}
+
+
 def assert_cache_equal(cache: kvq.Cache, ocache: dict):
     for name in ("k_codes", "v_codes"):
         got = getattr(cache, name).cpu().numpy()

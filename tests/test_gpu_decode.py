@@ -10,8 +10,8 @@ import torch
 import fp8_paged_kv_kvq_gb300 as kvq
 import oracle
 import workloads
-from kvq_testlib import (assert_attention_close, assert_cache_equal, build_paged, gpu_decode,
-                         oracle_decode)
+from kvq_testlib import (assert_attention_close, assert_cache_equal, build_custom, build_paged,
+                         gpu_decode, oracle_decode)
 
 pytestmark = pytest.mark.gpu
 
@@ -100,34 +100,19 @@ def test_load_balanced_split(R, Hq, H, lens):
     assert_attention_close(out, ref, f"balanced R={R} Hq={Hq} H={H}")
 
 
-def _build_custom(w, kv_per_request, spare_blocks=3):
-    """GPU and oracle caches from given bf16 K/V rows [L, H, D] per request."""
-    lens = np.array([k.shape[0] for k, _ in kv_per_request], dtype=np.int32)
-    bt, nblk = workloads.block_tables(lens, w.block_size, w.seed, spare_blocks=spare_blocks)
-    S = nblk * w.block_size
-    H, D = w.num_kv_heads, w.head_dim
-    cache = kvq.Cache.empty(S, H, D, w.block_size)
-    ocache = oracle.empty_cache(S, H, D)
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for r, (k, v) in enumerate(kv_per_request):
-        L = k.shape[0]
-        slots = workloads.token_slots(bt, r, L, w.block_size)
-        kvq.quantize_scatter(cache, k.cuda(), v.cuda(), torch.from_numpy(slots).cuda(), err)
-        oracle.quantize_scatter(workloads.bf16_bits(k).reshape(-1), H * D,
-                                workloads.bf16_bits(v).reshape(-1), H * D, L, H, D, slots, ocache)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    return {"cache": cache, "ocache": ocache, "bt": bt, "lens": lens, "S": S}
-
-
-@pytest.mark.parametrize("partition_tokens", [1024, 8192])
+@pytest.mark.parametrize("partition_tokens", [0, 1024, 8192])
 def test_verify_climbing_scores_move_every_reference(partition_tokens):
     """The verify shape (32 stacked rows per KV head) with keys that grow along
     the context in the query's direction, so every row's score climbs by about
     25 (log2 units) per 128 tokens and every stage moves every row's softmax
-    reference: the tcgen05 kernel switches through all of its accumulator
-    buffers and then rescales in place.  Value magnitudes grow too (the
-    running bound on the value scales moves)."""
+    reference: the partitioned tcgen05 kernel switches through all of its
+    accumulator buffers and then rescales in place; the rows-on-M kernel
+    (partition 0) moves references in the middle of chunks and rescales both
+    of its O buffers.  Value magnitudes grow too, sixfold over the longer
+    context (the running bound on the value scales moves).  (The stated bound
+    is absolute, for values of unit scale: with values grown 14-fold, the f16
+    rounding of P'' alone -- the same in both tensor-core kernels -- already
+    reaches 0.6 of it, so the growth stays moderate.)"""
     w = workloads.scaled(workloads.WORKLOADS["verify"], num_requests=2)
     R, Hq, H, D = w.rows_per_request, w.num_q_heads, w.num_kv_heads, w.head_dim
     G = Hq // H
@@ -137,9 +122,9 @@ def test_verify_climbing_scores_move_every_reference(partition_tokens):
     for L in (5120, 3001):
         t = torch.arange(L, dtype=torch.float32)[:, None, None]
         k = 0.012 * t * u[None] + 0.3 * torch.randn(L, H, D, generator=g)
-        v = torch.randn(L, H, D, generator=g) * (1.0 + t / 400.0)
+        v = torch.randn(L, H, D, generator=g) * (1.0 + t / 1000.0)
         kvs.append((k.to(torch.bfloat16), v.to(torch.bfloat16)))
-    built = _build_custom(w, kvs)
+    built = build_custom(w, kvs)
     q = (u.repeat_interleave(G, dim=0)[None].expand(2 * R, Hq, D) +
          0.1 * torch.randn(2 * R, Hq, D, generator=g)).to(torch.bfloat16)
     out = gpu_decode(built, q, R, w.sm_scale, partition_tokens=partition_tokens)

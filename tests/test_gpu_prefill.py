@@ -19,7 +19,7 @@ import torch
 import fp8_paged_kv_kvq_gb300 as kvq
 import oracle
 import workloads
-from kvq_testlib import assert_attention_close, build_paged
+from kvq_testlib import assert_attention_close, build_custom, build_paged
 
 pytestmark = pytest.mark.gpu
 
@@ -91,3 +91,35 @@ def test_prefill_twice_in_a_row_with_a_shared_workspace():
         torch.cuda.synchronize()
         ref = _oracle_by_head(built, workloads.bf16_bits(q), 384, 4, 4, w.sm_scale, lens)
         assert_attention_close(out, ref, f"prefill shared workspace, call {seed}")
+
+
+def test_prefill_climbing_scores_move_references_mid_chunk():
+    """Tiles of 128 rows store P'' 16 tokens at a time and move a row's
+    references before a group's exponentials, rescaling the P'' already in
+    tensor memory.  Keys that grow along the context in the query's direction
+    make every row's score climb by about 3 (log2 units) per 16 tokens, so
+    references move inside most chunks; value magnitudes grow too (the value
+    bound moves)."""
+    R, H, G, D = 256, 4, 4, 128
+    w = workloads.scaled(workloads.WORKLOADS["prefill"], num_requests=2, rows_per_request=R,
+                         num_q_heads=H * G, num_kv_heads=H, block_size=64)
+    g = workloads.generator(37, 2)
+    u = torch.randn(H, D, generator=g)
+    kvs = []
+    for L in (1536, 700):
+        t = torch.arange(L, dtype=torch.float32)[:, None, None]
+        k = 0.012 * t * u[None] + 0.3 * torch.randn(L, H, D, generator=g)
+        v = torch.randn(L, H, D, generator=g) * (1.0 + t / 300.0)
+        kvs.append((k.to(torch.bfloat16), v.to(torch.bfloat16)))
+    built = build_custom(w, kvs)
+    lens = built["lens"]
+    q = (u.repeat_interleave(G, dim=0)[None].expand(2 * R, H * G, D) +
+         0.1 * torch.randn(2 * R, H * G, D, generator=g)).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kvq.paged_decode(built["cache"], q.cuda(), torch.from_numpy(built["bt"]).cuda(),
+                           torch.from_numpy(lens).cuda(), int(lens.max()), w.sm_scale,
+                           rows_per_request=R, err_flags=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = _oracle_by_head(built, workloads.bf16_bits(q), R, G, H, w.sm_scale, lens)
+    assert_attention_close(out, ref, "prefill, climbing scores")
