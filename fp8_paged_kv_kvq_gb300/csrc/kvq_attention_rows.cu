@@ -58,12 +58,16 @@ namespace {
 
 constexpr int kRwTok = 128;                  // tokens per chunk
 constexpr int kRwStages = 3;                 // code ring depth
-constexpr int kRwSoftWarps = 4;
-constexpr int kRwConvWarps = 4;
-constexpr int kRwWarpTma = kRwSoftWarps + kRwConvWarps;
-constexpr int kRwWarpMma = kRwWarpTma + 1;       // QK^T issuer
-constexpr int kRwWarpPv = kRwWarpMma + 1;        // PV issuer
-constexpr int kRwThreads = (kRwWarpPv + 1) * 32;
+constexpr int kRwSoftWarps = 4;             // warps of a chunk group (one per lane quarter)
+constexpr int kRwGroups = 2;                 // chunk groups: chunk s goes to group s & 1
+constexpr int kRwGroupWarps = kRwGroups * kRwSoftWarps;   // warps 0-7
+constexpr int kRwConvWarps = 4;                             // warps 8-11: V -> f16
+constexpr int kRwWarpConv = kRwGroupWarps;
+constexpr int kRwWarpTma = kRwWarpConv + kRwConvWarps;      // warp 12
+constexpr int kRwWarpMma = kRwWarpTma + 1;                  // warp 13: QK^T issuer
+constexpr int kRwWarpPv = kRwWarpMma + 1;                   // warp 14: PV issuer
+constexpr int kRwThreads = 16 * 32;                         // warp 15 idle
+
 constexpr int kRwIdAhead = 4;                // chunks whose block ids are in flight
 constexpr int kRwMaxPagesPerChunk = 8;       // block size >= 16
 constexpr float kRwLazy = 14.0f;             // log2 of the largest unnormalised p
@@ -102,10 +106,10 @@ constexpr int kOffSc = kRwStages * kStageBytes;
 constexpr int kOffVf = kOffSc + kRwStages * 2 * kScBytes;
 constexpr int kOffQ = kOffVf + 2 * kVfBytes;                  // also the merge scratch
 constexpr int kOffTs = kOffQ + 2 * kQBytes;                   // [warp][K | V][128] fp32
-constexpr int kOffIds = kOffTs + kRwSoftWarps * 2 * kRwTok * 4;
+constexpr int kOffIds = kOffTs + kRwGroups * kRwSoftWarps * 2 * kRwTok * 4;
 constexpr int kOffRowf = kOffIds + (kRwIdAhead + 1) * kRwMaxPagesPerChunk * 4;
-constexpr int kOffMl = kOffRowf + 128 * 4;                    // [128 lanes] (m, l, E, -)
-constexpr int kOffPre = kOffMl + 128 * 16;
+constexpr int kOffMl = kOffRowf + 128 * 4;        // [group][128 lanes] (m, l, E, -)
+constexpr int kOffPre = kOffMl + kRwGroups * 128 * 16;
 constexpr int kOffBar = kOffPre + (kRowsMaxRequests + 4) * 4;
 constexpr int kBarKvFull = 0;
 constexpr int kBarKvEmpty = kBarKvFull + kRwStages;
@@ -189,11 +193,16 @@ __device__ __forceinline__ bool soft_barrier_or(bool flag) {
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
       " bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r) : "r"(flag ? 1u : 0u), "n"(kRwSoftWarps * 32) : "memory");
+      : "=r"(r) : "r"(flag ? 1u : 0u), "n"(kRwGroups * kRwSoftWarps * 32) : "memory");
   return r != 0;
 }
 
-__device__ __forceinline__ void soft_barrier() { named_barrier(1, kRwSoftWarps * 32); }
+__device__ __forceinline__ void soft_barrier() {
+  named_barrier(1, kRwGroups * kRwSoftWarps * 32);
+}
+
+// Barrier over group 0's warps (the unit's final merge).
+__device__ __forceinline__ void group0_barrier() { named_barrier(2, kRwSoftWarps * 32); }
 
 // Smallest e in [-126, 126] with 2^e >= v (v >= 0 given as its bits).
 __device__ __forceinline__ int rw_pow2_ceil(uint32_t bits) {
@@ -687,7 +696,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       mbar_init(BAR(kBarPvDone + b), 1);
     }
     mbar_init(BAR(kBarQReady), kRwSoftWarps);
-    mbar_init(BAR(kBarOFree), kRwSoftWarps);
+    mbar_init(BAR(kBarOFree), kRwGroups * kRwSoftWarps);
     *abort_s = 0;
     fence_mbarrier_init();
   }
@@ -853,14 +862,14 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       }
       if (any) mbar_wait_sleep_bounded(last_bar, last_par);
     }
-  } else if (warp >= kRwSoftWarps && warp < kRwWarpTma) {
+  } else if (warp >= kRwWarpConv && warp < kRwWarpTma) {
     // ------------------------------------------------ V codes -> f16 operand
     // Token t's codes -> f16, MN-major, 128-byte swizzle: dims 64j.. in block j
     // (16 KiB apart), token t at (t/8)*1024 + (t%8)*128, the chunk of dims
     // 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's range get zeros: their
     // stage rows hold stale codes, and a NaN code would poison the product
     // even at p = 0.
-    const int t = 32 * (warp - kRwSoftWarps) + lane;
+    const int t = 32 * (warp - kRwWarpConv) + lane;
     ChunkWalk w;
     w.start(pre, p.context_lens, geo, N, x_begin, x_end);
     for (int s = 0; w.valid; ++s) {
@@ -875,10 +884,12 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       for (int c = 0; c < 8; ++c) {
         uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
         if (valid) w4 = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (t & 7)) << 4));
-        const uint4 lo = make_uint4(codes2_to_f16x2<kFmt>(w4.x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.x >> 16),
-                                    codes2_to_f16x2<kFmt>(w4.y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.y >> 16));
-        const uint4 hi = make_uint4(codes2_to_f16x2<kFmt>(w4.z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.z >> 16),
-                                    codes2_to_f16x2<kFmt>(w4.w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.w >> 16));
+        const uint4 lo =
+            make_uint4(codes2_to_f16x2<kFmt>(w4.x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.x >> 16),
+                       codes2_to_f16x2<kFmt>(w4.y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.y >> 16));
+        const uint4 hi =
+            make_uint4(codes2_to_f16x2<kFmt>(w4.z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.z >> 16),
+                       codes2_to_f16x2<kFmt>(w4.w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.w >> 16));
         uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
         const int c0 = (2 * c) & 7;
         *reinterpret_cast<uint4 *>(blk + ((c0 ^ (t & 7)) << 4)) = lo;
@@ -892,40 +903,49 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       }
       w.next(pre, p.context_lens, geo, N);
     }
-  } else if (warp < kRwSoftWarps) {
-    // ----------------------------------------------------------- softmax
-    const int L32 = 32 * warp + lane;           // this thread's TMEM lane
+  } else if (warp < kRwGroupWarps) {
+    // ------------------------------------------------ chunk groups: softmax
+    // Group gp = warp / 4 takes the chunks s with s & 1 == gp: their P'' (a
+    // thread owns TMEM lane L of quarter warp % 4: row L % RC of the tile,
+    // copy L / RC, tokens [copy RC, copy RC + RC) of each chunk) and O buffer
+    // gp, under references of its own; the groups' partial rows are merged
+    // once per unit.  While one group works on chunk s, the other has chunk
+    // s + 1.
+    const int gp = warp / kRwSoftWarps, q4 = warp % kRwSoftWarps;
+    const int L32 = 32 * q4 + lane;             // this thread's TMEM lane
     const int copy = L32 / RC;                  // its token slice [copy RC, copy RC + RC)
     const int mrow = L32 % RC;                  // its row within the tile
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     float *ts = reinterpret_cast<float *>(smem + kOffTs) + warp * 2 * kRwTok;
     float4 *ml_s = reinterpret_cast<float4 *>(smem + kOffMl);
     bool aborted = false;
     if constexpr (RwCols<RC>::kSplitP) {
-      // both P'' buffers of this lane zero: a chunk writes only its slice's
-      // columns
+      // this group's P'' buffer zero in this lane: a chunk writes only its
+      // slice's columns
       float z[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) tmem_st32(tl + RwCols<RC>::P(0) + c, z);
+      for (int c = 0; c < 64; c += 32) tmem_st32(tl + RwCols<RC>::P(gp) + c, z);
       tmem_wait_st();
     }
     ChunkWalk w;
     w.start(pre, p.context_lens, geo, N, x_begin, x_end);
-    int s = 0;                                  // chunks consumed
+    int s = 0;                                  // chunks consumed (both groups')
     while (w.valid) {
       const Seg sg = w.sg;
       const int r = sg.r, h = sg.h;
       const int row0 = 128 * sg.t;              // the tile's first stacked row
       const int rows_here = min(p.M - row0, RC);
-      // ---- the unit's query tile: rows m < rows_here of the tile, every copy
-      //      (the previous unit's MMAs reading Q and its merge are finished)
-      rows_load_q<RC>(QArgs{p.q, p.R, p.Hq, p.G, p.qk_scale}, r, h, row0, rows_here, smem,
-                      rowf_s, warp, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(kBarQReady));
+      // ---- the unit's query tile (group 0): rows m < rows_here of the tile,
+      //      every copy (the previous unit's MMAs reading Q are finished)
+      if (gp == 0) {
+        rows_load_q<RC>(QArgs{p.q, p.R, p.Hq, p.G, p.qk_scale}, r, h, row0, rows_here, smem,
+                        rowf_s, q4, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(kBarQReady));
+      }
       if (soft_barrier_or(aborted || *abort_s)) {
         aborted = true;
         break;
@@ -937,13 +957,11 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       const float rowf = rowf_s[mrow];
       float m_ref = -INFINITY, lsum = 0.0f;
       int E = -126;
-      // the references O buffer b holds its rows under (written once chunk
-      // s_first + b has been issued)
-      float ref_o[2] = {-INFINITY, -INFINITY};
-      int e_o[2] = {-126, -126};
+      int mine = 0;                             // this group's chunks of the unit so far
       const int s_first = s;
       for (int k = 0; k < sg.n; ++k, ++s) {
-        const int b = s % kRwStages, sb = s & 1;
+        if ((s & 1) != gp) continue;
+        const int b = s % kRwStages, sb = gp;
         const int j0 = (sg.c0 + k) * kRwTok + copy * RC;   // this slice's first token
         bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
         ok = ok && rw_wait_fast(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s);
@@ -966,7 +984,9 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
         const uint32_t scol = tl + RwCols<RC>::S(sb) + copy * RC;
-        const uint32_t ocol = tl + kColO + 128 * sb;
+        const uint32_t ocol = tl + kColO + 128 * gp;
+        const float m0 = m_ref;                 // the references O buffer gp is under
+        const int e0 = E;
         // P'' of the slice (references moved on the way where needed)
         float lchunk = 0.0f;
         uint32_t pk[RC < 128 ? RC / 2 : 1];
@@ -975,8 +995,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         } else {
           rows_chunk_p<RC>(scol, BAR(kBarSFree + sb), lane, ts, ts + RC, lim, rowf, m_ref, E,
                            lchunk, lsum, pk);
-          // P'' buffer s & 1 and O buffer s & 1 were last read and written by
-          // PV(s - 2)
+          // P'' buffer gp and O buffer gp were last used by PV(s - 2)
           bool pv_ok = true;
           if (s >= 2) {
             const uint32_t pb = BAR(kBarPvDone + sb), ph = ((s >> 1) - 1) & 1;
@@ -988,26 +1007,13 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           }
           tc_fence_after();
         }
-        // O buffer s & 1 (no MMA in flight: PV(s - 2) has completed -- tiles
-        // of 128 rows: before QK(s) was issued -- and PV(s) waits for this
-        // chunk's Ready) follows the
-        // present references if a move left it behind; the two references are
-        // kept in registers: selected, not indexed
-        if (k >= 2) {
-          const float rb = sb ? ref_o[1] : ref_o[0];
-          const int eb = sb ? e_o[1] : e_o[0];
-          if (__any_sync(0xFFFFFFFFu, rb != m_ref || eb != E))
-            rows_rescale_o(ocol, (rb == -INFINITY) ? 0.0f : rw_ex2(rb - m_ref) * pow2f_down(eb - E));
-        }
-        if (sb) {
-          ref_o[1] = m_ref;
-          e_o[1] = E;
-        } else {
-          ref_o[0] = m_ref;
-          e_o[0] = E;
-        }
+        // O buffer gp holds the group's earlier chunks of the unit under the
+        // references of the chunk's start: brought to the present ones if they
+        // moved (no MMA in flight on it: PV(s - 2) has completed)
+        if (mine > 0 && __any_sync(0xFFFFFFFFu, m_ref != m0 || E != e0))
+          rows_rescale_o(ocol, (m0 == -INFINITY) ? 0.0f : rw_ex2(m0 - m_ref) * pow2f_down(e0 - E));
         lsum += lchunk;
-        // this slice's P'' columns of buffer s & 1 (the others stay zero)
+        // this slice's P'' columns of buffer gp (the others stay zero)
         if constexpr (RwCols<RC>::kSplitP) {
           const uint32_t pbase = tl + RwCols<RC>::P(sb) + copy * (RC / 2);
 #pragma unroll
@@ -1022,8 +1028,9 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(kBarReady + sb));
+        ++mine;
       }
-      // ---- the unit's piece: wait for its last PV
+      // ---- the unit's piece: wait for its last PV (the MMAs complete in order)
       if (!aborted && sg.n > 0) {
         const int se = s_first + sg.n - 1;
         if (!rw_wait_fast(BAR(kBarPvDone + (se & 1)), (se >> 1) & 1, abort_s)) aborted = true;
@@ -1036,28 +1043,29 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         break;
       }
       tc_fence_after();
-      // ---- merge the copies (token slices) of each row: exchange (m, l, E),
-      //      then add the scaled O rows copy after copy in shared memory; the
-      //      last copy's threads end up with the unit's rows
-      ml_s[L32] = make_float4(m_ref, lsum, static_cast<float>(E), 0.0f);
+      // ---- merge each row's partial results -- kRwGroups x kCopies of them
+      //      (group, token slice) -- exchanging (m, l, E); group 0 then reads
+      //      both groups' O buffers and adds the copies' rows one after
+      //      another in shared memory (the query tile's space, idle until the
+      //      next unit); the last copy's threads end up with the unit's rows
+      constexpr int kParts = kRwGroups * kCopies;
+      ml_s[gp * 128 + L32] = make_float4(m_ref, lsum, static_cast<float>(E), 0.0f);
       soft_barrier();
       float m_all = -INFINITY;
       int e_all = -126;
 #pragma unroll
-      for (int c = 0; c < kCopies; ++c) {
-        const float4 v = ml_s[c * RC + mrow];
+      for (int c = 0; c < kParts; ++c) {
+        const float4 v = ml_s[(c / kCopies) * 128 + (c % kCopies) * RC + mrow];
         m_all = fmaxf(m_all, v.x);
         if (v.x != -INFINITY) e_all = max(e_all, static_cast<int>(v.z));
       }
       float l_all = 0.0f;
 #pragma unroll
-      for (int c = 0; c < kCopies; ++c) {
-        const float4 v = ml_s[c * RC + mrow];
+      for (int c = 0; c < kParts; ++c) {
+        const float4 v = ml_s[(c / kCopies) * 128 + (c % kCopies) * RC + mrow];
         if (v.x != -INFINITY) l_all += rw_ex2(v.x - m_all) * v.y;
       }
-      const float f_me = (m_ref == -INFINITY) ? 0.0f
-                                              : rw_ex2(m_ref - m_all) * pow2f_down(E - e_all);
-      const bool writer = (copy == kCopies - 1) && row_ok;
+      const bool writer = gp == 0 && (copy == kCopies - 1) && row_ok;
       const bool direct = (sg.c0 == 0 && sg.n == sg.C);
       const float vsc = pow2f(e_all);           // undo the 2^-E of P''
       const int ir = ma / p.G, gq = ma - ir * p.G;
@@ -1066,66 +1074,70 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       const int slot = 2 * static_cast<int>(blockIdx.x) +
                        (static_cast<int>(blockIdx.x) == b_first ? 1 : 0);
       const float inv = (l_all > 0.0f) ? vsc / l_all : 0.0f;
-      // the two O buffers under this thread's final references (a buffer the
-      // unit never wrote -- one chunk -- is not read)
-      const int bf = s_first & 1;
-      const bool both = sg.n > 1;
-      float fo0 = (ref_o[0] == -INFINITY) ? 0.0f
-                                          : f_me * rw_ex2(ref_o[0] - m_ref) * pow2f_down(e_o[0] - E);
-      float fo1 = (ref_o[1] == -INFINITY) ? 0.0f
-                                          : f_me * rw_ex2(ref_o[1] - m_ref) * pow2f_down(e_o[1] - E);
-      if (bf) {                                 // fo0: the first chunk's buffer
-        const float t = fo0;
-        fo0 = fo1;
-        fo1 = t;
-      }
-      const uint32_t ob0 = tl + kColO + 128 * bf, ob1 = tl + kColO + 128 * (bf ^ 1);
-      float *acc = reinterpret_cast<float *>(smem + kOffQ);    // [dim][RC]
-      for (int c = 0; c < kCopies; ++c) {
-        if (copy == c) {
+      if (gp == 0) {
+        // this lane's rows of both O buffers under the unit's references (a
+        // buffer a group did not write in this unit -- one chunk -- is not read)
+        const float4 v1 = ml_s[128 + L32];
+        const float f0 = (m_ref == -INFINITY) ? 0.0f
+                                              : rw_ex2(m_ref - m_all) * pow2f_down(E - e_all);
+        const float f1 = (v1.x == -INFINITY)
+                             ? 0.0f
+                             : rw_ex2(v1.x - m_all) * pow2f_down(static_cast<int>(v1.z) - e_all);
+        const bool has0 = mine > 0;
+        const bool has1 = sg.n + (s_first & 1) >= 2;   // group 1 had a chunk of the unit
+        float *acc = reinterpret_cast<float *>(smem + kOffQ);    // [dim][RC]
+        for (int c = 0; c < kCopies; ++c) {
+          if (copy == c) {
 #pragma unroll 1
-          for (int pc = 0; pc < 4; ++pc) {
-            float o[32];
-            tmem_ld32(ob0 + 32 * pc, o);
+            for (int pc = 0; pc < 4; ++pc) {
+              float o[32];
+              if (has0) {
+                tmem_ld32(tl + kColO + 32 * pc, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= fo0;
-            if (both) {
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                float o2[16];
-                tmem_ld16(ob1 + 32 * pc + 16 * hh, o2);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) o[16 * hh + i] = fmaf(o2[i], fo1, o[16 * hh + i]);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (c > 0) o[i] += acc[(32 * pc + i) * RC + mrow];
-              if (c < kCopies - 1) acc[(32 * pc + i) * RC + mrow] = o[i];
-            }
-            if (c == kCopies - 1 && writer) {
-              if (direct) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + 32 * pc);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8)
-                  dst[c8] = make_uint4(pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv),
-                                       pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv),
-                                       pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv),
-                                       pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv));
+                for (int i = 0; i < 32; ++i) o[i] *= f0;
               } else {
-                float4 *dst = reinterpret_cast<float4 *>(
-                    p.o_part + (static_cast<int64_t>(slot) * RC + mrow) * kHeadDim + 32 * pc);
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4)
-                  dst[c4] = make_float4(o[4 * c4] * vsc, o[4 * c4 + 1] * vsc,
-                                        o[4 * c4 + 2] * vsc, o[4 * c4 + 3] * vsc);
+                for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+              }
+              if (has1) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  float o2[16];
+                  tmem_ld16(tl + kColO + 128 + 32 * pc + 16 * hh, o2);
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[16 * hh + i] = fmaf(o2[i], f1, o[16 * hh + i]);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                if (c > 0) o[i] += acc[(32 * pc + i) * RC + mrow];
+                if (c < kCopies - 1) acc[(32 * pc + i) * RC + mrow] = o[i];
+              }
+              if (c == kCopies - 1 && writer) {
+                if (direct) {
+                  uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + 32 * pc);
+#pragma unroll
+                  for (int c8 = 0; c8 < 4; ++c8)
+                    dst[c8] = make_uint4(pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv),
+                                         pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv),
+                                         pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv),
+                                         pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv));
+                } else {
+                  float4 *dst = reinterpret_cast<float4 *>(
+                      p.o_part + (static_cast<int64_t>(slot) * RC + mrow) * kHeadDim + 32 * pc);
+#pragma unroll
+                  for (int c4 = 0; c4 < 8; ++c4)
+                    dst[c4] = make_float4(o[4 * c4] * vsc, o[4 * c4 + 1] * vsc,
+                                          o[4 * c4 + 2] * vsc, o[4 * c4 + 3] * vsc);
+                }
               }
             }
           }
+          if (kCopies > 1) group0_barrier();
         }
-        if (kCopies > 1) soft_barrier();
       }
-      // the O rows have been read: the next unit's PVs may overwrite them
+      // the O rows have been read (group 1's arrival only counts): the next
+      // unit's PVs may overwrite them
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(kBarOFree));
@@ -1151,7 +1163,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if (*ticket_s) {
           // every piece of the unit: warp per row, lane per 4 dims, running
           // log-sum-exp over the pieces
-          for (int m = warp; m < rows_here; m += kRwSoftWarps) {
+          for (int m = warp; m < rows_here; m += kRwGroupWarps) {
             float mw = -INFINITY, ls = 0.0f;
             float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int bb = b_first; bb <= b_last; ++bb) {
@@ -1185,8 +1197,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     // units whose rows see no token: zero rows, spread over the grid
     if (!aborted) {
       const int n_units = N * p.H * p.T;
-      for (int u = blockIdx.x * kRwSoftWarps + warp; u < n_units;
-           u += gridDim.x * kRwSoftWarps) {
+      for (int u = blockIdx.x * kRwGroupWarps + warp; u < n_units;
+           u += gridDim.x * kRwGroupWarps) {
         const int t = u % p.T, rh = u / p.T, h = rh % p.H, r = rh / p.H;
         const int L = clamp_len(p.context_lens[r], p.ctx_limit);
         if (tile_tokens(geo, L, t) > 0) continue;
