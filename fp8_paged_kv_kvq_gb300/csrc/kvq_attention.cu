@@ -946,7 +946,11 @@ EncodeTiledFn encode_tiled_fn() {
 }  // namespace
 
 // A map over one code plane [num_slots, H, 128] uint8: boxes of `rows` slots of
-// one head, 128-byte swizzled in shared memory.
+// one head, 128-byte swizzled in shared memory.  A box row is one 128-byte
+// line and the next slot's row of the same head is H lines further, so L2
+// promotion stays at 128 bytes: wider promotion would fetch the neighbouring
+// head's line from DRAM, wasted unless that head's reader comes by while it
+// is still in L2.
 bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_slots, int H,
                             int rows) {
   EncodeTiledFn f = encode_tiled_fn();
@@ -959,7 +963,7 @@ bool encode_code_tensor_map(CUtensorMap *map, const uint8_t *codes, int64_t num_
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   return f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(codes), dims, strides,
            box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_code_tensor_map_strided(CUtensorMap *map, const uint8_t *codes, int64_t num_slots,

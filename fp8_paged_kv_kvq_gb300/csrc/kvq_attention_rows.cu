@@ -34,12 +34,13 @@
 //    K = 128 tokens, kind::f16, A = P'' = p v_scale 2^-E read from TMEM (the
 //    softmax writes it there as f16), B = the V codes converted exactly to f16
 //    (MN-major, 128-byte swizzle) by four converter warps.
-//  * Warp roles (352 threads): 0-3 softmax (TMEM lane quarters 0-3), 4-7 V
-//    conversion, 8 TMA (block ids fetched ahead by cp.async, one 3-D box per
-//    page and plane, one 2-D box of 4 heads' scales per page and plane), 9
-//    QK^T MMAs and 10 PV MMAs (one lane each: the two chains of tensor-core
-//    work run side by side).  TMEM: two S buffers, O, two P buffers (512
-//    columns).
+//  * Warp roles (512 threads): 0-3 and 4-7 two softmax groups (each covering
+//    TMEM lane quarters 0-3), group g taking the chunks s with s & 1 == g
+//    under references of its own and accumulating into O buffer g; 8-11 V
+//    conversion; 12 TMA (block ids fetched ahead by cp.async, one 3-D box per
+//    page and plane, one 2-D box of 4 heads' scales per page and plane); 13
+//    QK^T MMAs and 14 PV MMAs (one lane each: the two chains of tensor-core
+//    work run side by side); 15 idle.  TMEM layouts: see RwCols.
 //  * Every wait is bounded; a role that gives up raises a shared abort flag,
 //    the softmax warps agree on it at their barriers, copies and MMAs in
 //    flight complete, the CTA frees its tensor memory (KVQ_ERRF_WAIT_TIMEOUT).
@@ -73,13 +74,14 @@ constexpr int kRwMaxPagesPerChunk = 8;       // block size >= 16
 constexpr float kRwLazy = 14.0f;             // log2 of the largest unnormalised p
 constexpr float kRwOvershoot = 4.0f;         // a moved reference sits this far above the max
 
-// TMEM: S buffer b at columns 128 b .. 128 b + 127; once the softmax has read
-// S of chunk s it writes P'' of chunk s into the first 64 columns of the same
-// buffer (f16 pairs, the PV MMA's A operand).  O buffer b at 256 + 128 b: the
-// PV of chunk s accumulates into O buffer s & 1, so a reference move at
-// chunk s rescales buffer s & 1 -- last written by PV(s - 2), complete before
-// QK(s) was issued -- and buffer (s + 1) & 1 at chunk s + 1: neither waits for
-// an MMA in flight.  The epilogue adds the two with their references.
+// TMEM, tiles of 128 rows: S buffer b at columns 128 b .. 128 b + 127; once
+// the softmax has read S of chunk s it writes P'' of chunk s into the first 64
+// columns of the same buffer (f16 pairs, the PV MMA's A operand).  O buffer b
+// at 256 + 128 b: the PV of chunk s accumulates into O buffer s & 1, the
+// buffer of the softmax group that takes chunk s, so a reference move of that
+// group rescales only its own buffer -- last written by PV(s - 2), complete
+// before QK(s) was issued: no wait for an MMA in flight.  The epilogue adds
+// the two with their references.
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kRwTmemCols = 512;
@@ -739,6 +741,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     }
     uint32_t u = 0;
     bool bad = false, stop = false;
+    const uint64_t pol = l2_policy_evict_first();
     for (; iw.valid && !stop; ++u) {
       fetch(fw, (u + kRwIdAhead) % (kRwIdAhead + 1));
       fw.next(pre, p.context_lens, geo, N);
@@ -768,8 +771,11 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
               continue;
             }
             const int z = static_cast<int>((blk << p.log2_bs) | (j & ((1 << p.log2_bs) - 1)));
-            tma_load_3d(kdst + i * p.box * kHeadDim, &tm_kc, 0, h, z, fb);
-            tma_load_3d(vdst + i * p.box * kHeadDim, &tm_vc, 0, h, z, fb);
+            // the codes are read once: evict them first, so the scale lines
+            // (each 32-byte sector holds 8 heads' scales of a slot, wanted by
+            // 8 units at different times) stay in L2 longer
+            tma_load_3d_hint(kdst + i * p.box * kHeadDim, &tm_kc, 0, h, z, fb, pol);
+            tma_load_3d_hint(vdst + i * p.box * kHeadDim, &tm_vc, 0, h, z, fb, pol);
             tma_load_2d(ksd + i * p.box * 16, &tm_ks, h & ~3, z, fb);
             tma_load_2d(vsd + i * p.box * 16, &tm_vs, h & ~3, z, fb);
             bytes += 2u * p.box * kHeadDim + 2u * p.box * 16u;

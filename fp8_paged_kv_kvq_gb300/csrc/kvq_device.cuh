@@ -334,6 +334,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+// An L2 policy that marks lines first in line for eviction (data read once).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+// tma_load_3d under an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int x, int y,
+                                                 int z, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n"
+      :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y,
                                             uint32_t bar) {
   asm volatile(
