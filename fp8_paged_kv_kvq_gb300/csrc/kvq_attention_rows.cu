@@ -570,7 +570,9 @@ __device__ __forceinline__ void rows_chunk_p_direct(uint32_t scol, const float *
 
 // The unit's query tile (rows m < rows_here of tile row0, every copy) as two
 // e4m3 pieces per element in the K-major 128-byte swizzled layout, and each
-// row's factor 2^e sm_scale log2(e); each softmax warp takes every 4th row.
+// row's factor 2^e sm_scale log2(e).  The 8 softmax warps take every 8th row;
+// the rows are fetched into registers while the previous unit's epilogue
+// runs (the tile's space is its scratch) and stored afterwards.
 struct QArgs {
   const uint16_t *q;
   int32_t R, Hq, G;
@@ -578,26 +580,34 @@ struct QArgs {
 };
 
 template <int RC>
-__device__ __noinline__ void rows_load_q(const QArgs p, int r, int h, int row0, int rows_here,
-                                         uint8_t *smem, float *rowf_s, int warp, int lane) {
-  constexpr int kCopies = 128 / RC;
-  constexpr int kQRows = RC / kRwSoftWarps;          // rows per warp, loaded at once
-  uint2 qv[kQRows];
+struct QRows {
+  uint2 v[RC / kRwGroupWarps];                  // this warp's rows, 4 bf16 per lane
+};
+
+template <int RC>
+__device__ __forceinline__ void rows_fetch_q(QRows<RC> &f, const QArgs p, int r, int h,
+                                             int row0, int rows_here, int warp, int lane) {
 #pragma unroll
-  for (int i = 0; i < kQRows; ++i) {
-    const int m = warp + kRwSoftWarps * i;
-    qv[i] = make_uint2(0u, 0u);
+  for (int i = 0; i < RC / kRwGroupWarps; ++i) {
+    const int m = warp + kRwGroupWarps * i;
+    f.v[i] = make_uint2(0u, 0u);
     if (m < rows_here) {
       const int ma = row0 + m, ir = ma / p.G, gq = ma - ir * p.G;
-      qv[i] = *reinterpret_cast<const uint2 *>(
+      f.v[i] = *reinterpret_cast<const uint2 *>(
           p.q + ((static_cast<int64_t>(r) * p.R + ir) * p.Hq + h * p.G + gq) * kHeadDim +
           4 * lane);
     }
   }
+}
+
+template <int RC>
+__device__ __forceinline__ void rows_store_q(const QRows<RC> &f, float qk_scale, uint8_t *smem,
+                                             float *rowf_s, int warp, int lane) {
+  constexpr int kCopies = 128 / RC;
 #pragma unroll 1
-  for (int i = 0; i < kQRows; ++i) {
-    const int m = warp + kRwSoftWarps * i;
-    const uint2 v = qv[i];
+  for (int i = 0; i < RC / kRwGroupWarps; ++i) {
+    const int m = warp + kRwGroupWarps * i;
+    const uint2 v = f.v[i];
     float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
                        fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
 #pragma unroll
@@ -614,7 +624,7 @@ __device__ __noinline__ void rows_load_q(const QArgs p, int r, int h, int row0, 
                            bf16_hi(v.y) * inv};
       e4m3_pieces4(xs, c1w, c2w);
     }
-    if (lane == 0) rowf_s[m] = rx * p.qk_scale;
+    if (lane == 0) rowf_s[m] = rx * qk_scale;
 #pragma unroll
     for (int c = 0; c < kCopies; ++c) {
       const int row = c * RC + m;
@@ -697,7 +707,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       mbar_init(BAR(kBarReady + b), kRwSoftWarps + kRwConvWarps);
       mbar_init(BAR(kBarPvDone + b), 1);
     }
-    mbar_init(BAR(kBarQReady), kRwSoftWarps);
+    mbar_init(BAR(kBarQReady), kRwGroupWarps);
     mbar_init(BAR(kBarOFree), kRwGroups * kRwSoftWarps);
     *abort_s = 0;
     fence_mbarrier_init();
@@ -937,21 +947,24 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     }
     ChunkWalk w;
     w.start(pre, p.context_lens, geo, N, x_begin, x_end);
+    const QArgs qa{p.q, p.R, p.Hq, p.G, p.qk_scale};
+    QRows<RC> qrows;
+    if (w.valid)
+      rows_fetch_q<RC>(qrows, qa, w.sg.r, w.sg.h, 128 * w.sg.t, min(p.M - 128 * w.sg.t, RC),
+                       warp, lane);
     int s = 0;                                  // chunks consumed (both groups')
     while (w.valid) {
       const Seg sg = w.sg;
       const int r = sg.r, h = sg.h;
       const int row0 = 128 * sg.t;              // the tile's first stacked row
       const int rows_here = min(p.M - row0, RC);
-      // ---- the unit's query tile (group 0): rows m < rows_here of the tile,
-      //      every copy (the previous unit's MMAs reading Q are finished)
-      if (gp == 0) {
-        rows_load_q<RC>(QArgs{p.q, p.R, p.Hq, p.G, p.qk_scale}, r, h, row0, rows_here, smem,
-                        rowf_s, q4, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(kBarQReady));
-      }
+      // ---- the unit's query tile (fetched ahead): rows m < rows_here of the
+      //      tile, every copy (the previous unit's MMAs reading Q and its
+      //      merge are finished)
+      rows_store_q<RC>(qrows, p.qk_scale, smem, rowf_s, warp, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(kBarQReady));
       if (soft_barrier_or(aborted || *abort_s)) {
         aborted = true;
         break;
@@ -1036,6 +1049,12 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if (lane == 0) mbar_arrive(BAR(kBarReady + sb));
         ++mine;
       }
+      // ---- the next unit's query rows into registers: their loads overlap
+      //      this unit's epilogue
+      w.advance_segment(pre, p.context_lens, geo, N);
+      if (w.valid)
+        rows_fetch_q<RC>(qrows, qa, w.sg.r, w.sg.h, 128 * w.sg.t, min(p.M - 128 * w.sg.t, RC),
+                         warp, lane);
       // ---- the unit's piece: wait for its last PV (the MMAs complete in order)
       if (!aborted && sg.n > 0) {
         const int se = s_first + sg.n - 1;
@@ -1051,9 +1070,8 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       tc_fence_after();
       // ---- merge each row's partial results -- kRwGroups x kCopies of them
       //      (group, token slice) -- exchanging (m, l, E); group 0 then reads
-      //      both groups' O buffers and adds the copies' rows one after
-      //      another in shared memory (the query tile's space, idle until the
-      //      next unit); the last copy's threads end up with the unit's rows
+      //      both groups' O buffers and sums the slices through shared memory
+      //      (the query tile's space, idle until the next unit)
       constexpr int kParts = kRwGroups * kCopies;
       ml_s[gp * 128 + L32] = make_float4(m_ref, lsum, static_cast<float>(E), 0.0f);
       soft_barrier();
@@ -1091,55 +1109,97 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
                              : rw_ex2(v1.x - m_all) * pow2f_down(static_cast<int>(v1.z) - e_all);
         const bool has0 = mine > 0;
         const bool has1 = sg.n + (s_first & 1) >= 2;   // group 1 had a chunk of the unit
-        float *acc = reinterpret_cast<float *>(smem + kOffQ);    // [dim][RC]
-        for (int c = 0; c < kCopies; ++c) {
-          if (copy == c) {
+        // 32 dims of this lane's row from both buffers, under the unit's
+        // references
+        auto o_rows = [&](int d0, float (&o)[32]) {
+          if (has0) {
+            tmem_ld32(tl + kColO + d0, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= f0;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+          }
+          if (has1) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float o2[16];
+              tmem_ld16(tl + kColO + 128 + d0 + 16 * hh, o2);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[16 * hh + i] = fmaf(o2[i], f1, o[16 * hh + i]);
+            }
+          }
+        };
+        if constexpr (kCopies == 1) {
+          // one slice: the thread holds its whole row
 #pragma unroll 1
-            for (int pc = 0; pc < 4; ++pc) {
-              float o[32];
-              if (has0) {
-                tmem_ld32(tl + kColO + 32 * pc, o);
+          for (int pc = 0; pc < 4; ++pc) {
+            float o[32];
+            o_rows(32 * pc, o);
+            if (row_ok) {
+              if (direct) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + 32 * pc);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= f0;
+                for (int c8 = 0; c8 < 4; ++c8)
+                  dst[c8] = make_uint4(pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv),
+                                       pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv),
+                                       pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv),
+                                       pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv));
               } else {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.o_part + (static_cast<int64_t>(slot) * RC + mrow) * kHeadDim + 32 * pc);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-              }
-              if (has1) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  float o2[16];
-                  tmem_ld16(tl + kColO + 128 + 32 * pc + 16 * hh, o2);
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) o[16 * hh + i] = fmaf(o2[i], f1, o[16 * hh + i]);
-                }
-              }
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                if (c > 0) o[i] += acc[(32 * pc + i) * RC + mrow];
-                if (c < kCopies - 1) acc[(32 * pc + i) * RC + mrow] = o[i];
-              }
-              if (c == kCopies - 1 && writer) {
-                if (direct) {
-                  uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + 32 * pc);
-#pragma unroll
-                  for (int c8 = 0; c8 < 4; ++c8)
-                    dst[c8] = make_uint4(pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv),
-                                         pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv),
-                                         pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv),
-                                         pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv));
-                } else {
-                  float4 *dst = reinterpret_cast<float4 *>(
-                      p.o_part + (static_cast<int64_t>(slot) * RC + mrow) * kHeadDim + 32 * pc);
-#pragma unroll
-                  for (int c4 = 0; c4 < 8; ++c4)
-                    dst[c4] = make_float4(o[4 * c4] * vsc, o[4 * c4 + 1] * vsc,
-                                          o[4 * c4 + 2] * vsc, o[4 * c4 + 3] * vsc);
-                }
+                for (int c4 = 0; c4 < 8; ++c4)
+                  dst[c4] = make_float4(o[4 * c4] * vsc, o[4 * c4 + 1] * vsc,
+                                        o[4 * c4 + 2] * vsc, o[4 * c4 + 3] * vsc);
               }
             }
           }
-          if (kCopies > 1) group0_barrier();
+        } else {
+          // the slices' rows through shared memory (the query tile's space),
+          // 64 dims at a time: every thread puts its row's dims there, then
+          // sums the slices over kSl of them for its row and writes those
+          constexpr int kSl = 64 / kCopies;
+          float *xs = reinterpret_cast<float *>(smem + kOffQ);   // [copy][64 dims][RC]
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+            for (int pc = 0; pc < 2; ++pc) {
+              float o[32];
+              o_rows(64 * half + 32 * pc, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) xs[(copy * 64 + 32 * pc + i) * RC + mrow] = o[i];
+            }
+            group0_barrier();
+            float a[kSl];
+#pragma unroll
+            for (int j = 0; j < kSl; ++j) {
+              float t = 0.0f;
+#pragma unroll
+              for (int c = 0; c < kCopies; ++c) t += xs[(c * 64 + copy * kSl + j) * RC + mrow];
+              a[j] = t;
+            }
+            const int d0 = 64 * half + copy * kSl;
+            if (row_ok) {
+              if (direct) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * kHeadDim + d0);
+#pragma unroll
+                for (int c8 = 0; c8 < kSl / 8; ++c8)
+                  dst[c8] = make_uint4(pack_bf16x2(a[8 * c8] * inv, a[8 * c8 + 1] * inv),
+                                       pack_bf16x2(a[8 * c8 + 2] * inv, a[8 * c8 + 3] * inv),
+                                       pack_bf16x2(a[8 * c8 + 4] * inv, a[8 * c8 + 5] * inv),
+                                       pack_bf16x2(a[8 * c8 + 6] * inv, a[8 * c8 + 7] * inv));
+              } else {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.o_part + (static_cast<int64_t>(slot) * RC + mrow) * kHeadDim + d0);
+#pragma unroll
+                for (int c4 = 0; c4 < kSl / 4; ++c4)
+                  dst[c4] = make_float4(a[4 * c4] * vsc, a[4 * c4 + 1] * vsc,
+                                        a[4 * c4 + 2] * vsc, a[4 * c4 + 3] * vsc);
+              }
+            }
+            group0_barrier();                   // (before the next half overwrites xs)
+          }
         }
       }
       // the O rows have been read (group 1's arrival only counts): the next
@@ -1196,7 +1256,6 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         }
       }
       soft_barrier();                           // the merge scratch is free again
-      w.advance_segment(pre, p.context_lens, geo, N);
     }
     if (aborted && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
     if (aborted) *abort_s = 1;
