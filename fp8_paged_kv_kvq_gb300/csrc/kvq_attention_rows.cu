@@ -62,12 +62,10 @@ constexpr int kRwStages = 3;                 // code ring depth
 constexpr int kRwSoftWarps = 4;             // warps of a chunk group (one per lane quarter)
 constexpr int kRwGroups = 2;                 // chunk groups: chunk s goes to group s & 1
 constexpr int kRwGroupWarps = kRwGroups * kRwSoftWarps;   // warps 0-7
-constexpr int kRwConvWarps = 4;                             // warps 8-11: V -> f16
-constexpr int kRwWarpConv = kRwGroupWarps;
-constexpr int kRwWarpTma = kRwWarpConv + kRwConvWarps;      // warp 12
-constexpr int kRwWarpMma = kRwWarpTma + 1;                  // warp 13: QK^T issuer
-constexpr int kRwWarpPv = kRwWarpMma + 1;                   // warp 14: PV issuer
-constexpr int kRwThreads = 16 * 32;                         // warp 15 idle
+constexpr int kRwWarpTma = kRwGroupWarps;                   // warp 8
+constexpr int kRwWarpMma = kRwWarpTma + 1;                  // warp 9: QK^T issuer
+constexpr int kRwWarpPv = kRwWarpMma + 1;                   // warp 10: PV issuer
+constexpr int kRwThreads = (kRwWarpPv + 1) * 32;
 
 constexpr int kRwIdAhead = 4;                // chunks whose block ids are in flight
 constexpr int kRwMaxPagesPerChunk = 8;       // block size >= 16
@@ -699,12 +697,12 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
   if (tid == 32) {
     for (int s = 0; s < kRwStages; ++s) {
       mbar_init(BAR(kBarKvFull + s), 1);
-      mbar_init(BAR(kBarKvEmpty + s), 1 + kRwConvWarps + kRwSoftWarps);
+      mbar_init(BAR(kBarKvEmpty + s), 1 + kRwSoftWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(kBarSFull + b), 1);
       mbar_init(BAR(kBarSFree + b), kRwSoftWarps);
-      mbar_init(BAR(kBarReady + b), kRwSoftWarps + kRwConvWarps);
+      mbar_init(BAR(kBarReady + b), kRwSoftWarps);
       mbar_init(BAR(kBarPvDone + b), 1);
     }
     mbar_init(BAR(kBarQReady), kRwGroupWarps);
@@ -878,47 +876,6 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       }
       if (any) mbar_wait_sleep_bounded(last_bar, last_par);
     }
-  } else if (warp >= kRwWarpConv && warp < kRwWarpTma) {
-    // ------------------------------------------------ V codes -> f16 operand
-    // Token t's codes -> f16, MN-major, 128-byte swizzle: dims 64j.. in block j
-    // (16 KiB apart), token t at (t/8)*1024 + (t%8)*128, the chunk of dims
-    // 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's range get zeros: their
-    // stage rows hold stale codes, and a NaN code would poison the product
-    // even at p = 0.
-    const int t = 32 * (warp - kRwWarpConv) + lane;
-    ChunkWalk w;
-    w.start(pre, p.context_lens, geo, N, x_begin, x_end);
-    for (int s = 0; w.valid; ++s) {
-      const int b = s % kRwStages, vb = s & 1;
-      const bool valid = (w.sg.c0 + w.k) * kRwTok + t < w.sg.vis;
-      bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
-      if (s >= 2) ok = rw_wait_fast(BAR(kBarPvDone + vb), ((s >> 1) - 1) & 1, abort_s) && ok;
-      if (__any_sync(0xFFFFFFFFu, !ok)) break;
-      const uint8_t *vrow = smem + b * kStageBytes + kCodeBytes + t * kHeadDim;
-      uint8_t *vf = smem + kOffVf + vb * kVfBytes + (t >> 3) * 1024 + (t & 7) * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) w4 = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (t & 7)) << 4));
-        const uint4 lo =
-            make_uint4(codes2_to_f16x2<kFmt>(w4.x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.x >> 16),
-                       codes2_to_f16x2<kFmt>(w4.y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.y >> 16));
-        const uint4 hi =
-            make_uint4(codes2_to_f16x2<kFmt>(w4.z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.z >> 16),
-                       codes2_to_f16x2<kFmt>(w4.w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.w >> 16));
-        uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
-        const int c0 = (2 * c) & 7;
-        *reinterpret_cast<uint4 *>(blk + ((c0 ^ (t & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (t & 7)) << 4)) = hi;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(BAR(kBarReady + vb));
-        mbar_arrive(BAR(kBarKvEmpty + b));
-      }
-      w.next(pre, p.context_lens, geo, N);
-    }
   } else if (warp < kRwGroupWarps) {
     // ------------------------------------------------ chunk groups: softmax
     // Group gp = warp / 4 takes the chunks s with s & 1 == gp: their P'' (a
@@ -982,13 +939,44 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if ((s & 1) != gp) continue;
         const int b = s % kRwStages, sb = gp;
         const int j0 = (sg.c0 + k) * kRwTok + copy * RC;   // this slice's first token
+        // the stage's data, and the group's V operand, P'' and O buffers free
+        // (PV(s - 2), the group's previous chunk, has completed)
         bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
-        ok = ok && rw_wait_fast(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s);
+        if (s >= 2) ok = ok && rw_wait_fast(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s);
         if (__any_sync(0xFFFFFFFFu, !ok)) {
           aborted = true;
           break;
         }
         tc_fence_after();
+        // ---- first the stage's V codes -> f16 (thread L converts token L of
+        //      the chunk), while QK^T(s) runs: the stage is released as soon
+        //      as possible.  MN-major, 128-byte swizzle: dims 64j.. in block j
+        //      (16 KiB apart), token t at (t/8)*1024 + (t%8)*128, the chunk of
+        //      dims 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's range get
+        //      zeros: their stage rows hold stale codes, and a NaN code would
+        //      poison the product even at p = 0.
+        {
+          const int tv = L32;
+          const bool valid = (sg.c0 + k) * kRwTok + tv < sg.vis;
+          const uint8_t *vrow = smem + b * kStageBytes + kCodeBytes + tv * kHeadDim;
+          uint8_t *vf = smem + kOffVf + gp * kVfBytes + (tv >> 3) * 1024 + (tv & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+            if (valid) w4 = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (tv & 7)) << 4));
+            const uint4 lo =
+                make_uint4(codes2_to_f16x2<kFmt>(w4.x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.x >> 16),
+                           codes2_to_f16x2<kFmt>(w4.y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.y >> 16));
+            const uint4 hi =
+                make_uint4(codes2_to_f16x2<kFmt>(w4.z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.z >> 16),
+                           codes2_to_f16x2<kFmt>(w4.w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.w >> 16));
+            uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
+            const int c0 = (2 * c) & 7;
+            *reinterpret_cast<uint4 *>(blk + ((c0 ^ (tv & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (tv & 7)) << 4)) = hi;
+          }
+        }
+        fence_proxy_async_smem();
         // scales of head h for this warp's token slice, into its buffer [K | V]
         {
           const float *sc = reinterpret_cast<const float *>(smem + kOffSc + b * 2 * kScBytes);
@@ -1000,7 +988,12 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));
+        if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));   // codes and scales read
+        if (__any_sync(0xFFFFFFFFu, !rw_wait_fast(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s))) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
         const uint32_t scol = tl + RwCols<RC>::S(sb) + copy * RC;
         const uint32_t ocol = tl + kColO + 128 * gp;
@@ -1014,17 +1007,6 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         } else {
           rows_chunk_p<RC>(scol, BAR(kBarSFree + sb), lane, ts, ts + RC, lim, rowf, m_ref, E,
                            lchunk, lsum, pk);
-          // P'' buffer gp and O buffer gp were last used by PV(s - 2)
-          bool pv_ok = true;
-          if (s >= 2) {
-            const uint32_t pb = BAR(kBarPvDone + sb), ph = ((s >> 1) - 1) & 1;
-            pv_ok = rw_wait_fast(pb, ph, abort_s);
-          }
-          if (__any_sync(0xFFFFFFFFu, !pv_ok)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
         }
         // O buffer gp holds the group's earlier chunks of the unit under the
         // references of the chunk's start: brought to the present ones if they
