@@ -58,7 +58,7 @@ namespace kvq {
 namespace {
 
 constexpr int kRwTok = 128;                  // tokens per chunk
-constexpr int kRwStages = 3;                 // code ring depth
+constexpr int kRwStages = 5;                 // code ring depth
 constexpr int kRwSoftWarps = 4;             // warps of a chunk group (one per lane quarter)
 constexpr int kRwGroups = 2;                 // chunk groups: chunk s goes to group s & 1
 constexpr int kRwGroupWarps = kRwGroups * kRwSoftWarps;   // warps 0-7
@@ -100,16 +100,17 @@ struct RwCols {
 constexpr int kCodeBytes = kRwTok * kHeadDim;                 // one plane of a chunk
 constexpr int kStageBytes = 2 * kCodeBytes;                   // K codes | V codes
 constexpr int kScBytes = kRwTok * 16;                         // [token][4 heads] fp32
-constexpr int kVfBytes = kRwTok * kHeadDim * 2;               // f16 V operand
+constexpr int kVfBytes = kRwTok * kHeadDim * 2;               // f16 V operand = a stage
 constexpr int kQBytes = 128 * kHeadDim;                       // one e4m3 piece, 128 rows
 constexpr int kOffSc = kRwStages * kStageBytes;
-constexpr int kOffVf = kOffSc + kRwStages * 2 * kScBytes;
-constexpr int kOffQ = kOffVf + 2 * kVfBytes;                  // also the merge scratch
+constexpr int kOffQ = kOffSc + kRwStages * 2 * kScBytes;       // also the merge scratch
 constexpr int kOffTs = kOffQ + 2 * kQBytes;                   // [warp][K | V][128] fp32
-constexpr int kOffIds = kOffTs + kRwGroups * kRwSoftWarps * 2 * kRwTok * 4;
+constexpr int kOffIds = kOffTs + kRwGroupWarps * 2 * kRwTok * 4;
 constexpr int kOffRowf = kOffIds + (kRwIdAhead + 1) * kRwMaxPagesPerChunk * 4;
-constexpr int kOffMl = kOffRowf + 128 * 4;        // [group][128 lanes] (m, l, E, -)
-constexpr int kOffPre = kOffMl + kRwGroups * 128 * 16;
+// [group][128 lanes] (m, l, E, -): over the scale buffers, which only the
+// chunk loop uses (the epilogue starts once both groups have left it)
+constexpr int kOffMl = kOffTs;
+constexpr int kOffPre = kOffRowf + 128 * 4;
 constexpr int kOffBar = kOffPre + (kRowsMaxRequests + 4) * 4;
 constexpr int kBarKvFull = 0;
 constexpr int kBarKvEmpty = kBarKvFull + kRwStages;
@@ -126,7 +127,8 @@ constexpr int kNumBars = kBarOFree + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;              // tmem base, abort, ticket
 constexpr int kRwSmem = kOffMisc + 64 + 1024;
 
-static_assert(kOffSc % 1024 == 0 && kOffVf % 1024 == 0 && kOffQ % 1024 == 0,
+static_assert(kVfBytes == kStageBytes, "a stage holds its chunk's V operand after conversion");
+static_assert(kOffSc % 1024 == 0 && kOffQ % 1024 == 0,
               "operand buffers need 1024-byte alignment");
 static_assert(kOffBar % 8 == 0, "barrier alignment");
 static_assert(kRwSmem <= 227 * 1024, "shared memory budget");
@@ -203,6 +205,8 @@ __device__ __forceinline__ void soft_barrier() {
 
 // Barrier over group 0's warps (the unit's final merge).
 __device__ __forceinline__ void group0_barrier() { named_barrier(2, kRwSoftWarps * 32); }
+
+
 
 // Smallest e in [-126, 126] with 2^e >= v (v >= 0 given as its bits).
 __device__ __forceinline__ int rw_pow2_ceil(uint32_t bits) {
@@ -697,7 +701,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
   if (tid == 32) {
     for (int s = 0; s < kRwStages; ++s) {
       mbar_init(BAR(kBarKvFull + s), 1);
-      mbar_init(BAR(kBarKvEmpty + s), 1 + kRwSoftWarps);
+      mbar_init(BAR(kBarKvEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(kBarSFull + b), 1);
@@ -837,7 +841,6 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_e4m3(tmem + RwCols<RC>::S(sb), qb + 2 * kk, kd + 2 * kk, kQK, 1u);
         tc_commit(BAR(kBarSFull + sb));
-        tc_commit(BAR(kBarKvEmpty + b));
         last_bar = BAR(kBarSFull + sb);
         last_par = (s >> 1) & 1;
         any = true;
@@ -849,7 +852,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
   } else if (warp == kRwWarpPv) {
     // -------------------------------------------------------------- PV MMA
     if (lane == 0) {
-      const uint32_t vf0 = smem_addr(smem + kOffVf);
+      const uint32_t st0 = smem_addr(smem);
       uint32_t last_bar = 0, last_par = 0;
       bool any = false;
       ChunkWalk w;
@@ -863,12 +866,15 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if (!rw_wait_fast(BAR(kBarReady + cb), (s >> 1) & 1, abort_s)) break;
         if (first && w.seg >= 1 && !rw_wait_fast(BAR(kBarOFree), (w.seg - 1) & 1, abort_s)) break;
         tc_fence_after();
-        const uint64_t bd = smem_desc(vf0 + cb * kVfBytes, kVfBytes / 2, 1024, kSmemSwizzle128);
+        // the chunk's stage holds its V operand, converted in place
+        const uint64_t bd = smem_desc(st0 + (s % kRwStages) * kStageBytes, kVfBytes / 2, 1024,
+                                      kSmemSwizzle128);
 #pragma unroll
         for (int kk = 0; kk < kRwTok / 16; ++kk)
           tc_mma_f16_tmem_a(tmem + kColO + 128 * cb, tmem + RwCols<RC>::P(cb) + 8 * kk,
                             bd + (2048 >> 4) * kk, kIdescPV, (fresh && kk == 0) ? 0u : 1u);
         tc_commit(BAR(kBarPvDone + cb));
+        tc_commit(BAR(kBarKvEmpty + s % kRwStages));   // the stage is free again
         last_bar = BAR(kBarPvDone + cb);
         last_par = (s >> 1) & 1;
         any = true;
@@ -889,7 +895,6 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     const int copy = L32 / RC;                  // its token slice [copy RC, copy RC + RC)
     const int mrow = L32 % RC;                  // its row within the tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-    float *ts = reinterpret_cast<float *>(smem + kOffTs) + warp * 2 * kRwTok;
     float4 *ml_s = reinterpret_cast<float4 *>(smem + kOffMl);
     bool aborted = false;
     if constexpr (RwCols<RC>::kSplitP) {
@@ -939,45 +944,17 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         if ((s & 1) != gp) continue;
         const int b = s % kRwStages, sb = gp;
         const int j0 = (sg.c0 + k) * kRwTok + copy * RC;   // this slice's first token
-        // the stage's data, and the group's V operand, P'' and O buffers free
-        // (PV(s - 2), the group's previous chunk, has completed)
+        // the stage's data, and S(s) -- QK^T(s) has completed, so the
+        // stage's K codes are no longer needed
         bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
-        if (s >= 2) ok = ok && rw_wait_fast(BAR(kBarPvDone + sb), ((s >> 1) - 1) & 1, abort_s);
+        ok = ok && rw_wait_fast(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s);
         if (__any_sync(0xFFFFFFFFu, !ok)) {
           aborted = true;
           break;
         }
         tc_fence_after();
-        // ---- first the stage's V codes -> f16 (thread L converts token L of
-        //      the chunk), while QK^T(s) runs: the stage is released as soon
-        //      as possible.  MN-major, 128-byte swizzle: dims 64j.. in block j
-        //      (16 KiB apart), token t at (t/8)*1024 + (t%8)*128, the chunk of
-        //      dims 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's range get
-        //      zeros: their stage rows hold stale codes, and a NaN code would
-        //      poison the product even at p = 0.
-        {
-          const int tv = L32;
-          const bool valid = (sg.c0 + k) * kRwTok + tv < sg.vis;
-          const uint8_t *vrow = smem + b * kStageBytes + kCodeBytes + tv * kHeadDim;
-          uint8_t *vf = smem + kOffVf + gp * kVfBytes + (tv >> 3) * 1024 + (tv & 7) * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
-            if (valid) w4 = *reinterpret_cast<const uint4 *>(vrow + ((c ^ (tv & 7)) << 4));
-            const uint4 lo =
-                make_uint4(codes2_to_f16x2<kFmt>(w4.x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.x >> 16),
-                           codes2_to_f16x2<kFmt>(w4.y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.y >> 16));
-            const uint4 hi =
-                make_uint4(codes2_to_f16x2<kFmt>(w4.z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.z >> 16),
-                           codes2_to_f16x2<kFmt>(w4.w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4.w >> 16));
-            uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
-            const int c0 = (2 * c) & 7;
-            *reinterpret_cast<uint4 *>(blk + ((c0 ^ (tv & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (tv & 7)) << 4)) = hi;
-          }
-        }
-        fence_proxy_async_smem();
         // scales of head h for this warp's token slice, into its buffer [K | V]
+        float *ts = reinterpret_cast<float *>(smem + kOffTs) + warp * 2 * kRwTok;
         {
           const float *sc = reinterpret_cast<const float *>(smem + kOffSc + b * 2 * kScBytes);
 #pragma unroll
@@ -988,12 +965,6 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(kBarKvEmpty + b));   // codes and scales read
-        if (__any_sync(0xFFFFFFFFu, !rw_wait_fast(BAR(kBarSFull + sb), (s >> 1) & 1, abort_s))) {
-          aborted = true;
-          break;
-        }
-        tc_fence_after();
         const int lim = vis - j0;               // tokens jj < lim of the slice are seen
         const uint32_t scol = tl + RwCols<RC>::S(sb) + copy * RC;
         const uint32_t ocol = tl + kColO + 128 * gp;
@@ -1002,12 +973,58 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
         // P'' of the slice (references moved on the way where needed)
         float lchunk = 0.0f;
         uint32_t pk[RC < 128 ? RC / 2 : 1];
+        const float *ks = ts, *vs = ts + RC;
         if constexpr (RC == 128) {
-          rows_chunk_p_direct(scol, ts, ts + RC, lim, rowf, m_ref, E, lchunk, lsum);
+          rows_chunk_p_direct(scol, ks, vs, lim, rowf, m_ref, E, lchunk, lsum);
         } else {
-          rows_chunk_p<RC>(scol, BAR(kBarSFree + sb), lane, ts, ts + RC, lim, rowf, m_ref, E,
-                           lchunk, lsum, pk);
+          rows_chunk_p<RC>(scol, BAR(kBarSFree + sb), lane, ks, vs, lim, rowf, m_ref, E, lchunk,
+                           lsum, pk);
+          // P'' buffer gp and O buffer gp were last used by PV(s - 2)
+          if (s >= 2 && __any_sync(0xFFFFFFFFu, !rw_wait_fast(BAR(kBarPvDone + sb),
+                                                              ((s >> 1) - 1) & 1, abort_s))) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
         }
+        // ---- the stage's V codes -> f16 in place, the chunk's PV operand
+        //      (thread L converts token L): MN-major, 128-byte swizzle, dims
+        //      64j.. in block j -- block 0 over the K codes (read by QK^T(s),
+        //      complete), block 1 over the V codes, where token t's 128 bytes
+        //      of dims 64..127 land exactly on its own 128 code bytes (t*128 =
+        //      (t/8)*1024 + (t%8)*128), read before anything is written.
+        //      Within a block token t sits at (t/8)*1024 + (t%8)*128, the
+        //      chunk of dims 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's
+        //      range get zeros: their rows hold stale codes, and a NaN code
+        //      would poison the product even at p = 0.
+        {
+          const int tv = L32;
+          const bool valid = (sg.c0 + k) * kRwTok + tv < sg.vis;
+          uint8_t *stg = smem + b * kStageBytes;
+          uint4 w4[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            w4[c] = make_uint4(0u, 0u, 0u, 0u);
+            if (valid)
+              w4[c] = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + tv * kHeadDim +
+                                                        ((c ^ (tv & 7)) << 4));
+          }
+          uint8_t *vf = stg + (tv >> 3) * 1024 + (tv & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 lo = make_uint4(
+                codes2_to_f16x2<kFmt>(w4[c].x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].x >> 16),
+                codes2_to_f16x2<kFmt>(w4[c].y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].y >> 16));
+            const uint4 hi = make_uint4(
+                codes2_to_f16x2<kFmt>(w4[c].z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].z >> 16),
+                codes2_to_f16x2<kFmt>(w4[c].w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].w >> 16));
+            uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
+            const int c0 = (2 * c) & 7;
+            *reinterpret_cast<uint4 *>(blk + ((c0 ^ (tv & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (tv & 7)) << 4)) = hi;
+          }
+        }
+        fence_proxy_async_smem();
         // O buffer gp holds the group's earlier chunks of the unit under the
         // references of the chunk's start: brought to the present ones if they
         // moved (no MMA in flight on it: PV(s - 2) has completed)
