@@ -706,7 +706,9 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     for (int b = 0; b < 2; ++b) {
       mbar_init(BAR(kBarSFull + b), 1);
       mbar_init(BAR(kBarSFree + b), kRwSoftWarps);
-      mbar_init(BAR(kBarReady + b), kRwSoftWarps);
+      // P'' from the owner group, V from the other one (tiles of 128 rows)
+      // or from the owner too
+      mbar_init(BAR(kBarReady + b), (RC == 128 ? 2 : 1) * kRwSoftWarps);
       mbar_init(BAR(kBarPvDone + b), 1);
     }
     mbar_init(BAR(kBarQReady), kRwGroupWarps);
@@ -938,10 +940,65 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
       const float rowf = rowf_s[mrow];
       float m_ref = -INFINITY, lsum = 0.0f;
       int E = -126;
+      // ---- chunk s's V codes -> f16 in place in its stage, the chunk's PV
+      //      operand (thread L converts token L): MN-major, 128-byte swizzle,
+      //      dims 64j.. in block j -- block 0 over the K codes (read by
+      //      QK^T(s), complete), block 1 over the V codes, where token t's 128
+      //      bytes of dims 64..127 land exactly on its own 128 code bytes (t*128
+      //      = (t/8)*1024 + (t%8)*128), read before anything is written.
+      //      Within a block token t sits at (t/8)*1024 + (t%8)*128, the chunk of
+      //      dims 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's range get
+      //      zeros: their rows hold stale codes, and a NaN code would poison the
+      //      product even at p = 0.
+      auto convert_v = [&](int sc_, int kc_) {
+        const int tv = L32;
+        const bool valid = (sg.c0 + kc_) * kRwTok + tv < sg.vis;
+        uint8_t *stg = smem + (sc_ % kRwStages) * kStageBytes;
+        uint4 w4[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          w4[c] = make_uint4(0u, 0u, 0u, 0u);
+          if (valid)
+            w4[c] = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + tv * kHeadDim +
+                                                      ((c ^ (tv & 7)) << 4));
+        }
+        uint8_t *vf = stg + (tv >> 3) * 1024 + (tv & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 lo = make_uint4(
+              codes2_to_f16x2<kFmt>(w4[c].x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].x >> 16),
+              codes2_to_f16x2<kFmt>(w4[c].y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].y >> 16));
+          const uint4 hi = make_uint4(
+              codes2_to_f16x2<kFmt>(w4[c].z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].z >> 16),
+              codes2_to_f16x2<kFmt>(w4[c].w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].w >> 16));
+          uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
+          const int c0 = (2 * c) & 7;
+          *reinterpret_cast<uint4 *>(blk + ((c0 ^ (tv & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (tv & 7)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();
+      };
       int mine = 0;                             // this group's chunks of the unit so far
       const int s_first = s;
       for (int k = 0; k < sg.n; ++k, ++s) {
-        if ((s & 1) != gp) continue;
+        if ((s & 1) != gp) {
+          // ---- tiles of 128 rows: the other group's chunk's V operand, while
+          //      that group runs its (long) softmax; its PV waits for both.
+          //      (Smaller tiles: the owner converts, after its softmax.)
+          if constexpr (RC < 128) continue;
+          const int b = s % kRwStages;
+          bool ok = rw_wait_fast(BAR(kBarKvFull + b), (s / kRwStages) & 1, abort_s);
+          ok = ok && rw_wait_fast(BAR(kBarSFull + (s & 1)), (s >> 1) & 1, abort_s);
+          if (__any_sync(0xFFFFFFFFu, !ok)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          convert_v(s, k);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(kBarReady + (s & 1)));
+          continue;
+        }
         const int b = s % kRwStages, sb = gp;
         const int j0 = (sg.c0 + k) * kRwTok + copy * RC;   // this slice's first token
         // the stage's data, and S(s) -- QK^T(s) has completed, so the
@@ -987,44 +1044,7 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
           }
           tc_fence_after();
         }
-        // ---- the stage's V codes -> f16 in place, the chunk's PV operand
-        //      (thread L converts token L): MN-major, 128-byte swizzle, dims
-        //      64j.. in block j -- block 0 over the K codes (read by QK^T(s),
-        //      complete), block 1 over the V codes, where token t's 128 bytes
-        //      of dims 64..127 land exactly on its own 128 code bytes (t*128 =
-        //      (t/8)*1024 + (t%8)*128), read before anything is written.
-        //      Within a block token t sits at (t/8)*1024 + (t%8)*128, the
-        //      chunk of dims 8c'.. at (c' ^ (t % 8)).  Tokens past the unit's
-        //      range get zeros: their rows hold stale codes, and a NaN code
-        //      would poison the product even at p = 0.
-        {
-          const int tv = L32;
-          const bool valid = (sg.c0 + k) * kRwTok + tv < sg.vis;
-          uint8_t *stg = smem + b * kStageBytes;
-          uint4 w4[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            w4[c] = make_uint4(0u, 0u, 0u, 0u);
-            if (valid)
-              w4[c] = *reinterpret_cast<const uint4 *>(stg + kCodeBytes + tv * kHeadDim +
-                                                        ((c ^ (tv & 7)) << 4));
-          }
-          uint8_t *vf = stg + (tv >> 3) * 1024 + (tv & 7) * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 lo = make_uint4(
-                codes2_to_f16x2<kFmt>(w4[c].x & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].x >> 16),
-                codes2_to_f16x2<kFmt>(w4[c].y & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].y >> 16));
-            const uint4 hi = make_uint4(
-                codes2_to_f16x2<kFmt>(w4[c].z & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].z >> 16),
-                codes2_to_f16x2<kFmt>(w4[c].w & 0xFFFFu), codes2_to_f16x2<kFmt>(w4[c].w >> 16));
-            uint8_t *blk = vf + (c >> 2) * (kVfBytes / 2);
-            const int c0 = (2 * c) & 7;
-            *reinterpret_cast<uint4 *>(blk + ((c0 ^ (tv & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (tv & 7)) << 4)) = hi;
-          }
-        }
-        fence_proxy_async_smem();
+        if constexpr (RC < 128) convert_v(s, k);
         // O buffer gp holds the group's earlier chunks of the unit under the
         // references of the chunk's start: brought to the present ones if they
         // moved (no MMA in flight on it: PV(s - 2) has completed)
