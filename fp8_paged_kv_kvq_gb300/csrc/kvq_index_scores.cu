@@ -42,6 +42,7 @@ constexpr int kScThreads = (kScWarps + 1) * 32;      // + the producer warp
 constexpr int kScTile = 16;                          // tokens per MMA tile
 constexpr int kScChunk = 128;                        // tokens per stage
 constexpr int kScStages = 4;
+constexpr int kScIdAhead = 8;                        // chunks whose block ids are in flight
 constexpr int kScCols = 16;                          // stacked query vectors
 
 template <int kFormat>
@@ -50,7 +51,8 @@ struct ScFmt {
   static constexpr int kCodeBytes = kScChunk * kRowBytes;
   static constexpr int kStageBytes = kCodeBytes + kScChunk * 4;   // + scale / exponent words
   static constexpr int kOffBars = kScStages * kStageBytes;
-  static constexpr int kSmem = kOffBars + 2 * kScStages * 8 + 16;
+  static constexpr int kOffIds = kOffBars + 2 * kScStages * 8 + 16;   // [kScIdAhead + 1][32]
+  static constexpr int kSmem = kOffIds + (kScIdAhead + 1) * 32 * 4;
 };
 
 struct ScParams {
@@ -154,34 +156,40 @@ index_scores_kernel(const ScParams p) {
     const int seg = p.log2_bs >= 7 ? kScChunk : (1 << p.log2_bs);
     const int nseg = kScChunk / seg;
     bool bad = false, stop = false;
-    // this lane's block id for chunk (r, k); has = the segment starts before L
-    auto fetch = [&](int r, int k, int L, bool &has) -> uint32_t {
-      const int j = k * kScChunk + lane * seg;
-      has = lane < nseg && j < L;
-      return has ? static_cast<uint32_t>(
-                       __ldg(p.block_tables + static_cast<int64_t>(r) * p.max_blocks +
-                             (j >> p.log2_bs)))
-                 : 0u;
+    // Block ids go to shared memory by cp.async kScIdAhead chunks ahead of
+    // their stage (one commit group per chunk; lane i: page segment i), so no
+    // chunk waits for a block-table read.
+    int32_t *ids = reinterpret_cast<int32_t *>(smem + F::kOffIds);
+    const int nreq = static_cast<int>(p.total / p.nch);
+    int fr = r_begin, fk = k_begin, fu = 0;
+    int fL = sc_context(p, fr);
+    auto fetch_next = [&]() {
+      if (fu < n_units) {
+        const int j = fk * kScChunk + lane * seg;
+        const bool need = lane < nseg && j < fL;
+        const int32_t *src = p.block_tables + static_cast<int64_t>(fr) * p.max_blocks +
+                             (need ? (j >> p.log2_bs) : 0);
+        cp_async_4(ids + (fu % (kScIdAhead + 1)) * 32 + lane, src, need ? 4u : 0u);
+        if (++fk == p.nch) {
+          fk = 0;
+          if (++fr < nreq) fL = sc_context(p, fr);
+        }
+      }
+      cp_async_commit();
+      ++fu;
     };
+    for (int a = 0; a < kScIdAhead; ++a) fetch_next();
     int r = r_begin, k = k_begin;
     int L = sc_context(p, r);
-    bool has;
-    uint32_t blk = fetch(r, k, L, has);
     int u = 0;
     for (; u < n_units; ++u) {
-      // the next chunk's block id is read before this chunk's stage frees up
-      int rn = r, kn = k + 1;
-      if (kn == p.nch) {
-        kn = 0;
-        ++rn;
-      }
-      int Ln = L;
-      bool has_n = false;
-      uint32_t blk_n = 0;
-      if (u + 1 < n_units) {
-        if (rn != r) Ln = sc_context(p, rn);
-        blk_n = fetch(rn, kn, Ln, has_n);
-      }
+      fetch_next();                             // chunk u + kScIdAhead
+      cp_async_wait<kScIdAhead>();              // chunk u's ids have landed
+      __syncwarp();
+      const int j = k * kScChunk + lane * seg;
+      const bool has = lane < nseg && j < L;
+      const uint32_t blk = has ? static_cast<uint32_t>(ids[(u % (kScIdAhead + 1)) * 32 + lane])
+                               : 0u;
       const int st = u % kScStages;
       if (u >= kScStages) {
         if (lane == 0)
@@ -197,7 +205,6 @@ index_scores_kernel(const ScParams p) {
       if (lane == 0) mbar_arrive_expect_tx(fb, tx);
       __syncwarp();
       if (ok) {
-        const int j = k * kScChunk + lane * seg;
         const int64_t slot = (static_cast<int64_t>(blk) << p.log2_bs) |
                              (j & ((1 << p.log2_bs) - 1));
         uint8_t *sb = smem + st * F::kStageBytes;
@@ -209,12 +216,12 @@ index_scores_kernel(const ScParams p) {
         bulk_load(smem_addr(sb + F::kCodeBytes + lane * seg * 4), side,
                   static_cast<uint32_t>(seg * 4), fb);
       }
-      r = rn;
-      k = kn;
-      L = Ln;
-      blk = blk_n;
-      has = has_n;
+      if (++k == p.nch) {
+        k = 0;
+        if (++r < nreq) L = sc_context(p, r);
+      }
     }
+    cp_async_wait<0>();
     bad = __any_sync(0xFFFFFFFFu, bad);
     if (lane == 0) {
       if (bad && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
