@@ -755,7 +755,9 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
     }
     uint32_t u = 0;
     bool bad = false, stop = false;
-    const uint64_t pol = l2_policy_evict_first();
+    // a unit's codes are read once when a (request, KV head) has one tile of
+    // rows; with several tiles each re-reads them, and L2 should keep them
+    const uint64_t pol = p.T == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
     for (; iw.valid && !stop; ++u) {
       fetch(fw, (u + kRwIdAhead) % (kRwIdAhead + 1));
       fw.next(pre, p.context_lens, geo, N);
@@ -785,9 +787,9 @@ attn_rows_kernel(const RwParams p, const __grid_constant__ CUtensorMap tm_kc,
               continue;
             }
             const int z = static_cast<int>((blk << p.log2_bs) | (j & ((1 << p.log2_bs) - 1)));
-            // the codes are read once: evict them first, so the scale lines
-            // (each 32-byte sector holds 8 heads' scales of a slot, wanted by
-            // 8 units at different times) stay in L2 longer
+            // codes read once go first, so the scale lines (each 32-byte
+            // sector holds 8 heads' scales of a slot, wanted by 8 units at
+            // different times) stay in L2 longer
             tma_load_3d_hint(kdst + i * p.box * kHeadDim, &tm_kc, 0, h, z, fb, pol);
             tma_load_3d_hint(vdst + i * p.box * kHeadDim, &tm_vc, 0, h, z, fb, pol);
             tma_load_2d(ksd + i * p.box * 16, &tm_ks, h & ~3, z, fb);

@@ -340,6 +340,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
+// An L2 policy with the default eviction priority.
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
 // tma_load_3d under an L2 cache policy.
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, int x, int y,
                                                  int z, uint32_t bar, uint64_t policy) {
