@@ -309,6 +309,9 @@ class DeviceWorkload:
             w.num_requests, R, w.num_q_heads, H, w.block_size, self.max_ctx)
         self.n_parts = (self.max_ctx + self.P - 1) // self.P
         self.balanced = self.P_arg == 0 and self._balanced_mode()
+        # the load-balanced kernel stores the step's new rows itself
+        # (kvq_paged_decode_append_partials): the step has no store launch
+        self.fused = self.balanced
         # more than 8 stacked rows per KV head, partition left to the library:
         # the rows-on-M tensor-core kernel, which merges its pieces itself
         rows = R * w.group
@@ -366,6 +369,8 @@ class DeviceWorkload:
                         P(self.bt_d.data_ptr()), self.bt.shape[1], P(self.cl_d.data_ptr()),
                         self.max_ctx, ctypes.c_float(w.sm_scale), self.P_arg, P(self.out.data_ptr()),
                         P(self.ws.data_ptr()), self.ws.numel(), P(self.err.data_ptr()), sp)
+        self._a_args = (ctypes.byref(self._cst), P(self.new_k.data_ptr()), self.new_k.stride(0),
+                        P(self.new_v.data_ptr()), self.new_v.stride(0)) + self._p_args[1:]
         self._c_args = (ctypes.byref(self._cst), N, R, w.num_q_heads, self.bt.shape[1],
                         P(self.cl_d.data_ptr()), self.max_ctx, self.P_arg, P(self.out.data_ptr()),
                         P(self.ws.data_ptr()), self.ws.numel(), sp)
@@ -380,12 +385,14 @@ class DeviceWorkload:
         sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         cmax = (self.max_ctx + 15) // 16
         hg = w.num_kv_heads // 4
-        per_cta = (w.num_requests * hg * (cmax + 3) + 3 * sms - 1) // (3 * sms)
-        b = max(per_cta, (cmax + 14) // 15)
+        total_ub = w.num_requests * hg * (cmax + 3)
+        per_cta = (total_ub + 3 * sms - 1) // (3 * sms)
+        per_cta_w = (total_ub * 135 + 384 * sms - 1) // (384 * sms) + 1   # weighted ranges
+        b = max(per_cta, (cmax + 14) // 15, per_cta_w)
         page_ctas = hg * self.n_parts * w.num_requests
         return (rows <= 8 and w.block_size >= 16 and w.num_kv_heads % 4 == 0
                 and 1 <= w.num_requests <= 1024 and b * 16 // w.block_size + 2 <= 520
-                and page_ctas < 9 * sms)
+                and total_ub < 2 ** 31 and page_ctas < 9 * sms)
 
     def partials_kernel(self):
         """(kernel, source) the library launches for this shape's partials:
@@ -426,6 +433,26 @@ class DeviceWorkload:
         if st:
             raise RuntimeError(f"kvq_paged_decode_partials: status {st}")
 
+    def append_partials(self):
+        st = self.lib.kvq_paged_decode_append_partials(*self._a_args)
+        if st:
+            raise RuntimeError(f"kvq_paged_decode_append_partials: status {st}")
+
+    def store_and_partials(self, between=None):
+        """The step's store of its new rows and the attention's split-K launch:
+        one launch where the load-balanced kernel stores the rows itself, else
+        the store's launch, then (after `between`, an event record) the
+        partials."""
+        if self.fused:
+            if between is not None:
+                between()
+            self.append_partials()
+            return
+        self.quantize()
+        if between is not None:
+            between()
+        self.partials()
+
     def combine(self):
         st = self.lib.kvq_paged_decode_combine(*self._c_args)
         if st:
@@ -441,7 +468,7 @@ class DeviceWorkload:
             return self.layers
         if self.rows_kernel:
             return 2
-        return 2 + (1 if self.n_parts > 1 else 0)
+        return (1 if self.fused else 2) + (1 if self.n_parts > 1 else 0)
 
     # algorithmic bytes: attention = codes + scales + q + out + block tables +
     # context lengths; store = bf16 K/V read + codes + scales + slot ids, per
@@ -450,7 +477,9 @@ class DeviceWorkload:
         w = self.w
         T = self.new_k.shape[0]
         H, D = w.num_kv_heads, w.head_dim
-        return T * H * (2 * D * 2 + 2 * D + 2 * 4) + T * 8
+        # slot ids: none when the attention launch stores the rows at their
+        # block-table positions
+        return T * H * (2 * D * 2 + 2 * D + 2 * 4) + (0 if getattr(self, "fused", False) else T * 8)
 
     def store_bytes(self):
         return self.store_launches * self.store_bytes_per_launch()
@@ -554,10 +583,7 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
                 for e in evs[1:]:
                     e.record(stream)
             return
-        wl.quantize()
-        if split:
-            evs[1].record(stream)
-        wl.partials()
+        wl.store_and_partials((lambda: evs[1].record(stream)) if split else None)
         if split:
             evs[2].record(stream)
         wl.combine()
@@ -655,6 +681,13 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
         res["kernels_us"]["paged_decode_partials"] = round(1e3 * sum(st_p) / K, 3)
         res["kernels_us"]["paged_decode_combine"] = round(1e3 * sum(st_c) / K, 3)
         dom_ms, dom_bytes = sum(st_p) / K, wl.attn_bytes()
+        if wl.fused:
+            res["config"]["store"] = ("fused: the load-balanced kernel stores the step's new "
+                                      "rows itself (kvq_paged_decode_append_partials)")
+            res["kernels_us"]["quantize_scatter_note"] = (
+                "no store launch: paged_decode_partials is the append launch that stores "
+                "the new rows and runs the split-K attention")
+            dom_bytes += wl.store_bytes_per_launch()
         dom_name, dom_src = wl.partials_kernel()
     else:
         # one graph replay stores every layer: a launch's time is the step's share
@@ -726,7 +759,9 @@ def run_e2e(wl: DeviceWorkload, dev, K, world):
     (q, new K/V rows, slot ids, block tables, context lengths) are copied from
     pinned host memory and the output back, inside the timed region."""
     host = {}
-    for name in ("q", "new_k", "new_v", "new_slots", "bt_d", "cl_d"):
+    names = ("q", "new_k", "new_v", "bt_d", "cl_d") if wl.fused else \
+        ("q", "new_k", "new_v", "new_slots", "bt_d", "cl_d")
+    for name in names:
         t = getattr(wl, name)
         host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
@@ -737,8 +772,7 @@ def run_e2e(wl: DeviceWorkload, dev, K, world):
     def body():
         for name, t in host.items():
             getattr(wl, name).copy_(t, non_blocking=True)
-        wl.quantize()
-        wl.partials()
+        wl.store_and_partials()
         wl.combine()
         out_h.copy_(wl.out, non_blocking=True)
 

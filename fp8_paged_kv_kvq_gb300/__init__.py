@@ -105,6 +105,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                          ctypes.c_float, i32, P, P, sz, P, P]),
             "kvq_paged_decode_combine": (ctypes.c_int, [CP, i32, i32, i32, i32, P, i32, i32,
                                                         P, P, sz, P]),
+            "kvq_paged_decode_append_partials": (ctypes.c_int, [CP, P, i64, P, i64, P, i32, i32,
+                                                                i32, P, i32, P, i32,
+                                                                ctypes.c_float, i32, P, P, sz,
+                                                                P, P]),
+            "kvq_paged_decode_append": (ctypes.c_int, [CP, P, i64, P, i64, P, i32, i32, i32, P,
+                                                       i32, P, i32, ctypes.c_float, i32, P, P,
+                                                       sz, P, P]),
             "kvq_dequant_rows": (ctypes.c_int, [CP, P, i64, i32, P, P, P, P]),
             "kvq_quantize_scatter_unscaled": (ctypes.c_int, [CP, i32, P, i64, P, i64, i64, P,
                                                              P, P]),
@@ -284,6 +291,61 @@ def paged_decode(cache: Cache, q: torch.Tensor, block_tables: torch.Tensor,
                                    workspace.numel(), _ptr(err_flags), _stream(stream)),
            "kvq_paged_decode")
     return out
+
+
+def _append_rows(cache: Cache, k_new, v_new, n_rows: int):
+    H, D = cache.num_kv_heads, cache.head_dim
+    ks = _rows_view(k_new, H, D, "k_new")
+    vs = _rows_view(v_new, H, D, "v_new")
+    if k_new.shape[0] != n_rows or v_new.shape[0] != n_rows:
+        raise ValueError("k_new and v_new need num_requests * rows_per_request rows")
+    return ks, vs
+
+
+def paged_decode_append(cache: Cache, k_new: torch.Tensor, v_new: torch.Tensor,
+                        q: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                        max_context_len: int, sm_scale: float, rows_per_request: int = 1,
+                        partition_tokens: int = 0, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None,
+                        err_flags: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvq_paged_decode_append: one decode step -- the step's new K/V rows
+    [N*R, H, D] (views allowed) stored at positions L_r - R + i of each
+    request's block table, then the attention over the cache that holds them;
+    returns ``out`` (bf16, shape of q)."""
+    N, Hq, mb = _decode_args(cache, q, block_tables, context_lens, rows_per_request)
+    ks, vs = _append_rows(cache, k_new, v_new, N * rows_per_request)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        need = paged_decode_workspace_size(N, rows_per_request, Hq, cache.num_kv_heads,
+                                           cache.head_dim, cache.block_size, max_context_len,
+                                           partition_tokens)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = cache.struct()
+    _check(load().kvq_paged_decode_append(
+        ctypes.byref(st), _ptr(k_new), ks, _ptr(v_new), vs, _ptr(q), N, rows_per_request, Hq,
+        _ptr(block_tables), mb, _ptr(context_lens), max_context_len, float(sm_scale),
+        partition_tokens, _ptr(out), _ptr(workspace), workspace.numel(), _ptr(err_flags),
+        _stream(stream)), "kvq_paged_decode_append")
+    return out
+
+
+def paged_decode_append_partials(cache: Cache, k_new, v_new, q, block_tables, context_lens,
+                                 max_context_len: int, sm_scale: float, rows_per_request: int,
+                                 partition_tokens: int, out: torch.Tensor,
+                                 workspace: torch.Tensor | None,
+                                 err_flags: torch.Tensor | None = None, stream=None) -> None:
+    """kvq_paged_decode_append_partials (the step's store and split-K launch;
+    kvq_paged_decode_combine follows)."""
+    N, Hq, mb = _decode_args(cache, q, block_tables, context_lens, rows_per_request)
+    ks, vs = _append_rows(cache, k_new, v_new, N * rows_per_request)
+    st = cache.struct()
+    _check(load().kvq_paged_decode_append_partials(
+        ctypes.byref(st), _ptr(k_new), ks, _ptr(v_new), vs, _ptr(q), N, rows_per_request, Hq,
+        _ptr(block_tables), mb, _ptr(context_lens), max_context_len, float(sm_scale),
+        partition_tokens, _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(err_flags), _stream(stream)),
+        "kvq_paged_decode_append_partials")
 
 
 def paged_decode_partials(cache: Cache, q, block_tables, context_lens, max_context_len: int,

@@ -13,7 +13,7 @@
 
 namespace {
 
-constexpr int32_t kAbiVersion = 2;
+constexpr int32_t kAbiVersion = 3;
 constexpr int32_t kMaxRowsPerKvHead = 128;
 constexpr int32_t kMaxPartitionTokens = 1 << 20;
 
@@ -267,13 +267,18 @@ size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_re
   return workspace_for(s);
 }
 
-kvq_status kvq_paged_decode_partials(const kvq_cache *cache, const void *q, int32_t num_requests,
+namespace {
+
+// kvq_paged_decode_partials, with a decode step's new rows stored first when
+// `append` is given (inside the load-balanced kernel where the shape takes it)
+kvq_status decode_partials(const kvq_cache *cache, const void *q, int32_t num_requests,
                                      int32_t rows_per_request, int32_t num_q_heads,
                                      const int32_t *block_tables, int32_t max_blocks_per_req,
                                      const int32_t *context_lens, int32_t max_context_len,
                                      float sm_scale, int32_t partition_tokens, void *out,
                                      void *workspace, size_t workspace_bytes,
-                                     int32_t *err_flags, kvq_stream_t stream) {
+                                     int32_t *err_flags, kvq_stream_t stream,
+                                     const kvq::AppendRows *append) {
   kvq::AttnShape s;
   kvq_status st = make_shape(cache, num_requests, rows_per_request, num_q_heads,
                              max_blocks_per_req, max_context_len, partition_tokens, &s);
@@ -299,7 +304,50 @@ kvq_status kvq_paged_decode_partials(const kvq_cache *cache, const void *q, int3
   }
   return from_cuda(kvq::launch_attn_partials(*cache, s, q, block_tables, context_lens, sm_scale,
                                              out, workspace, err_flags,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+                                             reinterpret_cast<cudaStream_t>(stream), append));
+}
+
+}  // namespace
+
+kvq_status kvq_paged_decode_partials(const kvq_cache *cache, const void *q, int32_t num_requests,
+                                     int32_t rows_per_request, int32_t num_q_heads,
+                                     const int32_t *block_tables, int32_t max_blocks_per_req,
+                                     const int32_t *context_lens, int32_t max_context_len,
+                                     float sm_scale, int32_t partition_tokens, void *out,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *err_flags, kvq_stream_t stream) {
+  return decode_partials(cache, q, num_requests, rows_per_request, num_q_heads, block_tables,
+                         max_blocks_per_req, context_lens, max_context_len, sm_scale,
+                         partition_tokens, out, workspace, workspace_bytes, err_flags, stream,
+                         nullptr);
+}
+
+kvq_status kvq_paged_decode_append_partials(
+    const kvq_cache *cache, const void *k_new, int64_t k_token_stride, const void *v_new,
+    int64_t v_token_stride, const void *q, int32_t num_requests, int32_t rows_per_request,
+    int32_t num_q_heads, const int32_t *block_tables, int32_t max_blocks_per_req,
+    const int32_t *context_lens, int32_t max_context_len, float sm_scale,
+    int32_t partition_tokens, void *out, void *workspace, size_t workspace_bytes,
+    int32_t *err_flags, kvq_stream_t stream) {
+  kvq_status st = check_cache(cache, true);
+  if (st != KVQ_OK) return st;
+  if (num_requests > 0) {
+    if (k_new == nullptr || v_new == nullptr || k_token_stride < 0 || v_token_stride < 0 ||
+        rows_per_request < 1)
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || (k_token_stride % 8) != 0 ||
+        (v_token_stride % 8) != 0)
+      return KVQ_ERR_MISALIGNED;
+    // rows (token, K/V, head) of the store are numbered in 32 bits
+    if (static_cast<int64_t>(num_requests) * rows_per_request >
+        (int64_t(1) << 31) / (2 * cache->num_kv_heads) - 32)
+      return KVQ_ERR_UNSUPPORTED;
+  }
+  const kvq::AppendRows append{k_new, k_token_stride, v_new, v_token_stride};
+  return decode_partials(cache, q, num_requests, rows_per_request, num_q_heads, block_tables,
+                         max_blocks_per_req, context_lens, max_context_len, sm_scale,
+                         partition_tokens, out, workspace, workspace_bytes, err_flags, stream,
+                         &append);
 }
 
 kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests,
@@ -333,6 +381,25 @@ kvq_status kvq_paged_decode(const kvq_cache *cache, const void *q, int32_t num_r
       cache, q, num_requests, rows_per_request, num_q_heads, block_tables, max_blocks_per_req,
       context_lens, max_context_len, sm_scale, partition_tokens, out, workspace,
       workspace_bytes, err_flags, stream);
+  if (st != KVQ_OK) return st;
+  return kvq_paged_decode_combine(cache, num_requests, rows_per_request, num_q_heads,
+                                  max_blocks_per_req, context_lens, max_context_len,
+                                  partition_tokens, out, workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_paged_decode_append(const kvq_cache *cache, const void *k_new,
+                                   int64_t k_token_stride, const void *v_new,
+                                   int64_t v_token_stride, const void *q, int32_t num_requests,
+                                   int32_t rows_per_request, int32_t num_q_heads,
+                                   const int32_t *block_tables, int32_t max_blocks_per_req,
+                                   const int32_t *context_lens, int32_t max_context_len,
+                                   float sm_scale, int32_t partition_tokens, void *out,
+                                   void *workspace, size_t workspace_bytes, int32_t *err_flags,
+                                   kvq_stream_t stream) {
+  kvq_status st = kvq_paged_decode_append_partials(
+      cache, k_new, k_token_stride, v_new, v_token_stride, q, num_requests, rows_per_request,
+      num_q_heads, block_tables, max_blocks_per_req, context_lens, max_context_len, sm_scale,
+      partition_tokens, out, workspace, workspace_bytes, err_flags, stream);
   if (st != KVQ_OK) return st;
   return kvq_paged_decode_combine(cache, num_requests, rows_per_request, num_q_heads,
                                   max_blocks_per_req, context_lens, max_context_len,

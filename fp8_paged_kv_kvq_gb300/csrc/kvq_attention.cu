@@ -1007,7 +1007,18 @@ size_t attn_workspace_bytes(int64_t rows_total, int32_t num_partitions) {
 cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const void *q,
                                  const int32_t *block_tables, const int32_t *context_lens,
                                  float sm_scale, void *out, void *workspace,
-                                 int32_t *err_flags, cudaStream_t stream) {
+                                 int32_t *err_flags, cudaStream_t stream,
+                                 const AppendRows *append) {
+  // a decode step's new rows: stored inside the load-balanced kernel, else by
+  // the store's own launch ahead of the attention
+  if (append != nullptr && !(s.stream && !s.rows_kernel && s.rows_per_request <= kStreamNewRows)) {
+    const cudaError_t e = launch_quantize_positions(
+        c, append->k, append->k_stride, append->v, append->v_stride, s.num_requests,
+        s.rows_per_request, block_tables, s.max_blocks_per_req, context_lens, context_cap(s),
+        s.log2_block, err_flags, stream);
+    if (e != cudaSuccess) return e;
+    append = nullptr;
+  }
   AttnParams p;
   p.k_codes = c.k_codes;
   p.v_codes = c.v_codes;
@@ -1042,7 +1053,7 @@ cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const v
                             err_flags, stream);
   if (s.stream)
     return launch_attn_partials_stream(c, s, q, block_tables, context_lens, sm_scale, out,
-                                       workspace, err_flags, stream);
+                                       workspace, err_flags, stream, append);
   // the page-major kernel reads 4 heads per CTA: worth it once its grid is at
   // least ~3 waves (3 CTAs per SM); smaller grids go to one CTA per head
   const int64_t page_ctas =

@@ -15,21 +15,25 @@
 //  * The batch's work is the sequence of 16-token chunks ordered (request r,
 //    group g of 4 KV heads, chunk c): request r holds C_r = ceil(L_r / 16)
 //    chunks per group, at global chunk index (H/4) * sum_{r' < r} C_r' +
-//    g * C_r + c.  CTA b of the (3 per SM) grid takes the range
-//    [b B, (b + 1) B) with B = max(ceil(total / grid), ceil(C_max / 15)), so
-//    every CTA streams the same number of chunks whatever the context lengths
-//    (no partition tails, no waves), and one (request, head group) is cut into
-//    at most 16 pieces.
+//    g * C_r + c (plus a charge of a few positions per segment start).  The
+//    (3 per SM) grid splits it into contiguous ranges whatever the context
+//    lengths (no partition tails, no waves): weighted 135 : 128 : 121 over the
+//    grid's three thirds by block index, the measured ratio of their streaming
+//    rates when all three run together, or, for batches whose smallest
+//    weighted range would cut a (request, group) into more than 16 pieces,
+//    equal ranges of max(ceil(total / grid), ceil(C_max / 15)).
 //  * A CTA walks its range segment by segment (a segment: its chunks of one
-//    (request, head group)).  The producer warp stages the segment's block ids
-//    in shared memory and streams its chunks through the ring without stopping
-//    at segment ends; each head warp prepares the request's query pieces,
-//    runs the chunks and writes either the final row (a segment that is the
-//    whole request) or its (max, denominator, output) to partial slot
+//    (request, head group)).  The producer warp stages the next segment's
+//    block ids in shared memory and streams the chunks through the ring
+//    without stopping at segment ends; each head warp stages the next
+//    segment's query rows and context length by cp.async while the current
+//    segment runs, turns them into query pieces at the switch, runs the
+//    chunks and writes either the final row (a segment that is the whole
+//    request) or its (max, denominator, output) to partial slot
 //    b - first CTA of the (request, group).
-//  * CTA 0 writes B and the per-request chunk prefix into the workspace; the
-//    combine kernel (one warp per output row) reads them to find each row's
-//    slots.
+//  * CTA 0 writes the split and the per-request chunk prefix into the
+//    workspace; the combine kernel (one warp per output row) reads them to
+//    find each row's slots.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,6 +53,12 @@ constexpr int kStStages = 3;
 constexpr int kStRows = 8;                           // stacked query rows per KV head
 constexpr int kStMaxPages = 520;                     // block ids of one segment
 constexpr float kStLazyRescale = 8.0f;
+// Range weights of the grid's three thirds (blockIdx / (grid / 3)): with three
+// CTAs per SM, CTAs of the first third stream ~10 % faster than those of the
+// last whatever work they hold (a per-CTA timer trace of the decode batch, also
+// with the work order reversed), so equal ranges leave the last third ~4.5 us
+// behind.
+constexpr int64_t kStW0 = 135, kStW1 = 128, kStW2 = 121, kStWSum = kStW0 + kStW1 + kStW2;
 
 // shared memory from a 1024-byte aligned base; a stage is
 // [K: head][row][128 B] | [V: head][row][128 B] | K scales [row][head] | V scales
@@ -57,7 +67,13 @@ constexpr int kStScBytes = kChunk * kStHeads * 4;                     // 256 B
 constexpr int kStStageBytes = ((2 * kStCodeBytes + 2 * kStScBytes) + 1023) / 1024 * 1024;
 constexpr int kOffStQ = kStStages * kStStageBytes;                    // [head][2][8][128]
 constexpr int kOffStRowExp = kOffStQ + kStHeads * 2 * kStRows * kHeadDim;
-constexpr int kOffStPre = kOffStRowExp + kStHeads * kStRows * 4;      // [N + 1] int32
+// a decode step's new rows stored by this kernel: at most kStNewRows per request
+constexpr int kStNewRows = kStreamNewRows;
+constexpr int kOffStNew = kOffStRowExp + kStHeads * kStRows * 4;       // [head][row][K|V][256 B]
+constexpr int kOffStSlot = kOffStNew + kStHeads * kStNewRows * 2 * 2 * kHeadDim;   // int64 [stage]
+constexpr int kOffStLen = kOffStSlot + kStStages * 8;                  // [head][4] int32
+constexpr int kOffStSplit = kOffStLen + kStHeads * 16;   // int64: x_begin, x_end, B, total
+constexpr int kOffStPre = kOffStSplit + 32;                            // [N + 1] int32
 constexpr int kOffStBt = kOffStPre + (kStreamMaxRequests + 1 + 3) / 4 * 16;
 constexpr int kOffStBar = kOffStBt + 2 * kStMaxPages * 4;     // two segments' block ids
 constexpr int kOffStAbort = kOffStBar + 2 * kStStages * 8;
@@ -78,8 +94,18 @@ struct StParams {
   int32_t cmax;               // ceil(max context / 16)
   float *o_part;              // [rows][kStreamSlots][128]
   float2 *ml_part;            // [rows][kStreamSlots]
-  int32_t *plan;              // [0] B, [1] N, [2 ..] chunk prefix [N + 1]
+  int32_t *plan;              // [0] B, [1] N, [2] grid / 3, [3] 0, [4 ..] chunk prefix [N + 1]
   int32_t *err_flags;
+  // the step's new rows (k_new == nullptr: none; R <= kStNewRows): row
+  // r * R + i of request r goes to position L_r - R + i, stored by the CTA
+  // that streams its chunk
+  const uint16_t *k_new;
+  const uint16_t *v_new;
+  int64_t k_stride, v_stride;  // token pitch, elements
+  uint8_t *k_codes;
+  uint8_t *v_codes;
+  float *k_scales;
+  float *v_scales;
 };
 
 __device__ __forceinline__ float st_ex2(float x) {
@@ -123,8 +149,9 @@ __device__ __forceinline__ Segment locate(const int32_t *pre, int N, int hg, int
   s.r = lo;
   const int V = pre[lo + 1] - pre[lo];
   s.C = V - kStreamSwitchChunks;
+  // positions stay below 2^31 (attn_stream_shape_ok), so 32-bit division
   const int64_t off = x - static_cast<int64_t>(hg) * pre[lo];
-  s.g = static_cast<int>(off / V);
+  s.g = static_cast<int>(static_cast<uint32_t>(off) / static_cast<uint32_t>(V));
   const int64_t start = static_cast<int64_t>(hg) * pre[lo] + static_cast<int64_t>(s.g) * V;
   s.base = start + kStreamSwitchChunks;
   const int64_t end = start + V < x_end ? start + V : x_end;
@@ -138,6 +165,97 @@ __device__ __forceinline__ Segment locate(const int32_t *pre, int N, int hg, int
     s.n = static_cast<int>(end - xs);
   }
   return s;
+}
+
+// The split of the work sequence (total positions) over the grid: CTA b
+// takes [start(b), start(b + 1)).  Weighted (B == 0): the grid's thirds get
+// ranges in the ratio kStW0 : kStW1 : kStW2, every range at least b_min long;
+// else equal ranges of B positions (CTAs past the end idle).  owner(x) is the
+// CTA whose range holds position x.
+struct StSplit {
+  int64_t total;
+  int64_t B;
+  int64_t cls;                         // CTAs per third of the grid
+
+  __host__ __device__ int64_t wpre(int64_t b) const {   // weights of CTAs < b
+    const int64_t b0 = b < cls ? b : cls;
+    const int64_t b1 = b < cls ? 0 : (b < 2 * cls ? b - cls : cls);
+    const int64_t b2 = b < 2 * cls ? 0 : b - 2 * cls;
+    return kStW0 * b0 + kStW1 * b1 + kStW2 * b2;
+  }
+  __host__ __device__ int64_t start(int64_t b) const {
+    if (B > 0) return b * B < total ? b * B : total;
+    return total * wpre(b) / (kStWSum * cls);
+  }
+  __host__ __device__ int64_t owner(int64_t x) const {   // 0 <= x < total
+    if (B > 0) return x / B;
+    // the largest b with start(b) <= x, i.e. wpre(b) <= y
+    const int64_t y = ((x + 1) * kStWSum * cls - 1) / total;
+    const int64_t w1 = kStW0 * cls, w2 = w1 + kStW1 * cls;
+    const int64_t b = y < w1 ? y / kStW0 : (y < w2 ? cls + (y - w1) / kStW1 : 2 * cls + (y - w2) / kStW2);
+    return b < 3 * cls - 1 ? b : 3 * cls - 1;
+  }
+};
+
+// b_min: the shortest range that cuts no segment of <= cmax chunks into more
+// than kStreamSlots pieces.
+__host__ __device__ inline StSplit make_split(int64_t total, int64_t grid, int64_t cmax) {
+  const int64_t b_min0 = (cmax + kStreamSlots - 2) / (kStreamSlots - 1);
+  const int64_t b_min = b_min0 > 1 ? b_min0 : 1;
+  StSplit sp;
+  sp.total = total;
+  sp.cls = grid / 3;
+  sp.B = 0;
+  // every weighted range is at least floor(total kStW2 / (kStWSum cls)) long
+  if (grid % 3 != 0 || sp.cls == 0 || total * kStW2 / (kStWSum * sp.cls) < b_min) {
+    const int64_t B = (total + grid - 1) / grid;
+    sp.B = B > b_min ? B : b_min;
+  }
+  return sp;
+}
+
+// The step's new rows of one chunk, one warp for KV head h (tile w of the
+// stage): each row quantised with the store's codec (one row per warp pass,
+// 4 elements a lane), put into the stage's code tile (row tr of the 128-byte
+// swizzled tile) and scale column, and stored to the cache at slot0 + tr
+// (slot0 < 0: a page id out of range, nothing stored).  Rare (a chunk per
+// segment end): rolled loops keep the chunk loop free of spills.
+__device__ __forceinline__ void patch_new_rows(const StParams &p, uint8_t *stage, int w, int h,
+                                            int lane, int L, int j0, const uint8_t *newb,
+                                            int64_t slot0) {
+  uint8_t *kbm = stage + w * kChunk * kHeadDim;
+  uint8_t *vbm = kbm + kStCodeBytes;
+  float *ksm = reinterpret_cast<float *>(stage + 2 * kStCodeBytes) + w;
+  float *vsm = ksm + kStScBytes / 4;
+#pragma unroll 1
+  for (int i = 0; i < p.R; ++i) {
+    const int pos = L - p.R + i;
+    if (pos < j0 || pos >= j0 + kChunk) continue;
+    const int tr = pos - j0;
+#pragma unroll 1
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(newb + (2 * i + kv) * 2 * kHeadDim + 8 * lane);
+      uint32_t mg = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mg = __vmaxu2(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, off));
+      const float amax = __uint_as_float(max(mg & 0xFFFFu, mg >> 16) << 16);
+      uint32_t word = 0u;
+      float sc = 0.0f;
+      if (amax != 0.0f) {
+        sc = row_scale(amax);
+        word = (sc >= kMarksteinMinScale) ? encode4<true>(v.x, v.y, sc, __frcp_rn(sc))
+                                          : encode4<false>(v.x, v.y, sc, 0.0f);
+      }
+      *reinterpret_cast<uint32_t *>((kv ? vbm : kbm) + tr * kHeadDim +
+                                    (((lane >> 2) ^ (tr & 7)) << 4) + 4 * (lane & 3)) = word;
+      if (lane == 0) (kv ? vsm : ksm)[4 * tr] = sc;
+      if (slot0 >= 0) {
+        const int64_t row = (slot0 + tr) * p.H + h;
+        *reinterpret_cast<uint32_t *>((kv ? p.v_codes : p.k_codes) + row * kHeadDim + 4 * lane) = word;
+        if (lane == 0) (kv ? p.v_scales : p.k_scales)[row] = sc;
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kStThreads, 3)
@@ -189,7 +307,17 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       if (r < N) pre[r + 1] = carry + v;
       carry += __shfl_sync(0xFFFFFFFFu, v, 31);
     }
-    if (lane == 0) pre[0] = 0;
+    if (lane == 0) {
+      pre[0] = 0;
+      // the split and this CTA's range, once (64-bit divisions by every
+      // thread of the SM's three CTAs would hold up the range's first copy)
+      const StSplit sp = make_split(static_cast<int64_t>(p.H / kStHeads) * carry, gridDim.x, p.cmax);
+      int64_t *sx = reinterpret_cast<int64_t *>(smem + kOffStSplit);
+      sx[0] = sp.start(blockIdx.x);
+      sx[1] = sp.start(blockIdx.x + 1);
+      sx[2] = sp.B;
+      sx[3] = sp.total;
+    }
   }
   if (tid == 0) {
     for (int s = 0; s < kStStages; ++s) {
@@ -202,19 +330,17 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   }
   __syncthreads();
   const int hg = p.H / kStHeads;
-  const int64_t total = static_cast<int64_t>(hg) * pre[N];
-  int64_t B = (total + gridDim.x - 1) / gridDim.x;
-  const int64_t b_min = (p.cmax + kStreamSlots - 2) / (kStreamSlots - 1);
-  B = B > b_min ? B : b_min;
-  B = B > 0 ? B : 1;
-  const int64_t x_begin = static_cast<int64_t>(blockIdx.x) * B;
-  const int64_t x_end = total < x_begin + B ? total : x_begin + B;
+  const int64_t *sx = reinterpret_cast<const int64_t *>(smem + kOffStSplit);
+  const int64_t x_begin = sx[0];
+  const int64_t x_end = sx[1];
   if (blockIdx.x == 0) {
     if (tid == 0) {
-      p.plan[0] = static_cast<int32_t>(B);
+      p.plan[0] = static_cast<int32_t>(sx[2]);
       p.plan[1] = N;
+      p.plan[2] = static_cast<int32_t>(gridDim.x / 3);
+      p.plan[3] = 0;
     }
-    for (int i = tid; i <= N; i += kStThreads) p.plan[2 + i] = pre[i];
+    for (int i = tid; i <= N; i += kStThreads) p.plan[4 + i] = pre[i];
   }
   if (x_begin >= x_end) return;
 
@@ -234,15 +360,16 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         cp_async_4(bt_s + buf * kStMaxPages + i, bt + i, 4u);
       cp_async_commit();
     };
-    stage_ids(locate(pre, N, hg, x_begin, x_end), 0);
+    Segment sg = locate(pre, N, hg, x_begin, x_end);
+    if (sg.n > 0) stage_ids(sg, 0);
     int buf = 0;
-    for (int64_t x = x_begin; x < x_end && !stop; buf ^= 1) {
-      const Segment sg = locate(pre, N, hg, x, x_end);
-      if (sg.n == 0) break;
+    while (sg.n > 0 && !stop) {
       cp_async_wait<0>();              // this segment's ids (issued a segment ago)
       __syncwarp();
+      Segment nx;
+      nx.n = 0;
       if (sg.next < x_end) {
-        const Segment nx = locate(pre, N, hg, sg.next, x_end);
+        nx = locate(pre, N, hg, sg.next, x_end);
         if (nx.n > 0) stage_ids(nx, buf ^ 1);
       }
       const int32_t *ids = bt_s + buf * kStMaxPages;
@@ -261,10 +388,13 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
           const int pi = (j >> p.log2_bs) - p0;
           const uint32_t blk = (pi < kStMaxPages) ? static_cast<uint32_t>(ids[pi]) : 0xFFFFFFFFu;
           uint32_t bytes = 0;
+          int64_t *stage_slot = reinterpret_cast<int64_t *>(smem + kOffStSlot);
+          stage_slot[st] = -1;                       // read after the stage's full barrier
           if (blk >= p.num_blocks) {                 // also every negative id
             bad = true;
           } else {
             const int z = static_cast<int>((blk << p.log2_bs) | (j & ((1 << p.log2_bs) - 1)));
+            stage_slot[st] = z;
             const int h0 = kStHeads * sg.g;
             tma_load_3d(smem_addr(sb), &tmap_k, 0, z, h0, fb);
             tma_load_3d(smem_addr(sb + kStCodeBytes), &tmap_v, 0, z, h0, fb);
@@ -276,7 +406,8 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         }
       }
       stop = __shfl_sync(0xFFFFFFFFu, stop ? 1 : 0, 0) != 0;
-      x = sg.next;
+      sg = nx;
+      buf ^= 1;
     }
     if (lane == 0) {
       if (bad && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
@@ -289,8 +420,43 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
 
   // ------------------------------------------------------------ head warps
   const int w = warp;
-  uint8_t *plane = smem + kOffStQ + w * 2 * kStRows * kHeadDim;   // [2][8][128]
+  // [2][8][128]: the query pieces; while they sit in registers, the next
+  // segment's raw query rows [8][256 B] land here
+  uint8_t *plane = smem + kOffStQ + w * 2 * kStRows * kHeadDim;
   float *rexp = row_exp + w * kStRows;
+  int32_t *len_s = reinterpret_cast<int32_t *>(smem + kOffStLen) + 4 * w;
+  // the step's new rows of this warp's head, [row][K|V][256 B] bf16
+  uint8_t *newb = smem + kOffStNew + w * kStNewRows * 2 * 2 * kHeadDim;
+  const int64_t *stage_slot = reinterpret_cast<const int64_t *>(smem + kOffStSlot);
+  // a segment's query rows of this warp's head (16-byte cp.async, row m at
+  // m * 256) and its request's context length into shared memory
+  auto stage_q = [&](const Segment &sg) {
+    const int h = kStHeads * sg.g + w;
+    for (int c = lane; c < p.M * 16; c += 32) {
+      const int m = c >> 4, i = m / p.G, gq = m - i * p.G;
+      const uint16_t *src =
+          p.q + ((static_cast<int64_t>(sg.r) * p.R + i) * p.Hq + h * p.G + gq) * kHeadDim + 8 * (c & 15);
+      cp_async_16(plane + m * 2 * kHeadDim + 16 * (c & 15), src, 16u);
+    }
+    if (lane == 0) cp_async_4(len_s, p.context_lens + sg.r, 4u);
+    cp_async_commit();
+  };
+  // the step's new rows of a segment whose part in this range reaches its
+  // last two chunks (the rows' positions L - R .. L - 1 lie there)
+  auto stage_new = [&](const Segment &sg) {
+    if (p.k_new == nullptr || sg.c0 + sg.n + 1 < sg.C) return;
+    const int h = kStHeads * sg.g + w;
+    for (int c = lane; c < p.R * 2 * 16; c += 32) {
+      const int i = c >> 5, kv = (c >> 4) & 1, piece = c & 15;
+      const int64_t t = static_cast<int64_t>(sg.r) * p.R + i;
+      const uint16_t *src = (kv ? p.v_new + t * p.v_stride : p.k_new + t * p.k_stride) +
+                            h * kHeadDim + 8 * piece;
+      cp_async_16(newb + (2 * i + kv) * 2 * kHeadDim + 16 * piece, src, 16u);
+    }
+    cp_async_commit();
+  };
+  Segment sg = locate(pre, N, hg, x_begin, x_end);
+  if (sg.n > 0) stage_q(sg);
   // this lane's ldmatrix row address within a head's K tile, per k-step
   const int ld_row = (lane & 7) + 8 * ((lane >> 3) & 1);
   uint32_t ld_off[4];
@@ -299,67 +465,50 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
     ld_off[s2] = ld_row * kHeadDim + (((2 * s2 + (lane >> 4)) ^ (lane & 7)) << 4);
   uint32_t u = 0;                      // chunks consumed
   bool timed_out = false;
-  for (int64_t x = x_begin; x < x_end && !timed_out;) {
-    const Segment sg = locate(pre, N, hg, x, x_end);
-    if (sg.n == 0) break;
+  bool first_seg = true;
+  while (sg.n > 0 && !timed_out) {
     const int r = sg.r;
     const int h = kStHeads * sg.g + w;
-    int L = p.context_lens[r];
+    cp_async_wait<0>();                // this segment's rows (staged a segment ago)
+    __syncwarp();
+    int L = *len_s;
     L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
-    auto q_row = [&](int m) {   // m < M
-      const int i = m / p.G, gq = m - i * p.G;
-      return p.q + ((static_cast<int64_t>(r) * p.R + i) * p.Hq + h * p.G + gq) * kHeadDim;
-    };
-    // query rows (one round trip), exponents and the two e4m3 pieces of each
-    // element, q = 2^e (p1 + p2)
+    // exponents and the two e4m3 pieces of each element, q = 2^e (p1 + p2);
+    // rows past M get zero pieces
     {
       uint2 vq[kStRows];
 #pragma unroll
       for (int m = 0; m < kStRows; ++m)
-        vq[m] = (m < p.M) ? *reinterpret_cast<const uint2 *>(q_row(m) + 4 * lane)
+        vq[m] = (m < p.M) ? *reinterpret_cast<const uint2 *>(plane + m * 2 * kHeadDim + 8 * lane)
                           : make_uint2(0u, 0u);
-      __syncwarp();                    // the previous segment's planes are read
+      __syncwarp();                    // every lane holds its rows before the pieces overwrite them
 #pragma unroll
       for (int m = 0; m < kStRows; ++m) {
-        const uint2 v = vq[m];
-        float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                           fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-        int e = (ex == 0) ? -126 : ex - 127 - 7;
-        e = e < -126 ? -126 : (e > 126 ? 126 : e);
-        const float rx = (amax == 0.0f) ? 0.0f : __int_as_float((127 + e) << 23);   // 2^e
-        if (lane == 0) rexp[m] = rx;
         uint32_t c1w = 0u, c2w = 0u;
-        if (rx != 0.0f) {
-          const float inv = __int_as_float((254u << 23) - __float_as_uint(rx));
-          const float xs[4] = {bf16_lo(v.x) * inv, bf16_hi(v.x) * inv, bf16_lo(v.y) * inv,
-                               bf16_hi(v.y) * inv};
-          e4m3_pieces4(xs, c1w, c2w);
+        float rx = 0.0f;
+        if (m < p.M) {
+          const uint2 v = vq[m];
+          float amax = fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                             fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+          const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+          int e = (ex == 0) ? -126 : ex - 127 - 7;
+          e = e < -126 ? -126 : (e > 126 ? 126 : e);
+          rx = (amax == 0.0f) ? 0.0f : __int_as_float((127 + e) << 23);   // 2^e
+          if (rx != 0.0f) {
+            const float inv = __int_as_float((254u << 23) - __float_as_uint(rx));
+            const float xs[4] = {bf16_lo(v.x) * inv, bf16_hi(v.x) * inv, bf16_lo(v.y) * inv,
+                                 bf16_hi(v.y) * inv};
+            e4m3_pieces4(xs, c1w, c2w);
+          }
         }
+        if (lane == 0) rexp[m] = rx;
         *reinterpret_cast<uint32_t *>(plane + m * kHeadDim + 4 * lane) = c1w;
         *reinterpret_cast<uint32_t *>(plane + kStRows * kHeadDim + m * kHeadDim + 4 * lane) = c2w;
       }
       __syncwarp();
-    }
-    // the next segment's query rows and context length into L1 while this
-    // segment runs (its preparation then hits L1): lanes 2m, 2m + 1 take the
-    // two 128-byte lines of row m, lane 31 the context length
-    if (sg.next < x_end) {
-      const Segment nx = locate(pre, N, hg, sg.next, x_end);
-      const int hn = kStHeads * nx.g + w;
-      const int m = lane >> 1;
-      const void *a = nullptr;
-      if (m < p.M) {
-        const int i = m / p.G, gq = m - i * p.G;
-        a = p.q + ((static_cast<int64_t>(nx.r) * p.R + i) * p.Hq + hn * p.G + gq) * kHeadDim +
-            64 * (lane & 1);
-      } else if (lane == 31) {
-        a = p.context_lens + nx.r;
-      }
-      if (a != nullptr) asm volatile("prefetch.global.L1 [%0];" :: "l"(a));
     }
     // B fragments for k-step s2: b0 = dims 32 s2 + 4c + 0..3, b1 = + 16, row g
     uint32_t qb[4][2][2];
@@ -371,6 +520,15 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         qb[s2][pc][0] = *reinterpret_cast<const uint32_t *>(qr);
         qb[s2][pc][1] = *reinterpret_cast<const uint32_t *>(qr + 16);
       }
+    // the next segment's rows land in the planes while this one runs
+    if (sg.next < x_end) {
+      const Segment nx = locate(pre, N, hg, sg.next, x_end);
+      if (nx.n > 0) {
+        __syncwarp();                  // every lane has read its pieces
+        stage_q(nx);
+      }
+    }
+    stage_new(sg);
     // this thread's rows: n = 2c + e
     int vis[2];
     float rowf[2], m_run[2], l_run[2], thr[2], ms[2];
@@ -404,6 +562,15 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       const float *ksv = reinterpret_cast<const float *>(sbase + 2 * kStCodeBytes) + w;
       const float *vsv = reinterpret_cast<const float *>(sbase + 2 * kStCodeBytes + kStScBytes) + w;
       const int j0 = kChunk * (sg.c0 + k);
+      if (p.k_new != nullptr && j0 + kChunk > L - p.R) {
+        // the step's new rows in this chunk (the copy brought whatever the
+        // slots held)
+        cp_async_wait<0>();
+        __syncwarp();
+        patch_new_rows(p, smem + st * kStStageBytes, w, h, lane, L, j0, newb, stage_slot[st]);
+        fence_proxy_async_smem();      // before a later copy refills the stage
+        __syncwarp();
+      }
 
       // ---- S^T = K Q^T (K fragments by ldmatrix), two accumulation chains
       float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -552,9 +719,13 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+
     }
     timed_out = __any_sync(0xFFFFFFFFu, timed_out);
-    if (timed_out) break;
+    if (timed_out) {
+      cp_async_wait<0>();              // the next segment's rows land before the CTA leaves
+      break;
+    }
 
     // ---- the segment's (max, denominator, O) for this head's rows
 #pragma unroll
@@ -567,7 +738,16 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
     const float vsc = (ev == -1000) ? 0.0f : __int_as_float((127 + ev) << 23);   // undo 2^-ev
     const bool direct = (sg.c0 == 0 && sg.n == sg.C);
-    const int slot = static_cast<int>(blockIdx.x - sg.base / B);
+    // the piece slot of a cut segment: the CTA's index among those holding it
+    // (0 for every segment after the range's first, which starts inside it)
+    int slot = 0;
+    if (first_seg && !direct) {
+      StSplit sp;
+      sp.B = sx[2];
+      sp.total = sx[3];
+      sp.cls = gridDim.x / 3;
+      slot = static_cast<int>(blockIdx.x - sp.owner(sg.base));
+    }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int n = 2 * c4 + e;
@@ -592,7 +772,12 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
         if (g8 == 0) p.ml_part[sl] = make_float2(m_run[e], l_run[e]);
       }
     }
-    x = sg.next;
+    first_seg = false;
+    if (sg.next < x_end) {
+      sg = locate(pre, N, hg, sg.next, x_end);
+    } else {
+      sg.n = 0;
+    }
   }
   if (timed_out && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
 }
@@ -600,7 +785,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
 // ---------------------------------------------------------------------------
 // Combine for the stream layout: one warp per output row, eight rows per CTA.
 struct StCombineParams {
-  int32_t R, Hq, G, H;
+  int32_t N, R, Hq, G, H;
   int64_t rows_total;
   const int32_t *plan;
   const float *o_part;
@@ -620,36 +805,51 @@ attn_combine_stream_kernel(const StCombineParams p) {
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
   const int qh = static_cast<int>(row % p.Hq);
   const int g = (qh / p.G) / kStHeads;
-  const int64_t B = p.plan[0];
-  const int32_t *pre = p.plan + 2;
-  const int V = pre[r + 1] - pre[r];
+  const int32_t *pre = p.plan + 4;
+  const int hg = p.H / kStHeads;
+  // one memory round trip: the plan entries this row needs and its first
+  // eight piece slots, whether or not the pieces exist (a slot past the
+  // row's count holds whatever an earlier call left and is not read)
+  const int32_t plan_b = p.plan[0], plan_cls = p.plan[2];
+  const int32_t pre_r = pre[r], pre_r1 = pre[r + 1], pre_n = pre[p.N];
+  const float2 *ml = p.ml_part + row * kStreamSlots;
+  const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * kStreamSlots * kHeadDim) +
+                     lane;
+  float2 v[8];
+  float4 o[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[k] = ml[k];
+    o[k] = op[k * (kHeadDim / 4)];
+  }
+  StSplit split;
+  split.B = plan_b;
+  split.cls = plan_cls;
+  split.total = static_cast<int64_t>(hg) * pre_n;
+  const int V = pre_r1 - pre_r;
   uint2 packed = make_uint2(0u, 0u);
   if (V > 0) {
     const int C = V - kStreamSwitchChunks;
-    const int64_t base = static_cast<int64_t>(p.H / kStHeads) * pre[r] +
-                         static_cast<int64_t>(g) * V + kStreamSwitchChunks;
-    const int n = static_cast<int>((base + C - 1) / B - base / B) + 1;
+    const int64_t base = static_cast<int64_t>(hg) * pre_r + static_cast<int64_t>(g) * V +
+                         kStreamSwitchChunks;
+    const int n = static_cast<int>(split.owner(base + C - 1) - split.owner(base)) + 1;
     if (n <= 1) return;                // written by the partials kernel
-    const float2 *ml = p.ml_part + row * kStreamSlots;
-    const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * kStreamSlots * kHeadDim) +
-                       lane;
     float m_w = -INFINITY, lsum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q0 = 0; q0 < n; q0 += 8) {      // eight pieces per memory round trip
-      float2 v[8];
-      float4 o[8];
+    for (int q0 = 0; q0 < n; q0 += 8) {
+      if (q0 > 0) {                    // pieces 8 .. 15: a second round trip
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        v[k] = make_float2(-INFINITY, 0.0f);
-        o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q0 + k < n) {
-          v[k] = ml[q0 + k];
-          o[k] = op[static_cast<int64_t>(q0 + k) * (kHeadDim / 4)];
+        for (int k = 0; k < 8; ++k) {
+          if (q0 + k < n) {
+            v[k] = ml[q0 + k];
+            o[k] = op[static_cast<int64_t>(q0 + k) * (kHeadDim / 4)];
+          }
         }
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        if (v[k].x == -INFINITY) continue;        // a piece that saw no visible token
+        // a piece that saw no visible token, or no piece
+        if (q0 + k >= n || v[k].x == -INFINITY) continue;
         const float mn = fmaxf(m_w, v[k].x);
         const float a = st_ex2(m_w - mn), b = st_ex2(v[k].x - mn);
         lsum = lsum * a + v[k].y * b;
@@ -671,7 +871,7 @@ attn_combine_stream_kernel(const StCombineParams p) {
 }  // namespace
 
 size_t attn_stream_plan_bytes(int32_t num_requests) {
-  return (static_cast<size_t>(num_requests + 3) * 4 + 255) / 256 * 256;
+  return (static_cast<size_t>(num_requests + 5) * 4 + 255) / 256 * 256;
 }
 
 bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s) {
@@ -679,24 +879,38 @@ bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s) {
   const int64_t sms = s.sms > 0 ? s.sms : 152;
   const int64_t cmax = (static_cast<int64_t>(s.max_context_len) + kChunk - 1) / kChunk;
   const int64_t hg = num_kv_heads / kStHeads;
-  // chunks per CTA stay within the block-id window of one segment
-  const int64_t per_cta =
-      (s.num_requests * hg * (cmax + kStreamSwitchChunks) + 3 * sms - 1) / (3 * sms);
+  // chunks per CTA stay within the block-id window of one segment, whichever
+  // split the kernel takes for the batch's actual lengths (at most total_ub
+  // positions): equal ranges of max(ceil(total / grid), b_min), or weighted
+  // ranges of at most ceil(total kStW0 / (kStWSum grid / 3)) + 1
+  const int64_t total_ub = s.num_requests * hg * (cmax + kStreamSwitchChunks);
+  const int64_t grid = 3 * sms;
+  const int64_t per_cta = (total_ub + grid - 1) / grid;
+  const int64_t per_cta_w = (total_ub * kStW0 + kStWSum * sms - 1) / (kStWSum * sms) + 1;
   const int64_t b_min = (cmax + kStreamSlots - 2) / (kStreamSlots - 1);
-  const int64_t b = per_cta > b_min ? per_cta : b_min;
+  int64_t b = per_cta > b_min ? per_cta : b_min;
+  b = b > per_cta_w ? b : per_cta_w;
   return s.rows <= kStRows && bs >= kChunk && num_kv_heads % kStHeads == 0 &&
          s.num_requests >= 1 && s.num_requests <= kStreamMaxRequests &&
-         b * kChunk / bs + 2 <= kStMaxPages;
+         total_ub < (int64_t(1) << 31) && b * kChunk / bs + 2 <= kStMaxPages;
 }
 
 cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, const void *q,
                                         const int32_t *block_tables,
                                         const int32_t *context_lens, float sm_scale, void *out,
                                         void *workspace, int32_t *err_flags,
-                                        cudaStream_t stream) {
+                                        cudaStream_t stream, const AppendRows *append) {
   const int64_t rows_total =
       static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
   StParams p;
+  p.k_new = static_cast<const uint16_t *>(append ? append->k : nullptr);
+  p.v_new = static_cast<const uint16_t *>(append ? append->v : nullptr);
+  p.k_stride = append ? append->k_stride : 0;
+  p.v_stride = append ? append->v_stride : 0;
+  p.k_codes = c.k_codes;
+  p.v_codes = c.v_codes;
+  p.k_scales = c.k_scales;
+  p.v_scales = c.v_scales;
   p.num_blocks = static_cast<uint32_t>(c.num_slots >> s.log2_block);
   p.H = c.num_kv_heads;
   p.log2_bs = s.log2_block;
@@ -746,6 +960,7 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
 cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
                                        cudaStream_t stream) {
   StCombineParams p;
+  p.N = s.num_requests;
   p.R = s.rows_per_request;
   p.Hq = s.num_q_heads;
   p.G = s.group;

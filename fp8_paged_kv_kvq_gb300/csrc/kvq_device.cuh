@@ -102,6 +102,8 @@ __device__ __forceinline__ uint64_t div_markstein_x2(uint64_t x, uint64_t ns, ui
   return fma_f32x2(r1, y, q1);
 }
 
+
+
 // ---------------------------------------------------------------------------
 // Decode to bf16, exactly.  Placing the 7 magnitude bits of a code at bf16 bits
 // 10..4 (exponent low bits + top mantissa bits) and its sign at bit 15 gives a
@@ -199,6 +201,42 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// The row codec of the store (FreeToken PR #354 "feat(kvcache): store the KV
+// cache as fp8 e4m3 codes"; ROCm/ATOM PR #2655, K/V bullet): one fp32 scale
+// per (token, KV head) row, the row's largest magnitude over 448, and e4m3
+// codes of x / scale rounded to nearest even.
+
+constexpr float kInv448 = 1.0f / 448.0f;               // fl32(1 / 448): rounded by the compiler
+
+// fl32(amax / 448): Markstein's correction through the correctly rounded
+// constant reciprocal while no step underflows, else IEEE division.
+__device__ __forceinline__ float row_scale(float amax) {
+  return (amax >= kMarksteinMinScale) ? div_markstein(amax, 448.0f, kInv448)
+                                      : __fdiv_rn(amax, 448.0f);
+}
+
+// Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3):
+// fl32(x / s) then e4m3 round-to-nearest-even.  kFast divides through the
+// row's reciprocal y with Markstein's correction (exact for s >= 2^-90), two
+// elements per packed f32x2 operation; otherwise plain IEEE division.  The four sign bits of x (bytes 1 and 3 of
+// each bf16 pair) are ORed into the code bytes: a nonzero code already has
+// its sign, and a zero code takes the sign of its input (-0 stays 0x80).
+template <bool kFast>
+__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s, float y) {
+  float q[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+  if (kFast) {
+    const uint64_t ns = pack_f32x2(-s, -s), yy = pack_f32x2(y, y);
+    unpack_f32x2(div_markstein_x2(pack_f32x2(q[0], q[1]), ns, yy), q[0], q[1]);
+    unpack_f32x2(div_markstein_x2(pack_f32x2(q[2], q[3]), ns, yy), q[2], q[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q[e] = __fdiv_rn(q[e], s);
+  }
+  const uint32_t signs = prmt(w0, w1, 0x7531u) & 0x80808080u;
+  return e4m3x2_rn(q[0], q[1]) | (e4m3x2_rn(q[2], q[3]) << 16) | signs;
+}
 
 // ---------------------------------------------------------------------------
 // Asynchronous global -> shared copies (Ampere-style cp.async, available on
@@ -316,6 +354,12 @@ __device__ __forceinline__ void fence_mbarrier_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Orders this thread's generic-proxy global writes before async-proxy (TMA)
+// accesses that follow it through a barrier.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
 }
 
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.

@@ -60,9 +60,10 @@ struct AttnShape {
 // content of the workspace, carries another tag and is restarted.
 uint32_t next_call_tag();
 
-// The load-balanced decode kernel's layout: a plan ([0] chunks per CTA, [1]
-// requests, [2 ..] per-request chunk prefix) then partials in kStreamSlots
-// slots per output row.
+// The load-balanced decode kernel's layout: a plan ([0] equal range length or
+// 0 for the weighted split, [1] requests, [2] CTAs per third of the grid, [3]
+// 0, [4 ..] per-request chunk prefix) then partials in kStreamSlots slots per
+// output row.
 constexpr int32_t kStreamSlots = 16;
 // A segment (the chunks of one request and head group) is charged this many
 // extra chunks at its start, so a CTA whose range crosses into a new segment
@@ -70,6 +71,9 @@ constexpr int32_t kStreamSlots = 16;
 // correspondingly less work.
 constexpr int32_t kStreamSwitchChunks = 3;
 constexpr int32_t kStreamMaxRequests = 1024;
+// New rows per request that the load-balanced kernel stores itself (a decode
+// step's store fused into its attention); more take the store's own launch.
+constexpr int32_t kStreamNewRows = 2;
 size_t attn_stream_plan_bytes(int32_t num_requests);
 
 // Whether a shape suits the load-balanced kernel (apart from the cache's
@@ -77,11 +81,20 @@ size_t attn_stream_plan_bytes(int32_t num_requests);
 // groups of 4, at most kStreamMaxRequests requests, a segment's block ids
 // within its window.
 bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s);
+// The step's new K and V rows for a store fused into the attention: row
+// r * R + i (token pitch k_stride / v_stride elements, heads 128 elements
+// apart) goes to position L_r - R + i of request r.
+struct AppendRows {
+  const void *k;
+  int64_t k_stride;
+  const void *v;
+  int64_t v_stride;
+};
 cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, const void *q,
                                         const int32_t *block_tables,
                                         const int32_t *context_lens, float sm_scale, void *out,
                                         void *workspace, int32_t *err_flags,
-                                        cudaStream_t stream);
+                                        cudaStream_t stream, const AppendRows *append = nullptr);
 cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
                                        cudaStream_t stream);
 
@@ -93,6 +106,15 @@ cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k
                                     const void *v, int64_t v_stride, int64_t num_tokens,
                                     const int64_t *slot_ids, int32_t *err_flags,
                                     cudaStream_t stream);
+// The quantize-scatter of a decode step's new rows, slots from the block
+// tables: token r R + i to position L_r - R + i of request r (skipped when
+// negative; a page id out of range is skipped and flagged).
+cudaError_t launch_quantize_positions(const kvq_cache &c, const void *k, int64_t k_stride,
+                                     const void *v, int64_t v_stride, int32_t num_requests,
+                                     int32_t rows_per_request, const int32_t *block_tables,
+                                     int32_t max_blocks_per_req, const int32_t *context_lens,
+                                     int32_t ctx_limit, int32_t log2_block, int32_t *err_flags,
+                                     cudaStream_t stream);
 
 cudaError_t launch_dequant_rows(const kvq_cache &c, const int64_t *slot_ids, int64_t n,
                                 int32_t out_dtype, void *out_k, void *out_v,
@@ -119,7 +141,8 @@ cudaError_t launch_index_scores(const kvq_index_cache &c, int32_t log2_block, co
 cudaError_t launch_attn_partials(const kvq_cache &c, const AttnShape &s, const void *q,
                                  const int32_t *block_tables, const int32_t *context_lens,
                                  float sm_scale, void *out, void *workspace,
-                                 int32_t *err_flags, cudaStream_t stream);
+                                 int32_t *err_flags, cudaStream_t stream,
+                                 const AppendRows *append = nullptr);
 
 // Tensor map over one code plane [num_slots, H, 128] uint8: boxes of `rows`
 // slots of one head, 128-byte swizzled in shared memory.

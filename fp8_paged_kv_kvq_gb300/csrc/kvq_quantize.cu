@@ -47,7 +47,32 @@ struct QuantParams {
   int32_t *err_flags;
   uint64_t rows_per_token_magic;   // ceil(2^shift / (2H)): row id / (2H) by a multiply
   int32_t rows_per_token_shift;    // 32 + ceil(log2(2H))
+  // slot_ids == nullptr: token t = r R + i goes to position L_r - R + i of
+  // request r's block table (a decode step's new rows)
+  const int32_t *block_tables;
+  int32_t max_blocks;
+  const int32_t *context_lens;
+  int32_t R;
+  int32_t log2_bs;
+  int32_t ctx_limit;
 };
+
+// The slot of token t under the block-table positions (-1: skip; a page id out
+// of range is flagged).
+__device__ __forceinline__ int64_t position_slot(const QuantParams &p, int64_t t) {
+  const uint32_t r = static_cast<uint32_t>(t) / static_cast<uint32_t>(p.R);   // t < 2^31
+  const int i = static_cast<int>(static_cast<uint32_t>(t) - r * static_cast<uint32_t>(p.R));
+  int L = __ldg(p.context_lens + r);
+  L = L < 0 ? 0 : (L > p.ctx_limit ? p.ctx_limit : L);
+  const int pos = L - p.R + i;
+  if (pos < 0) return -1;
+  const uint32_t blk = static_cast<uint32_t>(__ldg(p.block_tables + static_cast<int64_t>(r) * p.max_blocks + (pos >> p.log2_bs)));
+  if (static_cast<int64_t>(blk) >= (p.num_slots >> p.log2_bs)) {
+    if (i == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_BLOCK_RANGE);
+    return -1;
+  }
+  return (static_cast<int64_t>(blk) << p.log2_bs) | (pos & ((1 << p.log2_bs) - 1));
+}
 
 __device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
   const uint32_t m = 0x7FFF7FFFu;
@@ -59,27 +84,6 @@ __device__ __forceinline__ uint32_t max_mag_bf16x2(uint4 a, uint4 b) {
   r = __vmaxu2(r, b.z & m);
   r = __vmaxu2(r, b.w & m);
   return r;
-}
-
-// Four codes from the two bf16 pairs (w0: elements 0,1; w1: elements 2,3):
-// fl32(x / s) then e4m3 round-to-nearest-even.  kFast divides through the
-// row's reciprocal y with Markstein's correction (exact for s >= 2^-90), two
-// elements per packed f32x2 operation; otherwise plain IEEE division.  The four sign bits of x (bytes 1 and 3 of
-// each bf16 pair) are ORed into the code bytes: a nonzero code already has
-// its sign, and a zero code takes the sign of its input (-0 stays 0x80).
-template <bool kFast>
-__device__ __forceinline__ uint32_t encode4(uint32_t w0, uint32_t w1, float s, float y) {
-  float q[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-  if (kFast) {
-    const uint64_t ns = pack_f32x2(-s, -s), yy = pack_f32x2(y, y);
-    unpack_f32x2(div_markstein_x2(pack_f32x2(q[0], q[1]), ns, yy), q[0], q[1]);
-    unpack_f32x2(div_markstein_x2(pack_f32x2(q[2], q[3]), ns, yy), q[2], q[3]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) q[e] = __fdiv_rn(q[e], s);
-  }
-  const uint32_t signs = prmt(w0, w1, 0x7531u) & 0x80808080u;
-  return e4m3x2_rn(q[0], q[1]) | (e4m3x2_rn(q[2], q[3]) << 16) | signs;
 }
 
 template <bool kFast>
@@ -96,7 +100,6 @@ constexpr int kLanesPerRow = 4;
 constexpr int kRowsPerWarp = 32 / kLanesPerRow;
 constexpr int kPerLane = kHeadDim / kLanesPerRow;      // elements
 constexpr int kVec = kPerLane / 16;                     // 16-element pieces per lane
-constexpr float kInv448 = 1.0f / 448.0f;               // fl32(1 / 448): rounded by the compiler
 
 __global__ void __launch_bounds__(kQuantWarps * 32, 12)
 quantize_scatter_kernel(const QuantParams p) {
@@ -121,7 +124,7 @@ quantize_scatter_kernel(const QuantParams p) {
     a[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k));
     b[k] = __ldg(reinterpret_cast<const uint4 *>(src + 16 * k + 8));
   }
-  const int64_t slot = __ldg(p.slot_ids + t);
+  const int64_t slot = p.slot_ids ? __ldg(p.slot_ids + t) : position_slot(p, t);
   if (slot < 0) return;
   if (slot >= p.num_slots) {
     if (sub == 0 && rem == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_SLOT_RANGE);
@@ -138,10 +141,7 @@ quantize_scatter_kernel(const QuantParams p) {
   for (int k = 0; k < kVec; ++k) out[k] = make_uint4(0u, 0u, 0u, 0u);
   float s = 0.0f;
   if (amax != 0.0f) {
-    // fl32(amax / 448): Markstein's correction through the correctly rounded
-    // constant reciprocal while no step underflows, else IEEE division
-    s = (amax >= kMarksteinMinScale) ? div_markstein(amax, 448.0f, kInv448)
-                                     : __fdiv_rn(amax, 448.0f);
+    s = row_scale(amax);
     if (s >= kMarksteinMinScale) {
       const float y = __frcp_rn(s);
 #pragma unroll
@@ -367,8 +367,7 @@ index_quantize_kernel(const IndexParams p) {
     uint4 out0 = make_uint4(0u, 0u, 0u, 0u), out1 = out0;
     float s = 0.0f;
     if (amax != 0.0f) {
-      s = (amax >= kMarksteinMinScale) ? div_markstein(amax, 448.0f, kInv448)
-                                       : __fdiv_rn(amax, 448.0f);
+      s = row_scale(amax);
       if (s >= kMarksteinMinScale) {
         const float y = __frcp_rn(s);
         out0 = encode16<true>(a[0], b[0], s, y);
@@ -481,6 +480,12 @@ QuantParams quant_params(const kvq_cache &c, const void *k, int64_t k_stride, co
   p.num_slots = c.num_slots;
   p.num_kv_heads = c.num_kv_heads;
   p.err_flags = err_flags;
+  p.block_tables = nullptr;
+  p.max_blocks = 0;
+  p.context_lens = nullptr;
+  p.R = 1;
+  p.log2_bs = 0;
+  p.ctx_limit = 0;
   {
     // n / d == (n * ceil(2^S / d)) >> S for every n < 2^31 when S = 32 + ceil(log2 d):
     // the multiplier's excess e = M d - 2^S is below d <= 2^(S-32), so n e < 2^S
@@ -500,6 +505,26 @@ cudaError_t launch_quantize_scatter(const kvq_cache &c, const void *k, int64_t k
                                     const int64_t *slot_ids, int32_t *err_flags,
                                     cudaStream_t stream) {
   const QuantParams p = quant_params(c, k, k_stride, v, v_stride, num_tokens, slot_ids, err_flags);
+  const int64_t rows = num_tokens * 2 * c.num_kv_heads;
+  const int64_t blocks = (rows + kQuantWarps * kRowsPerWarp - 1) / (kQuantWarps * kRowsPerWarp);
+  return launch_overlapped(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks)),
+                           dim3(kQuantWarps * 32), 0, stream, p);
+}
+
+cudaError_t launch_quantize_positions(const kvq_cache &c, const void *k, int64_t k_stride,
+                                     const void *v, int64_t v_stride, int32_t num_requests,
+                                     int32_t rows_per_request, const int32_t *block_tables,
+                                     int32_t max_blocks_per_req, const int32_t *context_lens,
+                                     int32_t ctx_limit, int32_t log2_block, int32_t *err_flags,
+                                     cudaStream_t stream) {
+  const int64_t num_tokens = static_cast<int64_t>(num_requests) * rows_per_request;
+  QuantParams p = quant_params(c, k, k_stride, v, v_stride, num_tokens, nullptr, err_flags);
+  p.block_tables = block_tables;
+  p.max_blocks = max_blocks_per_req;
+  p.context_lens = context_lens;
+  p.R = rows_per_request;
+  p.log2_bs = log2_block;
+  p.ctx_limit = ctx_limit;
   const int64_t rows = num_tokens * 2 * c.num_kv_heads;
   const int64_t blocks = (rows + kQuantWarps * kRowsPerWarp - 1) / (kQuantWarps * kRowsPerWarp);
   return launch_overlapped(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks)),

@@ -230,6 +230,48 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
                                     void *out, void *workspace, size_t workspace_bytes,
                                     kvq_stream_t stream);
 
+/* One decode step: the store of the step's new rows and the attention that
+ * reads them.  kvq_paged_decode_append_partials does what
+ * kvq_quantize_scatter of the new rows (slots from the block tables, below)
+ * followed by kvq_paged_decode_partials does, with the same arguments and
+ * results; kvq_paged_decode_append adds kvq_paged_decode_combine.  The store
+ * follows the cache format of the pages (FreeToken PR #354 "feat(kvcache):
+ * store the KV cache as fp8 e4m3 codes"; ROCm/ATOM PR #2655, K/V bullet) bit
+ * for bit; fusing it with the attention is this library's own step: where the
+ * shape takes the load-balanced kernel (kvq_paged_decode_partition_tokens), the
+ * CTA that streams a chunk holding new positions quantises and stores those
+ * rows before its copy engine reads the chunk, so the store costs no launch of
+ * its own; other shapes make the store's launch first.
+ *   k_new, v_new    device bf16; row r*rows_per_request + i (token pitch
+ *                   k_token_stride / v_token_stride elements, multiples of 8,
+ *                   16-byte aligned; head h at element h*head_dim) is new token
+ *                   i of request r, stored at position
+ *                   context_lens[r] - rows_per_request + i of its block table
+ *                   (the lengths count the new tokens).  Rows whose position is
+ *                   negative are not stored; a position whose page id is outside
+ *                   the cache is skipped and sets KVQ_ERRF_BLOCK_RANGE.
+ * Other arguments as for kvq_paged_decode. */
+kvq_status kvq_paged_decode_append_partials(const kvq_cache *cache, const void *k_new,
+                                            int64_t k_token_stride, const void *v_new,
+                                            int64_t v_token_stride, const void *q,
+                                            int32_t num_requests, int32_t rows_per_request,
+                                            int32_t num_q_heads, const int32_t *block_tables,
+                                            int32_t max_blocks_per_req,
+                                            const int32_t *context_lens, int32_t max_context_len,
+                                            float sm_scale, int32_t partition_tokens, void *out,
+                                            void *workspace, size_t workspace_bytes,
+                                            int32_t *err_flags, kvq_stream_t stream);
+
+kvq_status kvq_paged_decode_append(const kvq_cache *cache, const void *k_new,
+                                   int64_t k_token_stride, const void *v_new,
+                                   int64_t v_token_stride, const void *q, int32_t num_requests,
+                                   int32_t rows_per_request, int32_t num_q_heads,
+                                   const int32_t *block_tables, int32_t max_blocks_per_req,
+                                   const int32_t *context_lens, int32_t max_context_len,
+                                   float sm_scale, int32_t partition_tokens, void *out,
+                                   void *workspace, size_t workspace_bytes, int32_t *err_flags,
+                                   kvq_stream_t stream);
+
 /* kvq_paged_decode for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point; it exists for code that must not or
  * cannot call cudaMalloc where it decodes (inside an allocator or memory-pool

@@ -46,7 +46,7 @@ def _cache(head_dim=128, block_size=16, slots=64, ptr=0x10000):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.kvq_abi_version() == 2
+    assert lib.kvq_abi_version() == 3
     for s in range(6):
         assert lib.kvq_status_string(s)
 

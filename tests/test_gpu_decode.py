@@ -75,16 +75,26 @@ def test_verify_shapes(R, Hq, H, bs, partition_tokens):
     assert_attention_close(out, ref, f"R={R} Hq={Hq} H={H} P={partition_tokens}")
 
 
+def _many_lens(n, hi, seed):
+    return [int(x) for x in np.random.default_rng(seed).integers(0, hi + 1, n)]
+
+
 @pytest.mark.parametrize("R,Hq,H,lens", [
     (1, 32, 8, [0, 1, 15, 16, 17, 300, 1000, 2047, 33, 4096, 5, 0, 777]),
     (2, 16, 4, [3, 129, 640, 64, 2]),      # 8 stacked rows: 2 query rows x GQA 4
     (1, 8, 8, [6000, 20, 40]),             # one dominant request: 15 pieces per head group
+    # enough chunks for the weighted split, many short segments per CTA (the
+    # next segment's query rows staged while the current one runs)
+    (1, 32, 8, _many_lens(300, 700, 11)),
+    (2, 16, 4, _many_lens(200, 900, 12)),
 ])
 def test_load_balanced_split(R, Hq, H, lens):
     """The library's own choice for small batches of <= 8 stacked rows on
-    pages of >= 16 tokens: the batch's 16-token chunks spread evenly over a
-    persistent grid, a (request, head group) cut into up to 16 pieces that the
-    combine merges; empty contexts give zero rows."""
+    pages of >= 16 tokens: the batch's 16-token chunks spread over a
+    persistent grid (equal ranges, or ranges weighted by the grid's thirds
+    once every range still cuts a (request, head group) into at most 16
+    pieces), the pieces merged by the combine; empty contexts give zero
+    rows."""
     w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=len(lens),
                          rows_per_request=R, num_q_heads=Hq, num_kv_heads=H)
     lens = np.array(lens, dtype=np.int32)
@@ -210,14 +220,15 @@ def test_graph_capture_of_decode():
     assert_attention_close(out, ref, "graph replay")
 
 
-def _full_size(name, one_head=None):
+def _full_size(name, one_head=None, append=False):
     """The named workload at full size, in the configuration the benchmark
     times (default partition size, hence the same kernels and split), checked
     against the oracle on every (request, KV head) unit -- or, with `one_head`,
     on every request for that KV head.  The oracle quantises each unit's bf16
     rows itself (codes and both scale planes compared bit for bit) and computes
     its attention in fp64; the units run on all host cores (the oracle's C
-    calls release the GIL)."""
+    calls release the GIL).  With `append`, the cache holds each request's
+    first L - R tokens and the decode step's call stores the last R itself."""
     import concurrent.futures
     import os
     w = workloads.WORKLOADS[name]
@@ -230,14 +241,24 @@ def _full_size(name, one_head=None):
     ct = workloads.chunk_tokens(w)
     for r in range(w.num_requests):
         L = int(lens[r])
+        n_prev = L - R if append else L
         slots_all = workloads.token_slots(bt, r, L, w.block_size)
-        for c0 in range(0, L, ct):
-            n = min(ct, L - c0)
+        for c0 in range(0, n_prev, ct):
+            n = min(ct, n_prev - c0)
             k, v = workloads.request_kv(w, r, c0, n, device="cuda")
             kvq.quantize_scatter(cache, k, v, torch.from_numpy(slots_all[c0:c0 + n]).cuda(), err)
     q = workloads.queries(w, device="cuda")
-    out = kvq.paged_decode(cache, q, torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda(),
-                           int(lens.max()), w.sm_scale, rows_per_request=R, err_flags=err)
+    btd, cld = torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda()
+    if append:
+        new = [workloads.request_kv(w, r, int(lens[r]) - R, R, device="cuda")
+               for r in range(w.num_requests)]
+        out = kvq.paged_decode_append(cache, torch.cat([k for k, _ in new]),
+                                      torch.cat([v for _, v in new]), q, btd, cld,
+                                      int(lens.max()), w.sm_scale, rows_per_request=R,
+                                      err_flags=err)
+    else:
+        out = kvq.paged_decode(cache, q, btd, cld, int(lens.max()), w.sm_scale,
+                               rows_per_request=R, err_flags=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     out_h = out.float().cpu().numpy().astype(np.float64)
@@ -302,6 +323,12 @@ def _full_size(name, one_head=None):
 
 def test_decode_batch_full_size():
     _full_size("decode")
+
+
+def test_decode_step_with_append_full_size():
+    """The benchmark's decode step: the new row of every request stored by the
+    attention launch itself (kvq_paged_decode_append)."""
+    _full_size("decode", append=True)
 
 
 def test_verify_full_size():
