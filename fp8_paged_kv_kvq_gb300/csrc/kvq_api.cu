@@ -183,7 +183,7 @@ size_t workspace_for(const kvq::AttnShape &s) {
   const int64_t rows_total =
       static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
   if (s.stream)
-    return kvq::attn_stream_plan_bytes(s.num_requests) +
+    return kvq::attn_stream_pieces_bytes(s.num_requests, s.num_kv_heads) +
            kvq::attn_workspace_bytes(rows_total, kvq::kStreamSlots);
   return kvq::attn_workspace_bytes(rows_total, s.num_partitions);
 }

@@ -31,9 +31,10 @@
 //    chunks and writes either the final row (a segment that is the whole
 //    request) or its (max, denominator, output) to partial slot
 //    b - first CTA of the (request, group).
-//  * CTA 0 writes the split and the per-request chunk prefix into the
-//    workspace; the combine kernel (one warp per output row) reads them to
-//    find each row's slots.
+//  * The CTA holding a segment's first chunk writes the segment's piece count
+//    into the workspace (0 for a request with no cached token); the combine
+//    kernel (one warp per output row) reads it with all of the row's slots
+//    in one memory round trip.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -94,7 +95,7 @@ struct StParams {
   int32_t cmax;               // ceil(max context / 16)
   float *o_part;              // [rows][kStreamSlots][128]
   float2 *ml_part;            // [rows][kStreamSlots]
-  int32_t *plan;              // [0] B, [1] N, [2] grid / 3, [3] 0, [4 ..] chunk prefix [N + 1]
+  int32_t *pieces;            // [N][H / 4]: pieces of each (request, head group)
   int32_t *err_flags;
   // the step's new rows (k_new == nullptr: none; R <= kStNewRows): row
   // r * R + i of request r goes to position L_r - R + i, stored by the CTA
@@ -333,15 +334,10 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
   const int64_t *sx = reinterpret_cast<const int64_t *>(smem + kOffStSplit);
   const int64_t x_begin = sx[0];
   const int64_t x_end = sx[1];
-  if (blockIdx.x == 0) {
-    if (tid == 0) {
-      p.plan[0] = static_cast<int32_t>(sx[2]);
-      p.plan[1] = N;
-      p.plan[2] = static_cast<int32_t>(gridDim.x / 3);
-      p.plan[3] = 0;
-    }
-    for (int i = tid; i <= N; i += kStThreads) p.plan[4 + i] = pre[i];
-  }
+  // requests with no cached token: no pieces (the combine writes zero rows)
+  for (int r = blockIdx.x; r < N; r += gridDim.x)
+    if (pre[r + 1] == pre[r])
+      for (int g = tid; g < hg; g += kStThreads) p.pieces[static_cast<int64_t>(r) * hg + g] = 0;
   if (x_begin >= x_end) return;
 
   if (warp == kStHeads) {
@@ -748,6 +744,18 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       sp.cls = gridDim.x / 3;
       slot = static_cast<int>(blockIdx.x - sp.owner(sg.base));
     }
+    if (sg.c0 == 0 && w == 0 && lane == 0) {
+      // this CTA holds the segment's first chunk: its piece count
+      int n_pieces = 1;
+      if (!direct) {
+        StSplit sp;
+        sp.B = sx[2];
+        sp.total = sx[3];
+        sp.cls = gridDim.x / 3;
+        n_pieces = static_cast<int>(sp.owner(sg.base + sg.C - 1) - blockIdx.x) + 1;
+      }
+      p.pieces[static_cast<int64_t>(r) * hg + sg.g] = n_pieces;
+    }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int n = 2 * c4 + e;
@@ -785,9 +793,9 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
 // ---------------------------------------------------------------------------
 // Combine for the stream layout: one warp per output row, eight rows per CTA.
 struct StCombineParams {
-  int32_t N, R, Hq, G, H;
+  int32_t R, Hq, G, H;
   int64_t rows_total;
-  const int32_t *plan;
+  const int32_t *pieces;
   const float *o_part;
   const float2 *ml_part;
   uint16_t *out;
@@ -801,77 +809,51 @@ attn_combine_stream_kernel(const StCombineParams p) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kStCombineRows + (threadIdx.x >> 5);
   allow_dependents_launch();
   if (row >= p.rows_total) return;
-  grid_dependency_wait();              // the plan and the partials (any global read)
+  grid_dependency_wait();              // the piece counts and the partials (any global read)
   const int r = static_cast<int>(row / (static_cast<int64_t>(p.R) * p.Hq));
   const int qh = static_cast<int>(row % p.Hq);
   const int g = (qh / p.G) / kStHeads;
-  const int32_t *pre = p.plan + 4;
-  const int hg = p.H / kStHeads;
-  // one memory round trip: the plan entries this row needs and its first
-  // eight piece slots, whether or not the pieces exist (a slot past the
-  // row's count holds whatever an earlier call left and is not read)
-  const int32_t plan_b = p.plan[0], plan_cls = p.plan[2];
-  const int32_t pre_r = pre[r], pre_r1 = pre[r + 1], pre_n = pre[p.N];
+  // one memory round trip: the row's piece count and all of its slots,
+  // whether or not the pieces exist (a slot past the count holds whatever
+  // an earlier call left and is not used)
+  const int n = p.pieces[static_cast<int64_t>(r) * (p.H / kStHeads) + g];
   const float2 *ml = p.ml_part + row * kStreamSlots;
   const float4 *op = reinterpret_cast<const float4 *>(p.o_part + row * kStreamSlots * kHeadDim) +
                      lane;
-  float2 v[8];
-  float4 o[8];
+  float2 v[kStreamSlots];
+  float4 o[kStreamSlots];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < kStreamSlots; ++k) {
     v[k] = ml[k];
     o[k] = op[k * (kHeadDim / 4)];
   }
-  StSplit split;
-  split.B = plan_b;
-  split.cls = plan_cls;
-  split.total = static_cast<int64_t>(hg) * pre_n;
-  const int V = pre_r1 - pre_r;
-  uint2 packed = make_uint2(0u, 0u);
-  if (V > 0) {
-    const int C = V - kStreamSwitchChunks;
-    const int64_t base = static_cast<int64_t>(hg) * pre_r + static_cast<int64_t>(g) * V +
-                         kStreamSwitchChunks;
-    const int n = static_cast<int>(split.owner(base + C - 1) - split.owner(base)) + 1;
-    if (n <= 1) return;                // written by the partials kernel
-    float m_w = -INFINITY, lsum = 0.0f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q0 = 0; q0 < n; q0 += 8) {
-      if (q0 > 0) {                    // pieces 8 .. 15: a second round trip
+  if (n == 1) return;                  // written by the partials kernel
+  // n == 0: a request with no cached token gets a zero row
+  float m_w = -INFINITY, lsum = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (q0 + k < n) {
-            v[k] = ml[q0 + k];
-            o[k] = op[static_cast<int64_t>(q0 + k) * (kHeadDim / 4)];
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        // a piece that saw no visible token, or no piece
-        if (q0 + k >= n || v[k].x == -INFINITY) continue;
-        const float mn = fmaxf(m_w, v[k].x);
-        const float a = st_ex2(m_w - mn), b = st_ex2(v[k].x - mn);
-        lsum = lsum * a + v[k].y * b;
-        acc.x = acc.x * a + o[k].x * b;
-        acc.y = acc.y * a + o[k].y * b;
-        acc.z = acc.z * a + o[k].z * b;
-        acc.w = acc.w * a + o[k].w * b;
-        m_w = mn;
-      }
-    }
-    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  for (int k = 0; k < kStreamSlots; ++k) {
+    // no piece, or a piece that saw no visible token
+    if (k >= n || v[k].x == -INFINITY) continue;
+    const float mn = fmaxf(m_w, v[k].x);
+    const float a = st_ex2(m_w - mn), b = st_ex2(v[k].x - mn);
+    lsum = lsum * a + v[k].y * b;
+    acc.x = acc.x * a + o[k].x * b;
+    acc.y = acc.y * a + o[k].y * b;
+    acc.z = acc.z * a + o[k].z * b;
+    acc.w = acc.w * a + o[k].w * b;
+    m_w = mn;
   }
-  // a request with no cached token gets a zero row
+  const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+  const uint2 packed = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                  pack_bf16x2(acc.z * inv, acc.w * inv));
   *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + 4 * lane) = packed;
 }
 
 }  // namespace
 
-size_t attn_stream_plan_bytes(int32_t num_requests) {
-  return (static_cast<size_t>(num_requests + 5) * 4 + 255) / 256 * 256;
+size_t attn_stream_pieces_bytes(int32_t num_requests, int32_t num_kv_heads) {
+  return (static_cast<size_t>(num_requests) * (num_kv_heads / kStHeads) * 4 + 255) / 256 * 256;
 }
 
 bool attn_stream_shape_ok(int32_t num_kv_heads, const AttnShape &s) {
@@ -928,8 +910,8 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
   p.M = s.rows;
   p.qk_scale = sm_scale * 1.4426950408889634f;
   p.cmax = static_cast<int32_t>((static_cast<int64_t>(p.ctx_limit) + kChunk - 1) / kChunk);
-  p.plan = static_cast<int32_t *>(workspace);
-  char *parts = static_cast<char *>(workspace) + attn_stream_plan_bytes(s.num_requests);
+  p.pieces = static_cast<int32_t *>(workspace);
+  char *parts = static_cast<char *>(workspace) + attn_stream_pieces_bytes(s.num_requests, c.num_kv_heads);
   const size_t o = static_cast<size_t>(rows_total) * kStreamSlots * kHeadDim * sizeof(float);
   p.o_part = reinterpret_cast<float *>(parts);
   p.ml_part = reinterpret_cast<float2 *>(parts + (o + 255) / 256 * 256);
@@ -960,14 +942,14 @@ cudaError_t launch_attn_partials_stream(const kvq_cache &c, const AttnShape &s, 
 cudaError_t launch_attn_combine_stream(const AttnShape &s, void *out, void *workspace,
                                        cudaStream_t stream) {
   StCombineParams p;
-  p.N = s.num_requests;
   p.R = s.rows_per_request;
   p.Hq = s.num_q_heads;
   p.G = s.group;
   p.H = s.num_q_heads / s.group;
   p.rows_total = static_cast<int64_t>(s.num_requests) * s.rows_per_request * s.num_q_heads;
-  p.plan = static_cast<const int32_t *>(workspace);
-  const char *parts = static_cast<const char *>(workspace) + attn_stream_plan_bytes(s.num_requests);
+  p.pieces = static_cast<const int32_t *>(workspace);
+  const char *parts = static_cast<const char *>(workspace) +
+                      attn_stream_pieces_bytes(s.num_requests, s.num_q_heads / s.group);
   const size_t o = static_cast<size_t>(p.rows_total) * kStreamSlots * kHeadDim * sizeof(float);
   p.o_part = reinterpret_cast<const float *>(parts);
   p.ml_part = reinterpret_cast<const float2 *>(parts + (o + 255) / 256 * 256);

@@ -60,10 +60,9 @@ struct AttnShape {
 // content of the workspace, carries another tag and is restarted.
 uint32_t next_call_tag();
 
-// The load-balanced decode kernel's layout: a plan ([0] equal range length or
-// 0 for the weighted split, [1] requests, [2] CTAs per third of the grid, [3]
-// 0, [4 ..] per-request chunk prefix) then partials in kStreamSlots slots per
-// output row.
+// The load-balanced decode kernel's workspace: the piece count of each
+// (request, group of 4 KV heads) as int32, then partials in kStreamSlots slots
+// per output row.
 constexpr int32_t kStreamSlots = 16;
 // A segment (the chunks of one request and head group) is charged this many
 // extra chunks at its start, so a CTA whose range crosses into a new segment
@@ -74,7 +73,7 @@ constexpr int32_t kStreamMaxRequests = 1024;
 // New rows per request that the load-balanced kernel stores itself (a decode
 // step's store fused into its attention); more take the store's own launch.
 constexpr int32_t kStreamNewRows = 2;
-size_t attn_stream_plan_bytes(int32_t num_requests);
+size_t attn_stream_pieces_bytes(int32_t num_requests, int32_t num_kv_heads);
 
 // Whether a shape suits the load-balanced kernel (apart from the cache's
 // scale alignment): at most 8 stacked rows, pages of >= 16 tokens, KV heads in
