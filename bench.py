@@ -669,8 +669,9 @@ def _run_kvq_on_stream(args, rank, local, world, dev, wl, K, W):
     }
     if args.workload != "store":
         if wl.balanced:
-            res["config"]["split"] = ("load-balanced: the batch's 16-token chunks split evenly "
-                                      "over a persistent grid (3 CTAs per SM)")
+            res["config"]["split"] = ("load-balanced: the batch's 16-token chunks split over a "
+                                      "persistent grid (3 CTAs per SM, ranges weighted by the "
+                                      "grid's dispatch thirds)")
         elif wl.rows_kernel:
             res["config"]["split"] = ("load-balanced: the batch's 128-token chunks split evenly "
                                       "over a persistent grid (1 CTA per SM), cut units merged "
