@@ -107,7 +107,9 @@ def _many_lens(n, hi, seed):
     (2, 16, 4, 16, [17, 2, 1, 640, 64, 33], 0),     # rows across a chunk edge; a negative position
     (1, 32, 8, 16, _many_lens(300, 700, 21), 0),    # weighted split, many segments per CTA
     (2, 16, 4, 32, _many_lens(150, 900, 22), 0),
-    # other kernels: the store's own launch, then the attention
+    # other kernels, or more than two new rows: the store's own launch, then
+    # the attention
+    (4, 16, 8, 16, [4, 3, 100, 31, 2000], 0),       # 8 stacked rows, 4 new rows each
     (1, 32, 8, 16, [1, 15, 16, 17, 300, 1000, 33, 0, 4096, 5], 128),
     (4, 32, 8, 64, [4, 333, 520], 0),               # 16 stacked rows: the rows-on-M kernel
     (4, 32, 8, 64, [4, 333, 520], 256),             # the partitioned tensor-core kernel
@@ -194,3 +196,41 @@ def test_graph_capture_of_the_step():
                                     w.sm_scale)
     assert e == 0
     assert_attention_close(out, ref, "graph replay of the step")
+
+
+@pytest.mark.parametrize("P", [0, 128])
+def test_append_to_a_bad_page_is_flagged_and_skipped(P):
+    """A new row whose page id is out of range (too large, negative) is not
+    stored -- no write lands anywhere in the cache -- and the call sets
+    KVQ_ERRF_BLOCK_RANGE; the other requests' rows and outputs are those of
+    the oracle.  P = 0: the load-balanced kernel stores the rows; P = 128: the
+    store's own launch."""
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=4)
+    lens = [200, 333, 1000, 64]
+    st = _step(w, lens, 1, 9)
+    bs = w.block_size
+    bt_bad = st["bt"].copy()
+    bt_bad[1, (333 - 1) // bs] = 1 << 30          # the page of request 1's new row
+    bt_bad[3, (64 - 1) // bs] = -7                 # and of request 3's
+    before = {nm: getattr(st["cache"], nm).clone() for nm in ("k_codes", "v_codes", "k_scales",
+                                                                "v_scales")}
+    lens_a = st["lens"]
+    out = kvq.paged_decode_append(st["cache"], st["k_new"], st["v_new"], st["q"].cuda(),
+                                  torch.from_numpy(bt_bad).cuda(), torch.from_numpy(lens_a).cuda(),
+                                  int(lens_a.max()), w.sm_scale, partition_tokens=P,
+                                  err_flags=st["err"])
+    torch.cuda.synchronize()
+    assert int(st["err"].item()) & kvq.ERRF_BLOCK_RANGE
+    # only requests 0 and 2 stored their rows: every other slot is unchanged
+    bsz = st["cache"].block_size
+    new_slots = [int(workloads.token_slots(st["bt"], r, int(lens_a[r]), bsz)[-1]) for r in (0, 2)]
+    for nm, b in before.items():
+        now = getattr(st["cache"], nm)
+        changed = torch.nonzero((now != b).reshape(now.shape[0], -1).any(dim=1)).flatten().tolist()
+        assert set(changed) <= set(new_slots), (nm, changed, new_slots)
+    # requests 0 and 2 (pages intact) match the oracle
+    ref, e = oracle.paged_attention(st["ocache"], workloads.bf16_bits(st["q"]), len(lens), 1,
+                                    w.num_q_heads, st["bt"], lens_a, w.block_size, w.sm_scale)
+    assert e == 0
+    for r in (0, 2):
+        assert_attention_close(out[r:r + 1], ref[r:r + 1], f"append, bad pages elsewhere, r={r} P={P}")
