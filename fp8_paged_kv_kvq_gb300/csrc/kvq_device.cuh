@@ -356,12 +356,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
-// Orders this thread's generic-proxy global writes before async-proxy (TMA)
-// accesses that follow it through a barrier.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;\n" ::: "memory");
-}
-
 // 3-D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
                                             uint32_t bar) {
@@ -404,17 +398,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];\n"
       :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-
-// Prefetch one tiled box into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n"
-               :: "l"(tmap), "r"(x), "r"(y), "r"(z) : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n"
-               :: "l"(tmap), "r"(x), "r"(y) : "memory");
 }
 
 // Barrier `id` (1..15) over the first `count` threads that reach it.
