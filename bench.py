@@ -385,7 +385,7 @@ class DeviceWorkload:
         sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         cmax = (self.max_ctx + 15) // 16
         hg = w.num_kv_heads // 4
-        total_ub = w.num_requests * hg * (cmax + 3)
+        total_ub = w.num_requests * hg * (cmax + 5)
         per_cta = (total_ub + 3 * sms - 1) // (3 * sms)
         per_cta_w = (total_ub * 135 + 384 * sms - 1) // (384 * sms) + 1   # weighted ranges
         b = max(per_cta, (cmax + 14) // 15, per_cta_w)

@@ -68,7 +68,7 @@ constexpr int32_t kStreamSlots = 16;
 // extra chunks at its start, so a CTA whose range crosses into a new segment
 // (a second query preparation, during which its ring stands full) gets
 // correspondingly less work.
-constexpr int32_t kStreamSwitchChunks = 3;
+constexpr int32_t kStreamSwitchChunks = 5;
 constexpr int32_t kStreamMaxRequests = 1024;
 // New rows per request that the load-balanced kernel stores itself (a decode
 // step's store fused into its attention); more take the store's own launch.
