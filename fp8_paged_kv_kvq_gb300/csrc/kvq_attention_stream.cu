@@ -787,6 +787,7 @@ attn_stream_kernel(const StParams p, const __grid_constant__ CUtensorMap tmap_k,
       sg.n = 0;
     }
   }
+  cp_async_wait<0>();                  // new rows staged for a chunk past the range's end
   if (timed_out && lane == 0 && p.err_flags) atomicOr(p.err_flags, KVQ_ERRF_WAIT_TIMEOUT);
 }
 
