@@ -335,6 +335,13 @@ def test_verify_full_size():
     _full_size("verify", one_head=5)
 
 
+def test_verify_step_with_append_full_size():
+    """The verify step through kvq_paged_decode_append: 4 new rows per request
+    stored at their block-table positions by the store's own launch (more
+    than two rows per request), then the rows-on-M kernel."""
+    _full_size("verify", one_head=2, append=True)
+
+
 def test_long_context_full_size():
     _full_size("longctx")
 
