@@ -157,8 +157,8 @@ int32_t kvq_paged_decode_partition_tokens(int32_t num_requests, int32_t rows_per
  * num_q_heads * ceil(max_context_len / partition) * (head_dim + 2) * 4, each
  * of the two parts rounded up to 256.  With partition_tokens 0 the library's
  * own split decides (see kvq_paged_decode_partition_tokens): for <= 8 stacked
- * rows per KV head the split's plan (the request prefix) plus 16 pieces of
- * partial results per output row; for the rows-on-M kernel one 64-bit
+ * rows per KV head one piece count per (request, group of 4 KV heads) plus
+ * 16 pieces of partial results per output row; for the rows-on-M kernel one 64-bit
  * counter per (request, KV head, 128-row tile) plus two pieces of partial
  * results per SM.  Returns 0 for invalid arguments. */
 size_t kvq_paged_decode_workspace_size(int32_t num_requests, int32_t rows_per_request,

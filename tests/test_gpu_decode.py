@@ -490,7 +490,7 @@ def test_query_split_error_bound(R, G):
 ])
 def test_workspace_needs_no_initialisation(R, Hq, H, bs, lens):
     """A workspace full of arbitrary bytes (here 0xA5 and random) needs no
-    clearing: the load-balanced decode writes its plan every call, and the
+    clearing: the load-balanced decode writes its piece counts every call, and the
     rows-on-M kernel counts a cut unit's pieces in words tagged with the call.
     Calls in a row on it, and a captured CUDA graph replayed three times, all
     give the oracle's result."""

@@ -3,7 +3,7 @@ allocate device memory (it uses a fixed scratch array inside the library
 instead of a caller workspace).  Called through the C ABI and checked against
 kvq_paged_decode on the same inputs, twice in a row, with shapes that need the
 split-K scratch; with the default partition choice (the load-balanced kernel,
-which keeps its plan and piece slots in the array) against the oracle, twice
+which keeps its piece counts and slots in the array) against the oracle, twice
 in a row with different lengths; plus the refusal of a shape larger than the
 array.
 
@@ -71,7 +71,7 @@ def test_noalloc_decode_matches_the_workspace_decode_twice_in_a_row():
 
 def test_noalloc_default_partition_against_the_oracle():
     """partition_tokens = 0 on a small decode batch: the library picks its
-    load-balanced kernel, which keeps its plan and its piece slots in the
+    load-balanced kernel, which keeps its piece counts and slots in the
     scratch array.  Two calls in a row with different context lengths (and a
     different number of pieces per request) are checked against the oracle, so
     nothing the first call left in the array leaks into the second."""
