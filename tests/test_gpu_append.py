@@ -107,6 +107,7 @@ def _many_lens(n, hi, seed):
     (2, 16, 4, 16, [17, 2, 1, 640, 64, 33], 0),     # rows across a chunk edge; a negative position
     (1, 32, 8, 16, _many_lens(300, 700, 21), 0),    # weighted split, many segments per CTA
     (2, 16, 4, 32, _many_lens(150, 900, 22), 0),
+    (1, 8, 4, 16, _many_lens(1024, 40, 23), 0),    # 1024 requests
     # other kernels, or more than two new rows: the store's own launch, then
     # the attention
     (4, 16, 8, 16, [4, 3, 100, 31, 2000], 0),       # 8 stacked rows, 4 new rows each

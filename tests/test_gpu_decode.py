@@ -87,6 +87,7 @@ def _many_lens(n, hi, seed):
     # next segment's query rows staged while the current one runs)
     (1, 32, 8, _many_lens(300, 700, 11)),
     (2, 16, 4, _many_lens(200, 900, 12)),
+    (1, 8, 4, _many_lens(1024, 48, 13)),     # the most requests it takes: a full prefix
 ])
 def test_load_balanced_split(R, Hq, H, lens):
     """The library's own choice for small batches of <= 8 stacked rows on
