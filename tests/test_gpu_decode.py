@@ -111,6 +111,29 @@ def test_load_balanced_split(R, Hq, H, lens):
     assert_attention_close(out, ref, f"balanced R={R} Hq={Hq} H={H}")
 
 
+@pytest.mark.parametrize("R,Hq,H,bs", [
+    (4, 32, 8, 16),    # 16 stacked rows, 32-row tiles
+    (4, 64, 4, 32),    # 64 stacked rows, 64-row tiles
+])
+def test_rows_kernel_most_requests(R, Hq, H, bs):
+    """The rows-on-M kernel at the most requests it takes (1024: the request
+    prefix fills its shared-memory array), short ragged contexts and empty
+    requests among them, so that units are cut across CTAs all over the
+    batch."""
+    lens = np.array(_many_lens(1024, 300, 31), dtype=np.int32)
+    lens[:R] = np.arange(R)                   # contexts shorter than the rows
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=len(lens),
+                         rows_per_request=R, num_q_heads=Hq, num_kv_heads=H, block_size=bs)
+    built = build_paged(w, lens, gen_device="cuda")
+    q = _queries(w, len(lens), R, 8)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(built, q, R, w.sm_scale, err=err)
+    ref, _ = oracle_decode(built, q, R, Hq, w.sm_scale)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, f"1024 requests R={R} Hq={Hq} H={H}")
+
+
 @pytest.mark.parametrize("partition_tokens", [0, 1024, 8192])
 def test_verify_climbing_scores_move_every_reference(partition_tokens):
     """The verify shape (32 stacked rows per KV head) with keys that grow along
