@@ -191,7 +191,6 @@ attn_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tm_kc,
   uint32_t *vmax_s = reinterpret_cast<uint32_t *>(smem + kOffMisc + 96);  // [2][8]
   int *flag_s = reinterpret_cast<int *>(smem + kOffMisc + 160);           // [2][8] give-up
   int *red_i = reinterpret_cast<int *>(smem + kOffRed);
-  float *red_f = reinterpret_cast<float *>(smem + kOffRed);
   float *rowf_s = reinterpret_cast<float *>(smem + kOffRow);   // 2^e_m * sm_scale * log2e
   float *mcur_s = rowf_s + kTcRows;                            // row references
   float *lsum_s = rowf_s + 3 * kTcRows;                        // denominators
