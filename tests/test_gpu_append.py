@@ -108,6 +108,9 @@ def _many_lens(n, hi, seed):
     (1, 32, 8, 16, _many_lens(300, 700, 21), 0),    # weighted split, many segments per CTA
     (2, 16, 4, 32, _many_lens(150, 900, 22), 0),
     (1, 8, 4, 16, _many_lens(1024, 40, 23), 0),    # 1024 requests
+    # larger pages: the new rows at the end of a page, across two pages
+    (1, 32, 8, 64, [64, 65, 1, 2, 128, 129] + _many_lens(30, 3000, 24), 0),
+    (2, 16, 4, 256, [256, 257, 2, 3, 512] + _many_lens(25, 2500, 25), 0),
     # other kernels, or more than two new rows: the store's own launch, then
     # the attention
     (4, 16, 8, 16, [4, 3, 100, 31, 2000], 0),       # 8 stacked rows, 4 new rows each

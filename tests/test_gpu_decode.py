@@ -112,6 +112,29 @@ def test_load_balanced_split(R, Hq, H, lens):
 
 
 @pytest.mark.parametrize("R,Hq,H,bs", [
+    (1, 32, 8, 32),
+    (2, 16, 4, 64),
+    (1, 8, 4, 256),
+])
+def test_load_balanced_block_sizes(R, Hq, H, bs):
+    """The load-balanced kernel on pages of 32 to 256 tokens (a 16-token
+    chunk always lies within one page): contexts ending on and just past page
+    edges, long ones spanning many pages, empty requests."""
+    lens = [bs, bs + 1, 1, 0, 2 * bs - 1] + _many_lens(30, 3000, 40 + bs)
+    w = workloads.scaled(workloads.WORKLOADS["decode"], num_requests=len(lens),
+                         rows_per_request=R, num_q_heads=Hq, num_kv_heads=H, block_size=bs)
+    lens = np.array(lens, dtype=np.int32)
+    built = build_paged(w, lens)
+    q = _queries(w, len(lens), R, 9)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(built, q, R, w.sm_scale, err=err)
+    ref, _ = oracle_decode(built, q, R, Hq, w.sm_scale)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out, ref, f"balanced bs={bs} R={R} Hq={Hq} H={H}")
+
+
+@pytest.mark.parametrize("R,Hq,H,bs", [
     (4, 32, 8, 16),    # 16 stacked rows, 32-row tiles
     (4, 64, 4, 32),    # 64 stacked rows, 64-row tiles
 ])
