@@ -238,10 +238,13 @@ kvq_status kvq_paged_decode_combine(const kvq_cache *cache, int32_t num_requests
  * follows the cache format of the pages (FreeToken PR #354 "feat(kvcache):
  * store the KV cache as fp8 e4m3 codes"; ROCm/ATOM PR #2655, K/V bullet) bit
  * for bit; fusing it with the attention is this library's own step: where the
- * shape takes the load-balanced kernel (kvq_paged_decode_partition_tokens), the
- * CTA that streams a chunk holding new positions quantises and stores those
- * rows before its copy engine reads the chunk, so the store costs no launch of
- * its own; other shapes make the store's launch first.
+ * shape takes the load-balanced kernel (kvq_paged_decode_partition_tokens) and
+ * rows_per_request is at most 2, the CTA that streams a chunk holding new
+ * positions quantises those rows once the chunk has landed in its shared
+ * memory, writes their codes and scales over the slots' old contents there
+ * (the attention reads the new rows from that copy) and stores them to the
+ * cache, so the store costs no launch of its own and the copy never waits
+ * for it; other shapes make the store's launch first.
  *   k_new, v_new    device bf16; row r*rows_per_request + i (token pitch
  *                   k_token_stride / v_token_stride elements, multiples of 8,
  *                   16-byte aligned; head h at element h*head_dim) is new token
