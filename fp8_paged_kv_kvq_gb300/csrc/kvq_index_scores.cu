@@ -323,7 +323,10 @@ index_scores_kernel(const ScParams p) {
     }
     const uint8_t *sb = smem + st * F::kStageBytes;
     const uint32_t *sx = reinterpret_cast<const uint32_t *>(sb + F::kCodeBytes);
-#pragma unroll 1
+    // the warp's two tiles of the chunk unrolled, so that their conversions
+    // and MMA chains interleave (59.6 vs 61.8 us on 64 requests of MXFP4 keys,
+    // 55.9 vs 57.4 with FP8 keys; 96 registers either way)
+#pragma unroll
     for (int tile = warp; tile < kScChunk / kScTile; tile += kScWarps) {
       const int j0 = k * kScChunk + kScTile * tile;
       if (j0 >= p.max_len) break;
